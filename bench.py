@@ -1,0 +1,432 @@
+"""Benchmark of the greedy decode step (one JSON line on stdout).
+
+Workload (default ``dense4b``): a 36-layer 4B-class dense GQA decoder
+(H=2560, Hq=32, Hkv=8, D=128, I=9728, V=151936, tied embeddings, bf16
+weights N(0, 0.02), norm gains 1 + N(0, 0.02), seeded synthetic data), batch
+1, a 512-token uniform-random prompt through the teacher-forced prompt pass
+(untimed), then greedy decode steps through the native loop (CUDA-graph
+replays, EOS id 0 checked every 16 steps).  A "step" is one decode step of
+the whole model; the timed steps cycle over the workload's 256 decode
+positions 511..766 (the cache slots are rewritten on each pass).
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(bounded sample, rank 0 only).  With N > 1 (torchrun) every rank decodes its
+own replica (no collective on the data path) and rank 0 reports the total.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "greedy decode tok/s at b=1 (36-layer 4B-class); HBM GB/s vs 8 TB/s peak"
+POSITIONS_PER_PASS = 256
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="gemv", choices=["gemv", "reference"])
+    ap.add_argument("--workload", default="dense4b", choices=["dense4b", "layer4b"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- measured peaks
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def committed_traffic(kernel_tag: str):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, if present."""
+    p = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(p):
+        return None
+    m = re.search(r"dram bytes per launch[^0-9]*([0-9][0-9_,.]*)", open(p).read())
+    if not m:
+        return None
+    return float(m.group(1).replace(",", "").replace("_", ""))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def host_model(name, seed=0):
+    import synth
+    w = synth.workload(name)
+    m = w.model
+    layers = [synth.make_layer(seed, m, l) for l in range(m.n_layers)]
+    head = w.extra.get("lm_head", True)
+    E = synth.make_embedding(seed, m) if head else None
+    fn = synth.make_final_norm(seed, m) if head else None
+    return w, m, layers, E, fn
+
+
+def bytes_per_step(m, positions, B=1, head=True):
+    """Algorithmic HBM bytes of one step: every weight once, plus the KV rows read."""
+    H, Hq, Hkv, D, I, V = m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.intermediate, m.vocab
+    per_layer = 2 * (Hq * D * H + 2 * Hkv * D * H + H * Hq * D + 3 * I * H) + 2 * 2 * H
+    w = m.n_layers * per_layer + (2 * V * H + 2 * H if head else 0)
+    kv = sum(2 * m.n_layers * Hkv * D * 2 * (p + 1) for p in positions)
+    return w, kv
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import greedy_decode_step_gb300 as gd
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gd.lib()
+    w, m, layers_h, E_h, fn_h = host_model(args.workload)
+    B = 1
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    t0 = time.time()
+    layers = [{k: to_dev(v) for k, v in l.items()} for l in layers_h]
+    E = to_dev(E_h) if E_h is not None else None
+    fn = to_dev(fn_h) if fn_h is not None else None
+    model = gd.Model(m.n_layers, m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.intermediate, m.vocab,
+                     m.rms_eps, m.rope_theta, layers, embed=E, final_norm=fn, lm_head=E)
+    P = w.prompt_len
+    S_max = P + POSITIONS_PER_PASS + 8
+    st = gd.State(model, B, S_max, device=dev).init()
+    prompt_h = synth.make_tokens(w.seed, "prompt", (B, P), m.vocab)
+    prompt = torch.from_numpy(prompt_h).to(dev)
+    setup_s = time.time() - t0
+    stream = torch.cuda.current_stream(dev)
+
+    # prompt pass (untimed for the metric; reported)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gd.dec_prefill(model, st, prompt)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prefill_ms = e0.elapsed_time(e1)
+    pos0 = st.pos.clone()
+    tok0 = st.token.clone()
+
+    out = torch.empty((B, POSITIONS_PER_PASS), dtype=torch.int32, device=dev)
+
+    def restart():
+        st.pos.copy_(pos0)
+        st.token.copy_(tok0)
+
+    # warm-up: the first call also captures the 16-step graph
+    t_cap = time.time()
+    restart()
+    gd.dec_decode(model, st, max(16, args.warmup), w.eos_id, out)
+    torch.cuda.synchronize(dev)
+    capture_and_warmup_s = time.time() - t_cap
+
+    # timed: exactly K steps, in passes over the workload's decode positions
+    passes = []
+    left = args.steps
+    while left > 0:
+        passes.append(min(POSITIONS_PER_PASS, left))
+        left -= passes[-1]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    executed = 0
+    positions = []
+    with ClockSampler(local) as clk:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(passes))]
+        for i, n in enumerate(passes):
+            restart()
+            ev[2 * i].record(stream)
+            executed += gd.dec_decode(model, st, n, w.eos_id, out)
+            ev[2 * i + 1].record(stream)
+            positions += list(range(int(pos0[0]), int(pos0[0]) + n))
+        torch.cuda.synchronize(dev)
+    ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(passes)))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    tokens_out = out.cpu().numpy()
+    assert gd.device_error(clear=True) == 0
+
+    w_bytes, kv_bytes = bytes_per_step(m, positions, B)
+    step_bytes = w_bytes + kv_bytes / max(1, len(positions))
+    ms_per_step = ms / executed
+    tok_s = executed * B * world / (ms / 1e3)
+
+    # dominant kernel: the gate/up GEMV (half of every layer's bytes), launched
+    # alone through the C-ABI with the step's launch configuration, cycling
+    # over the 36 layers' weights (every launch streams its weights from HBM)
+    roof = glu_roofline(gd, torch, model, m, dev, stream)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(gd, torch, model, st, m, w, prompt_h, dev, stream, B)
+
+    launches_per_step = 5 * m.n_layers + 1
+    res = {
+        "metric": METRIC,
+        "value": round(tok_s, 2),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": executed,
+        "warmup": max(16, args.warmup),
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Philox N(0,0.02) weights, uniform prompt tokens)",
+        "config": {
+            "workload": "dense4b: 36 layers, H=2560, Hq=32, Hkv=8, D=128, I=9728, V=151936 tied; b=1; "
+                        "512-token prompt (teacher-forced, untimed); 256 greedy decode positions (511..766) "
+                        "per pass through the CUDA-graph decode loop, EOS id 0 checked every 16 steps",
+            "batch": B, "prompt_len": P, "decode_positions": [positions[0], positions[-1]] if positions else None,
+            "accumulate": "fp32", "weights": "bf16", "kv_cache": "bf16", "activations": "fp32",
+            "l2": "inputs larger than L2: every step streams 8.0 GB of weights (L2 129 MB)",
+            "parallelism": f"replicas x{world} (no collective)",
+            "prefill_ms": round(prefill_ms, 2), "capture_and_warmup_s": round(capture_and_warmup_s, 3),
+            "setup_s": round(setup_s, 2),
+            "step_bytes": int(step_bytes), "step_weight_bytes": int(w_bytes),
+            "step_hbm_gbs": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
+            "step_hbm_frac_of_measured": round(step_bytes / (ms_per_step / 1e3) / 1e9 / peaks()[0], 4),
+            "step_hbm_frac_of_8tbs": round(step_bytes / (ms_per_step / 1e3) / 8e12, 4),
+            "eos_hits": int(np.sum(tokens_out == w.eos_id)),
+        },
+        "roofline": roof,
+        "gpu_launches": executed * launches_per_step + 2 * len(passes),
+        "clocks": clk.summary(),
+    }
+    if e2e:
+        res["e2e"] = e2e
+    return res, (m, layers_h, E_h, fn_h, prompt_h)
+
+
+def glu_roofline(gd, torch, model, m, dev, stream, reps=3):
+    B = 1
+    y = torch.randn((B, m.hidden), device=dev, dtype=torch.float32)
+    h = torch.empty((B, m.intermediate), device=dev, dtype=torch.float32)
+    layers = model.layers
+    for l in layers[:4]:
+        gd.dec_glu_gemv(y, l["wg"], l["wu"], h)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    n = 0
+    for _ in range(reps):
+        for l in layers:
+            gd.dec_glu_gemv(y, l["wg"], l["wu"], h)
+            n += 1
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    avg_s = e0.elapsed_time(e1) / 1e3 / n
+    alg = 2 * 2 * m.intermediate * m.hidden + 4 * B * m.hidden + 4 * B * m.intermediate
+    peak, src = peaks()
+    achieved = alg / avg_s / 1e9
+    traffic = committed_traffic("gemv_glu_dense4b")
+    return {"kernel": "gemv_kernel<GLU,1> (gate/up GEMV + SiLU*mul)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{src} (burst copy; kernel timed alone)", "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg, "avg_launch_us": round(avg_s * 1e6, 2), "launches_timed": n}
+
+
+def end_to_end(gd, torch, model, st, m, w, prompt_h, dev, stream, B):
+    """The user call from host buffers: pinned prompt -> H2D, dec_generate
+    (prompt pass + 256 decode steps), D2H of the tokens."""
+    P = prompt_h.shape[1]
+    n = POSITIONS_PER_PASS
+    host_prompt = torch.from_numpy(prompt_h).pin_memory()
+    host_out = torch.empty((B, n), dtype=torch.int32).pin_memory()
+    dprompt = torch.empty((B, P), dtype=torch.int32, device=dev)
+    dout = torch.empty((B, n), dtype=torch.int32, device=dev)
+    st.pos.zero_()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    dprompt.copy_(host_prompt, non_blocking=True)
+    done = gd.dec_generate(model, st, dprompt, n, w.eos_id, dout)
+    host_out.copy_(dout, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    return {"value": round(done * B / (ms / 1e3), 2), "unit": "tok/s",
+            "h2d_bytes_per_step": round(B * P * 4 / done, 2), "d2h_bytes_per_step": B * 4,
+            "what": "pinned host prompt -> H2D -> dec_generate (512-token prompt pass + 256 decode steps) -> "
+                    "D2H tokens; tokens generated / wall time of the whole call"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_rate(m, layers_h, E_h, fn_h, max_steps, max_seconds=25.0, seed=0):
+    """Decode steps of the fp64 oracle on one host core at positions 511.. with a
+    511-token N(0,1) cache prefix (the oracle cannot afford the 511-step prompt pass)."""
+    import oracle
+    import synth
+    P = 511
+    S_max = P + max_steps + 2
+    kc, vc = [], []
+    for l in range(m.n_layers):
+        k = np.zeros((1, m.n_kv_heads, S_max, m.head_dim), np.uint16)
+        v = np.zeros_like(k)
+        synth.make_kv_prefix(seed, m, l, 0, P, "k", k[0])
+        synth.make_kv_prefix(seed, m, l, 0, P, "v", v[0])
+        kc.append(k)
+        vc.append(v)
+    om = oracle.Model(m, layers_h, E_h, fn_h, E_h, kc, vc)
+    t = int(synth.make_tokens(seed, "prompt", (1, 512), m.vocab)[0, -1])
+    done, t0 = 0, time.time()
+    while done < max_steps:
+        t, _, _ = om.step(0, P + done, token=t)
+        done += 1
+        if time.time() - t0 > max_seconds:
+            break
+    el = time.time() - t0
+    return done, el
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if "model name" in line or "CPU part" in line:
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        _, m, layers_h, E_h, fn_h = host_model(args.workload)
+        n = max(1, min(args.steps, 4))
+        done, el = oracle_rate(m, layers_h, E_h, fn_h, n, max_seconds=60.0)
+        v = done / el
+        line = {"metric": METRIC, "value": round(v, 5), "unit": "tok/s", "n_gpus": args.gpus, "steps": done,
+                "warmup": 0, "ms_per_step": round(el / done * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "config": {"workload": "dense4b (as the GPU arm), decode steps at positions 511.. over a "
+                                       "511-token N(0,1) cache prefix"},
+                "cpu_baseline": {"value": round(v, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{done} full decode steps (36 layers + LM head) of the fp64 oracle, "
+                                           f"single thread, {cpu_model()}"},
+                "e2e": {"value": round(v, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res, host = run_gpu(args, world, rank, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        m, layers_h, E_h, fn_h, _ = host
+        done, el = oracle_rate(m, layers_h, E_h, fn_h, 3, max_seconds=25.0)
+        res["cpu_baseline"] = {"value": round(done / el, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                               "sample": f"{done} full decode steps (36 layers + LM head) of the fp64 oracle at "
+                                         f"positions 511.. over a 511-token N(0,1) cache, single thread, "
+                                         f"{cpu_model()}"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

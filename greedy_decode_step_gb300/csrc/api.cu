@@ -1,0 +1,934 @@
+// C-ABI of libdec: argument checks, launch planning, the whole-step sequence
+// and the native decode loop (graph capture + replay, EOS check every 16
+// steps).  Declarations and the contract of every entry point are in
+// include/libdec.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dec_launch.cuh"
+#include "libdec.h"
+
+using namespace dec;
+
+// Per-device error word (see dec_device_error).
+__device__ uint32_t g_dec_device_error;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+#define DEC_CUDA(expr)                                                                     \
+  do {                                                                                     \
+    cudaError_t e_ = (expr);                                                               \
+    if (e_ != cudaSuccess) return fail(DEC_ECUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+#define DEC_CHECK(cond, code, ...)         \
+  do {                                     \
+    if (!(cond)) return fail(code, __VA_ARGS__); \
+  } while (0)
+
+#define DEC_TRY(expr)          \
+  do {                         \
+    int r_ = (expr);           \
+    if (r_ != DEC_OK) return r_; \
+  } while (0)
+
+// ------------------------------------------------------------------------------- device set-up
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  uint32_t* err = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  DEC_CUDA(cudaGetDevice(&dev));
+  DEC_CHECK(dev >= 0 && dev < kMaxDevices, DEC_EUNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    DEC_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    DEC_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    DEC_CHECK(major == 10 && minor == 3, DEC_EUNSUPPORTED, "libdec is built for sm_103 (GB300); device %d is sm_%d%d",
+              dev, major, minor);
+    DEC_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+    DEC_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_dec_device_error));
+    DEC_CUDA(allow_smem_qkv());
+    DEC_CUDA(allow_smem_glu());
+    DEC_CUDA(allow_smem_resid());
+    DEC_CUDA(allow_smem_head());
+    DEC_CUDA(allow_smem_attn());
+    d.ready = true;
+  }
+  *out = &d;
+  return DEC_OK;
+}
+
+// ------------------------------------------------------------------------------- checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define DEC_PTR(p) DEC_CHECK((p) != nullptr && aligned16(p), DEC_EINVAL, "%s must be a non-null 16-byte aligned pointer", #p)
+
+int check_batch(int B) {
+  DEC_CHECK(B >= 1 && B <= kMaxBatch, DEC_EUNSUPPORTED, "batch %d outside 1..%d", B, kMaxBatch);
+  return DEC_OK;
+}
+
+int check_row(int K, const char* what) {
+  DEC_CHECK(K >= 8 && K % 8 == 0 && K <= (1 << 20), DEC_EUNSUPPORTED, "%s = %d: rows must hold a multiple of 8 elements",
+            what, K);
+  return DEC_OK;
+}
+
+int check_heads(int Hq, int Hkv, int D) {
+  DEC_CHECK(D == 64 || D == 128, DEC_EUNSUPPORTED, "head_dim %d: supported 64 and 128", D);
+  DEC_CHECK(Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0, DEC_EINVAL, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  DEC_CHECK(Hq / Hkv <= kAttnMaxGroup, DEC_EUNSUPPORTED, "Hq/Hkv = %d above %d", Hq / Hkv, kAttnMaxGroup);
+  return DEC_OK;
+}
+
+int bt_bucket(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16; }
+
+uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// ------------------------------------------------------------------------------- small kernels
+
+__global__ void __launch_bounds__(kConsumerThreads) add_rmsnorm_kernel(const __grid_constant__ NormArgs a) {
+  __shared__ float red[kConsumerWarps];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x;
+  float* r = a.resid + static_cast<size_t>(b) * a.H;
+  if (a.tokens) {
+    const int tok = a.tokens[b];
+    const bool ok = tok >= 0 && tok < a.vocab;
+    if (!ok && threadIdx.x == 0) atomicOr(a.err, kErrTokenRange);
+    const uint16_t* er = a.embed + static_cast<size_t>(ok ? tok : 0) * a.H;
+    for (int i = threadIdx.x; i < a.H; i += kConsumerThreads)
+      r[i] = ok ? __uint_as_float(static_cast<uint32_t>(er[i]) << 16) : 0.f;
+  } else if (a.x) {
+    const float* x = a.x + static_cast<size_t>(b) * a.H;
+    for (int i = threadIdx.x; i < a.H; i += kConsumerThreads) r[i] = r[i] + x[i];
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  const float inv = block_rms_inv(r, a.H, a.eps, red);
+  float* y = a.y + static_cast<size_t>(b) * a.H;
+  for (int i = threadIdx.x; i < a.H; i += kConsumerThreads)
+    y[i] = (r[i] * inv) * __uint_as_float(static_cast<uint32_t>(a.gamma[i]) << 16);
+}
+
+
+__global__ void advance_kernel(int32_t* token, int32_t* pos, int B, const int32_t* prompt, int P, int col) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = threadIdx.x;
+  if (b < B) {
+    if (prompt) token[b] = prompt[static_cast<size_t>(b) * P + col];
+    pos[b] += 1;
+  }
+}
+
+__global__ void set_tokens_kernel(int32_t* token, int B, const int32_t* prompt, int P, int col) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = threadIdx.x;
+  if (b < B) token[b] = prompt[static_cast<size_t>(b) * P + col];
+}
+
+__global__ void ctrl_reset_kernel(Ctrl* c, int32_t* done, int B, int eos, int32_t* out, int cap) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    c->step = 0;
+    c->eos_id = eos;
+    c->all_done = 0;
+    c->out_cap = cap;
+    c->out_tokens = out;
+  }
+  if (threadIdx.x < B) done[threadIdx.x] = 0;
+}
+
+__global__ void ctrl_detach_kernel(Ctrl* c) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    c->out_tokens = nullptr;
+    c->out_cap = 0;
+  }
+}
+
+__global__ void pad_kernel(int32_t* out, int B, int cap, int from, int value) {
+  const int n = cap - from;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * n; i += gridDim.x * blockDim.x) {
+    const int b = i / n, c = from + i % n;
+    out[static_cast<size_t>(b) * cap + c] = value;
+  }
+}
+
+// ------------------------------------------------------------------------------- GEMV planning
+
+constexpr uint32_t kStageTarget = 20 * 1024;   // bytes of weight rows per ring stage
+constexpr int kChunksPerTask = 128;            // 1024 elements per warp task
+constexpr uint32_t kHeaderBytes = 1536;
+constexpr uint32_t kPartMaxBytes = 24 * 1024;
+constexpr uint32_t kXSmemMax = 64 * 1024;
+constexpr uint32_t kSmemBudget = 110 * 1024;   // two CTAs of neighbouring kernels fit one SM
+
+struct GemvPlan {
+  int grid = 0;
+  uint32_t smem = 0;
+};
+
+int plan_gemv(int kind, GemvArgs& a, int BT, int sms, bool want_x_smem, GemvPlan* pl) {
+  const int RU = (kind == kKindQKV || kind == kKindGLU) ? 2 : 1;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
+  const int C = a.K / kChunkElems;
+  if (kind == kKindHead) {
+    a.parts = 1;
+    a.chunks_per_part = C;
+  } else {
+    a.chunks_per_part = kChunksPerTask;
+    a.parts = (C + kChunksPerTask - 1) / kChunksPerTask;
+  }
+  a.units_per_stage = std::max<int>(1, static_cast<int>(kStageTarget / (RU * row_bytes)));
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.units_per_stage * RU) * row_bytes;
+  const uint32_t x_bytes = static_cast<uint32_t>(BT) * static_cast<uint32_t>(a.K) * 4u;
+  a.x_smem = (want_x_smem && x_bytes <= kXSmemMax) ? 1 : 0;
+  int upc = (a.n_units + sms - 1) / sms;
+  if (kind != kKindHead) {
+    const int max_upc = std::max<int>(1, static_cast<int>(kPartMaxBytes / (RU * a.parts * BT * 4)));
+    upc = std::min(upc, max_upc);
+  }
+  const int grid = (a.n_units + upc - 1) / upc;
+  a.units_per_cta = (a.n_units + grid - 1) / grid;
+  const uint32_t part_bytes =
+      kind == kKindHead ? 0u : static_cast<uint32_t>(a.units_per_cta * RU * a.parts * BT) * 4u;
+  a.off_x = kHeaderBytes;
+  a.off_part = align_up(a.off_x + (a.x_smem ? x_bytes : 0u), 16);
+  a.off_ring = align_up(a.off_part + part_bytes, 128);
+  const uint32_t budget = std::max(kSmemBudget, a.off_ring + 2 * stage_bytes);
+  int ns = static_cast<int>((std::min(budget, kSmemMax) - std::min(a.off_ring, kSmemMax)) / stage_bytes);
+  ns = std::min(ns, kMaxStages);
+  DEC_CHECK(ns >= 2, DEC_EUNSUPPORTED, "row of %d elements too long for the shared-memory ring", a.K);
+  a.n_slots = ns;
+  pl->grid = grid;
+  pl->smem = a.off_ring + static_cast<uint32_t>(ns) * stage_bytes;
+  return DEC_OK;
+}
+
+int run_gemv(int kind, GemvArgs& a, int B, const DeviceInfo* dv, bool want_x_smem, cudaStream_t st, bool pdl) {
+  const int BT = bt_bucket(B);
+  a.B = B;
+  a.err = dv->err;
+  GemvPlan pl;
+  DEC_TRY(plan_gemv(kind, a, BT, dv->sms, want_x_smem, &pl));
+  DEC_CHECK(!(a.norm_gamma || a.tokens) || a.x_smem, DEC_EUNSUPPORTED,
+            "fused RMSNorm needs the activations in shared memory (B=%d, K=%d)", B, a.K);
+  cudaError_t e;
+  switch (kind) {
+    case kKindQKV: e = launch_gemv_qkv(BT, a, pl.grid, pl.smem, st, pdl); break;
+    case kKindGLU: e = launch_gemv_glu(BT, a, pl.grid, pl.smem, st, pdl); break;
+    case kKindResid: e = launch_gemv_resid(BT, a, pl.grid, pl.smem, st, pdl); break;
+    default: e = launch_gemv_head(BT, a, pl.grid, pl.smem, st, pdl); break;
+  }
+  DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "gemv launch: %s", cudaGetErrorString(e));
+  return DEC_OK;
+}
+
+// Whether the RMSNorm can be folded into the next GEMV for this batch / width.
+bool norm_fusable(int B, int H) { return static_cast<uint32_t>(bt_bucket(B)) * H * 4u <= kXSmemMax; }
+
+int run_norm(const float* x, float* resid, const uint16_t* gamma, float* y, int B, int H, float eps,
+             const int32_t* tokens, const uint16_t* embed, int vocab, const DeviceInfo* dv, cudaStream_t st,
+             bool pdl) {
+  NormArgs n{x, resid, gamma, y, H, eps, tokens, embed, vocab, dv->err};
+  cudaError_t e = launch(add_rmsnorm_kernel, dim3(B), dim3(kConsumerThreads), 0, st, pdl, n);
+  DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "rmsnorm launch: %s", cudaGetErrorString(e));
+  return DEC_OK;
+}
+
+void fill_inv_freq(GemvArgs& a, int D, float theta) {
+  for (int i = 0; i < D / 2; ++i) a.inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / D);
+}
+
+// ------------------------------------------------------------------------------- attention planning
+
+int attn_splits(int B, int Hkv, int S_max, int sms, int requested) {
+  const int cap = std::max(1, (S_max + kAttnChunkMin - 1) / kAttnChunkMin);
+  if (requested > 0) return std::min(requested, cap);
+  const int want = (8 * sms + B * Hkv - 1) / (B * Hkv);
+  return std::max(1, std::min(want, cap));
+}
+
+size_t attn_part_bytes(int B, int Hq, int Hkv, int D, int n_split) {
+  return static_cast<size_t>(B) * Hkv * n_split * (Hq / Hkv) * (D + 2) * sizeof(float);
+}
+
+uint32_t attn_smem(int D) {
+  return 512u + static_cast<uint32_t>(kAttnMaxGroup * D * 4 + kAttnMaxGroup * kAttnTile * 4) +
+         static_cast<uint32_t>(kAttnSlots * 2 * kAttnTile * D * 2);
+}
+
+int run_attn(AttnArgs& a, int B, const DeviceInfo* dv, cudaStream_t st, bool pdl) {
+  a.err = dv->err;
+  cudaError_t e = launch_attn(a, B, attn_smem(a.D), st, pdl);
+  DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "attention launch: %s", cudaGetErrorString(e));
+  return DEC_OK;
+}
+
+// ------------------------------------------------------------------------------- state layout
+
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  }
+};
+
+struct StateWs {
+  Ctrl* ctrl;
+  int32_t* done;
+  unsigned long long* keys;
+  unsigned int* head_ticket;
+  unsigned int* attn_tickets;
+  float* q;
+  float* o;
+  float* h;
+  float* y;
+  float* attn_part;
+  int n_split;
+  size_t bytes;
+};
+
+StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char* base) {
+  Carve c;
+  StateWs w{};
+  const size_t Hq_D = static_cast<size_t>(m->n_heads) * m->head_dim;
+  const size_t o_ctrl = c.take(sizeof(Ctrl));
+  const size_t o_done = c.take(sizeof(int32_t) * kMaxBatch);
+  const size_t o_keys = c.take(sizeof(unsigned long long) * kMaxBatch);
+  const size_t o_tick = c.take(sizeof(unsigned int));
+  const size_t o_atick = c.take(sizeof(unsigned int) * B * m->n_kv_heads);
+  const size_t o_q = c.take(sizeof(float) * B * Hq_D);
+  const size_t o_o = c.take(sizeof(float) * B * Hq_D);
+  const size_t o_h = c.take(sizeof(float) * B * m->intermediate);
+  const size_t o_y = c.take(sizeof(float) * B * m->hidden);
+  w.n_split = attn_splits(B, m->n_kv_heads, S_max, sms, 0);
+  const size_t o_part = c.take(attn_part_bytes(B, m->n_heads, m->n_kv_heads, m->head_dim, w.n_split));
+  w.bytes = c.off;
+  if (base) {
+    w.ctrl = reinterpret_cast<Ctrl*>(base + o_ctrl);
+    w.done = reinterpret_cast<int32_t*>(base + o_done);
+    w.keys = reinterpret_cast<unsigned long long*>(base + o_keys);
+    w.head_ticket = reinterpret_cast<unsigned int*>(base + o_tick);
+    w.attn_tickets = reinterpret_cast<unsigned int*>(base + o_atick);
+    w.q = reinterpret_cast<float*>(base + o_q);
+    w.o = reinterpret_cast<float*>(base + o_o);
+    w.h = reinterpret_cast<float*>(base + o_h);
+    w.y = reinterpret_cast<float*>(base + o_y);
+    w.attn_part = reinterpret_cast<float*>(base + o_part);
+  }
+  return w;
+}
+
+struct StateInternal {
+  int device = -1;
+  int* pinned_word = nullptr;
+  cudaStream_t own_stream = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_out = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  uint64_t fingerprint = 0;
+  int graph_steps = 0;
+};
+
+uint64_t mix(uint64_t h, uint64_t v) {
+  h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+  return h;
+}
+
+uint64_t fingerprint(const dec_model* m, const dec_state* s) {
+  uint64_t h = 1469598103934665603ull;
+  const int ints[] = {m->n_layers, m->hidden, m->n_heads, m->n_kv_heads, m->head_dim, m->intermediate, m->vocab,
+                      s->batch, s->max_seq};
+  for (int v : ints) h = mix(h, static_cast<uint64_t>(static_cast<uint32_t>(v)));
+  uint32_t fe, ft;
+  std::memcpy(&fe, &m->rms_eps, 4);
+  std::memcpy(&ft, &m->rope_theta, 4);
+  h = mix(mix(h, fe), ft);
+  const void* ptrs[] = {m->embed, m->final_norm, m->lm_head, s->pos, s->token, s->residual, s->workspace};
+  for (const void* p : ptrs) h = mix(h, reinterpret_cast<uintptr_t>(p));
+  for (int l = 0; l < m->n_layers; ++l) {
+    const dec_layer_weights& w = m->layers[l];
+    const void* lp[] = {w.attn_norm, w.wq, w.wk, w.wv, w.wo, w.mlp_norm, w.wg, w.wu, w.wd, s->k_cache[l],
+                        s->v_cache[l]};
+    for (const void* p : lp) h = mix(h, reinterpret_cast<uintptr_t>(p));
+  }
+  return h;
+}
+
+// ------------------------------------------------------------------------------- model / state checks
+
+int check_model(const dec_model* m) {
+  DEC_CHECK(m != nullptr, DEC_EINVAL, "model is NULL");
+  DEC_CHECK(m->n_layers >= 1 && m->layers != nullptr, DEC_EINVAL, "model needs n_layers >= 1 and a layer array");
+  DEC_TRY(check_row(m->hidden, "hidden"));
+  DEC_TRY(check_row(m->intermediate, "intermediate"));
+  DEC_TRY(check_heads(m->n_heads, m->n_kv_heads, m->head_dim));
+  DEC_TRY(check_row(m->n_heads * m->head_dim, "n_heads*head_dim"));
+  DEC_CHECK(m->rms_eps >= 0.f && std::isfinite(m->rms_eps), DEC_EINVAL, "rms_eps must be finite and >= 0");
+  DEC_CHECK(m->rope_theta > 0.f && std::isfinite(m->rope_theta), DEC_EINVAL, "rope_theta must be finite and > 0");
+  if (m->embed || m->lm_head) DEC_CHECK(m->vocab >= 1, DEC_EINVAL, "vocab must be >= 1");
+  if (m->embed) DEC_CHECK(aligned16(m->embed), DEC_EINVAL, "embed must be 16-byte aligned");
+  if (m->lm_head) {
+    DEC_CHECK(aligned16(m->lm_head), DEC_EINVAL, "lm_head must be 16-byte aligned");
+    DEC_CHECK(m->final_norm != nullptr && aligned16(m->final_norm), DEC_EINVAL, "an LM head needs final_norm");
+  }
+  for (int l = 0; l < m->n_layers; ++l) {
+    const dec_layer_weights& w = m->layers[l];
+    const void* p[] = {w.attn_norm, w.wq, w.wk, w.wv, w.wo, w.mlp_norm, w.wg, w.wu, w.wd};
+    for (const void* q : p)
+      DEC_CHECK(q != nullptr && aligned16(q), DEC_EINVAL, "layer %d: weights must be non-null and 16-byte aligned", l);
+  }
+  return DEC_OK;
+}
+
+int check_state(const dec_model* m, const dec_state* s, bool need_internal) {
+  DEC_CHECK(s != nullptr, DEC_EINVAL, "state is NULL");
+  DEC_TRY(check_batch(s->batch));
+  DEC_CHECK(s->max_seq >= 1, DEC_EINVAL, "max_seq must be >= 1");
+  DEC_CHECK(s->k_cache != nullptr && s->v_cache != nullptr, DEC_EINVAL, "cache pointer arrays are NULL");
+  for (int l = 0; l < m->n_layers; ++l)
+    DEC_CHECK(s->k_cache[l] && s->v_cache[l] && aligned16(s->k_cache[l]) && aligned16(s->v_cache[l]), DEC_EINVAL,
+              "layer %d: cache pointers must be non-null and 16-byte aligned", l);
+  DEC_CHECK(s->pos && s->token && s->residual && s->workspace, DEC_EINVAL, "state buffers must be non-null");
+  DEC_CHECK(aligned16(s->residual) && (reinterpret_cast<uintptr_t>(s->workspace) & 255u) == 0, DEC_EINVAL,
+            "residual must be 16-byte and workspace 256-byte aligned");
+  if (need_internal) DEC_CHECK(s->internal != nullptr, DEC_EINVAL, "state not initialised (dec_state_init)");
+  return DEC_OK;
+}
+
+// ------------------------------------------------------------------------------- the step
+
+// Layers of one step; with `head`, also the LM head and the bookkeeping.
+int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
+                 cudaStream_t st) {
+  const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
+  const bool fuse = norm_fusable(B, H);
+  const bool pdl = true;
+  for (int l = 0; l < m->n_layers; ++l) {
+    const dec_layer_weights& lw = m->layers[l];
+    const bool gather = (l == 0 && m->embed != nullptr);
+    // attention block
+    {
+      GemvArgs a{};
+      a.w0 = static_cast<const uint16_t*>(lw.wq);
+      a.w1 = static_cast<const uint16_t*>(lw.wk);
+      a.w2 = static_cast<const uint16_t*>(lw.wv);
+      a.K = H;
+      a.n_units = (Hq + 2 * Hkv) * (D / 2);
+      a.out = w.q;
+      a.k_cache = static_cast<uint16_t*>(s->k_cache[l]);
+      a.v_cache = static_cast<uint16_t*>(s->v_cache[l]);
+      a.pos = s->pos;
+      a.Hq = Hq;
+      a.Hkv = Hkv;
+      a.D = D;
+      a.S_max = s->max_seq;
+      fill_inv_freq(a, D, m->rope_theta);
+      if (fuse) {
+        a.x = s->residual;
+        a.norm_gamma = static_cast<const uint16_t*>(lw.attn_norm);
+        a.eps = m->rms_eps;
+        if (gather) {
+          a.tokens = s->token;
+          a.embed = static_cast<const uint16_t*>(m->embed);
+          a.vocab = m->vocab;
+          a.resid_store = s->residual;
+        }
+      } else {
+        DEC_TRY(run_norm(nullptr, s->residual, static_cast<const uint16_t*>(lw.attn_norm), w.y, B, H, m->rms_eps,
+                         gather ? s->token : nullptr, static_cast<const uint16_t*>(m->embed), m->vocab, dv, st, pdl));
+        a.x = w.y;
+      }
+      DEC_TRY(run_gemv(kKindQKV, a, B, dv, true, st, pdl));
+
+      AttnArgs t{};
+      t.q = w.q;
+      t.k_cache = static_cast<const uint16_t*>(s->k_cache[l]);
+      t.v_cache = static_cast<const uint16_t*>(s->v_cache[l]);
+      t.pos = s->pos;
+      t.o = w.o;
+      t.part = w.attn_part;
+      t.tickets = w.attn_tickets;
+      t.Hq = Hq;
+      t.Hkv = Hkv;
+      t.D = D;
+      t.S_max = s->max_seq;
+      t.n_split = w.n_split;
+      t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+      DEC_TRY(run_attn(t, B, dv, st, pdl));
+
+      GemvArgs r{};
+      r.w0 = static_cast<const uint16_t*>(lw.wo);
+      r.K = Hq * D;
+      r.n_units = H;
+      r.x = w.o;
+      r.out = s->residual;
+      DEC_TRY(run_gemv(kKindResid, r, B, dv, true, st, pdl));
+    }
+    // MLP block
+    {
+      GemvArgs a{};
+      a.w0 = static_cast<const uint16_t*>(lw.wg);
+      a.w1 = static_cast<const uint16_t*>(lw.wu);
+      a.K = H;
+      a.n_units = I;
+      a.out = w.h;
+      if (fuse) {
+        a.x = s->residual;
+        a.norm_gamma = static_cast<const uint16_t*>(lw.mlp_norm);
+        a.eps = m->rms_eps;
+      } else {
+        DEC_TRY(run_norm(nullptr, s->residual, static_cast<const uint16_t*>(lw.mlp_norm), w.y, B, H, m->rms_eps,
+                         nullptr, nullptr, 0, dv, st, pdl));
+        a.x = w.y;
+      }
+      DEC_TRY(run_gemv(kKindGLU, a, B, dv, true, st, pdl));
+
+      GemvArgs r{};
+      r.w0 = static_cast<const uint16_t*>(lw.wd);
+      r.K = I;
+      r.n_units = H;
+      r.x = w.h;
+      r.out = s->residual;
+      DEC_TRY(run_gemv(kKindResid, r, B, dv, true, st, pdl));
+    }
+  }
+  if (head && m->lm_head) {
+    GemvArgs a{};
+    a.w0 = static_cast<const uint16_t*>(m->lm_head);
+    a.K = H;
+    a.n_units = m->vocab;
+    if (fuse) {
+      a.x = s->residual;
+      a.norm_gamma = static_cast<const uint16_t*>(m->final_norm);
+      a.eps = m->rms_eps;
+    } else {
+      DEC_TRY(run_norm(nullptr, s->residual, static_cast<const uint16_t*>(m->final_norm), w.y, B, H, m->rms_eps,
+                       nullptr, nullptr, 0, dv, st, pdl));
+      a.x = w.y;
+    }
+    a.argmax_keys = w.keys;
+    a.ticket = w.head_ticket;
+    a.book.enabled = 1;
+    a.book.token = s->token;
+    a.book.pos = s->pos;
+    a.book.done = w.done;
+    a.book.ctrl = w.ctrl;
+    DEC_TRY(run_gemv(kKindHead, a, B, dv, true, st, pdl));
+  } else {
+    cudaError_t e = launch(advance_kernel, dim3(1), dim3(32), 0, st, pdl, s->token, s->pos, B,
+                           static_cast<const int32_t*>(nullptr), 0, 0);
+    DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "advance launch: %s", cudaGetErrorString(e));
+  }
+  return DEC_OK;
+}
+
+int state_views(const dec_model* m, dec_state* s, const DeviceInfo* dv, StateWs* w) {
+  *w = carve_state(m, s->batch, s->max_seq, dv->sms, static_cast<unsigned char*>(s->workspace));
+  DEC_CHECK(s->workspace_bytes >= w->bytes, DEC_EINVAL, "workspace has %zu bytes, needs %zu", s->workspace_bytes,
+            w->bytes);
+  return DEC_OK;
+}
+
+}  // namespace
+
+// =============================================================================== C ABI
+
+extern "C" {
+
+const char* dec_last_error(void) { return g_last_error.c_str(); }
+
+const char* dec_version(void) { return "libdec 0.1 (sm_103a)"; }
+
+int dec_device_error(uint32_t* bits, int clear) {
+  DEC_CHECK(bits != nullptr, DEC_EINVAL, "bits is NULL");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  DEC_CUDA(cudaDeviceSynchronize());
+  DEC_CUDA(cudaMemcpy(bits, dv->err, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  if (clear) DEC_CUDA(cudaMemset(dv->err, 0, sizeof(uint32_t)));
+  return DEC_OK;
+}
+
+int dec_add_rmsnorm(const float* x, float* residual, const void* gamma, float* out, int B, int H, float eps,
+                    void* stream) {
+  DEC_TRY(check_batch(B));
+  DEC_TRY(check_row(H, "H"));
+  if (x) DEC_PTR(x);
+  DEC_PTR(residual);
+  DEC_PTR(gamma);
+  DEC_PTR(out);
+  DEC_CHECK(eps >= 0.f && std::isfinite(eps), DEC_EINVAL, "eps must be finite and >= 0");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  return run_norm(x, residual, static_cast<const uint16_t*>(gamma), out, B, H, eps, nullptr, nullptr, 0, dv,
+                  static_cast<cudaStream_t>(stream), false);
+}
+
+int dec_qkv_gemv_rope(const float* y, const void* Wq, const void* Wk, const void* Wv, const int32_t* pos,
+                      float rope_theta, float* q_out, void* k_cache, void* v_cache, int B, int H, int Hq, int Hkv,
+                      int D, int S_max, void* stream) {
+  DEC_TRY(check_batch(B));
+  DEC_TRY(check_row(H, "H"));
+  DEC_TRY(check_heads(Hq, Hkv, D));
+  DEC_PTR(y);
+  DEC_PTR(Wq);
+  DEC_PTR(Wk);
+  DEC_PTR(Wv);
+  DEC_CHECK(pos != nullptr, DEC_EINVAL, "pos is NULL");
+  DEC_PTR(q_out);
+  DEC_PTR(k_cache);
+  DEC_PTR(v_cache);
+  DEC_CHECK(S_max >= 1, DEC_EINVAL, "S_max must be >= 1");
+  DEC_CHECK(rope_theta > 0.f && std::isfinite(rope_theta), DEC_EINVAL, "rope_theta must be finite and > 0");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  GemvArgs a{};
+  a.w0 = static_cast<const uint16_t*>(Wq);
+  a.w1 = static_cast<const uint16_t*>(Wk);
+  a.w2 = static_cast<const uint16_t*>(Wv);
+  a.K = H;
+  a.n_units = (Hq + 2 * Hkv) * (D / 2);
+  a.x = y;
+  a.out = q_out;
+  a.k_cache = static_cast<uint16_t*>(k_cache);
+  a.v_cache = static_cast<uint16_t*>(v_cache);
+  a.pos = pos;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.S_max = S_max;
+  fill_inv_freq(a, D, rope_theta);
+  return run_gemv(kKindQKV, a, B, dv, true, static_cast<cudaStream_t>(stream), false);
+}
+
+size_t dec_attn_workspace_size(int B, int Hq, int Hkv, int D, int S_max, int num_splits) {
+  if (B < 1 || Hkv < 1 || Hq < Hkv || S_max < 1 || D < 1) return 0;
+  int sms = 152;
+  DeviceInfo* dv;
+  if (num_splits <= 0 && device_info(&dv) == DEC_OK) sms = dv->sms;
+  const int n = attn_splits(B, Hkv, S_max, sms, num_splits);
+  return 256 + (attn_part_bytes(B, Hq, Hkv, D, n) + 255) / 256 * 256 +
+         (sizeof(unsigned int) * B * Hkv + 255) / 256 * 256;
+}
+
+int dec_gqa_decode_attn(const float* q, const void* k_cache, const void* v_cache, const int32_t* pos, float* o,
+                        void* ws, size_t ws_bytes, int B, int Hq, int Hkv, int D, int S_max, int num_splits,
+                        void* stream) {
+  DEC_TRY(check_batch(B));
+  DEC_TRY(check_heads(Hq, Hkv, D));
+  DEC_PTR(q);
+  DEC_PTR(k_cache);
+  DEC_PTR(v_cache);
+  DEC_CHECK(pos != nullptr, DEC_EINVAL, "pos is NULL");
+  DEC_PTR(o);
+  DEC_CHECK(ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0, DEC_EINVAL,
+            "workspace must be non-null and 256-byte aligned");
+  DEC_CHECK(S_max >= 1, DEC_EINVAL, "S_max must be >= 1");
+  DEC_CHECK(num_splits >= 0, DEC_EINVAL, "num_splits must be >= 0");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  const int n = attn_splits(B, Hkv, S_max, dv->sms, num_splits);
+  const size_t part = (attn_part_bytes(B, Hq, Hkv, D, n) + 255) / 256 * 256;
+  const size_t need = 256 + part + (sizeof(unsigned int) * B * Hkv + 255) / 256 * 256;
+  DEC_CHECK(ws_bytes >= need, DEC_EINVAL, "attention workspace has %zu bytes, needs %zu", ws_bytes, need);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(base + 256 + part);
+  DEC_CUDA(cudaMemsetAsync(tickets, 0, sizeof(unsigned int) * B * Hkv, st));
+  AttnArgs t{};
+  t.q = q;
+  t.k_cache = static_cast<const uint16_t*>(k_cache);
+  t.v_cache = static_cast<const uint16_t*>(v_cache);
+  t.pos = pos;
+  t.o = o;
+  t.part = reinterpret_cast<float*>(base + 256);
+  t.tickets = tickets;
+  t.Hq = Hq;
+  t.Hkv = Hkv;
+  t.D = D;
+  t.S_max = S_max;
+  t.n_split = n;
+  t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  return run_attn(t, B, dv, st, false);
+}
+
+int dec_glu_gemv(const float* y, const void* Wg, const void* Wu, float* h, int B, int H, int I, void* stream) {
+  DEC_TRY(check_batch(B));
+  DEC_TRY(check_row(H, "H"));
+  DEC_CHECK(I >= 1, DEC_EINVAL, "I must be >= 1");
+  DEC_PTR(y);
+  DEC_PTR(Wg);
+  DEC_PTR(Wu);
+  DEC_PTR(h);
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  GemvArgs a{};
+  a.w0 = static_cast<const uint16_t*>(Wg);
+  a.w1 = static_cast<const uint16_t*>(Wu);
+  a.K = H;
+  a.n_units = I;
+  a.x = y;
+  a.out = h;
+  return run_gemv(kKindGLU, a, B, dv, true, static_cast<cudaStream_t>(stream), false);
+}
+
+int dec_down_gemv(const float* x, const void* W, float* residual, int B, int N_in, int N_out, void* stream) {
+  DEC_TRY(check_batch(B));
+  DEC_TRY(check_row(N_in, "N_in"));
+  DEC_CHECK(N_out >= 1, DEC_EINVAL, "N_out must be >= 1");
+  DEC_PTR(x);
+  DEC_PTR(W);
+  DEC_PTR(residual);
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  GemvArgs a{};
+  a.w0 = static_cast<const uint16_t*>(W);
+  a.K = N_in;
+  a.n_units = N_out;
+  a.x = x;
+  a.out = residual;
+  return run_gemv(kKindResid, a, B, dv, true, static_cast<cudaStream_t>(stream), false);
+}
+
+size_t dec_lmhead_workspace_size(int B) {
+  (void)B;
+  return 512;
+}
+
+int dec_lmhead_argmax(const float* residual, const void* final_norm, float eps, const void* W_lm, int32_t* token_out,
+                      float* logits_out, void* ws, size_t ws_bytes, int B, int H, int V, void* stream) {
+  DEC_TRY(check_batch(B));
+  DEC_TRY(check_row(H, "H"));
+  DEC_CHECK(V >= 1, DEC_EINVAL, "V must be >= 1");
+  DEC_PTR(residual);
+  DEC_PTR(final_norm);
+  DEC_PTR(W_lm);
+  DEC_CHECK(token_out != nullptr, DEC_EINVAL, "token_out is NULL");
+  if (logits_out) DEC_PTR(logits_out);
+  DEC_CHECK(ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && ws_bytes >= dec_lmhead_workspace_size(B),
+            DEC_EINVAL, "workspace must be 256-byte aligned with dec_lmhead_workspace_size() bytes");
+  DEC_CHECK(eps >= 0.f && std::isfinite(eps), DEC_EINVAL, "eps must be finite and >= 0");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  DEC_CUDA(cudaMemsetAsync(base, 0, 512, st));
+  const bool fuse = norm_fusable(B, H);
+  DEC_CHECK(fuse, DEC_EUNSUPPORTED, "B=%d with H=%d exceeds the fused-norm shared-memory budget", B, H);
+  GemvArgs a{};
+  a.w0 = static_cast<const uint16_t*>(W_lm);
+  a.K = H;
+  a.n_units = V;
+  a.x = residual;
+  a.norm_gamma = static_cast<const uint16_t*>(final_norm);
+  a.eps = eps;
+  a.logits = logits_out;
+  a.argmax_keys = reinterpret_cast<unsigned long long*>(base);
+  a.ticket = reinterpret_cast<unsigned int*>(base + 256);
+  a.token_out = token_out;
+  return run_gemv(kKindHead, a, B, dv, true, st, false);
+}
+
+size_t dec_state_workspace_size(const dec_model* m, int B, int S_max) {
+  if (!m || B < 1 || B > kMaxBatch || S_max < 1 || m->n_kv_heads < 1 || m->n_heads < m->n_kv_heads) return 0;
+  int sms = 152;
+  DeviceInfo* dv;
+  if (device_info(&dv) == DEC_OK) sms = dv->sms;
+  return carve_state(m, B, S_max, sms, nullptr).bytes;
+}
+
+int dec_state_init(const dec_model* m, dec_state* s, void* stream) {
+  DEC_TRY(check_model(m));
+  DEC_TRY(check_state(m, s, false));
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  StateWs w;
+  DEC_TRY(state_views(m, s, dv, &w));
+  if (s->internal) DEC_TRY(dec_state_release(s));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DEC_CUDA(cudaMemsetAsync(s->workspace, 0, w.bytes, st));
+  // no end-of-sequence token and no output buffer until dec_decode sets them
+  DEC_CUDA(launch(ctrl_reset_kernel, dim3(1), dim3(32), 0, st, false, w.ctrl, w.done, s->batch, -1,
+                  static_cast<int32_t*>(nullptr), 0));
+  auto* in = new StateInternal();
+  DEC_CUDA(cudaGetDevice(&in->device));
+  cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&in->pinned_word), sizeof(int));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&in->own_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&in->ev_in, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&in->ev_out, cudaEventDisableTiming);
+  s->internal = in;
+  if (e != cudaSuccess) {
+    dec_state_release(s);
+    return fail(DEC_ECUDA, "state set-up: %s", cudaGetErrorString(e));
+  }
+  return DEC_OK;
+}
+
+int dec_state_release(dec_state* s) {
+  DEC_CHECK(s != nullptr, DEC_EINVAL, "state is NULL");
+  auto* in = static_cast<StateInternal*>(s->internal);
+  if (!in) return DEC_OK;
+  if (in->exec) cudaGraphExecDestroy(in->exec);
+  if (in->ev_in) cudaEventDestroy(in->ev_in);
+  if (in->ev_out) cudaEventDestroy(in->ev_out);
+  if (in->own_stream) cudaStreamDestroy(in->own_stream);
+  if (in->pinned_word) cudaFreeHost(in->pinned_word);
+  delete in;
+  s->internal = nullptr;
+  return DEC_OK;
+}
+
+int dec_step(const dec_model* m, dec_state* s, void* stream) {
+  DEC_TRY(check_model(m));
+  DEC_TRY(check_state(m, s, false));
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  StateWs w;
+  DEC_TRY(state_views(m, s, dv, &w));
+  return enqueue_step(m, s, dv, w, true, static_cast<cudaStream_t>(stream));
+}
+
+int dec_prefill(const dec_model* m, dec_state* s, const int32_t* prompt, int P, void* stream) {
+  DEC_TRY(check_model(m));
+  DEC_TRY(check_state(m, s, false));
+  DEC_CHECK(m->embed != nullptr, DEC_EINVAL, "a prompt pass needs the embedding matrix");
+  DEC_CHECK(prompt != nullptr && P >= 1, DEC_EINVAL, "prompt must be non-null with P >= 1");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  StateWs w;
+  DEC_TRY(state_views(m, s, dv, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int B = s->batch;
+  DEC_CUDA(launch(set_tokens_kernel, dim3(1), dim3(32), 0, st, false, s->token, B, prompt, P, 0));
+  for (int i = 0; i + 1 < P; ++i) {
+    DEC_TRY(enqueue_step(m, s, dv, w, false, st));
+    // enqueue_step without a head ends in advance(pos); the prompt column
+    // for the next position is set here
+    DEC_CUDA(launch(set_tokens_kernel, dim3(1), dim3(32), 0, st, true, s->token, B, prompt, P, i + 1));
+  }
+  return DEC_OK;
+}
+
+int dec_decode(const dec_model* m, dec_state* s, int n_steps, int eos_id, int32_t* out_tokens, int* steps_done,
+               void* stream) {
+  DEC_TRY(check_model(m));
+  DEC_TRY(check_state(m, s, true));
+  DEC_CHECK(m->lm_head != nullptr, DEC_EINVAL, "decoding needs an LM head");
+  DEC_CHECK(n_steps >= 0, DEC_EINVAL, "n_steps must be >= 0");
+  DEC_CHECK(eos_id >= -1 && eos_id < m->vocab, DEC_EINVAL, "eos_id %d outside [-1, V)", eos_id);
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  StateWs w;
+  DEC_TRY(state_views(m, s, dv, &w));
+  auto* in = static_cast<StateInternal*>(s->internal);
+  if (steps_done) *steps_done = 0;
+  if (n_steps == 0) return DEC_OK;
+
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  cudaStream_t st = user ? user : in->own_stream;
+  if (!user) {
+    DEC_CUDA(cudaEventRecord(in->ev_in, user));
+    DEC_CUDA(cudaStreamWaitEvent(st, in->ev_in, 0));
+  }
+  const int B = s->batch;
+  DEC_CUDA(launch(ctrl_reset_kernel, dim3(1), dim3(32), 0, st, false, w.ctrl, w.done, B, eos_id, out_tokens, n_steps));
+
+  constexpr int kGraphSteps = 16;  // also the EOS check interval
+  const uint64_t fp = fingerprint(m, s);
+  if (n_steps >= kGraphSteps && (in->exec == nullptr || in->fingerprint != fp)) {
+    if (in->exec) {
+      cudaGraphExecDestroy(in->exec);
+      in->exec = nullptr;
+    }
+    cudaGraph_t g = nullptr;
+    DEC_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+    int rc = DEC_OK;
+    for (int i = 0; i < kGraphSteps && rc == DEC_OK; ++i) rc = enqueue_step(m, s, dv, w, true, st);
+    cudaError_t e = cudaStreamEndCapture(st, &g);
+    if (rc != DEC_OK) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "graph capture: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&in->exec, g, 0);
+    cudaGraphDestroy(g);
+    DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    in->fingerprint = fp;
+    in->graph_steps = kGraphSteps;
+  }
+
+  int done = 0;
+  bool all_done = false;
+  while (!all_done && done + kGraphSteps <= n_steps) {
+    DEC_CUDA(cudaGraphLaunch(in->exec, st));
+    done += kGraphSteps;
+    DEC_CUDA(cudaMemcpyAsync(in->pinned_word, &w.ctrl->all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
+    DEC_CUDA(cudaStreamSynchronize(st));
+    all_done = (*in->pinned_word != 0);
+  }
+  if (!all_done && done < n_steps) {
+    for (; done < n_steps; ++done) DEC_TRY(enqueue_step(m, s, dv, w, true, st));
+    DEC_CUDA(cudaMemcpyAsync(in->pinned_word, &w.ctrl->all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
+    DEC_CUDA(cudaStreamSynchronize(st));
+    all_done = (*in->pinned_word != 0);
+  }
+  if (out_tokens && done < n_steps)
+    DEC_CUDA(launch(pad_kernel, dim3(std::min(1024, (B * (n_steps - done) + 255) / 256)), dim3(256), 0, st, false,
+                    out_tokens, B, n_steps, done, eos_id));
+  // later dec_step calls must not write into this call's output buffer
+  DEC_CUDA(launch(ctrl_detach_kernel, dim3(1), dim3(32), 0, st, false, w.ctrl));
+  if (!user) {
+    DEC_CUDA(cudaEventRecord(in->ev_out, st));
+    DEC_CUDA(cudaStreamWaitEvent(user, in->ev_out, 0));
+  }
+  DEC_CUDA(cudaStreamSynchronize(st));
+  if (steps_done) *steps_done = done;
+  return DEC_OK;
+}
+
+int dec_generate(const dec_model* m, dec_state* s, const int32_t* prompt, int P, int n_steps, int eos_id,
+                 int32_t* out_tokens, int* steps_done, void* stream) {
+  DEC_TRY(dec_prefill(m, s, prompt, P, stream));
+  return dec_decode(m, s, n_steps, eos_id, out_tokens, steps_done, stream);
+}
+
+}  // extern "C"

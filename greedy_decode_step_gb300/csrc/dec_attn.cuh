@@ -1,0 +1,295 @@
+// GQA decode attention over a static bf16 KV cache, split along the keys.
+//
+// Grid (n_split, Hkv, B).  CTA (s, g, b) takes a contiguous key range of
+// sequence b and streams the K and V rows of KV head g through a shared-memory
+// ring (1-D bulk copies, one producer warp).  All Hq/Hkv query heads of the
+// group read the same K/V tile, so each KV byte leaves HBM once per step.
+// Within the range the softmax is the online form (running max, rescaled
+// sum); ranges are merged by log-sum-exp weights by the last CTA of the
+// group to finish (an atomic ticket; no CTA ever waits for another).
+//
+// Keys: the token at position p attends to cache slots 0..p, its own
+// (already stored) slot included.
+#pragma once
+
+#include "dec_common.cuh"
+
+namespace dec {
+
+constexpr int kAttnTile = 64;       // keys per stage
+constexpr int kAttnChunkMin = 32;   // fewest keys a split is given
+constexpr int kAttnMaxGroup = 16;   // query heads per KV head
+constexpr int kAttnSlots = 2;
+constexpr int kAttnWarps = 8;        // consumer warps
+constexpr int kAttnConsumers = 256;
+
+struct AttnArgs {
+  const float* q;             // [B][Hq][D]
+  const uint16_t* k_cache;    // [B][Hkv][S_max][D]
+  const uint16_t* v_cache;
+  const int32_t* pos;         // [B]
+  float* o;                   // [B][Hq][D]
+  float* part;                // [B][Hkv][n_split][G*(D+2)]: acc[G][D], m[G], l[G]
+  unsigned int* tickets;      // [B][Hkv], zero between launches
+  int Hq, Hkv, D, S_max, n_split;
+  float scale;                // 1/sqrt(D)
+  uint32_t* err;
+};
+
+// Key range of split s for a sequence of `len` keys (same plan in every CTA).
+__device__ __forceinline__ void attn_plan(int len, int n_split, int* chunk, int* n_active) {
+  int c = (len + n_split - 1) / n_split;
+  if (c < kAttnChunkMin) c = kAttnChunkMin;
+  *chunk = c;
+  *n_active = (len + c - 1) / c;
+}
+
+template <int D>
+__global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ AttnArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kAttnSlots;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 64);
+  int* is_last = reinterpret_cast<int*>(smem + 68);
+  float* m_run = reinterpret_cast<float*>(smem + 128);                 // [G]
+  float* l_run = m_run + kAttnMaxGroup;                                 // [G]
+  float* corr = l_run + kAttnMaxGroup;                                  // [G]
+  float* q_s = reinterpret_cast<float*>(smem + 512);                    // [G][D]
+  float* s_s = q_s + kAttnMaxGroup * D;                                 // [G][kAttnTile]
+  unsigned char* ring = reinterpret_cast<unsigned char*>(s_s + kAttnMaxGroup * kAttnTile);
+  constexpr uint32_t kRowBytes = D * 2;
+  constexpr uint32_t kTileBytes = kAttnTile * kRowBytes;   // one of K or V
+  constexpr int kChunks = D / 8;
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int G = a.Hq / a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int p = a.pos[b];
+  if (p < 0 || p >= a.S_max) {
+    if (split == 0 && g == 0 && threadIdx.x == 0) atomicOr(a.err, kErrPosRange);
+    return;
+  }
+  const int len = p + 1;
+  int chunk, n_active;
+  attn_plan(len, a.n_split, &chunk, &n_active);
+  if (split >= n_active) return;
+  const int k0 = split * chunk;
+  const int k1 = min(len, k0 + chunk);
+  const int n_tiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
+
+  const size_t head_off = (static_cast<size_t>(b) * a.Hkv + g) * a.S_max;
+  const uint16_t* Kg = a.k_cache + head_off * D;
+  const uint16_t* Vg = a.v_cache + head_off * D;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kAttnSlots; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kAttnWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+    q_s[i] = a.q[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i];
+  if (threadIdx.x < G) {
+    m_run[threadIdx.x] = -INFINITY;
+    l_run[threadIdx.x] = 0.f;
+  }
+  __syncthreads();
+
+  if (warp == 8) {
+    // ----------------------------------------------------------- producer warp
+    int issued = 0;
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_last();
+      for (int t = 0; t < n_tiles; ++t) {
+        const int slot = t % kAttnSlots;
+        if (t >= kAttnSlots) {
+          if (!mbar_wait(&empty[slot], ((t / kAttnSlots) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
+        }
+        const int j0 = k0 + t * kAttnTile;
+        const int nk = min(kAttnTile, k1 - j0);
+        unsigned char* dst = ring + static_cast<size_t>(slot) * 2 * kTileBytes;
+        mbar_arrive_expect_tx(&full[slot], 2u * nk * kRowBytes);
+        bulk_copy_g2s(dst, Kg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[slot], policy);
+        bulk_copy_g2s(dst + kTileBytes, Vg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[slot], policy);
+        issued = t + 1;
+      }
+    }
+    __syncwarp();
+    asm volatile("bar.sync 2, 288;" ::: "memory");
+    if (lane == 0) {
+      for (int t = max(0, issued - kAttnSlots); t < issued; ++t) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[t % kAttnSlots], (t / kAttnSlots) & 1)) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(a.err, kErrDrain);
+            break;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- consumer warps
+  const int tid = threadIdx.x;  // 0..255
+  constexpr int kPairsPerHead = D / 2;
+  // (head, dim-pair) slots of this thread for P.V: t, t+256, ...
+  constexpr int kMaxSlots = (kAttnMaxGroup * kPairsPerHead + 255) / 256;
+  float acc0[kMaxSlots], acc1[kMaxSlots];
+#pragma unroll
+  for (int i = 0; i < kMaxSlots; ++i) acc0[i] = acc1[i] = 0.f;
+  const int n_pairs = G * kPairsPerHead;
+
+  bool ok = true;
+  for (int t = 0; t < n_tiles; ++t) {
+    const int slot = t % kAttnSlots;
+    const int nk = min(kAttnTile, k1 - (k0 + t * kAttnTile));
+    int w_ok = 1;
+    if (lane == 0) w_ok = mbar_wait(&full[slot], (t / kAttnSlots) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
+    w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+    if (w_ok) (void)mbar_try_wait(&full[slot], (t / kAttnSlots) & 1);  // completed phase: acquire for every lane
+    // every consumer warp passes this barrier and gets the same verdict, so
+    // all warps leave together (none is left behind at a later barrier)
+    if (consumers_barrier_or(!w_ok)) {
+      ok = false;
+      break;
+    }
+    const uint4* Ks = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * 2 * kTileBytes);
+    const uint32_t* Vs = reinterpret_cast<const uint32_t*>(ring + static_cast<size_t>(slot) * 2 * kTileBytes +
+                                                           kTileBytes);
+    // scores: one (key, head) per thread per pass; chunk order rotated by key
+    // so that the eight lanes of a quarter-warp hit distinct banks
+    for (int idx = tid; idx < G * kAttnTile; idx += kAttnConsumers) {
+      const int h = idx / kAttnTile, j = idx - h * kAttnTile;
+      float sc = -INFINITY;
+      if (j < nk) {
+        const uint4* kr = Ks + j * kChunks;
+        const float* qh = q_s + h * D;
+        float accs = 0.f;
+#pragma unroll 4
+        for (int cc = 0; cc < kChunks; ++cc) {
+          const int c = (cc + j) & (kChunks - 1);
+          const uint4 w = kr[c];
+          const float4 q0 = reinterpret_cast<const float4*>(qh)[2 * c];
+          const float4 q1 = reinterpret_cast<const float4*>(qh)[2 * c + 1];
+          accs = fmaf(bf16lo(w.x), q0.x, accs);
+          accs = fmaf(bf16hi(w.x), q0.y, accs);
+          accs = fmaf(bf16lo(w.y), q0.z, accs);
+          accs = fmaf(bf16hi(w.y), q0.w, accs);
+          accs = fmaf(bf16lo(w.z), q1.x, accs);
+          accs = fmaf(bf16hi(w.z), q1.y, accs);
+          accs = fmaf(bf16lo(w.w), q1.z, accs);
+          accs = fmaf(bf16hi(w.w), q1.w, accs);
+        }
+        sc = accs * a.scale;
+      }
+      s_s[h * kAttnTile + j] = sc;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    // running max / sum per head (warp h)
+    for (int h = warp; h < G; h += kAttnWarps) {
+      float* sh = s_s + h * kAttnTile;
+      const float v0 = sh[lane], v1 = sh[lane + 32];
+      const float tmax = warp_max(fmaxf(v0, v1));
+      const float m_old = m_run[h];
+      const float m_new = fmaxf(m_old, tmax);
+      const float e0 = (lane < nk) ? expf(v0 - m_new) : 0.f;
+      const float e1 = (lane + 32 < nk) ? expf(v1 - m_new) : 0.f;
+      sh[lane] = e0;
+      sh[lane + 32] = e1;
+      const float tsum = warp_sum(e0 + e1);
+      if (lane == 0) {
+        const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+        corr[h] = c;
+        l_run[h] = l_run[h] * c + tsum;
+        m_run[h] = m_new;
+      }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    // P.V: thread slot (head h, dims 2dp, 2dp+1)
+#pragma unroll
+    for (int i = 0; i < kMaxSlots; ++i) {
+      const int pr = tid + i * kAttnConsumers;
+      if (pr < n_pairs) {
+        const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+        const float c = corr[h];
+        float x0 = acc0[i] * c, x1 = acc1[i] * c;
+        const float* ph = s_s + h * kAttnTile;
+        for (int j = 0; j < nk; ++j) {
+          const uint32_t v = Vs[j * kPairsPerHead + dp];
+          const float pj = ph[j];
+          x0 = fmaf(pj, bf16lo(v), x0);
+          x1 = fmaf(pj, bf16hi(v), x1);
+        }
+        acc0[i] = x0;
+        acc1[i] = x1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+  asm volatile("bar.sync 2, 288;" ::: "memory");
+  if (!ok) return;
+
+  if (n_active == 1) {
+#pragma unroll
+    for (int i = 0; i < kMaxSlots; ++i) {
+      const int pr = tid + i * kAttnConsumers;
+      if (pr < n_pairs) {
+        const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+        const float inv = 1.0f / l_run[h];
+        float* dst = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + 2 * dp;
+        dst[0] = acc0[i] * inv;
+        dst[1] = acc1[i] * inv;
+      }
+    }
+    return;
+  }
+
+  // partial of this split, then the last split of the group merges
+  const size_t stride = static_cast<size_t>(G) * (D + 2);
+  float* mine = a.part + ((static_cast<size_t>(b) * a.Hkv + g) * a.n_split + split) * stride;
+#pragma unroll
+  for (int i = 0; i < kMaxSlots; ++i) {
+    const int pr = tid + i * kAttnConsumers;
+    if (pr < n_pairs) {
+      const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+      mine[h * D + 2 * dp] = acc0[i];
+      mine[h * D + 2 * dp + 1] = acc1[i];
+    }
+  }
+  if (tid < G) {
+    mine[G * D + tid] = m_run[tid];
+    mine[G * D + G + tid] = l_run[tid];
+  }
+  __threadfence();
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  unsigned int* ticket = a.tickets + static_cast<size_t>(b) * a.Hkv + g;
+  if (tid == 0) *is_last = (atomicAdd(ticket, 1u) == static_cast<unsigned>(n_active - 1)) ? 1 : 0;
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (!*is_last) return;
+  __threadfence();
+  const float* base = a.part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
+  for (int idx = tid; idx < G * D; idx += kAttnConsumers) {
+    const int h = idx / D, d = idx - h * D;
+    float M = -INFINITY;
+    for (int s = 0; s < n_active; ++s) M = fmaxf(M, __ldcg(base + s * stride + G * D + h));
+    float L = 0.f, num = 0.f;
+    for (int s = 0; s < n_active; ++s) {
+      const float* ps = base + s * stride;
+      const float w = expf(__ldcg(ps + G * D + h) - M);
+      L = fmaf(w, __ldcg(ps + G * D + G + h), L);
+      num = fmaf(w, __ldcg(ps + h * D + d), num);
+    }
+    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] = num / L;
+  }
+  if (tid == 0) atomicExch(ticket, 0u);
+}
+
+}  // namespace dec

@@ -1,0 +1,523 @@
+// Kernels of the decode step.
+//
+// Every weight-streaming op of the step is one instantiation of gemv_kernel:
+// a warp-specialised CTA (one producer warp issuing 1-D bulk copies of whole
+// weight rows into a ring of shared-memory stages, eight consumer warps doing
+// the dot products) with a kind-specific epilogue:
+//
+//   kKindQKV    q,k,v = Wq y, Wk y, Wv y; rotate-half RoPE of q and k at the
+//               token's position; k, v stored (bf16) into the static cache
+//   kKindGLU    h = silu(Wg y) * (Wu y)
+//   kKindResid  r <- r + W x          (o_proj and down projection)
+//   kKindHead   logits = W_lm f, greedy argmax (lowest index on ties), and in
+//               step mode the token / position / EOS bookkeeping
+//
+// The RMSNorm that precedes QKV, GLU and the LM head is computed inside the
+// consumer prologue from the residual stream (each CTA recomputes it; the
+// vector is a few KB), so a layer needs no separate norm launch.
+//
+// Numerics: bf16 weights and cache entries, fp32 activations and fp32
+// accumulation.  Each output element is produced by a fixed warp/lane order
+// that does not depend on the grid, so results are bitwise reproducible and
+// equal between the fused step and the standalone calls.
+#pragma once
+
+#include "dec_common.cuh"
+
+namespace dec {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kGemvThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kMaxStages = 16;
+constexpr int kChunkElems = 8;                       // one 16-byte load of bf16
+constexpr int kMaxBatch = 16;
+
+enum GemvKind : int { kKindQKV = 0, kKindGLU = 1, kKindResid = 2, kKindHead = 3 };
+
+// Device control block of a decode state (lives in the state workspace).
+struct Ctrl {
+  int32_t step;        // decode steps completed since the last dec_decode set-up
+  int32_t eos_id;      // -1: no end-of-sequence token
+  int32_t all_done;    // every row has emitted eos_id
+  int32_t out_cap;     // columns of out_tokens
+  int32_t* out_tokens; // [B][out_cap] or null
+};
+
+struct StepBook {
+  int enabled;         // 1: the LM-head kernel advances the decode state
+  int32_t* token;      // [B] next input token
+  int32_t* pos;        // [B] next position
+  int32_t* done;       // [B] row has emitted eos
+  Ctrl* ctrl;
+};
+
+struct GemvArgs {
+  // weights: up to three row-major bf16 tensors with rows of K elements
+  const uint16_t* w0;
+  const uint16_t* w1;
+  const uint16_t* w2;
+  int K;
+  int n_units;          // work units (QKV: rotation pairs; GLU: gate/up row pairs; else rows)
+  int units_per_stage;  // US
+  int parts;            // P: a row's dot product is cut into P warp tasks
+  int chunks_per_part;  // CP (16-byte chunks)
+  int n_slots;          // ring stages
+  int units_per_cta;    // upper bound used to size the partial-sum buffer
+  int B;                // live batch rows
+  int x_smem;           // 1: activations staged in shared memory
+  uint32_t off_x, off_part, off_ring;  // dynamic shared-memory layout (bytes)
+  // input activation [B][K] fp32; with norm_gamma set it is the residual stream
+  const float* x;
+  const uint16_t* norm_gamma;
+  float eps;
+  const int32_t* tokens;  // non-null: x row b is the embedding row of tokens[b]
+  const uint16_t* embed;
+  int vocab;
+  float* resid_store;     // with tokens: CTA 0 writes the gathered rows here
+  // outputs
+  float* out;             // QKV: q [B][Hq*D]; GLU: h [B][I]; Resid: r [B][N] (+=)
+  uint16_t* k_cache;      // QKV: [B][Hkv][S_max][D]
+  uint16_t* v_cache;
+  const int32_t* pos;     // QKV: [B]
+  int Hq, Hkv, D, S_max;
+  float* logits;          // Head: optional [B][V]
+  unsigned long long* argmax_keys;  // Head: [B], zero between launches
+  unsigned int* ticket;             // Head: zero between launches
+  int32_t* token_out;               // Head: optional [B]
+  StepBook book;
+  uint32_t* err;
+  double inv_freq[64];    // QKV: theta^(-2i/D), i < D/2
+};
+
+// ----------------------------------------------------------------------------- RMSNorm helper
+// Normalisation factor 1/sqrt(mean(v^2) + eps) of v[0..H) computed by the 256
+// consumer threads (named barrier 1) in a fixed order.  `red` holds 8 floats.
+__device__ __forceinline__ float block_rms_inv(const float* v, int H, float eps, float* red) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  float ss = 0.f;
+  for (int i = t; i < H; i += kConsumerThreads) ss = fmaf(v[i], v[i], ss);
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) tot += red[w];
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  return 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+// RoPE angle of pair i at position p, reduced to [-pi, pi] in double precision
+// before the fp32 sine/cosine.
+__device__ __forceinline__ void rope_cos_sin(int p, double inv_freq, float* c, float* s) {
+  const double kTwoPiHi = 6.283185307179586232;       // nearest double to 2*pi
+  const double kTwoPiLo = 2.4492935982947064e-16;     // 2*pi - kTwoPiHi
+  const double ang = static_cast<double>(p) * inv_freq;
+  const double k = rint(ang * 0.15915494309189535);   // 1/(2*pi)
+  double red = fma(-k, kTwoPiHi, ang);
+  red = fma(-k, kTwoPiLo, red);
+  sincosf(static_cast<float>(red), s, c);
+}
+
+// ----------------------------------------------------------------------------- GEMV
+template <int KIND>
+__device__ __forceinline__ int rows_per_unit() {
+  return (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
+}
+
+// First element of row slot r (0 .. rows_per_unit-1) of unit u.
+template <int KIND>
+__device__ __forceinline__ const uint16_t* unit_row(const GemvArgs& a, int u, int r) {
+  const size_t K = static_cast<size_t>(a.K);
+  if constexpr (KIND == kKindQKV) {
+    const int half = a.D >> 1;
+    int hh = u / half;
+    const int row_in_head = (u - hh * half) + r * half;
+    if (hh < a.Hq) return a.w0 + (static_cast<size_t>(hh) * a.D + row_in_head) * K;
+    hh -= a.Hq;
+    if (hh < a.Hkv) return a.w1 + (static_cast<size_t>(hh) * a.D + row_in_head) * K;
+    hh -= a.Hkv;
+    return a.w2 + (static_cast<size_t>(hh) * a.D + row_in_head) * K;
+  } else if constexpr (KIND == kKindGLU) {
+    return (r == 0 ? a.w0 : a.w1) + static_cast<size_t>(u) * K;
+  } else {
+    return a.w0 + static_cast<size_t>(u) * K;
+  }
+}
+
+template <int KIND, int BT>
+__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 256);
+  int* is_last = reinterpret_cast<int*>(smem + 260);
+  float* red = reinterpret_cast<float*>(smem + 288);                    // 8 floats
+  float* head_val = reinterpret_cast<float*>(smem + 320);               // [8][BT]
+  uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 320 + 4 * kConsumerWarps * kMaxBatch);  // [8][BT]
+  float* xs = reinterpret_cast<float*>(smem + a.off_x);
+  float* part = reinterpret_cast<float*>(smem + a.off_part);
+  unsigned char* ring = smem + a.off_ring;
+
+  constexpr int RU = (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
+  const int US = a.units_per_stage;
+  const int P = a.parts;
+  const int CP = a.chunks_per_part;
+  const int NS = a.n_slots;
+  const int C = a.K / kChunkElems;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
+  const uint32_t stage_bytes = static_cast<uint32_t>(US * RU) * row_bytes;
+
+  const int u0 = static_cast<int>((static_cast<long long>(blockIdx.x) * a.n_units) / gridDim.x);
+  const int u1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.n_units) / gridDim.x);
+  const int n_cta_units = u1 - u0;
+  const int n_stages = (n_cta_units + US - 1) / US;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------- producer warp
+    // Weights never depend on earlier kernels: start streaming before the
+    // programmatic-dependency wait so the copies overlap the previous kernel.
+    int issued = 0;
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      bool triggered = false;
+      for (int s = 0; s < n_stages; ++s) {
+        const int slot = s % NS;
+        if (s >= NS) {
+          if (!mbar_wait(&empty[slot], ((s / NS) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
+        }
+        const int nu = min(US, n_cta_units - s * US);
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nu * RU) * row_bytes);
+        unsigned char* dst = ring + static_cast<size_t>(slot) * stage_bytes;
+        for (int r = 0; r < RU; ++r) {
+          const uint16_t* run = unit_row<KIND>(a, u0 + s * US, r);
+          int run_i = 0, run_len = 1;
+          for (int i = 1; i < nu; ++i) {
+            const uint16_t* p = unit_row<KIND>(a, u0 + s * US + i, r);
+            if (p == run + static_cast<size_t>(run_len) * a.K) {
+              ++run_len;
+            } else {
+              bulk_copy_g2s(dst + static_cast<size_t>(r * US + run_i) * row_bytes, run, run_len * row_bytes,
+                            &full[slot], policy);
+              run = p;
+              run_i = i;
+              run_len = 1;
+            }
+          }
+          bulk_copy_g2s(dst + static_cast<size_t>(r * US + run_i) * row_bytes, run, run_len * row_bytes,
+                        &full[slot], policy);
+        }
+        issued = s + 1;
+        if (issued == min(NS, n_stages)) {
+          pdl_launch_dependents();
+          triggered = true;
+        }
+      }
+      if (!triggered) pdl_launch_dependents();
+    }
+    __syncwarp();
+    if (lane != 0) pdl_launch_dependents();
+    asm volatile("bar.sync 2, 288;" ::: "memory");
+    // Drain: consumers have stopped reading the ring.  A stage is released
+    // only after its copy completed, so the only copies that can still be in
+    // flight are those of stages nobody waited for (after an abort).
+    if (lane == 0) {
+      for (int s = max(0, issued - NS); s < issued; ++s) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[s % NS], (s / NS) & 1)) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(a.err, kErrDrain);
+            break;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------------- consumer warps
+  pdl_wait();
+  pdl_launch_dependents();
+  const int B = a.B;
+
+  // Prologue: activations into shared memory, RMSNorm fused when requested.
+  if (a.x_smem) {
+    const int K = a.K;
+    for (int b = 0; b < B; ++b) {
+      float* xb = xs + static_cast<size_t>(b) * K;
+      if (a.tokens) {
+        int tok = a.tokens[b];
+        const bool ok = tok >= 0 && tok < a.vocab;
+        if (!ok && threadIdx.x == 0) atomicOr(a.err, kErrTokenRange);
+        const uint16_t* er = a.embed + static_cast<size_t>(ok ? tok : 0) * K;
+        for (int i = threadIdx.x; i < K; i += kConsumerThreads) {
+          const float v = ok ? __uint_as_float(static_cast<uint32_t>(er[i]) << 16) : 0.f;
+          xb[i] = v;
+          if (blockIdx.x == 0 && a.resid_store) a.resid_store[static_cast<size_t>(b) * K + i] = v;
+        }
+      } else {
+        const float* src = a.x + static_cast<size_t>(b) * K;
+        for (int i = threadIdx.x; i < K; i += kConsumerThreads) xb[i] = src[i];
+      }
+      if (a.norm_gamma) {
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        const float inv = block_rms_inv(xb, K, a.eps, red);
+        for (int i = threadIdx.x; i < K; i += kConsumerThreads)
+          xb[i] = (xb[i] * inv) * __uint_as_float(static_cast<uint32_t>(a.norm_gamma[i]) << 16);
+      }
+    }
+    for (int b = B; b < BT; ++b)
+      for (int i = threadIdx.x; i < K; i += kConsumerThreads) xs[static_cast<size_t>(b) * K + i] = 0.f;
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+
+  float best_v[BT];
+  uint32_t best_i[BT];
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+    best_v[b] = -INFINITY;
+    best_i[b] = 0xFFFFFFFFu;
+  }
+
+  const int tasks_full_stage = US * RU * P;
+  bool ok = true;
+  for (int s = 0; s < n_stages && ok; ++s) {
+    const int slot = s % NS;
+    const int nu = min(US, n_cta_units - s * US);
+    const int ntask = nu * RU * P;
+    const int rot = static_cast<int>((static_cast<long long>(s) * tasks_full_stage) % kConsumerWarps);
+    const int j0 = (warp - rot + kConsumerWarps) % kConsumerWarps;
+    // lane 0 polls (bounded); the verdict is warp-uniform
+    int w_ok = 1;
+    if (lane == 0) w_ok = mbar_wait(&full[slot], (s / NS) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
+    w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+    if (!w_ok) {
+      ok = false;
+      break;
+    }
+    (void)mbar_try_wait(&full[slot], (s / NS) & 1);  // completed phase: acquire for every lane
+    const unsigned char* stage = ring + static_cast<size_t>(slot) * stage_bytes;
+    for (int j = j0; j < ntask; j += kConsumerWarps) {
+      const int lr = j / P;
+      const int p = j - lr * P;
+      const int r = lr / nu;
+      const int i = lr - r * nu;
+      const uint4* wr = reinterpret_cast<const uint4*>(stage + static_cast<size_t>(r * US + i) * row_bytes);
+      const int cb = p * CP;
+      const int ce = min(C, cb + CP);
+      float acc[BT];
+#pragma unroll
+      for (int b = 0; b < BT; ++b) acc[b] = 0.f;
+      for (int c = cb + lane; c < ce; c += 32) {
+        const uint4 w = wr[c];
+        const float w0 = bf16lo(w.x), w1 = bf16hi(w.x), w2 = bf16lo(w.y), w3 = bf16hi(w.y);
+        const float w4 = bf16lo(w.z), w5 = bf16hi(w.z), w6 = bf16lo(w.w), w7 = bf16hi(w.w);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          float4 x0, x1;
+          if (a.x_smem) {
+            const float4* xp = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * a.K) + 2 * c;
+            x0 = xp[0];
+            x1 = xp[1];
+          } else {
+            const float4* xp = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.K) + 2 * c;
+            x0 = __ldg(xp);
+            x1 = __ldg(xp + 1);
+          }
+          float t = acc[b];
+          t = fmaf(w0, x0.x, t);
+          t = fmaf(w1, x0.y, t);
+          t = fmaf(w2, x0.z, t);
+          t = fmaf(w3, x0.w, t);
+          t = fmaf(w4, x1.x, t);
+          t = fmaf(w5, x1.y, t);
+          t = fmaf(w6, x1.z, t);
+          t = fmaf(w7, x1.w, t);
+          acc[b] = t;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < BT; ++b) acc[b] = warp_sum(acc[b]);
+      const int ul = s * US + i;
+      if constexpr (KIND == kKindHead) {
+        const uint32_t row = static_cast<uint32_t>(u0 + ul);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          if (b < B) {
+            if (a.logits && lane == 0) a.logits[static_cast<size_t>(b) * a.n_units + row] = acc[b];
+            // rows of one warp arrive in increasing order: strict > keeps the lowest index
+            if (acc[b] > best_v[b] || best_i[b] == 0xFFFFFFFFu) {
+              best_v[b] = acc[b];
+              best_i[b] = row;
+            }
+          }
+        }
+      } else {
+        if (lane == 0) {
+#pragma unroll
+          for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + r) * P + p) * BT + b] = acc[b];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+
+  asm volatile("bar.sync 2, 288;" ::: "memory");  // ring no longer read: the producer may drain and leave
+  const bool aborted = *abort_flag != 0;
+
+  // --------------------------------------------------------------- epilogues
+  if constexpr (KIND == kKindHead) {
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        head_val[warp * kMaxBatch + b] = best_v[b];
+        head_idx[warp * kMaxBatch + b] = best_i[b];
+      }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (threadIdx.x < B && !aborted) {
+      const int b = threadIdx.x;
+      float bv = -INFINITY;
+      uint32_t bi = 0xFFFFFFFFu;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float v = head_val[w * kMaxBatch + b];
+        const uint32_t ix = head_idx[w * kMaxBatch + b];
+        if (ix == 0xFFFFFFFFu) continue;
+        if (bi == 0xFFFFFFFFu || v > bv || (v == bv && ix < bi)) {
+          bv = v;
+          bi = ix;
+        }
+      }
+      if (bi != 0xFFFFFFFFu) atomicMax(&a.argmax_keys[b], argmax_key(bv, bi));
+    }
+    __threadfence();
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (threadIdx.x == 0) {
+      const unsigned int t = atomicAdd(a.ticket, 1u);
+      *is_last = (t == gridDim.x - 1) ? 1 : 0;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (*is_last && warp == 0) {
+      __threadfence();
+      int32_t emit = 0;
+      bool row_done = true;
+      const int b = lane;
+      if (b < B) {
+        const unsigned long long key = atomicExch(&a.argmax_keys[b], 0ull);
+        const int32_t tok = static_cast<int32_t>(argmax_key_index(key));
+        if (a.token_out) a.token_out[b] = tok;
+        if (a.book.enabled) {
+          Ctrl* c = a.book.ctrl;
+          const int eos = c->eos_id;
+          emit = a.book.done[b] ? eos : tok;
+          if (eos >= 0 && emit == eos) a.book.done[b] = 1;
+          row_done = a.book.done[b] != 0;
+          const int step = c->step;
+          if (c->out_tokens) {
+            if (step < c->out_cap)
+              c->out_tokens[static_cast<size_t>(b) * c->out_cap + step] = emit;
+            else
+              atomicOr(a.err, kErrOutRange);
+          }
+          a.book.token[b] = emit;
+          a.book.pos[b] += 1;
+        }
+      }
+      const unsigned all = __all_sync(0xffffffffu, row_done);
+      if (lane == 0) {
+        if (a.book.enabled) {
+          a.book.ctrl->all_done = all ? 1 : 0;
+          a.book.ctrl->step += 1;
+        }
+        atomicExch(a.ticket, 0u);
+      }
+    }
+    return;
+  } else {
+    if (aborted) return;
+    const int n_out = n_cta_units * B;
+    for (int idx = threadIdx.x; idx < n_out; idx += kConsumerThreads) {
+      const int ul = idx / B;
+      const int b = idx - ul * B;
+      const int u = u0 + ul;
+      float v[RU];
+#pragma unroll
+      for (int r = 0; r < RU; ++r) {
+        float sum = 0.f;
+        for (int p = 0; p < P; ++p) sum += part[((static_cast<size_t>(ul) * RU + r) * P + p) * BT + b];
+        v[r] = sum;
+      }
+      if constexpr (KIND == kKindResid) {
+        float* dst = a.out + static_cast<size_t>(b) * a.n_units + u;
+        *dst = *dst + v[0];
+      } else if constexpr (KIND == kKindGLU) {
+        a.out[static_cast<size_t>(b) * a.n_units + u] = silu_f32(v[0]) * v[1];
+      } else {  // kKindQKV
+        const int half = a.D >> 1;
+        const int hh = u / half;
+        const int j = u - hh * half;
+        const int p = a.pos[b];
+        float lo = v[0], hi = v[1];
+        if (hh < a.Hq + a.Hkv) {
+          float cs, sn;
+          rope_cos_sin(p, a.inv_freq[j], &cs, &sn);
+          const float l2 = lo * cs - hi * sn;
+          const float h2 = hi * cs + lo * sn;
+          lo = l2;
+          hi = h2;
+        }
+        if (hh < a.Hq) {
+          float* q = a.out + static_cast<size_t>(b) * a.Hq * a.D + static_cast<size_t>(hh) * a.D;
+          q[j] = lo;
+          q[j + half] = hi;
+        } else {
+          if (p < 0 || p >= a.S_max) {
+            atomicOr(a.err, kErrPosRange);
+            continue;
+          }
+          const bool is_k = hh < a.Hq + a.Hkv;
+          const int g = is_k ? hh - a.Hq : hh - a.Hq - a.Hkv;
+          uint16_t* cache = is_k ? a.k_cache : a.v_cache;
+          uint16_t* dst = cache + ((static_cast<size_t>(b) * a.Hkv + g) * a.S_max + p) * a.D;
+          dst[j] = f32_to_bf16(lo);
+          dst[j + half] = f32_to_bf16(hi);
+        }
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- standalone add + RMSNorm
+// One CTA of 256 threads per batch row: r <- r + x (x optional), y = norm(r) * gamma.
+// With `tokens` the residual row is first replaced by the embedding row.
+struct NormArgs {
+  const float* x;
+  float* resid;
+  const uint16_t* gamma;
+  float* y;
+  int H;
+  float eps;
+  const int32_t* tokens;
+  const uint16_t* embed;
+  int vocab;
+  uint32_t* err;
+};
+
+// add_rmsnorm_kernel (one CTA per row, same reduction as the fused prologue) is defined in api.cu.
+
+}  // namespace dec

@@ -1,0 +1,46 @@
+// Launch helpers shared by the translation units of libdec.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "dec_attn.cuh"
+#include "dec_kernels.cuh"
+
+namespace dec {
+
+constexpr uint32_t kSmemMax = 227 * 1024;
+
+// cudaLaunchKernelEx with programmatic dependent launch when `pdl` is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                   Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// One GEMV launch of kind KIND for batch bucket BT (1, 2, 4, 8 or 16).
+cudaError_t launch_gemv_qkv(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
+cudaError_t launch_gemv_glu(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
+cudaError_t launch_gemv_resid(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
+cudaError_t launch_gemv_head(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
+cudaError_t launch_attn(const AttnArgs& a, int B, uint32_t smem, cudaStream_t st, bool pdl);
+
+// Raise the dynamic shared-memory limit of every kernel of a unit (once per device).
+cudaError_t allow_smem_qkv();
+cudaError_t allow_smem_glu();
+cudaError_t allow_smem_resid();
+cudaError_t allow_smem_head();
+cudaError_t allow_smem_attn();
+
+}  // namespace dec

@@ -1,0 +1,27 @@
+// Instantiations of the streaming GEMV kernel for the qkv variant.
+#include "dec_launch.cuh"
+
+namespace dec {
+
+cudaError_t launch_gemv_qkv(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl) {
+  const dim3 g(grid), b(kGemvThreads);
+  switch (BT) {
+    case 1: return launch(gemv_kernel<kKindQKV, 1>, g, b, smem, st, pdl, a);
+    case 2: return launch(gemv_kernel<kKindQKV, 2>, g, b, smem, st, pdl, a);
+    case 4: return launch(gemv_kernel<kKindQKV, 4>, g, b, smem, st, pdl, a);
+    case 8: return launch(gemv_kernel<kKindQKV, 8>, g, b, smem, st, pdl, a);
+    default: return launch(gemv_kernel<kKindQKV, 16>, g, b, smem, st, pdl, a);
+  }
+}
+
+cudaError_t allow_smem_qkv() {
+  cudaError_t e;
+  const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 1>, at, kSmemMax)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 2>, at, kSmemMax)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 4>, at, kSmemMax)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 8>, at, kSmemMax)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemv_kernel<kKindQKV, 16>, at, kSmemMax);
+}
+
+}  // namespace dec
