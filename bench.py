@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--workload", default="dense4b", choices=["dense4b", "layer4b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--prompt", type=int, default=None, help="prompt length (default: the workload's 512)")
     return ap.parse_args()
 
 
@@ -177,10 +178,10 @@ def run_gpu(args, world, rank, local):
     fn = to_dev(fn_h) if fn_h is not None else None
     model = gd.Model(m.n_layers, m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.intermediate, m.vocab,
                      m.rms_eps, m.rope_theta, layers, embed=E, final_norm=fn, lm_head=E)
-    P = w.prompt_len
+    P = args.prompt or w.prompt_len
     S_max = P + POSITIONS_PER_PASS + 8
     st = gd.State(model, B, S_max, device=dev).init()
-    prompt_h = synth.make_tokens(w.seed, "prompt", (B, P), m.vocab)
+    prompt_h = synth.make_tokens(w.seed, "prompt", (B, w.prompt_len), m.vocab)[:, :P].copy()
     prompt = torch.from_numpy(prompt_h).to(dev)
     setup_s = time.time() - t0
     stream = torch.cuda.current_stream(dev)

@@ -1,0 +1,234 @@
+"""The full-size workloads, in the launch configuration the benchmark times
+(whole-step CUDA-graph decode loop), checked against the oracle on outputs it
+can afford one by one, and by properties that hold at any size.
+
+* dense4b   36 layers, H=2560, 32/8 heads, D=128, I=9728, V=151936, tied, b=1
+* dense4b_b8  the same model at b=8 with KV lengths U{1024..32768}
+* gqa12x3   24 layers, H=1536, 12/3 heads, I=8960, V=151936, b=16, KV 8192
+* gqa6x3    the query-to-KV-group mapping check (6 query heads, 3 KV heads)
+"""
+import multiprocessing as mp
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import MARGIN, HostModel, dev_bf16, dev_i32, make_caches, rel_err
+
+pytestmark = pytest.mark.gpu
+
+gd = pytest.importorskip("greedy_decode_step_gb300")
+
+
+@pytest.fixture(autouse=True)
+def _clean_error_word():
+    gd.lib()
+    gd.device_error(clear=True)
+    yield
+    assert gd.device_error(clear=True) == 0
+
+
+@pytest.fixture(scope="module")
+def dense4b():
+    w = synth.workload("dense4b")
+    hm = HostModel(w.model, w.seed)
+    return w, hm, hm.to_gpu()
+
+
+def _state(model, m, B, S_max, K=None, V=None):
+    kc = [dev_bf16(k) for k in K] if K is not None else None
+    vc = [dev_bf16(v) for v in V] if V is not None else None
+    return gd.State(model, B, S_max, k_cache=kc, v_cache=vc).init()
+
+
+# ----------------------------------------------------------------------------- dense4b, b=1
+
+def test_dense4b_short_prompt_tokens_match_oracle(dense4b):
+    """Full 36-layer model: 6-token prompt, 6 greedy steps, teacher-forced
+    with the oracle's own tokens; every token with an oracle margin above
+    1e-2 must match, and the final residual must be within the bar."""
+    w, hm, model = dense4b
+    m = w.model
+    P, n = 6, 6
+    prompt = synth.make_tokens(w.seed, "prompt", (1, w.prompt_len), m.vocab)[:, :P].copy()
+    S_max = P + n + 2
+    Kh = [np.zeros((1, m.n_kv_heads, S_max, m.head_dim), np.uint16) for _ in range(m.n_layers)]
+    Vh = [k.copy() for k in Kh]
+    om = oracle.Model(m, hm.layers, hm.embed, hm.final_norm, hm.lm_head, Kh, Vh)
+    st = _state(model, m, 1, S_max)
+    for i in range(P - 1):
+        om.step(0, i, token=int(prompt[0, i]))
+    gd.dec_prefill(model, st, dev_i32(prompt))
+    t = int(prompt[0, P - 1])
+    matched = 0
+    for s in range(n):
+        t_ref, logits, r = om.step(0, P - 1 + s, token=t)
+        gd.dec_step(model, st)
+        assert rel_err(st.residual[0].cpu().numpy(), r) < 1e-3
+        if oracle.top2_margin(logits) > MARGIN:
+            assert int(st.token[0]) == t_ref
+            matched += 1
+        st.token.fill_(t_ref)
+        t = t_ref
+    assert matched >= n // 2
+
+
+def test_dense4b_full_generation_is_deterministic_and_consistent(dense4b):
+    """The benchmark's exact configuration (512-token prompt, 256 steps,
+    EOS 0 every 16 steps): two runs give identical tokens; positions, token
+    range and the graph-vs-eager agreement on the first 32 steps hold."""
+    w, hm, model = dense4b
+    m = w.model
+    P, n = w.prompt_len, w.steps
+    prompt = dev_i32(synth.make_tokens(w.seed, "prompt", (1, P), m.vocab))
+    runs = []
+    for _ in range(2):
+        st = _state(model, m, 1, P + n + 8)
+        out = torch.empty((1, n), dtype=torch.int32, device="cuda")
+        done = gd.dec_generate(model, st, prompt, n, w.eos_id, out)
+        runs.append((done, out.cpu().numpy(), int(st.pos[0])))
+    assert runs[0][0] == runs[1][0]
+    assert np.array_equal(runs[0][1], runs[1][1])
+    done, toks, pos = runs[0]
+    assert np.all((toks >= 0) & (toks < m.vocab))
+    if w.eos_id not in toks[0, :done]:
+        assert done == n and pos == P - 1 + n
+    st = _state(model, m, 1, P + n + 8)
+    gd.dec_prefill(model, st, prompt)
+    for s in range(32):
+        gd.dec_step(model, st)
+        assert int(st.token[0]) == toks[0, s]
+
+
+# ----------------------------------------------------------------------------- batched, ragged
+
+def _oracle_rows(args):
+    """One sequence of a batched workload in the oracle (run in a worker process)."""
+    name, b, kv_len, tok0, n_steps, S_max = args
+    w = synth.workload(name)
+    m = w.model
+    hm = HostModel(m, w.seed)
+    kc, vc = [], []
+    for l in range(m.n_layers):
+        k = np.zeros((1, m.n_kv_heads, S_max, m.head_dim), np.uint16)
+        v = np.zeros_like(k)
+        synth.make_kv_prefix(w.seed, m, l, b, kv_len, "k", k[0])
+        synth.make_kv_prefix(w.seed, m, l, b, kv_len, "v", v[0])
+        kc.append(k)
+        vc.append(v)
+    om = oracle.Model(m, hm.layers, hm.embed, hm.final_norm, hm.lm_head, kc, vc)
+    toks, margins, resid = [], [], []
+    t = tok0
+    for s in range(n_steps):
+        t, logits, r = om.step(0, kv_len + s, token=t)
+        toks.append(t)
+        margins.append(oracle.top2_margin(logits))
+        resid.append(r)
+    return toks, margins, resid
+
+
+def _batched_case(name, n_check):
+    w = synth.workload(name)
+    m = w.model
+    B = w.batch
+    kv = list(w.kv_len)
+    S_max = max(kv) + w.steps + 1
+    hm = HostModel(m, w.seed)
+    model = hm.to_gpu()
+    K, V = make_caches(m, w.seed, B, S_max, kv)
+    st = _state(model, m, B, S_max, K, V)
+    del K, V
+    st.pos.copy_(dev_i32(kv))
+    tok0 = synth.make_tokens(w.seed, f"{name}.first", (B,), m.vocab)
+    st.token.copy_(dev_i32(tok0))
+    # the oracle's rows in worker processes; spawn starts them fresh, without this process's CUDA context
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(min(B, max(1, (os.cpu_count() or 2) - 1))) as pool:
+        async_res = pool.map_async(_oracle_rows, [(name, b, kv[b], int(tok0[b]), n_check, S_max) for b in range(B)])
+        # the GPU: the full run of the workload through the decode loop
+        out = torch.empty((B, w.steps), dtype=torch.int32, device="cuda")
+        st2 = None
+        done = gd.dec_decode(model, st, w.steps, -1, out)
+        assert done == w.steps
+        gpu_tokens = out.cpu().numpy()
+        assert np.all(st.pos.cpu().numpy() == np.array(kv) + w.steps)
+        # teacher-forced prefix on a fresh state for the residual comparison
+        K, V = make_caches(m, w.seed, B, S_max, kv)
+        st2 = _state(model, m, B, S_max, K, V)
+        del K, V
+        st2.pos.copy_(dev_i32(kv))
+        st2.token.copy_(dev_i32(tok0))
+        rows = async_res.get()
+    for s in range(n_check):
+        gd.dec_step(model, st2)
+        got = st2.token.cpu().numpy()
+        for b in range(B):
+            toks, margins, resid = rows[b]
+            assert rel_err(st2.residual[b].cpu().numpy(), resid[s]) < 1e-3, (b, s)
+            if margins[s] > MARGIN:
+                assert got[b] == toks[s], (b, s)
+        st2.token.copy_(dev_i32([rows[b][0][s] for b in range(B)]))
+    # the free-running decode loop agrees with the oracle while its tokens do
+    for b in range(B):
+        toks, margins, _ = rows[b]
+        for s in range(n_check):
+            if gpu_tokens[b, s] != toks[s]:
+                assert margins[s] <= MARGIN, (b, s)
+                break
+
+
+def test_dense4b_b8_ragged_kv():
+    """36 layers at b=8, KV lengths U{1024..32768}: 64 decode steps in the
+    loop; the first 2 steps of every row checked against the oracle."""
+    _batched_case("dense4b_b8", 2)
+
+
+def test_gqa12x3_b16():
+    """24 layers, Hq=12/Hkv=3, b=16, KV 8192: 128 decode steps in the loop;
+    the first 2 steps of every row checked against the oracle."""
+    _batched_case("gqa12x3", 2)
+
+
+# ----------------------------------------------------------------------------- GQA mapping
+
+def test_gqa6x3_mapping_in_a_whole_step():
+    """A one-layer Hq=6/Hkv=3 model whose value cache holds one constant per
+    KV head, with Wo reading one output dimension per query head: the step's
+    residual update names the KV group each query head read."""
+    w = synth.workload("gqa6x3")
+    m = w.model
+    Hq, Hkv, D, H = m.n_heads, m.n_kv_heads, m.head_dim, m.hidden
+    hm = HostModel(m, 0, embed=False, head=False)
+    lay = hm.layers[0]
+    lay["wv"] = np.zeros_like(lay["wv"])       # the new token's value is 0 ...
+    wo = np.zeros((H, Hq * D), np.float32)
+    for h in range(Hq):
+        wo[h, h * D] = 1.0                     # ... and residual[h] += o[h][0]
+    lay["wo"] = (wo.view(np.uint32) >> 16).astype(np.uint16)
+    lay["wd"] = np.zeros_like(lay["wd"])
+    S, S_max = 40, 64
+    K = np.zeros((1, Hkv, S_max, D), np.uint16)
+    V = np.zeros_like(K)
+    for g in range(Hkv):
+        K[0, g, :S] = synth.normal_bf16(1, f"k{g}", (S, D))
+        V[0, g, :S] = np.float32(g + 1).view(np.uint32) >> 16
+    model = hm.to_gpu()
+    st = _state(model, m, 1, S_max, [K], [V])
+    st.pos.fill_(S)
+    x = np.zeros((1, H), np.float32)
+    x[0, Hq:] = 1.0                            # a non-zero input for the norm
+    st.residual.copy_(torch.from_numpy(x).cuda())
+    gd.dec_step(model, st)
+    r = st.residual[0].cpu().numpy()
+    # the current token (value 0) takes part in the softmax, so o[h][0] is the
+    # constant of its group scaled by the weight of the 40 older keys
+    om = oracle.Model(m, [lay], None, None, None, [K.copy()], [V.copy()])
+    _, _, r_ref = om.step(0, S, x_in=x[0])
+    assert rel_err(r, r_ref) < 1e-4
+    assert np.all(r_ref[:Hq] > 0)
+    ratio = r_ref[:Hq] / r_ref[0]
+    np.testing.assert_allclose(ratio, [1, 1, 2, 2, 3, 3], rtol=0.2)  # the interleaved reading gives 1,2,3,1,2,3
+    np.testing.assert_allclose(r[:Hq] / r[0], ratio, rtol=1e-4)
