@@ -158,6 +158,57 @@ def bytes_per_step(m, positions, B=1, head=True):
     return w, kv
 
 
+def run_layer(args, world, rank, local):
+    """One 4B-class layer (no embedding, no LM head) stepped K times at the
+    4096-token cache length: per-layer timing and profiling."""
+    import torch
+    import greedy_decode_step_gb300 as gd
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w, m, layers_h, _, _ = host_model("layer4b")
+    B, L0 = 1, w.kv_len[0]
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    model = gd.Model(m.n_layers, m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.intermediate, m.vocab,
+                     m.rms_eps, m.rope_theta, [{k: to_dev(v) for k, v in l.items()} for l in layers_h])
+    S_max = L0 + args.steps + args.warmup + 8
+    kc = np.zeros((B, m.n_kv_heads, S_max, m.head_dim), np.uint16)
+    vc = np.zeros_like(kc)
+    synth.make_kv_prefix(w.seed, m, 0, 0, L0, "k", kc[0])
+    synth.make_kv_prefix(w.seed, m, 0, 0, L0, "v", vc[0])
+    st = gd.State(model, B, S_max, device=dev, k_cache=[to_dev(kc)], v_cache=[to_dev(vc)]).init()
+    st.pos.fill_(L0)
+    st.residual.copy_(torch.from_numpy(synth.make_residual(w.seed, B, m.hidden)).to(dev))
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        gd.dec_step(model, st)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            gd.dec_step(model, st)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    assert gd.device_error(clear=True) == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    w_bytes, kv_bytes = bytes_per_step(m, [L0 + args.warmup], B, head=False)
+    gbs = (w_bytes + kv_bytes) / (ms / 1e3) / 1e9
+    res = {"metric": "one 4B-class layer step (b=1, 4096-token cache)", "value": round(ms * 1e3, 2),
+           "unit": "us/step", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+           "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": "layer4b: H=2560, Hq=32, Hkv=8, D=128, I=9728, b=1, eager dec_step with PDL",
+                      "step_bytes": int(w_bytes + kv_bytes), "step_hbm_gbs": round(gbs, 1),
+                      "step_hbm_frac_of_measured": round(gbs / peaks()[0], 4)},
+           "roofline": glu_roofline(gd, torch, model, m, dev, stream, reps=20),
+           "gpu_launches": 5 * args.steps, "clocks": clk.summary()}
+    return res, None
+
+
 def run_gpu(args, world, rank, local):
     import torch
     import greedy_decode_step_gb300 as gd
@@ -412,8 +463,11 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-    res, host = run_gpu(args, world, rank, local)
-    if rank == 0 and not args.no_cpu_baseline:
+    if args.workload == "layer4b":
+        res, host = run_layer(args, world, rank, local)
+    else:
+        res, host = run_gpu(args, world, rank, local)
+    if rank == 0 and host is not None and not args.no_cpu_baseline:
         m, layers_h, E_h, fn_h, _ = host
         done, el = oracle_rate(m, layers_h, E_h, fn_h, 3, max_seconds=25.0)
         res["cpu_baseline"] = {"value": round(done / el, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
