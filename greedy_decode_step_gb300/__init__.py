@@ -61,6 +61,7 @@ _SIGNATURES = {
     "dec_qkv_gemv_rope": (_I, [_P, _P, _P, _P, _P, _F, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "dec_attn_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "dec_gqa_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _I, _P]),
+    "dec_gqa_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "dec_glu_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "dec_down_gemv": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "dec_lmhead_workspace_size": (_S, [_I]),
@@ -167,6 +168,17 @@ def dec_gqa_decode_attn(q, k_cache, v_cache, pos, o, ws=None, num_splits: int = 
                                      _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), B, Hq, Hkv, D, S_max,
                                      num_splits, _stream(stream)))
     return ws
+
+
+def dec_gqa_decode_attn_noalloc(q, k_cache, v_cache, pos, o, num_splits: int = 0, stream=None):
+    """dec_gqa_decode_attn on the library's built-in scratch: for callers that
+    cannot provide (or allocate) a workspace.  Calls that may overlap on the
+    GPU share that scratch and must be serialised by the caller."""
+    B, Hq, D = q.shape
+    _, Hkv, S_max, _ = k_cache.shape
+    _check(lib().dec_gqa_decode_attn_noalloc(_ptr(q, _f32, "q"), _ptr(k_cache, _bf16, "k_cache"),
+                                             _ptr(v_cache, _bf16, "v_cache"), _ptr(pos, _i32, "pos"),
+                                             _ptr(o, _f32, "o"), B, Hq, Hkv, D, S_max, num_splits, _stream(stream)))
 
 
 def dec_glu_gemv(y, Wg, Wu, h, stream=None):

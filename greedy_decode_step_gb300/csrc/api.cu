@@ -932,3 +932,84 @@ int dec_generate(const dec_model* m, dec_state* s, const int32_t* prompt, int P,
 }
 
 }  // extern "C"
+
+// =============================================================================== attention without allocation
+//
+// Built-in scratch for dec_gqa_decode_attn_noalloc.  Some callers cannot hand
+// the library any device memory of its own: a host application that owns
+// every device allocation through its own pool, or a latency-critical loop in
+// which a cudaMalloc (which can synchronise the device) is not acceptable.
+// This array is their scratch.  It is a file-scope device array, so every
+// GPU that loads the library holds these bytes until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array, looked up once per device (the host
+// symbol itself is only a stand-in and must never reach a kernel).
+void* g_noalloc_scratch_dev[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  DEC_CUDA(cudaGetDevice(&dev));
+  DEC_CHECK(dev >= 0 && dev < kMaxDevices, DEC_EUNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_scratch_dev[dev] == nullptr) {
+    void* p = nullptr;
+    DEC_CUDA(cudaGetSymbolAddress(&p, g_attn_noalloc_scratch));
+    DEC_CHECK(p != nullptr, DEC_ECUDA, "no device address for the built-in scratch");
+    g_noalloc_scratch_dev[dev] = p;
+  }
+  *out = g_noalloc_scratch_dev[dev];
+  return DEC_OK;
+}
+
+}  // namespace
+
+extern "C" int dec_gqa_decode_attn_noalloc(const float* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* pos, float* o, int B, int Hq, int Hkv, int D, int S_max,
+                                           int num_splits, void* stream) {
+  DEC_TRY(check_batch(B));
+  DEC_TRY(check_heads(Hq, Hkv, D));
+  DEC_PTR(q);
+  DEC_PTR(k_cache);
+  DEC_PTR(v_cache);
+  DEC_CHECK(pos != nullptr, DEC_EINVAL, "pos is NULL");
+  DEC_PTR(o);
+  DEC_CHECK(S_max >= 1, DEC_EINVAL, "S_max must be >= 1");
+  DEC_CHECK(num_splits >= 0, DEC_EINVAL, "num_splits must be >= 0");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  const int n = attn_splits(B, Hkv, S_max, dv->sms, num_splits);
+  const size_t part = (attn_part_bytes(B, Hq, Hkv, D, n) + 255) / 256 * 256;
+  const size_t tick = (sizeof(unsigned int) * B * Hkv + 255) / 256 * 256;
+  const size_t need = 256 + part + tick;
+  DEC_CHECK(need <= kNoAllocScratchBytes, DEC_ECAPACITY,
+            "this shape needs %zu bytes of attention scratch but the built-in scratch holds %zu; use "
+            "dec_gqa_decode_attn with a caller workspace (or fewer splits)",
+            need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  DEC_TRY(noalloc_scratch(&scratch));
+  unsigned char* base = static_cast<unsigned char*>(scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(base + 256 + part);
+  // the array keeps the previous call's contents: the merge tickets must start at zero
+  DEC_CUDA(cudaMemsetAsync(tickets, 0, sizeof(unsigned int) * B * Hkv, st));
+  AttnArgs t{};
+  t.q = q;
+  t.k_cache = static_cast<const uint16_t*>(k_cache);
+  t.v_cache = static_cast<const uint16_t*>(v_cache);
+  t.pos = pos;
+  t.o = o;
+  t.part = reinterpret_cast<float*>(base + 256);
+  t.tickets = tickets;
+  t.Hq = Hq;
+  t.Hkv = Hkv;
+  t.D = D;
+  t.S_max = S_max;
+  t.n_split = n;
+  t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  return run_attn(t, B, dv, st, false);
+}

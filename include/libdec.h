@@ -115,6 +115,26 @@ int dec_gqa_decode_attn(const float* q, const void* k_cache, const void* v_cache
                         void* stream);
 
 /*
+ * dec_gqa_decode_attn without a caller workspace and without any allocation.
+ * The paper has no counterpart of this call.
+ *
+ * For callers that cannot give the library device memory of its own -- a
+ * host application whose memory pool owns every device allocation, or a
+ * latency-critical loop in which cudaMalloc (which may synchronise the
+ * device) is not acceptable.  Same arguments, result and numerics as
+ * dec_gqa_decode_attn, minus the workspace.  Its scratch is a built-in
+ * device array of 4 MiB per GPU (held by every GPU that loads the library
+ * until the process exits); a shape whose split plan needs more returns
+ * DEC_ECAPACITY and launches nothing.  It calls no cudaMalloc or cudaFree.
+ * The first call on each device looks up the array's device address: make
+ * that first call before any stream capture.  All calls share the one
+ * array: calls that can overlap on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller.
+ */
+int dec_gqa_decode_attn_noalloc(const float* q, const void* k_cache, const void* v_cache, const int32_t* pos,
+                                float* o, int B, int Hq, int Hkv, int D, int S_max, int num_splits, void* stream);
+
+/*
  * Dual-weight gate/up GEMV with SiLU*mul ("dual_gemv_silu_mul"):
  *   h[b] = silu(Wg y[b]) * (Wu y[b]),  silu(z) = z / (1 + e^-z)
  * y: fp32 [B][H]; Wg, Wu: bf16 [I][H]; h: fp32 [B][I].
