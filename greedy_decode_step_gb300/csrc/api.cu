@@ -51,71 +51,6 @@ int fail(int code, const char* fmt, ...) {
     if (r_ != DEC_OK) return r_; \
   } while (0)
 
-// ------------------------------------------------------------------------------- device set-up
-
-constexpr int kMaxDevices = 64;
-
-struct DeviceInfo {
-  bool ready = false;
-  int sms = 0;
-  uint32_t* err = nullptr;
-};
-DeviceInfo g_devices[kMaxDevices];
-std::mutex g_dev_mu;
-
-int device_info(DeviceInfo** out) {
-  int dev = 0;
-  DEC_CUDA(cudaGetDevice(&dev));
-  DEC_CHECK(dev >= 0 && dev < kMaxDevices, DEC_EUNSUPPORTED, "device index %d", dev);
-  std::lock_guard<std::mutex> lock(g_dev_mu);
-  DeviceInfo& d = g_devices[dev];
-  if (!d.ready) {
-    int major = 0, minor = 0;
-    DEC_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
-    DEC_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
-    DEC_CHECK(major == 10 && minor == 3, DEC_EUNSUPPORTED, "libdec is built for sm_103 (GB300); device %d is sm_%d%d",
-              dev, major, minor);
-    DEC_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
-    DEC_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_dec_device_error));
-    DEC_CUDA(allow_smem_qkv());
-    DEC_CUDA(allow_smem_glu());
-    DEC_CUDA(allow_smem_resid());
-    DEC_CUDA(allow_smem_head());
-    DEC_CUDA(allow_smem_attn());
-    d.ready = true;
-  }
-  *out = &d;
-  return DEC_OK;
-}
-
-// ------------------------------------------------------------------------------- checks
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-#define DEC_PTR(p) DEC_CHECK((p) != nullptr && aligned16(p), DEC_EINVAL, "%s must be a non-null 16-byte aligned pointer", #p)
-
-int check_batch(int B) {
-  DEC_CHECK(B >= 1 && B <= kMaxBatch, DEC_EUNSUPPORTED, "batch %d outside 1..%d", B, kMaxBatch);
-  return DEC_OK;
-}
-
-int check_row(int K, const char* what) {
-  DEC_CHECK(K >= 8 && K % 8 == 0 && K <= (1 << 20), DEC_EUNSUPPORTED, "%s = %d: rows must hold a multiple of 8 elements",
-            what, K);
-  return DEC_OK;
-}
-
-int check_heads(int Hq, int Hkv, int D) {
-  DEC_CHECK(D == 64 || D == 128, DEC_EUNSUPPORTED, "head_dim %d: supported 64 and 128", D);
-  DEC_CHECK(Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0, DEC_EINVAL, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
-  DEC_CHECK(Hq / Hkv <= kAttnMaxGroup, DEC_EUNSUPPORTED, "Hq/Hkv = %d above %d", Hq / Hkv, kAttnMaxGroup);
-  return DEC_OK;
-}
-
-int bt_bucket(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16; }
-
-uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
-
 // ------------------------------------------------------------------------------- small kernels
 
 __global__ void __launch_bounds__(kConsumerThreads) add_rmsnorm_kernel(const __grid_constant__ NormArgs a) {
@@ -136,7 +71,7 @@ __global__ void __launch_bounds__(kConsumerThreads) add_rmsnorm_kernel(const __g
     for (int i = threadIdx.x; i < a.H; i += kConsumerThreads) r[i] = r[i] + x[i];
   }
   asm volatile("bar.sync 1, 256;" ::: "memory");
-  const float inv = block_rms_inv(r, a.H, a.eps, red);
+  const float inv = block_rms_inv<false>(r, a.H, a.eps, red);
   float* y = a.y + static_cast<size_t>(b) * a.H;
   for (int i = threadIdx.x; i < a.H; i += kConsumerThreads)
     y[i] = (r[i] * inv) * __uint_as_float(static_cast<uint32_t>(a.gamma[i]) << 16);
@@ -190,51 +125,143 @@ __global__ void pad_kernel(int32_t* out, int B, int cap, int from, int value) {
   }
 }
 
+// ------------------------------------------------------------------------------- device set-up
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  uint32_t* err = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  DEC_CUDA(cudaGetDevice(&dev));
+  DEC_CHECK(dev >= 0 && dev < kMaxDevices, DEC_EUNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    DEC_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    DEC_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    DEC_CHECK(major == 10 && minor == 3, DEC_EUNSUPPORTED, "libdec is built for sm_103 (GB300); device %d is sm_%d%d",
+              dev, major, minor);
+    DEC_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+    DEC_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_dec_device_error));
+    DEC_CUDA(allow_smem_qkv());
+    DEC_CUDA(allow_smem_glu());
+    DEC_CUDA(allow_smem_resid());
+    DEC_CUDA(allow_smem_head());
+    DEC_CUDA(allow_smem_attn());
+    DEC_CUDA(prefer_max_carveout(add_rmsnorm_kernel));
+    DEC_CUDA(prefer_max_carveout(advance_kernel));
+    DEC_CUDA(prefer_max_carveout(set_tokens_kernel));
+    d.ready = true;
+  }
+  *out = &d;
+  return DEC_OK;
+}
+
+// ------------------------------------------------------------------------------- checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define DEC_PTR(p) DEC_CHECK((p) != nullptr && aligned16(p), DEC_EINVAL, "%s must be a non-null 16-byte aligned pointer", #p)
+
+int check_batch(int B) {
+  DEC_CHECK(B >= 1 && B <= kMaxBatch, DEC_EUNSUPPORTED, "batch %d outside 1..%d", B, kMaxBatch);
+  return DEC_OK;
+}
+
+int check_row(int K, const char* what) {
+  DEC_CHECK(K >= 8 && K % 8 == 0 && K <= (1 << 20), DEC_EUNSUPPORTED, "%s = %d: rows must hold a multiple of 8 elements",
+            what, K);
+  return DEC_OK;
+}
+
+int check_heads(int Hq, int Hkv, int D) {
+  DEC_CHECK(D == 64 || D == 128, DEC_EUNSUPPORTED, "head_dim %d: supported 64 and 128", D);
+  DEC_CHECK(Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0, DEC_EINVAL, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  DEC_CHECK(Hq / Hkv <= kAttnMaxGroup, DEC_EUNSUPPORTED, "Hq/Hkv = %d above %d", Hq / Hkv, kAttnMaxGroup);
+  return DEC_OK;
+}
+
+int bt_bucket(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16; }
+
+uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
 // ------------------------------------------------------------------------------- GEMV planning
 
-constexpr uint32_t kStageTarget = 20 * 1024;   // bytes of weight rows per ring stage
-constexpr int kChunksPerTask = 128;            // 1024 elements per warp task
-constexpr uint32_t kHeaderBytes = 1536;
+constexpr uint32_t kPartTarget = 24 * 1024;    // shared-memory path: bytes of the rows worked on side by side
+constexpr uint32_t kCopyTarget = 40 * 1024;    // bytes of one bulk copy (one ring stage)
+constexpr uint32_t kRingTarget = 96 * 1024;    // bytes in flight per CTA (two CTAs of adjacent kernels share an SM)
 constexpr uint32_t kPartMaxBytes = 24 * 1024;
 constexpr uint32_t kXSmemMax = 64 * 1024;
-constexpr uint32_t kSmemBudget = 110 * 1024;   // two CTAs of neighbouring kernels fit one SM
 
 struct GemvPlan {
   int grid = 0;
   uint32_t smem = 0;
+  bool xreg = false;
 };
 
+// Warp roles: NSLOT rows are worked on side by side and every row is cut into
+// P = 8 / NSLOT parts; warp w takes part w % P.
+//  * register path (b <= 2): P is the smallest power of two that leaves at
+//    most kXregIt 16-byte chunks per lane, so the warp's activation slice
+//    fits in registers; a stage holds at most kXregRows rows per warp.
+//  * shared-memory path: NSLOT is the largest power of two whose rows fit
+//    kPartTarget (the LM head keeps whole rows per warp).
+// A ring stage is one bulk copy of about kCopyTarget bytes.
 int plan_gemv(int kind, GemvArgs& a, int BT, int sms, bool want_x_smem, GemvPlan* pl) {
   const int RU = (kind == kKindQKV || kind == kKindGLU) ? 2 : 1;
   const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
   const int C = a.K / kChunkElems;
-  if (kind == kKindHead) {
-    a.parts = 1;
-    a.chunks_per_part = C;
-  } else {
-    a.chunks_per_part = kChunksPerTask;
-    a.parts = (C + kChunksPerTask - 1) / kChunksPerTask;
-  }
-  a.units_per_stage = std::max<int>(1, static_cast<int>(kStageTarget / (RU * row_bytes)));
-  const uint32_t stage_bytes = static_cast<uint32_t>(a.units_per_stage * RU) * row_bytes;
+  const bool norm_in = a.norm_gamma != nullptr || a.tokens != nullptr;
   const uint32_t x_bytes = static_cast<uint32_t>(BT) * static_cast<uint32_t>(a.K) * 4u;
-  a.x_smem = (want_x_smem && x_bytes <= kXSmemMax) ? 1 : 0;
+  const bool x_fits = want_x_smem && x_bytes <= kXSmemMax;
+  int p_reg = 1;
+  while (p_reg < kConsumerWarps && (C + p_reg - 1) / p_reg > 32 * kXregIt) p_reg *= 2;
+  const bool xreg = BT <= 2 && (C + p_reg - 1) / p_reg <= 32 * kXregIt && (!norm_in || x_fits);
+  int nslot;
+  if (xreg) {
+    nslot = kConsumerWarps / p_reg;
+    a.rows_per_stage = std::max(1, std::min<int>(static_cast<int>(kCopyTarget / row_bytes), kXregRows * nslot));
+    a.x_smem = norm_in ? 1 : 0;
+  } else {
+    nslot = kConsumerWarps;
+    if (kind != kKindHead)
+      while (nslot > 1 && static_cast<uint32_t>(nslot) * row_bytes > kPartTarget) nslot /= 2;
+    const int m = std::max<int>(1, static_cast<int>(kCopyTarget / (static_cast<uint32_t>(nslot) * row_bytes)));
+    a.rows_per_stage = nslot * m;
+    a.x_smem = x_fits ? 1 : 0;
+  }
+  pl->xreg = xreg;
+  a.parts = kConsumerWarps / nslot;
+  a.chunks_per_part = (C + a.parts - 1) / a.parts;
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.rows_per_stage) * row_bytes;
+  const bool uses_part = kind != kKindHead || xreg;
   int upc = (a.n_units + sms - 1) / sms;
-  if (kind != kKindHead) {
+  if (uses_part) {
     const int max_upc = std::max<int>(1, static_cast<int>(kPartMaxBytes / (RU * a.parts * BT * 4)));
     upc = std::min(upc, max_upc);
   }
   const int grid = (a.n_units + upc - 1) / upc;
   a.units_per_cta = (a.n_units + grid - 1) / grid;
-  const uint32_t part_bytes =
-      kind == kKindHead ? 0u : static_cast<uint32_t>(a.units_per_cta * RU * a.parts * BT) * 4u;
-  a.off_x = kHeaderBytes;
+  // stage table: full stages plus at most one partial stage per run
+  const int runs = kind == kKindQKV ? 2 * (a.units_per_cta / std::max(1, a.D / 2) + 2) : RU;
+  a.max_stages = (a.units_per_cta * RU + a.rows_per_stage - 1) / a.rows_per_stage + runs;
+  const uint32_t part_bytes = uses_part ? static_cast<uint32_t>(a.units_per_cta * RU * a.parts * BT) * 4u : 0u;
+  a.off_x = align_up(kGemvHeaderBytes + static_cast<uint32_t>(a.max_stages) * sizeof(StageDesc), 16);
   a.off_part = align_up(a.off_x + (a.x_smem ? x_bytes : 0u), 16);
   a.off_ring = align_up(a.off_part + part_bytes, 128);
-  const uint32_t budget = std::max(kSmemBudget, a.off_ring + 2 * stage_bytes);
-  int ns = static_cast<int>((std::min(budget, kSmemMax) - std::min(a.off_ring, kSmemMax)) / stage_bytes);
-  ns = std::min(ns, kMaxStages);
-  DEC_CHECK(ns >= 2, DEC_EUNSUPPORTED, "row of %d elements too long for the shared-memory ring", a.K);
+  int ns = static_cast<int>(kRingTarget / stage_bytes);
+  ns = std::max(2, std::min(ns, kMaxStages));
+  while (ns > 2 && a.off_ring + static_cast<uint32_t>(ns) * stage_bytes > kSmemMax) --ns;
+  DEC_CHECK(a.off_ring + static_cast<uint32_t>(ns) * stage_bytes <= kSmemMax, DEC_EUNSUPPORTED,
+            "row of %d elements too long for the shared-memory ring", a.K);
   a.n_slots = ns;
   pl->grid = grid;
   pl->smem = a.off_ring + static_cast<uint32_t>(ns) * stage_bytes;
@@ -251,10 +278,10 @@ int run_gemv(int kind, GemvArgs& a, int B, const DeviceInfo* dv, bool want_x_sme
             "fused RMSNorm needs the activations in shared memory (B=%d, K=%d)", B, a.K);
   cudaError_t e;
   switch (kind) {
-    case kKindQKV: e = launch_gemv_qkv(BT, a, pl.grid, pl.smem, st, pdl); break;
-    case kKindGLU: e = launch_gemv_glu(BT, a, pl.grid, pl.smem, st, pdl); break;
-    case kKindResid: e = launch_gemv_resid(BT, a, pl.grid, pl.smem, st, pdl); break;
-    default: e = launch_gemv_head(BT, a, pl.grid, pl.smem, st, pdl); break;
+    case kKindQKV: e = launch_gemv_qkv(BT, pl.xreg, a, pl.grid, pl.smem, st, pdl); break;
+    case kKindGLU: e = launch_gemv_glu(BT, pl.xreg, a, pl.grid, pl.smem, st, pdl); break;
+    case kKindResid: e = launch_gemv_resid(BT, pl.xreg, a, pl.grid, pl.smem, st, pdl); break;
+    default: e = launch_gemv_head(BT, pl.xreg, a, pl.grid, pl.smem, st, pdl); break;
   }
   DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "gemv launch: %s", cudaGetErrorString(e));
   return DEC_OK;

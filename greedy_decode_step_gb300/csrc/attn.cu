@@ -10,9 +10,9 @@ cudaError_t launch_attn(const AttnArgs& a, int B, uint32_t smem, cudaStream_t st
 }
 
 cudaError_t allow_smem_attn() {
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  cudaError_t e = allow_smem(attn_kernel<64>);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  return allow_smem(attn_kernel<128>);
 }
 
 }  // namespace dec

@@ -68,6 +68,15 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
   pdl_wait();
   pdl_launch_dependents();
 
+  // the group's query vectors (independent of the key plan) are fetched while
+  // the position is read
+  constexpr int kQPerThread = (kAttnMaxGroup * D + 287) / 288;
+  float qv[kQPerThread];
+#pragma unroll
+  for (int j = 0; j < kQPerThread; ++j) {
+    const int i = threadIdx.x + j * 288;
+    qv[j] = i < G * D ? a.q[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i] : 0.f;
+  }
   const int p = a.pos[b];
   if (p < 0 || p >= a.S_max) {
     if (split == 0 && g == 0 && threadIdx.x == 0) atomicOr(a.err, kErrPosRange);
@@ -85,16 +94,32 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
   const uint16_t* Kg = a.k_cache + head_off * D;
   const uint16_t* Vg = a.v_cache + head_off * D;
 
-  if (threadIdx.x == 0) {
+  // the producer lane sets up the barriers and issues the first tiles at once
+  int issued = 0;
+  uint64_t policy = 0;
+  if (warp == 8 && lane == 0) {
     for (int i = 0; i < kAttnSlots; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kAttnWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
+    policy = l2_policy_evict_last();
+    for (int t = 0; t < min(n_tiles, kAttnSlots); ++t) {
+      const int j0 = k0 + t * kAttnTile;
+      const int nk = min(kAttnTile, k1 - j0);
+      unsigned char* dst = ring + static_cast<size_t>(t) * 2 * kTileBytes;
+      mbar_arrive_expect_tx(&full[t], 2u * nk * kRowBytes);
+      bulk_copy_g2s(dst, Kg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[t], policy);
+      bulk_copy_g2s(dst + kTileBytes, Vg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[t], policy);
+      issued = t + 1;
+    }
   }
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-    q_s[i] = a.q[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i];
+#pragma unroll
+  for (int j = 0; j < kQPerThread; ++j) {
+    const int i = threadIdx.x + j * 288;
+    if (i < G * D) q_s[i] = qv[j];
+  }
   if (threadIdx.x < G) {
     m_run[threadIdx.x] = -INFINITY;
     l_run[threadIdx.x] = 0.f;
@@ -103,14 +128,10 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
 
   if (warp == 8) {
     // ----------------------------------------------------------- producer warp
-    int issued = 0;
     if (lane == 0) {
-      const uint64_t policy = l2_policy_evict_last();
-      for (int t = 0; t < n_tiles; ++t) {
+      for (int t = issued; t < n_tiles; ++t) {
         const int slot = t % kAttnSlots;
-        if (t >= kAttnSlots) {
-          if (!mbar_wait(&empty[slot], ((t / kAttnSlots) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
-        }
+        if (!mbar_wait(&empty[slot], ((t / kAttnSlots) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
         const int j0 = k0 + t * kAttnTile;
         const int nk = min(kAttnTile, k1 - j0);
         unsigned char* dst = ring + static_cast<size_t>(slot) * 2 * kTileBytes;
@@ -275,19 +296,46 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
   asm volatile("bar.sync 1, 256;" ::: "memory");
   if (!*is_last) return;
   __threadfence();
+  // Merge by log-sum-exp weights: o = sum_s w_s acc_s with
+  // w_s = exp(m_s - M) / sum_s' exp(m_s' - M) l_s'.  The split maxima and
+  // sums are staged in shared memory (the ring is free now) in one parallel
+  // pass, and each thread issues its accumulator loads together.
   const float* base = a.part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
+  float* ms = reinterpret_cast<float*>(ring);          // [n_active][G] split maxima, then weights
+  float* ls = ms + a.n_split * G;                      // [n_active][G] split sums
+  float* mh = ls + a.n_split * G;                      // [G] overall max, [G] 1 / overall sum
+  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
+    const int sp = i / G, h = i - sp * G;
+    ms[i] = __ldcg(base + sp * stride + G * D + h);
+    ls[i] = __ldcg(base + sp * stride + G * D + G + h);
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < n_active; ++sp) M = fmaxf(M, ms[sp * G + tid]);
+    float L = 0.f;
+    for (int sp = 0; sp < n_active; ++sp) L = fmaf(expf(ms[sp * G + tid] - M), ls[sp * G + tid], L);
+    mh[tid] = M;
+    mh[G + tid] = 1.0f / L;
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
+    const int h = i % G;
+    ms[i] = expf(ms[i] - mh[h]) * mh[G + h];
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
   for (int idx = tid; idx < G * D; idx += kAttnConsumers) {
     const int h = idx / D, d = idx - h * D;
-    float M = -INFINITY;
-    for (int s = 0; s < n_active; ++s) M = fmaxf(M, __ldcg(base + s * stride + G * D + h));
-    float L = 0.f, num = 0.f;
-    for (int s = 0; s < n_active; ++s) {
-      const float* ps = base + s * stride;
-      const float w = expf(__ldcg(ps + G * D + h) - M);
-      L = fmaf(w, __ldcg(ps + G * D + G + h), L);
-      num = fmaf(w, __ldcg(ps + h * D + d), num);
+    float num = 0.f;
+    for (int s0 = 0; s0 < n_active; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = s0 + j < n_active ? __ldcg(base + (s0 + j) * stride + h * D + d) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < n_active) num = fmaf(ms[(s0 + j) * G + h], v[j], num);
     }
-    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] = num / L;
+    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] = num;
   }
   if (tid == 0) atomicExch(ticket, 0u);
 }

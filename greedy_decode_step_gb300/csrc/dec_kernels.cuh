@@ -32,6 +32,10 @@ constexpr int kGemvThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kMaxStages = 16;
 constexpr int kChunkElems = 8;                       // one 16-byte load of bf16
 constexpr int kMaxBatch = 16;
+constexpr int kMaxIt = 8;                            // 16-byte chunks per lane per block (shared-memory path)
+constexpr int kXregIt = 5;                           // chunks per lane of a warp's part (register path)
+constexpr int kXregRows = 2;                         // rows per warp per stage (register path)
+constexpr uint32_t kGemvHeaderBytes = 1536;          // barriers, flags, reductions; the stage table follows
 
 enum GemvKind : int { kKindQKV = 0, kKindGLU = 1, kKindResid = 2, kKindHead = 3 };
 
@@ -59,7 +63,8 @@ struct GemvArgs {
   const uint16_t* w2;
   int K;
   int n_units;          // work units (QKV: rotation pairs; GLU: gate/up row pairs; else rows)
-  int units_per_stage;  // US
+  int rows_per_stage;   // rows of one bulk copy
+  int max_stages;       // capacity of the stage table
   int parts;            // P: a row's dot product is cut into P warp tasks
   int chunks_per_part;  // CP (16-byte chunks)
   int n_slots;          // ring stages
@@ -90,13 +95,25 @@ struct GemvArgs {
   double inv_freq[64];    // QKV: theta^(-2i/D), i < D/2
 };
 
+// ----------------------------------------------------------------------------- activation layout
+// Activations staged in shared memory use a split layout: for element e of a
+// K-vector, the low four of each 8-element chunk go to the first half and the
+// high four to the second half, so lane l's 16-byte reads of chunk c are
+// contiguous across the warp (no bank conflicts).
+__device__ __forceinline__ int xsplit(int e, int K) { return ((e >> 2) & 1) * (K >> 1) + ((e >> 3) << 2) + (e & 3); }
+
 // ----------------------------------------------------------------------------- RMSNorm helper
 // Normalisation factor 1/sqrt(mean(v^2) + eps) of v[0..H) computed by the 256
-// consumer threads (named barrier 1) in a fixed order.  `red` holds 8 floats.
+// consumer threads (named barrier 1) in a fixed order over the element index
+// (the same order for the split layout).  `red` holds 8 floats.
+template <bool SPLIT>
 __device__ __forceinline__ float block_rms_inv(const float* v, int H, float eps, float* red) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   float ss = 0.f;
-  for (int i = t; i < H; i += kConsumerThreads) ss = fmaf(v[i], v[i], ss);
+  for (int i = t; i < H; i += kConsumerThreads) {
+    const float x = v[SPLIT ? xsplit(i, H) : i];
+    ss = fmaf(x, x, ss);
+  }
   ss = warp_sum(ss);
   if (lane == 0) red[warp] = ss;
   asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -105,6 +122,19 @@ __device__ __forceinline__ float block_rms_inv(const float* v, int H, float eps,
   for (int w = 0; w < kConsumerWarps; ++w) tot += red[w];
   asm volatile("bar.sync 1, 256;" ::: "memory");
   return 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
+}
+
+// Dot product of 8 bf16 weights with 8 fp32 activations (one dependent chain).
+__device__ __forceinline__ float dot8(const uint4 w, const float* x) {
+  float t = bf16lo(w.x) * x[0];
+  t = fmaf(bf16hi(w.x), x[1], t);
+  t = fmaf(bf16lo(w.y), x[2], t);
+  t = fmaf(bf16hi(w.y), x[3], t);
+  t = fmaf(bf16lo(w.z), x[4], t);
+  t = fmaf(bf16hi(w.z), x[5], t);
+  t = fmaf(bf16lo(w.w), x[6], t);
+  t = fmaf(bf16hi(w.w), x[7], t);
+  return t;
 }
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
@@ -122,12 +152,18 @@ __device__ __forceinline__ void rope_cos_sin(int p, double inv_freq, float* c, f
 }
 
 // ----------------------------------------------------------------------------- GEMV
-template <int KIND>
-__device__ __forceinline__ int rows_per_unit() {
-  return (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
-}
+// A CTA owns the units [u0, u1).  Its rows are streamed as a sequence of
+// stages; each stage is ONE bulk copy of up to `rows_per_stage` consecutive
+// rows of one weight tensor (a "run").  Large single copies matter: the TMA
+// engine's throughput per SM grows with the size of each copy.
+struct StageDesc {
+  int ul0;    // first local unit of the stage
+  int nrows;  // rows in the stage (consecutive units)
+  int r;      // row slot within the unit (QKV: 0 = pair's first half, 1 = second; GLU: 0 = gate, 1 = up)
+  int pad;
+};
 
-// First element of row slot r (0 .. rows_per_unit-1) of unit u.
+// First element of row slot r of unit u.
 template <int KIND>
 __device__ __forceinline__ const uint16_t* unit_row(const GemvArgs& a, int u, int r) {
   const size_t K = static_cast<size_t>(a.K);
@@ -147,33 +183,60 @@ __device__ __forceinline__ const uint16_t* unit_row(const GemvArgs& a, int u, in
   }
 }
 
-template <int KIND, int BT>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+// Builds the stage table of a CTA (runs split into stages); returns the count.
+// QKV: per head touched, the run of first-half rows then the run of
+// second-half rows; GLU: gate rows then up rows; otherwise one run.
+template <int KIND>
+__device__ int build_stages(const GemvArgs& a, int u0, int n, int rps, StageDesc* out, int max_out) {
+  int cnt = 0;
+  auto add_run = [&](int ul0, int len, int r) {
+    for (int o = 0; o < len && cnt < max_out; o += rps) out[cnt++] = StageDesc{ul0 + o, min(rps, len - o), r, 0};
+  };
+  if constexpr (KIND == kKindQKV) {
+    const int half = a.D >> 1;
+    for (int ul = 0; ul < n;) {
+      const int end = min(n, ul + (half - (u0 + ul) % half));
+      add_run(ul, end - ul, 0);
+      add_run(ul, end - ul, 1);
+      ul = end;
+    }
+  } else if constexpr (KIND == kKindGLU) {
+    add_run(0, n, 0);
+    add_run(0, n, 1);
+  } else {
+    add_run(0, n, 0);
+  }
+  return cnt;
+}
+
+template <int KIND, int BT, bool XREG>
+__global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 256);
   int* is_last = reinterpret_cast<int*>(smem + 260);
+  int* n_stages_s = reinterpret_cast<int*>(smem + 264);
   float* red = reinterpret_cast<float*>(smem + 288);                    // 8 floats
   float* head_val = reinterpret_cast<float*>(smem + 320);               // [8][BT]
   uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 320 + 4 * kConsumerWarps * kMaxBatch);  // [8][BT]
+  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + kGemvHeaderBytes);
   float* xs = reinterpret_cast<float*>(smem + a.off_x);
   float* part = reinterpret_cast<float*>(smem + a.off_part);
   unsigned char* ring = smem + a.off_ring;
 
   constexpr int RU = (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
-  const int US = a.units_per_stage;
-  const int P = a.parts;
+  const int P = a.parts;                      // warps per row
+  const int NSLOT = kConsumerWarps / P;       // rows processed side by side
   const int CP = a.chunks_per_part;
   const int NS = a.n_slots;
   const int C = a.K / kChunkElems;
   const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
-  const uint32_t stage_bytes = static_cast<uint32_t>(US * RU) * row_bytes;
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.rows_per_stage) * row_bytes;
 
   const int u0 = static_cast<int>((static_cast<long long>(blockIdx.x) * a.n_units) / gridDim.x);
   const int u1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.n_units) / gridDim.x);
   const int n_cta_units = u1 - u0;
-  const int n_stages = (n_cta_units + US - 1) / US;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -183,9 +246,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_cons
       mbar_init(&empty[i], kConsumerWarps);
     }
     *abort_flag = 0;
+    *n_stages_s = build_stages<KIND>(a, u0, n_cta_units, a.rows_per_stage, desc, a.max_stages);
     fence_mbar_init();
   }
   __syncthreads();
+  const int n_stages = *n_stages_s;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer warp
@@ -200,27 +265,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_cons
         if (s >= NS) {
           if (!mbar_wait(&empty[slot], ((s / NS) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
         }
-        const int nu = min(US, n_cta_units - s * US);
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nu * RU) * row_bytes);
-        unsigned char* dst = ring + static_cast<size_t>(slot) * stage_bytes;
-        for (int r = 0; r < RU; ++r) {
-          const uint16_t* run = unit_row<KIND>(a, u0 + s * US, r);
-          int run_i = 0, run_len = 1;
-          for (int i = 1; i < nu; ++i) {
-            const uint16_t* p = unit_row<KIND>(a, u0 + s * US + i, r);
-            if (p == run + static_cast<size_t>(run_len) * a.K) {
-              ++run_len;
-            } else {
-              bulk_copy_g2s(dst + static_cast<size_t>(r * US + run_i) * row_bytes, run, run_len * row_bytes,
-                            &full[slot], policy);
-              run = p;
-              run_i = i;
-              run_len = 1;
-            }
-          }
-          bulk_copy_g2s(dst + static_cast<size_t>(r * US + run_i) * row_bytes, run, run_len * row_bytes,
-                        &full[slot], policy);
-        }
+        const StageDesc d = desc[s];
+        const uint32_t bytes = static_cast<uint32_t>(d.nrows) * row_bytes;
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        bulk_copy_g2s(ring + static_cast<size_t>(slot) * stage_bytes, unit_row<KIND>(a, u0 + d.ul0, d.r), bytes,
+                      &full[slot], policy);
         issued = s + 1;
         if (issued == min(NS, n_stages)) {
           pdl_launch_dependents();
@@ -253,10 +302,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_cons
   pdl_wait();
   pdl_launch_dependents();
   const int B = a.B;
+  const int K = a.K;
 
-  // Prologue: activations into shared memory, RMSNorm fused when requested.
+  // Prologue: activations into shared memory in the split layout (see
+  // xsplit), the RMSNorm folded in when requested.
   if (a.x_smem) {
-    const int K = a.K;
     for (int b = 0; b < B; ++b) {
       float* xb = xs + static_cast<size_t>(b) * K;
       if (a.tokens) {
@@ -266,24 +316,35 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_cons
         const uint16_t* er = a.embed + static_cast<size_t>(ok ? tok : 0) * K;
         for (int i = threadIdx.x; i < K; i += kConsumerThreads) {
           const float v = ok ? __uint_as_float(static_cast<uint32_t>(er[i]) << 16) : 0.f;
-          xb[i] = v;
+          xb[xsplit(i, K)] = v;
           if (blockIdx.x == 0 && a.resid_store) a.resid_store[static_cast<size_t>(b) * K + i] = v;
         }
       } else {
         const float* src = a.x + static_cast<size_t>(b) * K;
-        for (int i = threadIdx.x; i < K; i += kConsumerThreads) xb[i] = src[i];
+        for (int i = threadIdx.x; i < K; i += kConsumerThreads) xb[xsplit(i, K)] = src[i];
       }
       if (a.norm_gamma) {
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        const float inv = block_rms_inv(xb, K, a.eps, red);
-        for (int i = threadIdx.x; i < K; i += kConsumerThreads)
-          xb[i] = (xb[i] * inv) * __uint_as_float(static_cast<uint32_t>(a.norm_gamma[i]) << 16);
+        const float inv = block_rms_inv<true>(xb, K, a.eps, red);
+        for (int i = threadIdx.x; i < K; i += kConsumerThreads) {
+          const int e = xsplit(i, K);
+          xb[e] = (xb[e] * inv) * __uint_as_float(static_cast<uint32_t>(a.norm_gamma[i]) << 16);
+        }
       }
     }
     for (int b = B; b < BT; ++b)
       for (int i = threadIdx.x; i < K; i += kConsumerThreads) xs[static_cast<size_t>(b) * K + i] = 0.f;
   }
   asm volatile("bar.sync 1, 256;" ::: "memory");
+
+  // Fixed roles: warp w always takes part (w % P) of rows w / P, w / P +
+  // NSLOT, ... of every stage, so its slice of the activations never changes
+  // and can live in registers.
+  const int my_p = warp % P;
+  const int my_slot = warp / P;
+  const int cb = my_p * CP;
+  const int ce = min(C, cb + CP);
+  const int nit = ce > cb ? (ce - cb + 31) / 32 : 0;
 
   float best_v[BT];
   uint32_t best_i[BT];
@@ -293,88 +354,165 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_cons
     best_i[b] = 0xFFFFFFFFu;
   }
 
-  const int tasks_full_stage = US * RU * P;
   bool ok = true;
-  for (int s = 0; s < n_stages && ok; ++s) {
-    const int slot = s % NS;
-    const int nu = min(US, n_cta_units - s * US);
-    const int ntask = nu * RU * P;
-    const int rot = static_cast<int>((static_cast<long long>(s) * tasks_full_stage) % kConsumerWarps);
-    const int j0 = (warp - rot + kConsumerWarps) % kConsumerWarps;
-    // lane 0 polls (bounded); the verdict is warp-uniform
-    int w_ok = 1;
-    if (lane == 0) w_ok = mbar_wait(&full[slot], (s / NS) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
-    w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-    if (!w_ok) {
-      ok = false;
-      break;
-    }
-    (void)mbar_try_wait(&full[slot], (s / NS) & 1);  // completed phase: acquire for every lane
-    const unsigned char* stage = ring + static_cast<size_t>(slot) * stage_bytes;
-    for (int j = j0; j < ntask; j += kConsumerWarps) {
-      const int lr = j / P;
-      const int p = j - lr * P;
-      const int r = lr / nu;
-      const int i = lr - r * nu;
-      const uint4* wr = reinterpret_cast<const uint4*>(stage + static_cast<size_t>(r * US + i) * row_bytes);
-      const int cb = p * CP;
-      const int ce = min(C, cb + CP);
-      float acc[BT];
+  if constexpr (XREG) {
+    // ---- register path (b <= 2): the warp's activation slice lives in
+    // registers; a stage's rows are copied to registers and the stage is
+    // released BEFORE the arithmetic, so the math never holds up the ring.
+    float xr[kXregIt][BT][8];
 #pragma unroll
-      for (int b = 0; b < BT; ++b) acc[b] = 0.f;
-      for (int c = cb + lane; c < ce; c += 32) {
-        const uint4 w = wr[c];
-        const float w0 = bf16lo(w.x), w1 = bf16hi(w.x), w2 = bf16lo(w.y), w3 = bf16hi(w.y);
-        const float w4 = bf16lo(w.z), w5 = bf16hi(w.z), w6 = bf16lo(w.w), w7 = bf16hi(w.w);
+    for (int it = 0; it < kXregIt; ++it) {
+      const int c = cb + lane + 32 * it;
+      const bool in = it < nit && c < ce;
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          float4 x0, x1;
+      for (int b = 0; b < BT; ++b) {
+        float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+        if (in) {
           if (a.x_smem) {
-            const float4* xp = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * a.K) + 2 * c;
-            x0 = xp[0];
-            x1 = xp[1];
-          } else {
-            const float4* xp = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * a.K) + 2 * c;
-            x0 = __ldg(xp);
-            x1 = __ldg(xp + 1);
+            lo = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K)[c];
+            hi = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K + K / 2)[c];
+          } else if (b < B) {
+            const float4* xp = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * K) + 2 * c;
+            lo = xp[0];
+            hi = xp[1];
           }
-          float t = acc[b];
-          t = fmaf(w0, x0.x, t);
-          t = fmaf(w1, x0.y, t);
-          t = fmaf(w2, x0.z, t);
-          t = fmaf(w3, x0.w, t);
-          t = fmaf(w4, x1.x, t);
-          t = fmaf(w5, x1.y, t);
-          t = fmaf(w6, x1.z, t);
-          t = fmaf(w7, x1.w, t);
-          acc[b] = t;
+        }
+        xr[it][b][0] = lo.x; xr[it][b][1] = lo.y; xr[it][b][2] = lo.z; xr[it][b][3] = lo.w;
+        xr[it][b][4] = hi.x; xr[it][b][5] = hi.y; xr[it][b][6] = hi.z; xr[it][b][7] = hi.w;
+      }
+    }
+    for (int s = 0; s < n_stages; ++s) {
+      const int slot = s % NS;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&full[slot], (s / NS) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      if (!w_ok) {
+        ok = false;
+        break;
+      }
+      (void)mbar_try_wait(&full[slot], (s / NS) & 1);  // completed phase: acquire for every lane
+      const StageDesc d = desc[s];
+      // rows of this warp: i with (i + rot) % NSLOT == my_slot, at most kXregRows
+      const int rot = (s * a.rows_per_stage) % NSLOT;
+      const int first = (my_slot - rot + NSLOT) % NSLOT;
+      uint4 wv[kXregRows][kXregIt];
+      int nmine = 0;
+#pragma unroll
+      for (int k = 0; k < kXregRows; ++k) {
+        const int i = first + k * NSLOT;
+        const bool have = i < d.nrows;
+        const uint4* wr = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes +
+                                                         static_cast<size_t>(have ? i : 0) * row_bytes);
+#pragma unroll
+        for (int it = 0; it < kXregIt; ++it) {
+          const int c = cb + lane + 32 * it;
+          wv[k][it] = (have && it < nit && c < ce) ? wr[c] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        nmine += have ? 1 : 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+#pragma unroll
+      for (int k = 0; k < kXregRows; ++k) {
+        if (k < nmine) {
+          float acc[BT];
+#pragma unroll
+          for (int b = 0; b < BT; ++b) acc[b] = 0.f;
+#pragma unroll
+          for (int it = 0; it < kXregIt; ++it) {
+            if (it < nit) {
+#pragma unroll
+              for (int b = 0; b < BT; ++b) acc[b] += dot8(wv[k][it], xr[it][b]);
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < BT; ++b) acc[b] = warp_sum(acc[b]);
+          const int ul = d.ul0 + first + k * NSLOT;
+          if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = acc[b];
+          }
         }
       }
+    }
+  } else {
+    // ---- shared-memory path (b > 2 or very long rows): activations read
+    // from shared or global memory chunk by chunk; a stage is released after
+    // its rows are done.
+    for (int s = 0; s < n_stages && ok; ++s) {
+      const int slot = s % NS;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&full[slot], (s / NS) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      if (!w_ok) {
+        ok = false;
+        break;
+      }
+      (void)mbar_try_wait(&full[slot], (s / NS) & 1);  // completed phase: acquire for every lane
+      const StageDesc d = desc[s];
+      for (int i = my_slot; i < d.nrows; i += NSLOT) {
+        const uint4* wr = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes +
+                                                         static_cast<size_t>(i) * row_bytes);
+        float acc[BT];
 #pragma unroll
-      for (int b = 0; b < BT; ++b) acc[b] = warp_sum(acc[b]);
-      const int ul = s * US + i;
-      if constexpr (KIND == kKindHead) {
-        const uint32_t row = static_cast<uint32_t>(u0 + ul);
+        for (int b = 0; b < BT; ++b) acc[b] = 0.f;
+        for (int it0 = 0; it0 < nit; it0 += kMaxIt) {
+          uint4 wv[kMaxIt];
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          if (b < B) {
-            if (a.logits && lane == 0) a.logits[static_cast<size_t>(b) * a.n_units + row] = acc[b];
-            // rows of one warp arrive in increasing order: strict > keeps the lowest index
-            if (acc[b] > best_v[b] || best_i[b] == 0xFFFFFFFFu) {
-              best_v[b] = acc[b];
-              best_i[b] = row;
+          for (int it = 0; it < kMaxIt; ++it) {
+            const int c = cb + lane + 32 * (it0 + it);
+            wv[it] = (it0 + it < nit && c < ce) ? wr[c] : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int it = 0; it < kMaxIt; ++it) {
+            if (it0 + it < nit) {
+              const int c = min(cb + lane + 32 * (it0 + it), C - 1);
+#pragma unroll
+              for (int b = 0; b < BT; ++b) {
+                float xv[8];
+                float4 lo, hi;
+                if (a.x_smem) {
+                  lo = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K)[c];
+                  hi = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K + K / 2)[c];
+                } else {
+                  const float4* xp = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * K) + 2 * c;
+                  lo = __ldg(xp);
+                  hi = __ldg(xp + 1);
+                }
+                xv[0] = lo.x; xv[1] = lo.y; xv[2] = lo.z; xv[3] = lo.w;
+                xv[4] = hi.x; xv[5] = hi.y; xv[6] = hi.z; xv[7] = hi.w;
+                acc[b] += dot8(wv[it], xv);
+              }
             }
           }
         }
-      } else {
-        if (lane == 0) {
 #pragma unroll
-          for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + r) * P + p) * BT + b] = acc[b];
+        for (int b = 0; b < BT; ++b) acc[b] = warp_sum(acc[b]);
+        const int ul = d.ul0 + i;
+        if constexpr (KIND == kKindHead) {
+          const uint32_t row = static_cast<uint32_t>(u0 + ul);
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            if (b < B) {
+              if (a.logits && lane == 0) a.logits[static_cast<size_t>(b) * a.n_units + row] = acc[b];
+              // a warp's rows arrive in increasing order: strict > keeps the lowest index
+              if (acc[b] > best_v[b] || best_i[b] == 0xFFFFFFFFu) {
+                best_v[b] = acc[b];
+                best_i[b] = row;
+              }
+            }
+          }
+        } else {
+          if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+              part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = acc[b];
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
   }
 
   asm volatile("bar.sync 2, 288;" ::: "memory");  // ring no longer read: the producer may drain and leave
@@ -382,6 +520,39 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const __grid_cons
 
   // --------------------------------------------------------------- epilogues
   if constexpr (KIND == kKindHead) {
+    if constexpr (XREG) {
+      // logits from the partial sums: thread t takes rows t, t+256, ...
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      for (int ul = threadIdx.x; ul < n_cta_units; ul += kConsumerThreads) {
+        const uint32_t row = static_cast<uint32_t>(u0 + ul);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          if (b < B) {
+            float v = 0.f;
+            for (int p = 0; p < P; ++p) v += part[(static_cast<size_t>(ul) * P + p) * BT + b];
+            if (a.logits) a.logits[static_cast<size_t>(b) * a.n_units + row] = v;
+            if (v > best_v[b] || best_i[b] == 0xFFFFFFFFu) {  // increasing rows: strict > keeps the lowest
+              best_v[b] = v;
+              best_i[b] = row;
+            }
+          }
+        }
+      }
+      // warp-level argmax (value, then lower index) into lane 0
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, best_v[b], o);
+          const uint32_t oi = __shfl_xor_sync(0xffffffffu, best_i[b], o);
+          if (oi != 0xFFFFFFFFu &&
+              (best_i[b] == 0xFFFFFFFFu || ov > best_v[b] || (ov == best_v[b] && oi < best_i[b]))) {
+            best_v[b] = ov;
+            best_i[b] = oi;
+          }
+        }
+      }
+    }
     if (lane == 0) {
 #pragma unroll
       for (int b = 0; b < BT; ++b) {

@@ -29,11 +29,32 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-// One GEMV launch of kind KIND for batch bucket BT (1, 2, 4, 8 or 16).
-cudaError_t launch_gemv_qkv(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
-cudaError_t launch_gemv_glu(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
-cudaError_t launch_gemv_resid(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
-cudaError_t launch_gemv_head(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl);
+// Lets a kernel use up to kSmemMax bytes of dynamic shared memory and asks
+// for the largest shared-memory carveout, so that every SM is configured the
+// same way and CTAs of consecutive kernels can be resident side by side (the
+// next kernel's weight stream starts while the current one finishes).
+template <typename Kern>
+cudaError_t prefer_max_carveout(Kern kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
+template <typename Kern>
+cudaError_t allow_smem(Kern kernel) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
+// One GEMV launch for batch bucket BT (1, 2, 4, 8 or 16); xreg selects the
+// register-resident activation variant (BT <= 2).
+cudaError_t launch_gemv_qkv(int BT, bool xreg, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st,
+                             bool pdl);
+cudaError_t launch_gemv_glu(int BT, bool xreg, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st,
+                             bool pdl);
+cudaError_t launch_gemv_resid(int BT, bool xreg, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st,
+                             bool pdl);
+cudaError_t launch_gemv_head(int BT, bool xreg, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st,
+                             bool pdl);
 cudaError_t launch_attn(const AttnArgs& a, int B, uint32_t smem, cudaStream_t st, bool pdl);
 
 // Raise the dynamic shared-memory limit of every kernel of a unit (once per device).

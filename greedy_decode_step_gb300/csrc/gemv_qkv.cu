@@ -3,25 +3,31 @@
 
 namespace dec {
 
-cudaError_t launch_gemv_qkv(int BT, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st, bool pdl) {
+cudaError_t launch_gemv_qkv(int BT, bool xreg, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st,
+                             bool pdl) {
   const dim3 g(grid), b(kGemvThreads);
   switch (BT) {
-    case 1: return launch(gemv_kernel<kKindQKV, 1>, g, b, smem, st, pdl, a);
-    case 2: return launch(gemv_kernel<kKindQKV, 2>, g, b, smem, st, pdl, a);
-    case 4: return launch(gemv_kernel<kKindQKV, 4>, g, b, smem, st, pdl, a);
-    case 8: return launch(gemv_kernel<kKindQKV, 8>, g, b, smem, st, pdl, a);
-    default: return launch(gemv_kernel<kKindQKV, 16>, g, b, smem, st, pdl, a);
+    case 1:
+      return xreg ? launch(gemv_kernel<kKindQKV, 1, true>, g, b, smem, st, pdl, a)
+                  : launch(gemv_kernel<kKindQKV, 1, false>, g, b, smem, st, pdl, a);
+    case 2:
+      return xreg ? launch(gemv_kernel<kKindQKV, 2, true>, g, b, smem, st, pdl, a)
+                  : launch(gemv_kernel<kKindQKV, 2, false>, g, b, smem, st, pdl, a);
+    case 4: return launch(gemv_kernel<kKindQKV, 4, false>, g, b, smem, st, pdl, a);
+    case 8: return launch(gemv_kernel<kKindQKV, 8, false>, g, b, smem, st, pdl, a);
+    default: return launch(gemv_kernel<kKindQKV, 16, false>, g, b, smem, st, pdl, a);
   }
 }
 
 cudaError_t allow_smem_qkv() {
   cudaError_t e;
-  const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 1>, at, kSmemMax)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 2>, at, kSmemMax)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 4>, at, kSmemMax)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<kKindQKV, 8>, at, kSmemMax)) != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_kernel<kKindQKV, 16>, at, kSmemMax);
+  if ((e = allow_smem(gemv_kernel<kKindQKV, 1, true>)) != cudaSuccess) return e;
+  if ((e = allow_smem(gemv_kernel<kKindQKV, 1, false>)) != cudaSuccess) return e;
+  if ((e = allow_smem(gemv_kernel<kKindQKV, 2, true>)) != cudaSuccess) return e;
+  if ((e = allow_smem(gemv_kernel<kKindQKV, 2, false>)) != cudaSuccess) return e;
+  if ((e = allow_smem(gemv_kernel<kKindQKV, 4, false>)) != cudaSuccess) return e;
+  if ((e = allow_smem(gemv_kernel<kKindQKV, 8, false>)) != cudaSuccess) return e;
+  return allow_smem(gemv_kernel<kKindQKV, 16, false>);
 }
 
 }  // namespace dec
