@@ -156,6 +156,7 @@ int device_info(DeviceInfo** out) {
     DEC_CUDA(allow_smem_resid());
     DEC_CUDA(allow_smem_head());
     DEC_CUDA(allow_smem_attn());
+    DEC_CUDA(allow_smem_step());
     DEC_CUDA(prefer_max_carveout(add_rmsnorm_kernel));
     DEC_CUDA(prefer_max_carveout(advance_kernel));
     DEC_CUDA(prefer_max_carveout(set_tokens_kernel));
@@ -217,10 +218,10 @@ struct GemvPlan {
 // A ring stage is one bulk copy of about kCopyTarget bytes.
 int plan_gemv(int kind, GemvArgs& a, int BT, int sms, bool want_x_smem, GemvPlan* pl) {
   const int RU = (kind == kKindQKV || kind == kKindGLU) ? 2 : 1;
-  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
-  const int C = a.K / kChunkElems;
-  const bool norm_in = a.norm_gamma != nullptr || a.tokens != nullptr;
-  const uint32_t x_bytes = static_cast<uint32_t>(BT) * static_cast<uint32_t>(a.K) * 4u;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.sh.K) * 2u;
+  const int C = a.sh.K / kChunkElems;
+  const bool norm_in = a.io.norm_gamma != nullptr || a.io.tokens != nullptr;
+  const uint32_t x_bytes = static_cast<uint32_t>(BT) * static_cast<uint32_t>(a.sh.K) * 4u;
   const bool x_fits = want_x_smem && x_bytes <= kXSmemMax;
   int p_reg = 1;
   while (p_reg < kConsumerWarps && (C + p_reg - 1) / p_reg > 32 * kXregIt) p_reg *= 2;
@@ -228,41 +229,39 @@ int plan_gemv(int kind, GemvArgs& a, int BT, int sms, bool want_x_smem, GemvPlan
   int nslot;
   if (xreg) {
     nslot = kConsumerWarps / p_reg;
-    a.rows_per_stage = std::max(1, std::min<int>(static_cast<int>(kCopyTarget / row_bytes), kXregRows * nslot));
-    a.x_smem = norm_in ? 1 : 0;
+    a.sh.rows_per_stage = std::max(1, std::min<int>(static_cast<int>(kCopyTarget / row_bytes), kXregRows * nslot));
+    a.io.x_smem = norm_in ? 1 : 0;
   } else {
     nslot = kConsumerWarps;
     if (kind != kKindHead)
       while (nslot > 1 && static_cast<uint32_t>(nslot) * row_bytes > kPartTarget) nslot /= 2;
     const int m = std::max<int>(1, static_cast<int>(kCopyTarget / (static_cast<uint32_t>(nslot) * row_bytes)));
-    a.rows_per_stage = nslot * m;
-    a.x_smem = x_fits ? 1 : 0;
+    a.sh.rows_per_stage = nslot * m;
+    a.io.x_smem = x_fits ? 1 : 0;
   }
   pl->xreg = xreg;
-  a.parts = kConsumerWarps / nslot;
-  a.chunks_per_part = (C + a.parts - 1) / a.parts;
-  const uint32_t stage_bytes = static_cast<uint32_t>(a.rows_per_stage) * row_bytes;
+  a.sh.parts = kConsumerWarps / nslot;
+  a.sh.chunks_per_part = (C + a.sh.parts - 1) / a.sh.parts;
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.sh.rows_per_stage) * row_bytes;
   const bool uses_part = kind != kKindHead || xreg;
-  int upc = (a.n_units + sms - 1) / sms;
+  int upc = (a.sh.n_units + sms - 1) / sms;
   if (uses_part) {
-    const int max_upc = std::max<int>(1, static_cast<int>(kPartMaxBytes / (RU * a.parts * BT * 4)));
+    const int max_upc = std::max<int>(1, static_cast<int>(kPartMaxBytes / (RU * a.sh.parts * BT * 4)));
     upc = std::min(upc, max_upc);
   }
-  const int grid = (a.n_units + upc - 1) / upc;
-  a.units_per_cta = (a.n_units + grid - 1) / grid;
-  // stage table: full stages plus at most one partial stage per run
-  const int runs = kind == kKindQKV ? 2 * (a.units_per_cta / std::max(1, a.D / 2) + 2) : RU;
-  a.max_stages = (a.units_per_cta * RU + a.rows_per_stage - 1) / a.rows_per_stage + runs;
-  const uint32_t part_bytes = uses_part ? static_cast<uint32_t>(a.units_per_cta * RU * a.parts * BT) * 4u : 0u;
-  a.off_x = align_up(kGemvHeaderBytes + static_cast<uint32_t>(a.max_stages) * sizeof(StageDesc), 16);
-  a.off_part = align_up(a.off_x + (a.x_smem ? x_bytes : 0u), 16);
+  const int grid = (a.sh.n_units + upc - 1) / upc;
+  a.units_per_cta = (a.sh.n_units + grid - 1) / grid;
+  const uint32_t part_bytes = uses_part ? static_cast<uint32_t>(a.units_per_cta * RU * a.sh.parts * BT) * 4u : 0u;
+  a.off_x = kGemvHeaderBytes;
+  a.off_part = align_up(a.off_x + (a.io.x_smem ? x_bytes : 0u), 16);
   a.off_ring = align_up(a.off_part + part_bytes, 128);
   int ns = static_cast<int>(kRingTarget / stage_bytes);
   ns = std::max(2, std::min(ns, kMaxStages));
   while (ns > 2 && a.off_ring + static_cast<uint32_t>(ns) * stage_bytes > kSmemMax) --ns;
   DEC_CHECK(a.off_ring + static_cast<uint32_t>(ns) * stage_bytes <= kSmemMax, DEC_EUNSUPPORTED,
-            "row of %d elements too long for the shared-memory ring", a.K);
+            "row of %d elements too long for the shared-memory ring", a.sh.K);
   a.n_slots = ns;
+  a.slot_bytes = stage_bytes;
   pl->grid = grid;
   pl->smem = a.off_ring + static_cast<uint32_t>(ns) * stage_bytes;
   return DEC_OK;
@@ -270,12 +269,12 @@ int plan_gemv(int kind, GemvArgs& a, int BT, int sms, bool want_x_smem, GemvPlan
 
 int run_gemv(int kind, GemvArgs& a, int B, const DeviceInfo* dv, bool want_x_smem, cudaStream_t st, bool pdl) {
   const int BT = bt_bucket(B);
-  a.B = B;
-  a.err = dv->err;
+  a.io.B = B;
+  a.io.err = dv->err;
   GemvPlan pl;
   DEC_TRY(plan_gemv(kind, a, BT, dv->sms, want_x_smem, &pl));
-  DEC_CHECK(!(a.norm_gamma || a.tokens) || a.x_smem, DEC_EUNSUPPORTED,
-            "fused RMSNorm needs the activations in shared memory (B=%d, K=%d)", B, a.K);
+  DEC_CHECK(!(a.io.norm_gamma || a.io.tokens) || a.io.x_smem, DEC_EUNSUPPORTED,
+            "fused RMSNorm needs the activations in shared memory (B=%d, K=%d)", B, a.sh.K);
   cudaError_t e;
   switch (kind) {
     case kKindQKV: e = launch_gemv_qkv(BT, pl.xreg, a, pl.grid, pl.smem, st, pdl); break;
@@ -350,6 +349,8 @@ struct StateWs {
   float* h;
   float* y;
   float* attn_part;
+  unsigned int* grid_bar;
+  int* abort_all;
   int n_split;
   size_t bytes;
 };
@@ -369,6 +370,8 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   const size_t o_y = c.take(sizeof(float) * B * m->hidden);
   w.n_split = attn_splits(B, m->n_kv_heads, S_max, sms, 0);
   const size_t o_part = c.take(attn_part_bytes(B, m->n_heads, m->n_kv_heads, m->head_dim, w.n_split));
+  const size_t o_gbar = c.take(sizeof(unsigned int));
+  const size_t o_abort = c.take(sizeof(int));
   w.bytes = c.off;
   if (base) {
     w.ctrl = reinterpret_cast<Ctrl*>(base + o_ctrl);
@@ -381,6 +384,8 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
     w.h = reinterpret_cast<float*>(base + o_h);
     w.y = reinterpret_cast<float*>(base + o_y);
     w.attn_part = reinterpret_cast<float*>(base + o_part);
+    w.grid_bar = reinterpret_cast<unsigned int*>(base + o_gbar);
+    w.abort_all = reinterpret_cast<int*>(base + o_abort);
   }
   return w;
 }
@@ -463,9 +468,126 @@ int check_state(const dec_model* m, const dec_state* s, bool need_internal) {
 
 // ------------------------------------------------------------------------------- the step
 
+// ------------------------------------------------------------------------------- persistent step kernel
+
+// Plan of one phase of the step kernel (register path only); false if the
+// row length does not fit it.
+bool step_phase_plan(int K, int n_units, int RU, int BT, int sms, StepPlan* out, uint32_t* part_bytes) {
+  const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
+  const int C = K / kChunkElems;
+  int p = 1;
+  while (p < kConsumerWarps && (C + p - 1) / p > 32 * kXregIt) p *= 2;
+  if ((C + p - 1) / p > 32 * kXregIt) return false;
+  const int nslot = kConsumerWarps / p;
+  const int rps = std::min<int>(static_cast<int>(kStepSlotBytes / row_bytes), kXregRows * nslot);
+  if (rps < 1) return false;
+  out->parts = p;
+  out->chunks_per_part = (C + p - 1) / p;
+  out->rows_per_stage = rps;
+  const int upc = (n_units + sms - 1) / sms;
+  *part_bytes = static_cast<uint32_t>(upc * RU * p * BT) * 4u;
+  return true;
+}
+
+// Fills the step kernel's arguments; false if the model / batch is outside
+// what it handles (then the step runs as single-op kernels).
+bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, StepArgs* a,
+               uint32_t* smem, int* BT) {
+  const int B = s->batch;
+  if (B > 2 || m->n_layers > kStepMaxLayers) return false;
+  *BT = bt_bucket(B);
+  const int H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
+  uint32_t part = 0, pb = 0;
+  if (!step_phase_plan(H, (Hq + 2 * Hkv) * (D / 2), 2, *BT, dv->sms, &a->plan[kPhQKV], &pb)) return false;
+  part = std::max(part, pb);
+  if (!step_phase_plan(Hq * D, H, 1, *BT, dv->sms, &a->plan[kPhO], &pb)) return false;
+  part = std::max(part, pb);
+  if (!step_phase_plan(H, I, 2, *BT, dv->sms, &a->plan[kPhGLU], &pb)) return false;
+  part = std::max(part, pb);
+  if (!step_phase_plan(I, H, 1, *BT, dv->sms, &a->plan[kPhDown], &pb)) return false;
+  part = std::max(part, pb);
+  if (m->lm_head) {
+    if (!step_phase_plan(H, m->vocab, 1, *BT, dv->sms, &a->plan[kPhHead], &pb)) return false;
+    part = std::max(part, pb);
+  }
+  const uint32_t x_bytes = static_cast<uint32_t>(*BT) * H * 4u;
+  const uint32_t attn_bytes = 256u + kAttnMaxGroup * D * 4u + kAttnMaxGroup * kAttnTile * 4u +
+                              2u * 2u * kAttnTile * D * 2u;
+  a->off_x = kStepHeaderBytes;
+  a->off_part = align_up(a->off_x + x_bytes, 16);
+  a->off_attn = align_up(a->off_part + part, 128);
+  a->off_ring = align_up(a->off_attn + attn_bytes, 128);
+  if (a->off_ring + 2 * kStepSlotBytes > kSmemMax) return false;
+  a->n_slots = std::min<int>(4, static_cast<int>((kSmemMax - a->off_ring) / kStepSlotBytes));
+  // the log-sum-exp merge uses the tile area as scratch
+  if (2u * (static_cast<uint32_t>(w.n_split) * (Hq / Hkv) + Hq / Hkv) * 4u > 2u * 2u * kAttnTile * D * 2u) return false;
+  *smem = a->off_ring + static_cast<uint32_t>(a->n_slots) * kStepSlotBytes;
+  a->L = m->n_layers;
+  a->H = H;
+  a->Hq = Hq;
+  a->Hkv = Hkv;
+  a->D = D;
+  a->I = I;
+  a->V = m->vocab;
+  a->B = B;
+  a->S_max = s->max_seq;
+  a->eps = m->rms_eps;
+  a->embed = static_cast<const uint16_t*>(m->embed);
+  a->final_norm = static_cast<const uint16_t*>(m->final_norm);
+  a->lm_head = static_cast<const uint16_t*>(m->lm_head);
+  a->token = s->token;
+  a->pos = s->pos;
+  a->resid = s->residual;
+  a->q = w.q;
+  a->o = w.o;
+  a->h = w.h;
+  a->attn_part = w.attn_part;
+  a->attn_tickets = w.attn_tickets;
+  a->n_split = w.n_split;
+  a->attn_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  a->argmax_keys = w.keys;
+  a->head_ticket = w.head_ticket;
+  a->book.enabled = 1;
+  a->book.token = s->token;
+  a->book.pos = s->pos;
+  a->book.done = w.done;
+  a->book.ctrl = w.ctrl;
+  a->grid_bar = w.grid_bar;
+  a->abort_all = w.abort_all;
+  a->err = dv->err;
+  for (int i = 0; i < D / 2; ++i) a->inv_freq[i] = std::pow(static_cast<double>(m->rope_theta), -2.0 * i / D);
+  for (int l = 0; l < m->n_layers; ++l) {
+    const dec_layer_weights& lw = m->layers[l];
+    StepLayer& L = a->layers[l];
+    L.attn_norm = static_cast<const uint16_t*>(lw.attn_norm);
+    L.wq = static_cast<const uint16_t*>(lw.wq);
+    L.wk = static_cast<const uint16_t*>(lw.wk);
+    L.wv = static_cast<const uint16_t*>(lw.wv);
+    L.wo = static_cast<const uint16_t*>(lw.wo);
+    L.mlp_norm = static_cast<const uint16_t*>(lw.mlp_norm);
+    L.wg = static_cast<const uint16_t*>(lw.wg);
+    L.wu = static_cast<const uint16_t*>(lw.wu);
+    L.wd = static_cast<const uint16_t*>(lw.wd);
+    L.kc = static_cast<uint16_t*>(s->k_cache[l]);
+    L.vc = static_cast<uint16_t*>(s->v_cache[l]);
+  }
+  return true;
+}
+
 // Layers of one step; with `head`, also the LM head and the bookkeeping.
 int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
                  cudaStream_t st) {
+  if (head || !m->lm_head) {
+    // b <= 2: the whole step is one persistent kernel
+    static thread_local StepArgs sa;  // ~6 KB: kept off the stack
+    uint32_t smem = 0;
+    int BT = 1;
+    if (plan_step(m, s, dv, w, &sa, &smem, &BT)) {
+      cudaError_t e = launch_step(BT, sa, dv->sms, smem, st);
+      DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "step kernel launch: %s", cudaGetErrorString(e));
+      return DEC_OK;
+    }
+  }
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
   const bool fuse = norm_fusable(B, H);
   const bool pdl = true;
@@ -475,34 +597,34 @@ int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, c
     // attention block
     {
       GemvArgs a{};
-      a.w0 = static_cast<const uint16_t*>(lw.wq);
-      a.w1 = static_cast<const uint16_t*>(lw.wk);
-      a.w2 = static_cast<const uint16_t*>(lw.wv);
-      a.K = H;
-      a.n_units = (Hq + 2 * Hkv) * (D / 2);
-      a.out = w.q;
-      a.k_cache = static_cast<uint16_t*>(s->k_cache[l]);
-      a.v_cache = static_cast<uint16_t*>(s->v_cache[l]);
-      a.pos = s->pos;
-      a.Hq = Hq;
-      a.Hkv = Hkv;
-      a.D = D;
-      a.S_max = s->max_seq;
+      a.sh.w0 = static_cast<const uint16_t*>(lw.wq);
+      a.sh.w1 = static_cast<const uint16_t*>(lw.wk);
+      a.sh.w2 = static_cast<const uint16_t*>(lw.wv);
+      a.sh.K = H;
+      a.sh.n_units = (Hq + 2 * Hkv) * (D / 2);
+      a.io.out = w.q;
+      a.io.k_cache = static_cast<uint16_t*>(s->k_cache[l]);
+      a.io.v_cache = static_cast<uint16_t*>(s->v_cache[l]);
+      a.io.pos = s->pos;
+      a.sh.Hq = Hq;
+      a.sh.Hkv = Hkv;
+      a.sh.D = D;
+      a.io.S_max = s->max_seq;
       fill_inv_freq(a, D, m->rope_theta);
       if (fuse) {
-        a.x = s->residual;
-        a.norm_gamma = static_cast<const uint16_t*>(lw.attn_norm);
-        a.eps = m->rms_eps;
+        a.io.x = s->residual;
+        a.io.norm_gamma = static_cast<const uint16_t*>(lw.attn_norm);
+        a.io.eps = m->rms_eps;
         if (gather) {
-          a.tokens = s->token;
-          a.embed = static_cast<const uint16_t*>(m->embed);
-          a.vocab = m->vocab;
-          a.resid_store = s->residual;
+          a.io.tokens = s->token;
+          a.io.embed = static_cast<const uint16_t*>(m->embed);
+          a.io.vocab = m->vocab;
+          a.io.resid_store = s->residual;
         }
       } else {
         DEC_TRY(run_norm(nullptr, s->residual, static_cast<const uint16_t*>(lw.attn_norm), w.y, B, H, m->rms_eps,
                          gather ? s->token : nullptr, static_cast<const uint16_t*>(m->embed), m->vocab, dv, st, pdl));
-        a.x = w.y;
+        a.io.x = w.y;
       }
       DEC_TRY(run_gemv(kKindQKV, a, B, dv, true, st, pdl));
 
@@ -523,62 +645,62 @@ int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, c
       DEC_TRY(run_attn(t, B, dv, st, pdl));
 
       GemvArgs r{};
-      r.w0 = static_cast<const uint16_t*>(lw.wo);
-      r.K = Hq * D;
-      r.n_units = H;
-      r.x = w.o;
-      r.out = s->residual;
+      r.sh.w0 = static_cast<const uint16_t*>(lw.wo);
+      r.sh.K = Hq * D;
+      r.sh.n_units = H;
+      r.io.x = w.o;
+      r.io.out = s->residual;
       DEC_TRY(run_gemv(kKindResid, r, B, dv, true, st, pdl));
     }
     // MLP block
     {
       GemvArgs a{};
-      a.w0 = static_cast<const uint16_t*>(lw.wg);
-      a.w1 = static_cast<const uint16_t*>(lw.wu);
-      a.K = H;
-      a.n_units = I;
-      a.out = w.h;
+      a.sh.w0 = static_cast<const uint16_t*>(lw.wg);
+      a.sh.w1 = static_cast<const uint16_t*>(lw.wu);
+      a.sh.K = H;
+      a.sh.n_units = I;
+      a.io.out = w.h;
       if (fuse) {
-        a.x = s->residual;
-        a.norm_gamma = static_cast<const uint16_t*>(lw.mlp_norm);
-        a.eps = m->rms_eps;
+        a.io.x = s->residual;
+        a.io.norm_gamma = static_cast<const uint16_t*>(lw.mlp_norm);
+        a.io.eps = m->rms_eps;
       } else {
         DEC_TRY(run_norm(nullptr, s->residual, static_cast<const uint16_t*>(lw.mlp_norm), w.y, B, H, m->rms_eps,
                          nullptr, nullptr, 0, dv, st, pdl));
-        a.x = w.y;
+        a.io.x = w.y;
       }
       DEC_TRY(run_gemv(kKindGLU, a, B, dv, true, st, pdl));
 
       GemvArgs r{};
-      r.w0 = static_cast<const uint16_t*>(lw.wd);
-      r.K = I;
-      r.n_units = H;
-      r.x = w.h;
-      r.out = s->residual;
+      r.sh.w0 = static_cast<const uint16_t*>(lw.wd);
+      r.sh.K = I;
+      r.sh.n_units = H;
+      r.io.x = w.h;
+      r.io.out = s->residual;
       DEC_TRY(run_gemv(kKindResid, r, B, dv, true, st, pdl));
     }
   }
   if (head && m->lm_head) {
     GemvArgs a{};
-    a.w0 = static_cast<const uint16_t*>(m->lm_head);
-    a.K = H;
-    a.n_units = m->vocab;
+    a.sh.w0 = static_cast<const uint16_t*>(m->lm_head);
+    a.sh.K = H;
+    a.sh.n_units = m->vocab;
     if (fuse) {
-      a.x = s->residual;
-      a.norm_gamma = static_cast<const uint16_t*>(m->final_norm);
-      a.eps = m->rms_eps;
+      a.io.x = s->residual;
+      a.io.norm_gamma = static_cast<const uint16_t*>(m->final_norm);
+      a.io.eps = m->rms_eps;
     } else {
       DEC_TRY(run_norm(nullptr, s->residual, static_cast<const uint16_t*>(m->final_norm), w.y, B, H, m->rms_eps,
                        nullptr, nullptr, 0, dv, st, pdl));
-      a.x = w.y;
+      a.io.x = w.y;
     }
-    a.argmax_keys = w.keys;
-    a.ticket = w.head_ticket;
-    a.book.enabled = 1;
-    a.book.token = s->token;
-    a.book.pos = s->pos;
-    a.book.done = w.done;
-    a.book.ctrl = w.ctrl;
+    a.io.argmax_keys = w.keys;
+    a.io.ticket = w.head_ticket;
+    a.io.book.enabled = 1;
+    a.io.book.token = s->token;
+    a.io.book.pos = s->pos;
+    a.io.book.done = w.done;
+    a.io.book.ctrl = w.ctrl;
     DEC_TRY(run_gemv(kKindHead, a, B, dv, true, st, pdl));
   } else {
     cudaError_t e = launch(advance_kernel, dim3(1), dim3(32), 0, st, pdl, s->token, s->pos, B,
@@ -649,20 +771,20 @@ int dec_qkv_gemv_rope(const float* y, const void* Wq, const void* Wk, const void
   DeviceInfo* dv;
   DEC_TRY(device_info(&dv));
   GemvArgs a{};
-  a.w0 = static_cast<const uint16_t*>(Wq);
-  a.w1 = static_cast<const uint16_t*>(Wk);
-  a.w2 = static_cast<const uint16_t*>(Wv);
-  a.K = H;
-  a.n_units = (Hq + 2 * Hkv) * (D / 2);
-  a.x = y;
-  a.out = q_out;
-  a.k_cache = static_cast<uint16_t*>(k_cache);
-  a.v_cache = static_cast<uint16_t*>(v_cache);
-  a.pos = pos;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.S_max = S_max;
+  a.sh.w0 = static_cast<const uint16_t*>(Wq);
+  a.sh.w1 = static_cast<const uint16_t*>(Wk);
+  a.sh.w2 = static_cast<const uint16_t*>(Wv);
+  a.sh.K = H;
+  a.sh.n_units = (Hq + 2 * Hkv) * (D / 2);
+  a.io.x = y;
+  a.io.out = q_out;
+  a.io.k_cache = static_cast<uint16_t*>(k_cache);
+  a.io.v_cache = static_cast<uint16_t*>(v_cache);
+  a.io.pos = pos;
+  a.sh.Hq = Hq;
+  a.sh.Hkv = Hkv;
+  a.sh.D = D;
+  a.io.S_max = S_max;
   fill_inv_freq(a, D, rope_theta);
   return run_gemv(kKindQKV, a, B, dv, true, static_cast<cudaStream_t>(stream), false);
 }
@@ -729,12 +851,12 @@ int dec_glu_gemv(const float* y, const void* Wg, const void* Wu, float* h, int B
   DeviceInfo* dv;
   DEC_TRY(device_info(&dv));
   GemvArgs a{};
-  a.w0 = static_cast<const uint16_t*>(Wg);
-  a.w1 = static_cast<const uint16_t*>(Wu);
-  a.K = H;
-  a.n_units = I;
-  a.x = y;
-  a.out = h;
+  a.sh.w0 = static_cast<const uint16_t*>(Wg);
+  a.sh.w1 = static_cast<const uint16_t*>(Wu);
+  a.sh.K = H;
+  a.sh.n_units = I;
+  a.io.x = y;
+  a.io.out = h;
   return run_gemv(kKindGLU, a, B, dv, true, static_cast<cudaStream_t>(stream), false);
 }
 
@@ -748,11 +870,11 @@ int dec_down_gemv(const float* x, const void* W, float* residual, int B, int N_i
   DeviceInfo* dv;
   DEC_TRY(device_info(&dv));
   GemvArgs a{};
-  a.w0 = static_cast<const uint16_t*>(W);
-  a.K = N_in;
-  a.n_units = N_out;
-  a.x = x;
-  a.out = residual;
+  a.sh.w0 = static_cast<const uint16_t*>(W);
+  a.sh.K = N_in;
+  a.sh.n_units = N_out;
+  a.io.x = x;
+  a.io.out = residual;
   return run_gemv(kKindResid, a, B, dv, true, static_cast<cudaStream_t>(stream), false);
 }
 
@@ -782,16 +904,16 @@ int dec_lmhead_argmax(const float* residual, const void* final_norm, float eps, 
   const bool fuse = norm_fusable(B, H);
   DEC_CHECK(fuse, DEC_EUNSUPPORTED, "B=%d with H=%d exceeds the fused-norm shared-memory budget", B, H);
   GemvArgs a{};
-  a.w0 = static_cast<const uint16_t*>(W_lm);
-  a.K = H;
-  a.n_units = V;
-  a.x = residual;
-  a.norm_gamma = static_cast<const uint16_t*>(final_norm);
-  a.eps = eps;
-  a.logits = logits_out;
-  a.argmax_keys = reinterpret_cast<unsigned long long*>(base);
-  a.ticket = reinterpret_cast<unsigned int*>(base + 256);
-  a.token_out = token_out;
+  a.sh.w0 = static_cast<const uint16_t*>(W_lm);
+  a.sh.K = H;
+  a.sh.n_units = V;
+  a.io.x = residual;
+  a.io.norm_gamma = static_cast<const uint16_t*>(final_norm);
+  a.io.eps = eps;
+  a.io.logits = logits_out;
+  a.io.argmax_keys = reinterpret_cast<unsigned long long*>(base);
+  a.io.ticket = reinterpret_cast<unsigned int*>(base + 256);
+  a.io.token_out = token_out;
   return run_gemv(kKindHead, a, B, dv, true, st, false);
 }
 

@@ -36,12 +36,198 @@ struct AttnArgs {
   uint32_t* err;
 };
 
+// (head, dim-pair) slots per consumer thread for P.V
+template <int D>
+__host__ __device__ constexpr int attn_slots() {
+  return (kAttnMaxGroup * (D / 2) + kAttnConsumers - 1) / kAttnConsumers;
+}
+
 // Key range of split s for a sequence of `len` keys (same plan in every CTA).
 __device__ __forceinline__ void attn_plan(int len, int n_split, int* chunk, int* n_active) {
   int c = (len + n_split - 1) / n_split;
   if (c < kAttnChunkMin) c = kAttnChunkMin;
   *chunk = c;
   *n_active = (len + c - 1) / c;
+}
+
+// One K/V tile of up to kAttnTile keys for the G query heads of a group:
+// scores (one (key, head) per thread per pass, chunk order rotated by key so
+// that the eight lanes of a quarter-warp hit distinct banks), the online
+// softmax update (warp h owns head h) and P.V (thread slot (head, dim pair)).
+// Run by the 256 consumer threads; ends without a barrier (the caller syncs
+// before the tile's shared memory is reused).
+template <int D>
+__device__ __forceinline__ void attn_tile_math(const uint4* Ks, const uint32_t* Vs, int nk, int G, float scale,
+                                               const float* q_s, float* s_s, float* m_run, float* l_run, float* corr,
+                                               float (&acc0)[attn_slots<D>()], float (&acc1)[attn_slots<D>()]) {
+  constexpr int kChunks = D / 8;
+  constexpr int kPairsPerHead = D / 2;
+  constexpr int kMaxSlots = attn_slots<D>();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_pairs = G * kPairsPerHead;
+    // scores: one (key, head) per thread per pass; chunk order rotated by key
+    // so that the eight lanes of a quarter-warp hit distinct banks
+    for (int idx = tid; idx < G * kAttnTile; idx += kAttnConsumers) {
+      const int h = idx / kAttnTile, j = idx - h * kAttnTile;
+      float sc = -INFINITY;
+      if (j < nk) {
+        const uint4* kr = Ks + j * kChunks;
+        const float* qh = q_s + h * D;
+        float accs = 0.f;
+#pragma unroll 4
+        for (int cc = 0; cc < kChunks; ++cc) {
+          const int c = (cc + j) & (kChunks - 1);
+          const uint4 w = kr[c];
+          const float4 q0 = reinterpret_cast<const float4*>(qh)[2 * c];
+          const float4 q1 = reinterpret_cast<const float4*>(qh)[2 * c + 1];
+          accs = fmaf(bf16lo(w.x), q0.x, accs);
+          accs = fmaf(bf16hi(w.x), q0.y, accs);
+          accs = fmaf(bf16lo(w.y), q0.z, accs);
+          accs = fmaf(bf16hi(w.y), q0.w, accs);
+          accs = fmaf(bf16lo(w.z), q1.x, accs);
+          accs = fmaf(bf16hi(w.z), q1.y, accs);
+          accs = fmaf(bf16lo(w.w), q1.z, accs);
+          accs = fmaf(bf16hi(w.w), q1.w, accs);
+        }
+        sc = accs * scale;
+      }
+      s_s[h * kAttnTile + j] = sc;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    // running max / sum per head (warp h)
+    for (int h = warp; h < G; h += kAttnWarps) {
+      float* sh = s_s + h * kAttnTile;
+      const float v0 = sh[lane], v1 = sh[lane + 32];
+      const float tmax = warp_max(fmaxf(v0, v1));
+      const float m_old = m_run[h];
+      const float m_new = fmaxf(m_old, tmax);
+      const float e0 = (lane < nk) ? expf(v0 - m_new) : 0.f;
+      const float e1 = (lane + 32 < nk) ? expf(v1 - m_new) : 0.f;
+      sh[lane] = e0;
+      sh[lane + 32] = e1;
+      const float tsum = warp_sum(e0 + e1);
+      if (lane == 0) {
+        const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+        corr[h] = c;
+        l_run[h] = l_run[h] * c + tsum;
+        m_run[h] = m_new;
+      }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    // P.V: thread slot (head h, dims 2dp, 2dp+1)
+#pragma unroll
+    for (int i = 0; i < kMaxSlots; ++i) {
+      const int pr = tid + i * kAttnConsumers;
+      if (pr < n_pairs) {
+        const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+        const float c = corr[h];
+        float x0 = acc0[i] * c, x1 = acc1[i] * c;
+        const float* ph = s_s + h * kAttnTile;
+        for (int j = 0; j < nk; ++j) {
+          const uint32_t v = Vs[j * kPairsPerHead + dp];
+          const float pj = ph[j];
+          x0 = fmaf(pj, bf16lo(v), x0);
+          x1 = fmaf(pj, bf16hi(v), x1);
+        }
+        acc0[i] = x0;
+        acc1[i] = x1;
+      }
+    }
+}
+
+// After the last tile: with one split the output is final; otherwise the
+// split's partial (unnormalised accumulator, running max and sum) goes to
+// global memory and the last split of the group to finish (atomic ticket)
+// merges all of them by log-sum-exp weights.  `scratch` is shared memory the
+// merge may use (at least 2*(n_split*G + G) floats).  256 consumer threads.
+template <int D>
+__device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int split, int n_active, int G,
+                                            const float (&acc0)[attn_slots<D>()], const float (&acc1)[attn_slots<D>()],
+                                            const float* m_run, const float* l_run, int* is_last, float* scratch) {
+  constexpr int kPairsPerHead = D / 2;
+  constexpr int kMaxSlots = attn_slots<D>();
+  const int tid = threadIdx.x;
+  const int n_pairs = G * kPairsPerHead;
+  if (n_active == 1) {
+#pragma unroll
+    for (int i = 0; i < kMaxSlots; ++i) {
+      const int pr = tid + i * kAttnConsumers;
+      if (pr < n_pairs) {
+        const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+        const float inv = 1.0f / l_run[h];
+        float* dst = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + 2 * dp;
+        dst[0] = acc0[i] * inv;
+        dst[1] = acc1[i] * inv;
+      }
+    }
+    return;
+  }
+
+  // partial of this split, then the last split of the group merges
+  const size_t stride = static_cast<size_t>(G) * (D + 2);
+  float* mine = a.part + ((static_cast<size_t>(b) * a.Hkv + g) * a.n_split + split) * stride;
+#pragma unroll
+  for (int i = 0; i < kMaxSlots; ++i) {
+    const int pr = tid + i * kAttnConsumers;
+    if (pr < n_pairs) {
+      const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+      mine[h * D + 2 * dp] = acc0[i];
+      mine[h * D + 2 * dp + 1] = acc1[i];
+    }
+  }
+  if (tid < G) {
+    mine[G * D + tid] = m_run[tid];
+    mine[G * D + G + tid] = l_run[tid];
+  }
+  __threadfence();
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  unsigned int* ticket = a.tickets + static_cast<size_t>(b) * a.Hkv + g;
+  if (tid == 0) *is_last = (atomicAdd(ticket, 1u) == static_cast<unsigned>(n_active - 1)) ? 1 : 0;
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (!*is_last) return;
+  __threadfence();
+  // Merge by log-sum-exp weights: o = sum_s w_s acc_s with
+  // w_s = exp(m_s - M) / sum_s' exp(m_s' - M) l_s'.  The split maxima and
+  // sums are staged in shared memory (the ring is free now) in one parallel
+  // pass, and each thread issues its accumulator loads together.
+  const float* base = a.part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
+  float* ms = scratch;          // [n_active][G] split maxima, then weights
+  float* ls = ms + a.n_split * G;                      // [n_active][G] split sums
+  float* mh = ls + a.n_split * G;                      // [G] overall max, [G] 1 / overall sum
+  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
+    const int sp = i / G, h = i - sp * G;
+    ms[i] = __ldcg(base + sp * stride + G * D + h);
+    ls[i] = __ldcg(base + sp * stride + G * D + G + h);
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < n_active; ++sp) M = fmaxf(M, ms[sp * G + tid]);
+    float L = 0.f;
+    for (int sp = 0; sp < n_active; ++sp) L = fmaf(expf(ms[sp * G + tid] - M), ls[sp * G + tid], L);
+    mh[tid] = M;
+    mh[G + tid] = 1.0f / L;
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
+    const int h = i % G;
+    ms[i] = expf(ms[i] - mh[h]) * mh[G + h];
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  for (int idx = tid; idx < G * D; idx += kAttnConsumers) {
+    const int h = idx / D, d = idx - h * D;
+    float num = 0.f;
+    for (int s0 = 0; s0 < n_active; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = s0 + j < n_active ? __ldcg(base + (s0 + j) * stride + h * D + d) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < n_active) num = fmaf(ms[(s0 + j) * G + h], v[j], num);
+    }
+    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] = num;
+  }
+  if (tid == 0) atomicExch(ticket, 0u);
 }
 
 template <int D>
@@ -159,13 +345,10 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
 
   // ------------------------------------------------------------- consumer warps
   const int tid = threadIdx.x;  // 0..255
-  constexpr int kPairsPerHead = D / 2;
-  // (head, dim-pair) slots of this thread for P.V: t, t+256, ...
-  constexpr int kMaxSlots = (kAttnMaxGroup * kPairsPerHead + 255) / 256;
+  constexpr int kMaxSlots = attn_slots<D>();
   float acc0[kMaxSlots], acc1[kMaxSlots];
 #pragma unroll
   for (int i = 0; i < kMaxSlots; ++i) acc0[i] = acc1[i] = 0.f;
-  const int n_pairs = G * kPairsPerHead;
 
   bool ok = true;
   for (int t = 0; t < n_tiles; ++t) {
@@ -184,160 +367,14 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
     const uint4* Ks = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * 2 * kTileBytes);
     const uint32_t* Vs = reinterpret_cast<const uint32_t*>(ring + static_cast<size_t>(slot) * 2 * kTileBytes +
                                                            kTileBytes);
-    // scores: one (key, head) per thread per pass; chunk order rotated by key
-    // so that the eight lanes of a quarter-warp hit distinct banks
-    for (int idx = tid; idx < G * kAttnTile; idx += kAttnConsumers) {
-      const int h = idx / kAttnTile, j = idx - h * kAttnTile;
-      float sc = -INFINITY;
-      if (j < nk) {
-        const uint4* kr = Ks + j * kChunks;
-        const float* qh = q_s + h * D;
-        float accs = 0.f;
-#pragma unroll 4
-        for (int cc = 0; cc < kChunks; ++cc) {
-          const int c = (cc + j) & (kChunks - 1);
-          const uint4 w = kr[c];
-          const float4 q0 = reinterpret_cast<const float4*>(qh)[2 * c];
-          const float4 q1 = reinterpret_cast<const float4*>(qh)[2 * c + 1];
-          accs = fmaf(bf16lo(w.x), q0.x, accs);
-          accs = fmaf(bf16hi(w.x), q0.y, accs);
-          accs = fmaf(bf16lo(w.y), q0.z, accs);
-          accs = fmaf(bf16hi(w.y), q0.w, accs);
-          accs = fmaf(bf16lo(w.z), q1.x, accs);
-          accs = fmaf(bf16hi(w.z), q1.y, accs);
-          accs = fmaf(bf16lo(w.w), q1.z, accs);
-          accs = fmaf(bf16hi(w.w), q1.w, accs);
-        }
-        sc = accs * a.scale;
-      }
-      s_s[h * kAttnTile + j] = sc;
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    // running max / sum per head (warp h)
-    for (int h = warp; h < G; h += kAttnWarps) {
-      float* sh = s_s + h * kAttnTile;
-      const float v0 = sh[lane], v1 = sh[lane + 32];
-      const float tmax = warp_max(fmaxf(v0, v1));
-      const float m_old = m_run[h];
-      const float m_new = fmaxf(m_old, tmax);
-      const float e0 = (lane < nk) ? expf(v0 - m_new) : 0.f;
-      const float e1 = (lane + 32 < nk) ? expf(v1 - m_new) : 0.f;
-      sh[lane] = e0;
-      sh[lane + 32] = e1;
-      const float tsum = warp_sum(e0 + e1);
-      if (lane == 0) {
-        const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
-        corr[h] = c;
-        l_run[h] = l_run[h] * c + tsum;
-        m_run[h] = m_new;
-      }
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    // P.V: thread slot (head h, dims 2dp, 2dp+1)
-#pragma unroll
-    for (int i = 0; i < kMaxSlots; ++i) {
-      const int pr = tid + i * kAttnConsumers;
-      if (pr < n_pairs) {
-        const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
-        const float c = corr[h];
-        float x0 = acc0[i] * c, x1 = acc1[i] * c;
-        const float* ph = s_s + h * kAttnTile;
-        for (int j = 0; j < nk; ++j) {
-          const uint32_t v = Vs[j * kPairsPerHead + dp];
-          const float pj = ph[j];
-          x0 = fmaf(pj, bf16lo(v), x0);
-          x1 = fmaf(pj, bf16hi(v), x1);
-        }
-        acc0[i] = x0;
-        acc1[i] = x1;
-      }
-    }
+    attn_tile_math<D>(Ks, Vs, nk, G, a.scale, q_s, s_s, m_run, l_run, corr, acc0, acc1);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
   }
   asm volatile("bar.sync 2, 288;" ::: "memory");
   if (!ok) return;
 
-  if (n_active == 1) {
-#pragma unroll
-    for (int i = 0; i < kMaxSlots; ++i) {
-      const int pr = tid + i * kAttnConsumers;
-      if (pr < n_pairs) {
-        const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
-        const float inv = 1.0f / l_run[h];
-        float* dst = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + 2 * dp;
-        dst[0] = acc0[i] * inv;
-        dst[1] = acc1[i] * inv;
-      }
-    }
-    return;
-  }
-
-  // partial of this split, then the last split of the group merges
-  const size_t stride = static_cast<size_t>(G) * (D + 2);
-  float* mine = a.part + ((static_cast<size_t>(b) * a.Hkv + g) * a.n_split + split) * stride;
-#pragma unroll
-  for (int i = 0; i < kMaxSlots; ++i) {
-    const int pr = tid + i * kAttnConsumers;
-    if (pr < n_pairs) {
-      const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
-      mine[h * D + 2 * dp] = acc0[i];
-      mine[h * D + 2 * dp + 1] = acc1[i];
-    }
-  }
-  if (tid < G) {
-    mine[G * D + tid] = m_run[tid];
-    mine[G * D + G + tid] = l_run[tid];
-  }
-  __threadfence();
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  unsigned int* ticket = a.tickets + static_cast<size_t>(b) * a.Hkv + g;
-  if (tid == 0) *is_last = (atomicAdd(ticket, 1u) == static_cast<unsigned>(n_active - 1)) ? 1 : 0;
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  if (!*is_last) return;
-  __threadfence();
-  // Merge by log-sum-exp weights: o = sum_s w_s acc_s with
-  // w_s = exp(m_s - M) / sum_s' exp(m_s' - M) l_s'.  The split maxima and
-  // sums are staged in shared memory (the ring is free now) in one parallel
-  // pass, and each thread issues its accumulator loads together.
-  const float* base = a.part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
-  float* ms = reinterpret_cast<float*>(ring);          // [n_active][G] split maxima, then weights
-  float* ls = ms + a.n_split * G;                      // [n_active][G] split sums
-  float* mh = ls + a.n_split * G;                      // [G] overall max, [G] 1 / overall sum
-  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
-    const int sp = i / G, h = i - sp * G;
-    ms[i] = __ldcg(base + sp * stride + G * D + h);
-    ls[i] = __ldcg(base + sp * stride + G * D + G + h);
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < n_active; ++sp) M = fmaxf(M, ms[sp * G + tid]);
-    float L = 0.f;
-    for (int sp = 0; sp < n_active; ++sp) L = fmaf(expf(ms[sp * G + tid] - M), ls[sp * G + tid], L);
-    mh[tid] = M;
-    mh[G + tid] = 1.0f / L;
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
-    const int h = i % G;
-    ms[i] = expf(ms[i] - mh[h]) * mh[G + h];
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  for (int idx = tid; idx < G * D; idx += kAttnConsumers) {
-    const int h = idx / D, d = idx - h * D;
-    float num = 0.f;
-    for (int s0 = 0; s0 < n_active; s0 += 8) {
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = s0 + j < n_active ? __ldcg(base + (s0 + j) * stride + h * D + d) : 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (s0 + j < n_active) num = fmaf(ms[(s0 + j) * G + h], v[j], num);
-    }
-    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] = num;
-  }
-  if (tid == 0) atomicExch(ticket, 0u);
+  attn_finish<D>(a, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last, reinterpret_cast<float*>(ring));
 }
 
 }  // namespace dec

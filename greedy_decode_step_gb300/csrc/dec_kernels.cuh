@@ -35,7 +35,7 @@ constexpr int kMaxBatch = 16;
 constexpr int kMaxIt = 8;                            // 16-byte chunks per lane per block (shared-memory path)
 constexpr int kXregIt = 5;                           // chunks per lane of a warp's part (register path)
 constexpr int kXregRows = 2;                         // rows per warp per stage (register path)
-constexpr uint32_t kGemvHeaderBytes = 1536;          // barriers, flags, reductions; the stage table follows
+constexpr uint32_t kGemvHeaderBytes = 1536;          // barriers, flags and reduction scratch
 
 enum GemvKind : int { kKindQKV = 0, kKindGLU = 1, kKindResid = 2, kKindHead = 3 };
 
@@ -56,23 +56,22 @@ struct StepBook {
   Ctrl* ctrl;
 };
 
-struct GemvArgs {
-  // weights: up to three row-major bf16 tensors with rows of K elements
-  const uint16_t* w0;
+// What the producer and the consumers of a GEMV both need to walk its rows.
+struct GemvShape {
+  const uint16_t* w0;   // up to three row-major bf16 tensors with rows of K elements
   const uint16_t* w1;
   const uint16_t* w2;
   int K;
   int n_units;          // work units (QKV: rotation pairs; GLU: gate/up row pairs; else rows)
-  int rows_per_stage;   // rows of one bulk copy
-  int max_stages;       // capacity of the stage table
-  int parts;            // P: a row's dot product is cut into P warp tasks
+  int D, Hq, Hkv;       // QKV: head layout of the unit space
+  int parts;            // P: a row's dot product is cut into P warp parts
   int chunks_per_part;  // CP (16-byte chunks)
-  int n_slots;          // ring stages
-  int units_per_cta;    // upper bound used to size the partial-sum buffer
-  int B;                // live batch rows
-  int x_smem;           // 1: activations staged in shared memory
-  uint32_t off_x, off_part, off_ring;  // dynamic shared-memory layout (bytes)
-  // input activation [B][K] fp32; with norm_gamma set it is the residual stream
+  int rows_per_stage;   // rows of one bulk copy
+};
+
+// Inputs and outputs of a GEMV's consumers.
+struct GemvIO {
+  // activation [B][K] fp32; with norm_gamma set it is the residual stream
   const float* x;
   const uint16_t* norm_gamma;
   float eps;
@@ -80,19 +79,29 @@ struct GemvArgs {
   const uint16_t* embed;
   int vocab;
   float* resid_store;     // with tokens: CTA 0 writes the gathered rows here
-  // outputs
+  int B;
+  int x_smem;             // 1: activations staged in shared memory
   float* out;             // QKV: q [B][Hq*D]; GLU: h [B][I]; Resid: r [B][N] (+=)
   uint16_t* k_cache;      // QKV: [B][Hkv][S_max][D]
   uint16_t* v_cache;
   const int32_t* pos;     // QKV: [B]
-  int Hq, Hkv, D, S_max;
+  int S_max;
   float* logits;          // Head: optional [B][V]
   unsigned long long* argmax_keys;  // Head: [B], zero between launches
   unsigned int* ticket;             // Head: zero between launches
   int32_t* token_out;               // Head: optional [B]
   StepBook book;
   uint32_t* err;
-  double inv_freq[64];    // QKV: theta^(-2i/D), i < D/2
+};
+
+struct GemvArgs {
+  GemvShape sh;
+  GemvIO io;
+  int n_slots;          // ring stages
+  int units_per_cta;    // upper bound used to size the partial-sum buffer
+  uint32_t off_x, off_part, off_ring;  // dynamic shared-memory layout (bytes)
+  uint32_t slot_bytes;
+  double inv_freq[64];  // QKV: theta^(-2i/D), i < D/2
 };
 
 // ----------------------------------------------------------------------------- activation layout
@@ -151,64 +160,438 @@ __device__ __forceinline__ void rope_cos_sin(int p, double inv_freq, float* c, f
   sincosf(static_cast<float>(red), s, c);
 }
 
-// ----------------------------------------------------------------------------- GEMV
-// A CTA owns the units [u0, u1).  Its rows are streamed as a sequence of
-// stages; each stage is ONE bulk copy of up to `rows_per_stage` consecutive
-// rows of one weight tensor (a "run").  Large single copies matter: the TMA
-// engine's throughput per SM grows with the size of each copy.
+// ----------------------------------------------------------------------------- GEMV: stages
+// A CTA owns the units [u0, u0 + n).  Its rows are streamed as a sequence of
+// stages; each stage is ONE bulk copy of up to rows_per_stage consecutive rows
+// of one weight tensor (a "run").  Large single copies matter: the TMA
+// engine's throughput per SM grows with the size of each copy.  Runs, in
+// streaming order: QKV -- per head touched, the first-half rows of its pairs,
+// then the second-half rows; GLU -- gate rows, then up rows; else one run.
 struct StageDesc {
   int ul0;    // first local unit of the stage
   int nrows;  // rows in the stage (consecutive units)
   int r;      // row slot within the unit (QKV: 0 = pair's first half, 1 = second; GLU: 0 = gate, 1 = up)
-  int pad;
 };
 
 // First element of row slot r of unit u.
 template <int KIND>
-__device__ __forceinline__ const uint16_t* unit_row(const GemvArgs& a, int u, int r) {
-  const size_t K = static_cast<size_t>(a.K);
+__device__ __forceinline__ const uint16_t* unit_row(const GemvShape& sh, int u, int r) {
+  const size_t K = static_cast<size_t>(sh.K);
   if constexpr (KIND == kKindQKV) {
-    const int half = a.D >> 1;
+    const int half = sh.D >> 1;
     int hh = u / half;
     const int row_in_head = (u - hh * half) + r * half;
-    if (hh < a.Hq) return a.w0 + (static_cast<size_t>(hh) * a.D + row_in_head) * K;
-    hh -= a.Hq;
-    if (hh < a.Hkv) return a.w1 + (static_cast<size_t>(hh) * a.D + row_in_head) * K;
-    hh -= a.Hkv;
-    return a.w2 + (static_cast<size_t>(hh) * a.D + row_in_head) * K;
+    if (hh < sh.Hq) return sh.w0 + (static_cast<size_t>(hh) * sh.D + row_in_head) * K;
+    hh -= sh.Hq;
+    if (hh < sh.Hkv) return sh.w1 + (static_cast<size_t>(hh) * sh.D + row_in_head) * K;
+    hh -= sh.Hkv;
+    return sh.w2 + (static_cast<size_t>(hh) * sh.D + row_in_head) * K;
   } else if constexpr (KIND == kKindGLU) {
-    return (r == 0 ? a.w0 : a.w1) + static_cast<size_t>(u) * K;
+    return (r == 0 ? sh.w0 : sh.w1) + static_cast<size_t>(u) * K;
   } else {
-    return a.w0 + static_cast<size_t>(u) * K;
+    return sh.w0 + static_cast<size_t>(u) * K;
   }
 }
 
-// Builds the stage table of a CTA (runs split into stages); returns the count.
-// QKV: per head touched, the run of first-half rows then the run of
-// second-half rows; GLU: gate rows then up rows; otherwise one run.
-template <int KIND>
-__device__ int build_stages(const GemvArgs& a, int u0, int n, int rps, StageDesc* out, int max_out) {
-  int cnt = 0;
-  auto add_run = [&](int ul0, int len, int r) {
-    for (int o = 0; o < len && cnt < max_out; o += rps) out[cnt++] = StageDesc{ul0 + o, min(rps, len - o), r, 0};
-  };
+// Visits the runs of a CTA in streaming order: f(ul0, len, r) returns true to stop.
+template <int KIND, typename F>
+__device__ __forceinline__ void for_each_run(const GemvShape& sh, int u0, int n, F&& f) {
   if constexpr (KIND == kKindQKV) {
-    const int half = a.D >> 1;
+    const int half = sh.D >> 1;
     for (int ul = 0; ul < n;) {
       const int end = min(n, ul + (half - (u0 + ul) % half));
-      add_run(ul, end - ul, 0);
-      add_run(ul, end - ul, 1);
+      if (f(ul, end - ul, 0)) return;
+      if (f(ul, end - ul, 1)) return;
       ul = end;
     }
   } else if constexpr (KIND == kKindGLU) {
-    add_run(0, n, 0);
-    add_run(0, n, 1);
+    if (f(0, n, 0)) return;
+    f(0, n, 1);
   } else {
-    add_run(0, n, 0);
+    f(0, n, 0);
   }
+}
+
+template <int KIND>
+__device__ __forceinline__ int count_stages(const GemvShape& sh, int u0, int n) {
+  int cnt = 0;
+  const int rps = sh.rows_per_stage;
+  for_each_run<KIND>(sh, u0, n, [&](int, int len, int) {
+    cnt += (len + rps - 1) / rps;
+    return false;
+  });
   return cnt;
 }
 
+template <int KIND>
+__device__ __forceinline__ StageDesc nth_stage(const GemvShape& sh, int u0, int n, int s) {
+  StageDesc d{0, 0, 0};
+  const int rps = sh.rows_per_stage;
+  for_each_run<KIND>(sh, u0, n, [&](int ul0, int len, int r) {
+    const int k = (len + rps - 1) / rps;
+    if (s < k) {
+      d = StageDesc{ul0 + s * rps, min(rps, len - s * rps), r};
+      return true;
+    }
+    s -= k;
+    return false;
+  });
+  return d;
+}
+
+// Units of CTA `cta` out of `ncta` (contiguous, sizes differ by at most one).
+__device__ __forceinline__ void cta_units(int n_units, int cta, int ncta, int* u0, int* n) {
+  const int a0 = static_cast<int>((static_cast<long long>(cta) * n_units) / ncta);
+  const int a1 = static_cast<int>((static_cast<long long>(cta + 1) * n_units) / ncta);
+  *u0 = a0;
+  *n = a1 - a0;
+}
+
+// The ring of shared-memory stages shared by a producer warp and 8 consumer warps.
+struct Ring {
+  uint64_t* full;
+  uint64_t* empty;
+  unsigned char* base;
+  int ns;
+  uint32_t slot_bytes;
+  volatile int* abort;
+  uint32_t* err;
+};
+
+// Producer: issues the stages of one GEMV; `sg` counts stages over the
+// ring's whole life (slot sg % ns, phase sg / ns).  Returns false on abort.
+template <int KIND>
+__device__ bool produce_stages(const GemvShape& sh, int u0, int n, const Ring& R, int& sg, uint64_t policy) {
+  const int total = count_stages<KIND>(sh, u0, n);
+  const uint32_t row_bytes = static_cast<uint32_t>(sh.K) * 2u;
+  for (int s = 0; s < total; ++s, ++sg) {
+    const int slot = sg % R.ns;
+    if (sg >= R.ns && !mbar_wait(&R.empty[slot], ((sg / R.ns) - 1) & 1, R.abort, R.err, kErrWaitEmpty)) return false;
+    const StageDesc d = nth_stage<KIND>(sh, u0, n, s);
+    const uint32_t bytes = static_cast<uint32_t>(d.nrows) * row_bytes;
+    mbar_arrive_expect_tx(&R.full[slot], bytes);
+    bulk_copy_g2s(R.base + static_cast<size_t>(slot) * R.slot_bytes, unit_row<KIND>(sh, u0 + d.ul0, d.r), bytes,
+                  &R.full[slot], policy);
+  }
+  return true;
+}
+
+// Producer epilogue: after the consumers stopped reading the ring, wait
+// (bounded) for copies nobody waited for (only after an abort).
+__device__ __forceinline__ void drain_ring(const Ring& R, int sg_issued) {
+  for (int s = max(0, sg_issued - R.ns); s < sg_issued; ++s) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&R.full[s % R.ns], (s / R.ns) & 1)) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(R.err, kErrDrain);
+        break;
+      }
+    }
+  }
+}
+
+// Consumer wait for stage sg: lane 0 polls (bounded), the verdict is
+// warp-uniform, then every lane acquires the completed phase.
+__device__ __forceinline__ bool consumer_wait(const Ring& R, int sg) {
+  const int lane = threadIdx.x & 31;
+  const int slot = sg % R.ns;
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(&R.full[slot], (sg / R.ns) & 1, R.abort, R.err, kErrWaitFull) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_try_wait(&R.full[slot], (sg / R.ns) & 1);
+  return ok != 0;
+}
+
+// ----------------------------------------------------------------------------- GEMV: consumer pieces
+// Prologue: the B activation rows into shared memory (split layout), with the
+// RMSNorm folded in when io.norm_gamma is set.  256 consumer threads.
+template <int BT>
+__device__ void stage_activations(const GemvIO& io, int K, float* xs, float* red) {
+  for (int b = 0; b < io.B; ++b) {
+    float* xb = xs + static_cast<size_t>(b) * K;
+    if (io.tokens) {
+      int tok = io.tokens[b];
+      const bool ok = tok >= 0 && tok < io.vocab;
+      if (!ok && threadIdx.x == 0) atomicOr(io.err, kErrTokenRange);
+      const uint16_t* er = io.embed + static_cast<size_t>(ok ? tok : 0) * K;
+      for (int i = threadIdx.x; i < K; i += kConsumerThreads) {
+        const float v = ok ? __uint_as_float(static_cast<uint32_t>(er[i]) << 16) : 0.f;
+        xb[xsplit(i, K)] = v;
+        if (blockIdx.x == 0 && io.resid_store) io.resid_store[static_cast<size_t>(b) * K + i] = v;
+      }
+    } else {
+      const float* src = io.x + static_cast<size_t>(b) * K;
+      for (int i = threadIdx.x; i < K; i += kConsumerThreads) xb[xsplit(i, K)] = src[i];
+    }
+    if (io.norm_gamma) {
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const float inv = block_rms_inv<true>(xb, K, io.eps, red);
+      for (int i = threadIdx.x; i < K; i += kConsumerThreads) {
+        const int e = xsplit(i, K);
+        xb[e] = (xb[e] * inv) * __uint_as_float(static_cast<uint32_t>(io.norm_gamma[i]) << 16);
+      }
+    }
+  }
+  for (int b = io.B; b < BT; ++b)
+    for (int i = threadIdx.x; i < K; i += kConsumerThreads) xs[static_cast<size_t>(b) * K + i] = 0.f;
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// Register path: the warp's slice [cb, ce) of the activations (chunk c of
+// lane l is cb + l + 32*it), from shared memory (split layout) or global.
+template <int BT>
+__device__ __forceinline__ void load_xreg(const GemvIO& io, int K, const float* xs, int cb, int ce, int nit,
+                                          float (&xr)[kXregIt][BT][8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int it = 0; it < kXregIt; ++it) {
+    const int c = cb + lane + 32 * it;
+    const bool in = it < nit && c < ce;
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+      if (in) {
+        if (io.x_smem) {
+          lo = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K)[c];
+          hi = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K + K / 2)[c];
+        } else if (b < io.B) {
+          const float4* xp = reinterpret_cast<const float4*>(io.x + static_cast<size_t>(b) * K) + 2 * c;
+          lo = xp[0];
+          hi = xp[1];
+        }
+      }
+      xr[it][b][0] = lo.x; xr[it][b][1] = lo.y; xr[it][b][2] = lo.z; xr[it][b][3] = lo.w;
+      xr[it][b][4] = hi.x; xr[it][b][5] = hi.y; xr[it][b][6] = hi.z; xr[it][b][7] = hi.w;
+    }
+  }
+}
+
+// Register path stage loop: a stage's rows of this warp (at most kXregRows,
+// row i with (i + rot) % NSLOT == slot) are copied into registers and the
+// stage is released BEFORE the arithmetic, so the math never holds up the
+// ring.  Partial sums go to part[((ul*RU + r)*P + p)*BT + b].
+template <int KIND, int BT>
+__device__ bool consume_xreg(const GemvShape& sh, int u0, int n, const Ring& R, int& sg,
+                             const float (&xr)[kXregIt][BT][8], int cb, int ce, int nit, float* part) {
+  constexpr int RU = (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = sh.parts;
+  const int NSLOT = kConsumerWarps / P;
+  const int my_p = warp % P, my_slot = warp / P;
+  const uint32_t row_bytes = static_cast<uint32_t>(sh.K) * 2u;
+  const int total = count_stages<KIND>(sh, u0, n);
+  for (int s = 0; s < total; ++s, ++sg) {
+    if (!consumer_wait(R, sg)) return false;
+    const int slot = sg % R.ns;
+    const StageDesc d = nth_stage<KIND>(sh, u0, n, s);
+    const int rot = (s * sh.rows_per_stage) % NSLOT;
+    const int first = (my_slot - rot + NSLOT) % NSLOT;
+    uint4 wv[kXregRows][kXregIt];
+    int nmine = 0;
+#pragma unroll
+    for (int k = 0; k < kXregRows; ++k) {
+      const int i = first + k * NSLOT;
+      const bool have = i < d.nrows;
+      const uint4* wr = reinterpret_cast<const uint4*>(R.base + static_cast<size_t>(slot) * R.slot_bytes +
+                                                       static_cast<size_t>(have ? i : 0) * row_bytes);
+#pragma unroll
+      for (int it = 0; it < kXregIt; ++it) {
+        const int c = cb + lane + 32 * it;
+        wv[k][it] = (have && it < nit && c < ce) ? wr[c] : make_uint4(0u, 0u, 0u, 0u);
+      }
+      nmine += have ? 1 : 0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[slot]);
+#pragma unroll
+    for (int k = 0; k < kXregRows; ++k) {
+      if (k < nmine) {
+        float acc[BT];
+#pragma unroll
+        for (int b = 0; b < BT; ++b) acc[b] = 0.f;
+#pragma unroll
+        for (int it = 0; it < kXregIt; ++it) {
+          if (it < nit) {
+#pragma unroll
+            for (int b = 0; b < BT; ++b) acc[b] += dot8(wv[k][it], xr[it][b]);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < BT; ++b) acc[b] = warp_sum(acc[b]);
+        const int ul = d.ul0 + first + k * NSLOT;
+        if (lane == 0) {
+#pragma unroll
+          for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = acc[b];
+        }
+      }
+    }
+  }
+  return true;
+}
+
+// Output of unit u for row b from its partial sums (QKV, GLU, residual).
+template <int KIND, int BT>
+__device__ void gemv_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int n, const float* part,
+                              const double* inv_freq) {
+  constexpr int RU = (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
+  const int P = sh.parts;
+  const int B = io.B;
+  const int n_out = n * B;
+  for (int idx = threadIdx.x; idx < n_out; idx += kConsumerThreads) {
+    const int ul = idx / B;
+    const int b = idx - ul * B;
+    const int u = u0 + ul;
+    float v[RU];
+#pragma unroll
+    for (int r = 0; r < RU; ++r) {
+      float sum = 0.f;
+      for (int p = 0; p < P; ++p) sum += part[((static_cast<size_t>(ul) * RU + r) * P + p) * BT + b];
+      v[r] = sum;
+    }
+    if constexpr (KIND == kKindResid) {
+      float* dst = io.out + static_cast<size_t>(b) * sh.n_units + u;
+      *dst = *dst + v[0];
+    } else if constexpr (KIND == kKindGLU) {
+      io.out[static_cast<size_t>(b) * sh.n_units + u] = silu_f32(v[0]) * v[1];
+    } else if constexpr (KIND == kKindQKV) {
+      const int half = sh.D >> 1;
+      const int hh = u / half;
+      const int j = u - hh * half;
+      const int p = io.pos[b];
+      float lo = v[0], hi = v[1];
+      if (hh < sh.Hq + sh.Hkv) {
+        float cs, sn;
+        rope_cos_sin(p, inv_freq[j], &cs, &sn);
+        const float l2 = lo * cs - hi * sn;
+        const float h2 = hi * cs + lo * sn;
+        lo = l2;
+        hi = h2;
+      }
+      if (hh < sh.Hq) {
+        float* q = io.out + static_cast<size_t>(b) * sh.Hq * sh.D + static_cast<size_t>(hh) * sh.D;
+        q[j] = lo;
+        q[j + half] = hi;
+      } else {
+        if (p < 0 || p >= io.S_max) {
+          atomicOr(io.err, kErrPosRange);
+          continue;
+        }
+        const bool is_k = hh < sh.Hq + sh.Hkv;
+        const int g = is_k ? hh - sh.Hq : hh - sh.Hq - sh.Hkv;
+        uint16_t* cache = is_k ? io.k_cache : io.v_cache;
+        uint16_t* dst = cache + ((static_cast<size_t>(b) * sh.Hkv + g) * io.S_max + p) * sh.D;
+        dst[j] = f32_to_bf16(lo);
+        dst[j + half] = f32_to_bf16(hi);
+      }
+    }
+  }
+}
+
+// Best (value, index) per row b: higher value first, then the lower index.
+__device__ __forceinline__ void better(float& bv, uint32_t& bi, float v, uint32_t i) {
+  if (i != 0xFFFFFFFFu && (bi == 0xFFFFFFFFu || v > bv || (v == bv && i < bi))) {
+    bv = v;
+    bi = i;
+  }
+}
+
+// LM head epilogue: CTA-best of every row b -> atomicMax on its argmax key;
+// the last CTA to finish (ticket) reads the winners and, in step mode, does
+// the bookkeeping (token, position, output column, EOS state).  When
+// `from_part` is set the CTA's logits are first assembled from the partial
+// sums of the register path.  head_val/head_idx: [8][kMaxBatch] shared.
+template <int BT>
+__device__ void head_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int n, const float* part,
+                              bool from_part, float (&best_v)[BT], uint32_t (&best_i)[BT], float* head_val,
+                              uint32_t* head_idx, int* is_last) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = io.B;
+  const int P = sh.parts;
+  if (from_part) {
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    for (int ul = threadIdx.x; ul < n; ul += kConsumerThreads) {
+      const uint32_t row = static_cast<uint32_t>(u0 + ul);
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        if (b < B) {
+          float v = 0.f;
+          for (int p = 0; p < P; ++p) v += part[(static_cast<size_t>(ul) * P + p) * BT + b];
+          if (io.logits) io.logits[static_cast<size_t>(b) * sh.n_units + row] = v;
+          better(best_v[b], best_i[b], v, row);
+        }
+      }
+    }
+  }
+  // warp-level reduction into lane 0
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best_v[b], o);
+      const uint32_t oi = __shfl_xor_sync(0xffffffffu, best_i[b], o);
+      better(best_v[b], best_i[b], ov, oi);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      head_val[warp * kMaxBatch + b] = best_v[b];
+      head_idx[warp * kMaxBatch + b] = best_i[b];
+    }
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (threadIdx.x < B) {
+    const int b = threadIdx.x;
+    float bv = -INFINITY;
+    uint32_t bi = 0xFFFFFFFFu;
+    for (int w = 0; w < kConsumerWarps; ++w) better(bv, bi, head_val[w * kMaxBatch + b], head_idx[w * kMaxBatch + b]);
+    if (bi != 0xFFFFFFFFu) atomicMax(&io.argmax_keys[b], argmax_key(bv, bi));
+  }
+  __threadfence();
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (threadIdx.x == 0) {
+    const unsigned int t = atomicAdd(io.ticket, 1u);
+    *is_last = (t == gridDim.x - 1) ? 1 : 0;
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  if (*is_last && warp == 0) {
+    __threadfence();
+    int32_t emit = 0;
+    bool row_done = true;
+    const int b = lane;
+    if (b < B) {
+      const unsigned long long key = atomicExch(&io.argmax_keys[b], 0ull);
+      const int32_t tok = static_cast<int32_t>(argmax_key_index(key));
+      if (io.token_out) io.token_out[b] = tok;
+      if (io.book.enabled) {
+        Ctrl* c = io.book.ctrl;
+        const int eos = c->eos_id;
+        emit = io.book.done[b] ? eos : tok;
+        if (eos >= 0 && emit == eos) io.book.done[b] = 1;
+        row_done = io.book.done[b] != 0;
+        const int step = c->step;
+        if (c->out_tokens) {
+          if (step < c->out_cap)
+            c->out_tokens[static_cast<size_t>(b) * c->out_cap + step] = emit;
+          else
+            atomicOr(io.err, kErrOutRange);
+        }
+        io.book.token[b] = emit;
+        io.book.pos[b] += 1;
+      }
+    }
+    const unsigned all = __all_sync(0xffffffffu, row_done);
+    if (lane == 0) {
+      if (io.book.enabled) {
+        io.book.ctrl->all_done = all ? 1 : 0;
+        io.book.ctrl->step += 1;
+      }
+      atomicExch(io.ticket, 0u);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- GEMV kernel
 template <int KIND, int BT, bool XREG>
 __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -216,132 +599,57 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 2 : 1) gemv_kernel(con
   uint64_t* empty = full + kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 256);
   int* is_last = reinterpret_cast<int*>(smem + 260);
-  int* n_stages_s = reinterpret_cast<int*>(smem + 264);
   float* red = reinterpret_cast<float*>(smem + 288);                    // 8 floats
-  float* head_val = reinterpret_cast<float*>(smem + 320);               // [8][BT]
-  uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 320 + 4 * kConsumerWarps * kMaxBatch);  // [8][BT]
-  StageDesc* desc = reinterpret_cast<StageDesc*>(smem + kGemvHeaderBytes);
+  float* head_val = reinterpret_cast<float*>(smem + 320);               // [8][kMaxBatch]
+  uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 320 + 4 * kConsumerWarps * kMaxBatch);
   float* xs = reinterpret_cast<float*>(smem + a.off_x);
   float* part = reinterpret_cast<float*>(smem + a.off_part);
-  unsigned char* ring = smem + a.off_ring;
 
   constexpr int RU = (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
-  const int P = a.parts;                      // warps per row
-  const int NSLOT = kConsumerWarps / P;       // rows processed side by side
-  const int CP = a.chunks_per_part;
-  const int NS = a.n_slots;
-  const int C = a.K / kChunkElems;
-  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
-  const uint32_t stage_bytes = static_cast<uint32_t>(a.rows_per_stage) * row_bytes;
-
-  const int u0 = static_cast<int>((static_cast<long long>(blockIdx.x) * a.n_units) / gridDim.x);
-  const int u1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.n_units) / gridDim.x);
-  const int n_cta_units = u1 - u0;
-
+  const GemvShape& sh = a.sh;
+  const GemvIO& io = a.io;
+  const Ring R{full, empty, smem + a.off_ring, a.n_slots, a.slot_bytes, abort_flag, io.err};
+  int u0, n;
+  cta_units(sh.n_units, blockIdx.x, gridDim.x, &u0, &n);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < R.ns; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
     *abort_flag = 0;
-    *n_stages_s = build_stages<KIND>(a, u0, n_cta_units, a.rows_per_stage, desc, a.max_stages);
     fence_mbar_init();
   }
   __syncthreads();
-  const int n_stages = *n_stages_s;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer warp
     // Weights never depend on earlier kernels: start streaming before the
     // programmatic-dependency wait so the copies overlap the previous kernel.
-    int issued = 0;
+    int sg = 0;
     if (lane == 0) {
-      const uint64_t policy = l2_policy_evict_first();
-      bool triggered = false;
-      for (int s = 0; s < n_stages; ++s) {
-        const int slot = s % NS;
-        if (s >= NS) {
-          if (!mbar_wait(&empty[slot], ((s / NS) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
-        }
-        const StageDesc d = desc[s];
-        const uint32_t bytes = static_cast<uint32_t>(d.nrows) * row_bytes;
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_copy_g2s(ring + static_cast<size_t>(slot) * stage_bytes, unit_row<KIND>(a, u0 + d.ul0, d.r), bytes,
-                      &full[slot], policy);
-        issued = s + 1;
-        if (issued == min(NS, n_stages)) {
-          pdl_launch_dependents();
-          triggered = true;
-        }
-      }
-      if (!triggered) pdl_launch_dependents();
+      produce_stages<KIND>(sh, u0, n, R, sg, l2_policy_evict_first());
+      pdl_launch_dependents();
     }
     __syncwarp();
     if (lane != 0) pdl_launch_dependents();
     asm volatile("bar.sync 2, 288;" ::: "memory");
-    // Drain: consumers have stopped reading the ring.  A stage is released
-    // only after its copy completed, so the only copies that can still be in
-    // flight are those of stages nobody waited for (after an abort).
-    if (lane == 0) {
-      for (int s = max(0, issued - NS); s < issued; ++s) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&full[s % NS], (s / NS) & 1)) {
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(a.err, kErrDrain);
-            break;
-          }
-        }
-      }
-    }
+    if (lane == 0) drain_ring(R, sg);
     return;
   }
 
   // --------------------------------------------------------------- consumer warps
   pdl_wait();
   pdl_launch_dependents();
-  const int B = a.B;
-  const int K = a.K;
-
-  // Prologue: activations into shared memory in the split layout (see
-  // xsplit), the RMSNorm folded in when requested.
-  if (a.x_smem) {
-    for (int b = 0; b < B; ++b) {
-      float* xb = xs + static_cast<size_t>(b) * K;
-      if (a.tokens) {
-        int tok = a.tokens[b];
-        const bool ok = tok >= 0 && tok < a.vocab;
-        if (!ok && threadIdx.x == 0) atomicOr(a.err, kErrTokenRange);
-        const uint16_t* er = a.embed + static_cast<size_t>(ok ? tok : 0) * K;
-        for (int i = threadIdx.x; i < K; i += kConsumerThreads) {
-          const float v = ok ? __uint_as_float(static_cast<uint32_t>(er[i]) << 16) : 0.f;
-          xb[xsplit(i, K)] = v;
-          if (blockIdx.x == 0 && a.resid_store) a.resid_store[static_cast<size_t>(b) * K + i] = v;
-        }
-      } else {
-        const float* src = a.x + static_cast<size_t>(b) * K;
-        for (int i = threadIdx.x; i < K; i += kConsumerThreads) xb[xsplit(i, K)] = src[i];
-      }
-      if (a.norm_gamma) {
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        const float inv = block_rms_inv<true>(xb, K, a.eps, red);
-        for (int i = threadIdx.x; i < K; i += kConsumerThreads) {
-          const int e = xsplit(i, K);
-          xb[e] = (xb[e] * inv) * __uint_as_float(static_cast<uint32_t>(a.norm_gamma[i]) << 16);
-        }
-      }
-    }
-    for (int b = B; b < BT; ++b)
-      for (int i = threadIdx.x; i < K; i += kConsumerThreads) xs[static_cast<size_t>(b) * K + i] = 0.f;
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-
-  // Fixed roles: warp w always takes part (w % P) of rows w / P, w / P +
-  // NSLOT, ... of every stage, so its slice of the activations never changes
-  // and can live in registers.
+  const int K = sh.K;
+  const int C = K / kChunkElems;
+  const int P = sh.parts;
+  const int CP = sh.chunks_per_part;
+  if (io.x_smem) stage_activations<BT>(io, K, xs, red);
   const int my_p = warp % P;
   const int my_slot = warp / P;
+  const int NSLOT = kConsumerWarps / P;
   const int cb = my_p * CP;
   const int ce = min(C, cb + CP);
   const int nit = ce > cb ? (ce - cb + 31) / 32 : 0;
@@ -355,127 +663,51 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 2 : 1) gemv_kernel(con
   }
 
   bool ok = true;
+  int sg = 0;
   if constexpr (XREG) {
-    // ---- register path (b <= 2): the warp's activation slice lives in
-    // registers; a stage's rows are copied to registers and the stage is
-    // released BEFORE the arithmetic, so the math never holds up the ring.
     float xr[kXregIt][BT][8];
-#pragma unroll
-    for (int it = 0; it < kXregIt; ++it) {
-      const int c = cb + lane + 32 * it;
-      const bool in = it < nit && c < ce;
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-        if (in) {
-          if (a.x_smem) {
-            lo = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K)[c];
-            hi = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K + K / 2)[c];
-          } else if (b < B) {
-            const float4* xp = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * K) + 2 * c;
-            lo = xp[0];
-            hi = xp[1];
-          }
-        }
-        xr[it][b][0] = lo.x; xr[it][b][1] = lo.y; xr[it][b][2] = lo.z; xr[it][b][3] = lo.w;
-        xr[it][b][4] = hi.x; xr[it][b][5] = hi.y; xr[it][b][6] = hi.z; xr[it][b][7] = hi.w;
-      }
-    }
-    for (int s = 0; s < n_stages; ++s) {
-      const int slot = s % NS;
-      int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(&full[slot], (s / NS) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
-      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-      if (!w_ok) {
-        ok = false;
-        break;
-      }
-      (void)mbar_try_wait(&full[slot], (s / NS) & 1);  // completed phase: acquire for every lane
-      const StageDesc d = desc[s];
-      // rows of this warp: i with (i + rot) % NSLOT == my_slot, at most kXregRows
-      const int rot = (s * a.rows_per_stage) % NSLOT;
-      const int first = (my_slot - rot + NSLOT) % NSLOT;
-      uint4 wv[kXregRows][kXregIt];
-      int nmine = 0;
-#pragma unroll
-      for (int k = 0; k < kXregRows; ++k) {
-        const int i = first + k * NSLOT;
-        const bool have = i < d.nrows;
-        const uint4* wr = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes +
-                                                         static_cast<size_t>(have ? i : 0) * row_bytes);
-#pragma unroll
-        for (int it = 0; it < kXregIt; ++it) {
-          const int c = cb + lane + 32 * it;
-          wv[k][it] = (have && it < nit && c < ce) ? wr[c] : make_uint4(0u, 0u, 0u, 0u);
-        }
-        nmine += have ? 1 : 0;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-#pragma unroll
-      for (int k = 0; k < kXregRows; ++k) {
-        if (k < nmine) {
-          float acc[BT];
-#pragma unroll
-          for (int b = 0; b < BT; ++b) acc[b] = 0.f;
-#pragma unroll
-          for (int it = 0; it < kXregIt; ++it) {
-            if (it < nit) {
-#pragma unroll
-              for (int b = 0; b < BT; ++b) acc[b] += dot8(wv[k][it], xr[it][b]);
-            }
-          }
-#pragma unroll
-          for (int b = 0; b < BT; ++b) acc[b] = warp_sum(acc[b]);
-          const int ul = d.ul0 + first + k * NSLOT;
-          if (lane == 0) {
-#pragma unroll
-            for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = acc[b];
-          }
-        }
-      }
-    }
+    load_xreg<BT>(io, K, xs, cb, ce, nit, xr);
+    ok = consume_xreg<KIND, BT>(sh, u0, n, R, sg, xr, cb, ce, nit, part);
   } else {
-    // ---- shared-memory path (b > 2 or very long rows): activations read
-    // from shared or global memory chunk by chunk; a stage is released after
-    // its rows are done.
-    for (int s = 0; s < n_stages && ok; ++s) {
-      const int slot = s % NS;
-      int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(&full[slot], (s / NS) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
-      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-      if (!w_ok) {
+    // shared-memory path (b > 2 or very long rows): activations read from
+    // shared or global memory chunk by chunk; a stage is released after its
+    // rows are done
+    const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
+    const int total = count_stages<KIND>(sh, u0, n);
+    for (int s = 0; s < total && ok; ++s, ++sg) {
+      if (!consumer_wait(R, sg)) {
         ok = false;
         break;
       }
-      (void)mbar_try_wait(&full[slot], (s / NS) & 1);  // completed phase: acquire for every lane
-      const StageDesc d = desc[s];
+      const int slot = sg % R.ns;
+      const StageDesc d = nth_stage<KIND>(sh, u0, n, s);
       for (int i = my_slot; i < d.nrows; i += NSLOT) {
-        const uint4* wr = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes +
+        const uint4* wr = reinterpret_cast<const uint4*>(R.base + static_cast<size_t>(slot) * R.slot_bytes +
                                                          static_cast<size_t>(i) * row_bytes);
         float acc[BT];
 #pragma unroll
         for (int b = 0; b < BT; ++b) acc[b] = 0.f;
-        for (int it0 = 0; it0 < nit; it0 += kMaxIt) {
+        const int nitb = ce > cb ? (ce - cb + 31) / 32 : 0;
+        for (int it0 = 0; it0 < nitb; it0 += kMaxIt) {
           uint4 wv[kMaxIt];
 #pragma unroll
           for (int it = 0; it < kMaxIt; ++it) {
             const int c = cb + lane + 32 * (it0 + it);
-            wv[it] = (it0 + it < nit && c < ce) ? wr[c] : make_uint4(0u, 0u, 0u, 0u);
+            wv[it] = (it0 + it < nitb && c < ce) ? wr[c] : make_uint4(0u, 0u, 0u, 0u);
           }
 #pragma unroll
           for (int it = 0; it < kMaxIt; ++it) {
-            if (it0 + it < nit) {
+            if (it0 + it < nitb) {
               const int c = min(cb + lane + 32 * (it0 + it), C - 1);
 #pragma unroll
               for (int b = 0; b < BT; ++b) {
                 float xv[8];
                 float4 lo, hi;
-                if (a.x_smem) {
+                if (io.x_smem) {
                   lo = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K)[c];
                   hi = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K + K / 2)[c];
                 } else {
-                  const float4* xp = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(b) * K) + 2 * c;
+                  const float4* xp = reinterpret_cast<const float4*>(io.x + static_cast<size_t>(b) * K) + 2 * c;
                   lo = __ldg(xp);
                   hi = __ldg(xp + 1);
                 }
@@ -493,183 +725,30 @@ __global__ void __launch_bounds__(kGemvThreads, BT == 1 ? 2 : 1) gemv_kernel(con
           const uint32_t row = static_cast<uint32_t>(u0 + ul);
 #pragma unroll
           for (int b = 0; b < BT; ++b) {
-            if (b < B) {
-              if (a.logits && lane == 0) a.logits[static_cast<size_t>(b) * a.n_units + row] = acc[b];
-              // a warp's rows arrive in increasing order: strict > keeps the lowest index
-              if (acc[b] > best_v[b] || best_i[b] == 0xFFFFFFFFu) {
-                best_v[b] = acc[b];
-                best_i[b] = row;
-              }
+            if (b < io.B) {
+              if (io.logits && lane == 0) io.logits[static_cast<size_t>(b) * sh.n_units + row] = acc[b];
+              better(best_v[b], best_i[b], acc[b], row);
             }
           }
         } else {
           if (lane == 0) {
 #pragma unroll
-            for (int b = 0; b < BT; ++b)
-              part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = acc[b];
+            for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = acc[b];
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (lane == 0) mbar_arrive(&R.empty[slot]);
     }
   }
 
   asm volatile("bar.sync 2, 288;" ::: "memory");  // ring no longer read: the producer may drain and leave
-  const bool aborted = *abort_flag != 0;
-
-  // --------------------------------------------------------------- epilogues
+  if (*abort_flag || !ok) return;
   if constexpr (KIND == kKindHead) {
-    if constexpr (XREG) {
-      // logits from the partial sums: thread t takes rows t, t+256, ...
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      for (int ul = threadIdx.x; ul < n_cta_units; ul += kConsumerThreads) {
-        const uint32_t row = static_cast<uint32_t>(u0 + ul);
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          if (b < B) {
-            float v = 0.f;
-            for (int p = 0; p < P; ++p) v += part[(static_cast<size_t>(ul) * P + p) * BT + b];
-            if (a.logits) a.logits[static_cast<size_t>(b) * a.n_units + row] = v;
-            if (v > best_v[b] || best_i[b] == 0xFFFFFFFFu) {  // increasing rows: strict > keeps the lowest
-              best_v[b] = v;
-              best_i[b] = row;
-            }
-          }
-        }
-      }
-      // warp-level argmax (value, then lower index) into lane 0
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, best_v[b], o);
-          const uint32_t oi = __shfl_xor_sync(0xffffffffu, best_i[b], o);
-          if (oi != 0xFFFFFFFFu &&
-              (best_i[b] == 0xFFFFFFFFu || ov > best_v[b] || (ov == best_v[b] && oi < best_i[b]))) {
-            best_v[b] = ov;
-            best_i[b] = oi;
-          }
-        }
-      }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        head_val[warp * kMaxBatch + b] = best_v[b];
-        head_idx[warp * kMaxBatch + b] = best_i[b];
-      }
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (threadIdx.x < B && !aborted) {
-      const int b = threadIdx.x;
-      float bv = -INFINITY;
-      uint32_t bi = 0xFFFFFFFFu;
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float v = head_val[w * kMaxBatch + b];
-        const uint32_t ix = head_idx[w * kMaxBatch + b];
-        if (ix == 0xFFFFFFFFu) continue;
-        if (bi == 0xFFFFFFFFu || v > bv || (v == bv && ix < bi)) {
-          bv = v;
-          bi = ix;
-        }
-      }
-      if (bi != 0xFFFFFFFFu) atomicMax(&a.argmax_keys[b], argmax_key(bv, bi));
-    }
-    __threadfence();
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (threadIdx.x == 0) {
-      const unsigned int t = atomicAdd(a.ticket, 1u);
-      *is_last = (t == gridDim.x - 1) ? 1 : 0;
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (*is_last && warp == 0) {
-      __threadfence();
-      int32_t emit = 0;
-      bool row_done = true;
-      const int b = lane;
-      if (b < B) {
-        const unsigned long long key = atomicExch(&a.argmax_keys[b], 0ull);
-        const int32_t tok = static_cast<int32_t>(argmax_key_index(key));
-        if (a.token_out) a.token_out[b] = tok;
-        if (a.book.enabled) {
-          Ctrl* c = a.book.ctrl;
-          const int eos = c->eos_id;
-          emit = a.book.done[b] ? eos : tok;
-          if (eos >= 0 && emit == eos) a.book.done[b] = 1;
-          row_done = a.book.done[b] != 0;
-          const int step = c->step;
-          if (c->out_tokens) {
-            if (step < c->out_cap)
-              c->out_tokens[static_cast<size_t>(b) * c->out_cap + step] = emit;
-            else
-              atomicOr(a.err, kErrOutRange);
-          }
-          a.book.token[b] = emit;
-          a.book.pos[b] += 1;
-        }
-      }
-      const unsigned all = __all_sync(0xffffffffu, row_done);
-      if (lane == 0) {
-        if (a.book.enabled) {
-          a.book.ctrl->all_done = all ? 1 : 0;
-          a.book.ctrl->step += 1;
-        }
-        atomicExch(a.ticket, 0u);
-      }
-    }
-    return;
+    head_epilogue<BT>(sh, io, u0, n, part, XREG, best_v, best_i, head_val, head_idx, is_last);
   } else {
-    if (aborted) return;
-    const int n_out = n_cta_units * B;
-    for (int idx = threadIdx.x; idx < n_out; idx += kConsumerThreads) {
-      const int ul = idx / B;
-      const int b = idx - ul * B;
-      const int u = u0 + ul;
-      float v[RU];
-#pragma unroll
-      for (int r = 0; r < RU; ++r) {
-        float sum = 0.f;
-        for (int p = 0; p < P; ++p) sum += part[((static_cast<size_t>(ul) * RU + r) * P + p) * BT + b];
-        v[r] = sum;
-      }
-      if constexpr (KIND == kKindResid) {
-        float* dst = a.out + static_cast<size_t>(b) * a.n_units + u;
-        *dst = *dst + v[0];
-      } else if constexpr (KIND == kKindGLU) {
-        a.out[static_cast<size_t>(b) * a.n_units + u] = silu_f32(v[0]) * v[1];
-      } else {  // kKindQKV
-        const int half = a.D >> 1;
-        const int hh = u / half;
-        const int j = u - hh * half;
-        const int p = a.pos[b];
-        float lo = v[0], hi = v[1];
-        if (hh < a.Hq + a.Hkv) {
-          float cs, sn;
-          rope_cos_sin(p, a.inv_freq[j], &cs, &sn);
-          const float l2 = lo * cs - hi * sn;
-          const float h2 = hi * cs + lo * sn;
-          lo = l2;
-          hi = h2;
-        }
-        if (hh < a.Hq) {
-          float* q = a.out + static_cast<size_t>(b) * a.Hq * a.D + static_cast<size_t>(hh) * a.D;
-          q[j] = lo;
-          q[j + half] = hi;
-        } else {
-          if (p < 0 || p >= a.S_max) {
-            atomicOr(a.err, kErrPosRange);
-            continue;
-          }
-          const bool is_k = hh < a.Hq + a.Hkv;
-          const int g = is_k ? hh - a.Hq : hh - a.Hq - a.Hkv;
-          uint16_t* cache = is_k ? a.k_cache : a.v_cache;
-          uint16_t* dst = cache + ((static_cast<size_t>(b) * a.Hkv + g) * a.S_max + p) * a.D;
-          dst[j] = f32_to_bf16(lo);
-          dst[j + half] = f32_to_bf16(hi);
-        }
-      }
-    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    gemv_epilogue<KIND, BT>(sh, io, u0, n, part, a.inv_freq);
   }
 }
 

@@ -5,6 +5,7 @@
 
 #include "dec_attn.cuh"
 #include "dec_kernels.cuh"
+#include "dec_step.cuh"
 
 namespace dec {
 
@@ -63,5 +64,9 @@ cudaError_t allow_smem_glu();
 cudaError_t allow_smem_resid();
 cudaError_t allow_smem_head();
 cudaError_t allow_smem_attn();
+cudaError_t allow_smem_step();
+
+// One persistent whole-step launch (cooperative: all CTAs resident).
+cudaError_t launch_step(int BT, const StepArgs& a, int grid, uint32_t smem, cudaStream_t st);
 
 }  // namespace dec

@@ -1,0 +1,438 @@
+// Persistent whole-step kernel: one launch runs a full decode step -- every
+// layer's QKV+RoPE, attention, o_proj, gate/up and down, then the LM head and
+// the bookkeeping -- with one CTA per SM.
+//
+// Why: a decode step is ~180 short, memory-bound GEMVs; launched one by one,
+// each pays a ring fill, a prologue and a tail, and the weight stream stops at
+// every boundary.  Here one producer warp per CTA streams the CTA's share of
+// ALL the step's weights (layer after layer) through a ring of shared-memory
+// stages without ever waiting for the math, and the eight consumer warps move
+// from phase to phase through grid-wide barriers.  While consumers wait at a
+// barrier (or work on attention) the producer is already filling the ring
+// with the next phase's rows, so HBM keeps streaming across phase boundaries.
+//
+// The arithmetic of every phase is the same device code as the single-op
+// kernels (same warp roles, lane mapping and reduction order), so a fused step
+// equals the composition of the single-op calls bit for bit.
+//
+// Cross-CTA waits (the grid barrier) are bounded: on expiry a CTA raises a
+// grid-wide abort word and an error bit, and every CTA stops at its next wait.
+#pragma once
+
+#include "dec_attn.cuh"
+#include "dec_kernels.cuh"
+
+namespace dec {
+
+constexpr int kStepMaxLayers = 64;
+constexpr uint32_t kStepSlotBytes = 40 * 1024;
+constexpr uint32_t kStepHeaderBytes = 2048;
+
+enum StepPhase : int { kPhQKV = 0, kPhO = 1, kPhGLU = 2, kPhDown = 3, kPhHead = 4, kNumPhases = 5 };
+
+struct StepLayer {
+  const uint16_t* attn_norm;
+  const uint16_t* wq;
+  const uint16_t* wk;
+  const uint16_t* wv;
+  const uint16_t* wo;
+  const uint16_t* mlp_norm;
+  const uint16_t* wg;
+  const uint16_t* wu;
+  const uint16_t* wd;
+  uint16_t* kc;
+  uint16_t* vc;
+};
+
+struct StepPlan {
+  int parts;
+  int chunks_per_part;
+  int rows_per_stage;
+};
+
+struct StepArgs {
+  int L, H, Hq, Hkv, D, I, V, B, S_max;
+  float eps;
+  const uint16_t* embed;       // null: the residual stream holds the input
+  const uint16_t* final_norm;
+  const uint16_t* lm_head;     // null: no head (positions still advance)
+  int32_t* token;
+  int32_t* pos;
+  float* resid;
+  float* q;
+  float* o;
+  float* h;
+  float* attn_part;
+  unsigned int* attn_tickets;
+  int n_split;
+  float attn_scale;
+  unsigned long long* argmax_keys;
+  unsigned int* head_ticket;
+  StepBook book;
+  unsigned int* grid_bar;      // sense-reversing grid barrier word (zero at rest)
+  int* abort_all;              // raised when any CTA gives up
+  uint32_t* err;
+  int n_slots;
+  uint32_t off_x, off_part, off_attn, off_ring;
+  StepPlan plan[kNumPhases];
+  double inv_freq[64];
+  StepLayer layers[kStepMaxLayers];
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier over the consumer warps of all CTAs (sense-reversing: the
+// word's top bit flips once per barrier and the word returns to its start
+// value, so it needs no reset).  Bounded: returns false when the grid aborts.
+__device__ inline bool grid_sync(const StepArgs& a, volatile int* abort_cta) {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  int bad = 0;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
+    const unsigned int old = atomicAdd(a.grid_bar, inc);
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
+      if ((ld_acquire_u32(a.grid_bar) ^ old) & 0x80000000u) break;
+      if ((i & 31u) == 31u) {
+        if (*reinterpret_cast<volatile int*>(a.abort_all)) {
+          bad = 1;
+          break;
+        }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.err, kErrGridWait);
+          atomicExch(a.abort_all, 1);
+          bad = 1;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    if (bad) *abort_cta = 1;
+  }
+  return !consumers_barrier_or(bad != 0);
+}
+
+// Rows and plan of one phase of one layer.
+__device__ __forceinline__ GemvShape phase_shape(const StepArgs& a, int ph, int l) {
+  GemvShape sh{};
+  const StepPlan& p = a.plan[ph];
+  sh.parts = p.parts;
+  sh.chunks_per_part = p.chunks_per_part;
+  sh.rows_per_stage = p.rows_per_stage;
+  sh.D = a.D;
+  sh.Hq = a.Hq;
+  sh.Hkv = a.Hkv;
+  if (ph == kPhHead) {
+    sh.w0 = a.lm_head;
+    sh.K = a.H;
+    sh.n_units = a.V;
+    return sh;
+  }
+  const StepLayer& w = a.layers[l];
+  switch (ph) {
+    case kPhQKV:
+      sh.w0 = w.wq;
+      sh.w1 = w.wk;
+      sh.w2 = w.wv;
+      sh.K = a.H;
+      sh.n_units = (a.Hq + 2 * a.Hkv) * (a.D / 2);
+      break;
+    case kPhO:
+      sh.w0 = w.wo;
+      sh.K = a.Hq * a.D;
+      sh.n_units = a.H;
+      break;
+    case kPhGLU:
+      sh.w0 = w.wg;
+      sh.w1 = w.wu;
+      sh.K = a.H;
+      sh.n_units = a.I;
+      break;
+    default:  // kPhDown
+      sh.w0 = w.wd;
+      sh.K = a.I;
+      sh.n_units = a.H;
+      break;
+  }
+  return sh;
+}
+
+template <int KIND>
+__device__ __forceinline__ bool produce_phase(const StepArgs& a, int ph, int l, const Ring& R, int& sg,
+                                              uint64_t policy) {
+  const GemvShape sh = phase_shape(a, ph, l);
+  int u0, n;
+  cta_units(sh.n_units, blockIdx.x, gridDim.x, &u0, &n);
+  return produce_stages<KIND>(sh, u0, n, R, sg, policy);
+}
+
+// One GEMV phase on the consumer side: activations, the stage stream, the
+// epilogue.  Returns false on abort.
+template <int KIND, int BT>
+__device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io, const Ring& R, int& sg, float* xs,
+                              float* red, float* part, float (&best_v)[BT], uint32_t (&best_i)[BT], float* head_val,
+                              uint32_t* head_idx, int* is_last) {
+  const GemvShape sh = phase_shape(a, ph, l);
+  int u0, n;
+  cta_units(sh.n_units, blockIdx.x, gridDim.x, &u0, &n);
+  const int K = sh.K;
+  if (io.x_smem) stage_activations<BT>(io, K, xs, red);
+  const int warp = threadIdx.x >> 5;
+  const int C = K / kChunkElems;
+  const int cb = (warp % sh.parts) * sh.chunks_per_part;
+  const int ce = min(C, cb + sh.chunks_per_part);
+  const int nit = ce > cb ? (ce - cb + 31) / 32 : 0;
+  float xr[kXregIt][BT][8];
+  load_xreg<BT>(io, K, xs, cb, ce, nit, xr);
+  const bool ok = consume_xreg<KIND, BT>(sh, u0, n, R, sg, xr, cb, ce, nit, part);
+  if (consumers_barrier_or(!ok || *R.abort)) return false;
+  if constexpr (KIND == kKindHead) {
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      best_v[b] = -INFINITY;
+      best_i[b] = 0xFFFFFFFFu;
+    }
+    head_epilogue<BT>(sh, io, u0, n, part, true, best_v, best_i, head_val, head_idx, is_last);
+  } else {
+    gemv_epilogue<KIND, BT>(sh, io, u0, n, part, a.inv_freq);
+  }
+  return true;
+}
+
+// Attention phase of layer l: work items (b, g, split) go round-robin over the
+// CTAs; each item streams its key range through two shared-memory tile slots
+// (bulk copies issued by consumer thread 0) and finishes like the
+// single-op attention kernel (partials + last-split merge).
+template <int D>
+__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, uint64_t* tfull, int (&tcount)[2],
+                                volatile int* abort_cta, int* is_last) {
+  constexpr uint32_t kRowBytes = D * 2;
+  constexpr uint32_t kTileBytes = kAttnTile * kRowBytes;
+  constexpr int kMaxSlots = attn_slots<D>();
+  float* m_run = reinterpret_cast<float*>(area);
+  float* l_run = m_run + kAttnMaxGroup;
+  float* corr = l_run + kAttnMaxGroup;
+  float* q_s = reinterpret_cast<float*>(area + 256);
+  float* s_s = q_s + kAttnMaxGroup * D;
+  unsigned char* tiles = reinterpret_cast<unsigned char*>(s_s + kAttnMaxGroup * kAttnTile);
+  const int tid = threadIdx.x;
+  const int G = a.Hq / a.Hkv;
+  const StepLayer& w = a.layers[l];
+  AttnArgs t{};
+  t.q = a.q;
+  t.k_cache = w.kc;
+  t.v_cache = w.vc;
+  t.pos = a.pos;
+  t.o = a.o;
+  t.part = a.attn_part;
+  t.tickets = a.attn_tickets;
+  t.Hq = a.Hq;
+  t.Hkv = a.Hkv;
+  t.D = D;
+  t.S_max = a.S_max;
+  t.n_split = a.n_split;
+  t.scale = a.attn_scale;
+  t.err = a.err;
+  const int items = a.B * a.Hkv * a.n_split;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int b = it / (a.Hkv * a.n_split);
+    const int rem = it - b * a.Hkv * a.n_split;
+    const int g = rem / a.n_split;
+    const int split = rem - g * a.n_split;
+    const int p = a.pos[b];
+    if (p < 0 || p >= a.S_max) {
+      if (split == 0 && g == 0 && tid == 0) atomicOr(a.err, kErrPosRange);
+      continue;
+    }
+    int chunk, n_active;
+    attn_plan(p + 1, a.n_split, &chunk, &n_active);
+    if (split >= n_active) continue;
+    const int k0 = split * chunk;
+    const int k1 = min(p + 1, k0 + chunk);
+    const int n_tiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
+    const size_t head_off = (static_cast<size_t>(b) * a.Hkv + g) * a.S_max;
+    const uint16_t* Kg = w.kc + head_off * D;
+    const uint16_t* Vg = w.vc + head_off * D;
+    auto issue = [&](int tt) {
+      const int slot = tt & 1;
+      const int j0 = k0 + tt * kAttnTile;
+      const int nk = min(kAttnTile, k1 - j0);
+      unsigned char* dst = tiles + static_cast<size_t>(slot) * 2 * kTileBytes;
+      mbar_arrive_expect_tx(&tfull[slot], 2u * nk * kRowBytes);
+      bulk_copy_g2s(dst, Kg + static_cast<size_t>(j0) * D, nk * kRowBytes, &tfull[slot], l2_policy_evict_last());
+      bulk_copy_g2s(dst + kTileBytes, Vg + static_cast<size_t>(j0) * D, nk * kRowBytes, &tfull[slot],
+                    l2_policy_evict_last());
+    };
+    if (tid == 0) {
+      // the cache slot of the current token was written by generic stores
+      // (QKV epilogue, any CTA): order them before the async-proxy reads
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      for (int tt = 0; tt < min(n_tiles, 2); ++tt) issue(tt);
+    }
+    for (int i = tid; i < G * D; i += kConsumerThreads)
+      q_s[i] = a.q[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i];
+    if (tid < G) {
+      m_run[tid] = -INFINITY;
+      l_run[tid] = 0.f;
+    }
+    float acc0[kMaxSlots], acc1[kMaxSlots];
+#pragma unroll
+    for (int i = 0; i < kMaxSlots; ++i) acc0[i] = acc1[i] = 0.f;
+    for (int tt = 0; tt < n_tiles; ++tt) {
+      const int slot = tt & 1;
+      int ok = 1;
+      if (tid == 0) {
+        ok = mbar_wait(&tfull[slot], tcount[slot] & 1, abort_cta, a.err, kErrWaitFull) ? 1 : 0;
+        if (!ok) atomicExch(a.abort_all, 1);
+      }
+      tcount[slot] += 1;
+      if (consumers_barrier_or(!ok)) return false;
+      const int nk = min(kAttnTile, k1 - (k0 + tt * kAttnTile));
+      const uint4* Ks = reinterpret_cast<const uint4*>(tiles + static_cast<size_t>(slot) * 2 * kTileBytes);
+      const uint32_t* Vs =
+          reinterpret_cast<const uint32_t*>(tiles + static_cast<size_t>(slot) * 2 * kTileBytes + kTileBytes);
+      attn_tile_math<D>(Ks, Vs, nk, G, a.attn_scale, q_s, s_s, m_run, l_run, corr, acc0, acc1);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (tid == 0 && tt + 2 < n_tiles) issue(tt + 2);
+    }
+    attn_finish<D>(t, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last, reinterpret_cast<float*>(tiles));
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+  }
+  return true;
+}
+
+template <int BT, int D>
+__global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;                                   // 2 attention tile barriers
+  volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + 512);
+  int* is_last = reinterpret_cast<int*>(smem + 516);
+  float* red = reinterpret_cast<float*>(smem + 576);                      // 8 floats
+  float* head_val = reinterpret_cast<float*>(smem + 640);                 // [8][kMaxBatch]
+  uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 640 + 4 * kConsumerWarps * kMaxBatch);
+  float* xs = reinterpret_cast<float*>(smem + a.off_x);
+  float* part = reinterpret_cast<float*>(smem + a.off_part);
+  unsigned char* attn_area = smem + a.off_attn;
+  const Ring R{full, empty, smem + a.off_ring, a.n_slots, kStepSlotBytes, abort_cta, a.err};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R.ns; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    *abort_cta = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------- producer warp
+    int sg = 0;
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      bool ok = true;
+      for (int l = 0; l < a.L && ok; ++l) {
+        ok = produce_phase<kKindQKV>(a, kPhQKV, l, R, sg, policy) &&
+             produce_phase<kKindResid>(a, kPhO, l, R, sg, policy) &&
+             produce_phase<kKindGLU>(a, kPhGLU, l, R, sg, policy) &&
+             produce_phase<kKindResid>(a, kPhDown, l, R, sg, policy);
+      }
+      if (ok && a.lm_head) produce_phase<kKindHead>(a, kPhHead, 0, R, sg, policy);
+    }
+    __syncwarp();
+    asm volatile("bar.sync 2, 288;" ::: "memory");
+    if (lane == 0) drain_ring(R, sg);
+    return;
+  }
+
+  // --------------------------------------------------------------- consumer warps
+  int sg = 0;
+  int tcount[2] = {0, 0};
+  float best_v[BT];
+  uint32_t best_i[BT];
+  bool ok = true;
+  GemvIO io{};
+  io.B = a.B;
+  io.eps = a.eps;
+  io.err = a.err;
+  io.S_max = a.S_max;
+  io.pos = a.pos;
+  for (int l = 0; l < a.L && ok; ++l) {
+    const StepLayer& w = a.layers[l];
+    // q, k, v with RoPE; k, v into the cache
+    io.x = a.resid;
+    io.norm_gamma = w.attn_norm;
+    io.tokens = (l == 0 && a.embed) ? a.token : nullptr;
+    io.embed = a.embed;
+    io.vocab = a.V;
+    io.resid_store = a.resid;
+    io.x_smem = 1;
+    io.out = a.q;
+    io.k_cache = w.kc;
+    io.v_cache = w.vc;
+    ok = consume_phase<kKindQKV, BT>(a, kPhQKV, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
+                                     is_last) &&
+         grid_sync(a, abort_cta);
+    if (!ok) break;
+    ok = attention_phase<D>(a, l, attn_area, tfull, tcount, abort_cta, is_last) && grid_sync(a, abort_cta);
+    if (!ok) break;
+    // r += Wo o
+    io.x = a.o;
+    io.norm_gamma = nullptr;
+    io.tokens = nullptr;
+    io.resid_store = nullptr;
+    io.x_smem = 0;
+    io.out = a.resid;
+    ok = consume_phase<kKindResid, BT>(a, kPhO, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
+                                       is_last) &&
+         grid_sync(a, abort_cta);
+    if (!ok) break;
+    // h = silu(Wg y) * (Wu y), y = norm(r)
+    io.x = a.resid;
+    io.norm_gamma = w.mlp_norm;
+    io.x_smem = 1;
+    io.out = a.h;
+    ok = consume_phase<kKindGLU, BT>(a, kPhGLU, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
+                                     is_last) &&
+         grid_sync(a, abort_cta);
+    if (!ok) break;
+    // r += Wd h
+    io.x = a.h;
+    io.norm_gamma = nullptr;
+    io.x_smem = 0;
+    io.out = a.resid;
+    ok = consume_phase<kKindResid, BT>(a, kPhDown, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
+                                       is_last) &&
+         grid_sync(a, abort_cta);
+  }
+  if (ok) {
+    if (a.lm_head) {
+      io.x = a.resid;
+      io.norm_gamma = a.final_norm;
+      io.x_smem = 1;
+      io.out = nullptr;
+      io.logits = nullptr;
+      io.argmax_keys = a.argmax_keys;
+      io.ticket = a.head_ticket;
+      io.token_out = nullptr;
+      io.book = a.book;
+      consume_phase<kKindHead, BT>(a, kPhHead, 0, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
+                                   is_last);
+    } else if (blockIdx.x == 0 && threadIdx.x < a.B) {
+      a.pos[threadIdx.x] += 1;
+    }
+  }
+  asm volatile("bar.sync 2, 288;" ::: "memory");  // the producer may drain and leave
+}
+
+}  // namespace dec
