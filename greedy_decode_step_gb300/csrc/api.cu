@@ -304,11 +304,15 @@ void fill_inv_freq(GemvArgs& a, int D, float theta) {
 
 // ------------------------------------------------------------------------------- attention planning
 
+// Key splits per (row, KV head): one wave of work items (one per SM) while
+// the cache is short, more splits once a split would cover over ~1024 keys on
+// average (long or batched caches, where balance matters more than latency).
 int attn_splits(int B, int Hkv, int S_max, int sms, int requested) {
   const int cap = std::max(1, (S_max + kAttnChunkMin - 1) / kAttnChunkMin);
   if (requested > 0) return std::min(requested, cap);
-  const int want = (8 * sms + B * Hkv - 1) / (B * Hkv);
-  return std::max(1, std::min(want, cap));
+  const int one_wave = std::max(1, sms / (B * Hkv));
+  const int by_len = static_cast<int>(static_cast<long long>(S_max) * B * Hkv / (static_cast<long long>(sms) * 1024)) + 1;
+  return std::max(1, std::min(std::max(one_wave, by_len), cap));
 }
 
 size_t attn_part_bytes(int B, int Hq, int Hkv, int D, int n_split) {
@@ -511,8 +515,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
     part = std::max(part, pb);
   }
   const uint32_t x_bytes = static_cast<uint32_t>(*BT) * H * 4u;
-  const uint32_t attn_bytes = 256u + kAttnMaxGroup * D * 4u + kAttnMaxGroup * kAttnTile * 4u +
-                              2u * 2u * kAttnTile * D * 2u;
+  const uint32_t attn_bytes = 256u + kAttnMaxGroup * D * 4u + kAttnMaxGroup * kAttnTile * 4u + 2u * kAttnTile * D * 2u;
   a->off_x = kStepHeaderBytes;
   a->off_part = align_up(a->off_x + x_bytes, 16);
   a->off_attn = align_up(a->off_part + part, 128);
@@ -520,7 +523,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   if (a->off_ring + 2 * kStepSlotBytes > kSmemMax) return false;
   a->n_slots = std::min<int>(4, static_cast<int>((kSmemMax - a->off_ring) / kStepSlotBytes));
   // the log-sum-exp merge uses the tile area as scratch
-  if (2u * (static_cast<uint32_t>(w.n_split) * (Hq / Hkv) + Hq / Hkv) * 4u > 2u * 2u * kAttnTile * D * 2u) return false;
+  if (2u * (static_cast<uint32_t>(w.n_split) * (Hq / Hkv) + Hq / Hkv) * 4u > 2u * kAttnTile * D * 2u) return false;
   *smem = a->off_ring + static_cast<uint32_t>(a->n_slots) * kStepSlotBytes;
   a->L = m->n_layers;
   a->H = H;

@@ -321,7 +321,7 @@ __device__ void stage_activations(const GemvIO& io, int K, float* xs, float* red
       }
     } else {
       const float* src = io.x + static_cast<size_t>(b) * K;
-      for (int i = threadIdx.x; i < K; i += kConsumerThreads) xb[xsplit(i, K)] = src[i];
+      for (int i = threadIdx.x; i < K; i += kConsumerThreads) xb[xsplit(i, K)] = __ldcg(src + i);
     }
     if (io.norm_gamma) {
       asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -356,8 +356,8 @@ __device__ __forceinline__ void load_xreg(const GemvIO& io, int K, const float* 
           hi = reinterpret_cast<const float4*>(xs + static_cast<size_t>(b) * K + K / 2)[c];
         } else if (b < io.B) {
           const float4* xp = reinterpret_cast<const float4*>(io.x + static_cast<size_t>(b) * K) + 2 * c;
-          lo = xp[0];
-          hi = xp[1];
+          lo = __ldcg(xp);
+          hi = __ldcg(xp + 1);
         }
       }
       xr[it][b][0] = lo.x; xr[it][b][1] = lo.y; xr[it][b][2] = lo.z; xr[it][b][3] = lo.w;
@@ -403,26 +403,47 @@ __device__ bool consume_xreg(const GemvShape& sh, int u0, int n, const Ring& R, 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&R.empty[slot]);
+    // Both rows at once (absent rows hold zeros): paired fp32 FMAs into two
+    // accumulator pairs per (row, batch row), then one butterfly for the two
+    // rows -- the first exchange hands row 1 to the upper half-warp.
+    float sum[kXregRows][BT];
 #pragma unroll
     for (int k = 0; k < kXregRows; ++k) {
-      if (k < nmine) {
-        float acc[BT];
 #pragma unroll
-        for (int b = 0; b < BT; ++b) acc[b] = 0.f;
+      for (int b = 0; b < BT; ++b) {
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
         for (int it = 0; it < kXregIt; ++it) {
           if (it < nit) {
-#pragma unroll
-            for (int b = 0; b < BT; ++b) acc[b] += dot8(wv[k][it], xr[it][b]);
+            const uint4 w = wv[k][it];
+            const float* x = xr[it][b];
+            a0 = __ffma2_rn(make_float2(bf16lo(w.x), bf16hi(w.x)), make_float2(x[0], x[1]), a0);
+            a1 = __ffma2_rn(make_float2(bf16lo(w.y), bf16hi(w.y)), make_float2(x[2], x[3]), a1);
+            a0 = __ffma2_rn(make_float2(bf16lo(w.z), bf16hi(w.z)), make_float2(x[4], x[5]), a0);
+            a1 = __ffma2_rn(make_float2(bf16lo(w.w), bf16hi(w.w)), make_float2(x[6], x[7]), a1);
           }
         }
+        sum[k][b] = (a0.x + a1.x) + (a0.y + a1.y);
+      }
+    }
+    static_assert(kXregRows == 2, "the butterfly pairs two rows");
+    const bool upper = lane >= 16;
 #pragma unroll
-        for (int b = 0; b < BT; ++b) acc[b] = warp_sum(acc[b]);
+    for (int b = 0; b < BT; ++b) {
+      float v = upper ? sum[1][b] : sum[0][b];
+      v += __shfl_xor_sync(0xffffffffu, upper ? sum[0][b] : sum[1][b], 16);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      sum[0][b] = v;
+    }
+    if ((lane & 15) == 0) {
+      const int k = upper ? 1 : 0;
+      if (k < nmine) {
         const int ul = d.ul0 + first + k * NSLOT;
-        if (lane == 0) {
 #pragma unroll
-          for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = acc[b];
-        }
+        for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = sum[0][b];
       }
     }
   }
@@ -450,14 +471,14 @@ __device__ void gemv_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int
     }
     if constexpr (KIND == kKindResid) {
       float* dst = io.out + static_cast<size_t>(b) * sh.n_units + u;
-      *dst = *dst + v[0];
+      *dst = __ldcg(dst) + v[0];
     } else if constexpr (KIND == kKindGLU) {
       io.out[static_cast<size_t>(b) * sh.n_units + u] = silu_f32(v[0]) * v[1];
     } else if constexpr (KIND == kKindQKV) {
       const int half = sh.D >> 1;
       const int hh = u / half;
       const int j = u - hh * half;
-      const int p = io.pos[b];
+      const int p = __ldcg(io.pos + b);
       float lo = v[0], hi = v[1];
       if (hh < sh.Hq + sh.Hkv) {
         float cs, sn;

@@ -205,21 +205,21 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
 }
 
 // Attention phase of layer l: work items (b, g, split) go round-robin over the
-// CTAs; each item streams its key range through two shared-memory tile slots
-// (bulk copies issued by consumer thread 0) and finishes like the
-// single-op attention kernel (partials + last-split merge).
+// CTAs (one per CTA while the cache is short); each item brings its query
+// vectors and key/value tiles into shared memory with plain 16-byte loads
+// through L2 (not the TMA engine, whose queue is full of the producer's
+// weight copies), runs the same tile math as the single-op attention kernel
+// and finishes the same way (partials + last-split merge).
 template <int D>
-__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, uint64_t* tfull, int (&tcount)[2],
-                                volatile int* abort_cta, int* is_last) {
-  constexpr uint32_t kRowBytes = D * 2;
-  constexpr uint32_t kTileBytes = kAttnTile * kRowBytes;
+__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, int* is_last) {
+  constexpr int kRowChunks = D / 8;  // 16-byte chunks per cache row
   constexpr int kMaxSlots = attn_slots<D>();
   float* m_run = reinterpret_cast<float*>(area);
   float* l_run = m_run + kAttnMaxGroup;
   float* corr = l_run + kAttnMaxGroup;
   float* q_s = reinterpret_cast<float*>(area + 256);
   float* s_s = q_s + kAttnMaxGroup * D;
-  unsigned char* tiles = reinterpret_cast<unsigned char*>(s_s + kAttnMaxGroup * kAttnTile);
+  uint4* tile = reinterpret_cast<uint4*>(s_s + kAttnMaxGroup * kAttnTile);  // K rows then V rows
   const int tid = threadIdx.x;
   const int G = a.Hq / a.Hkv;
   const StepLayer& w = a.layers[l];
@@ -244,7 +244,7 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, u
     const int rem = it - b * a.Hkv * a.n_split;
     const int g = rem / a.n_split;
     const int split = rem - g * a.n_split;
-    const int p = a.pos[b];
+    const int p = __ldcg(a.pos + b);
     if (p < 0 || p >= a.S_max) {
       if (split == 0 && g == 0 && tid == 0) atomicOr(a.err, kErrPosRange);
       continue;
@@ -256,26 +256,10 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, u
     const int k1 = min(p + 1, k0 + chunk);
     const int n_tiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
     const size_t head_off = (static_cast<size_t>(b) * a.Hkv + g) * a.S_max;
-    const uint16_t* Kg = w.kc + head_off * D;
-    const uint16_t* Vg = w.vc + head_off * D;
-    auto issue = [&](int tt) {
-      const int slot = tt & 1;
-      const int j0 = k0 + tt * kAttnTile;
-      const int nk = min(kAttnTile, k1 - j0);
-      unsigned char* dst = tiles + static_cast<size_t>(slot) * 2 * kTileBytes;
-      mbar_arrive_expect_tx(&tfull[slot], 2u * nk * kRowBytes);
-      bulk_copy_g2s(dst, Kg + static_cast<size_t>(j0) * D, nk * kRowBytes, &tfull[slot], l2_policy_evict_last());
-      bulk_copy_g2s(dst + kTileBytes, Vg + static_cast<size_t>(j0) * D, nk * kRowBytes, &tfull[slot],
-                    l2_policy_evict_last());
-    };
-    if (tid == 0) {
-      // the cache slot of the current token was written by generic stores
-      // (QKV epilogue, any CTA): order them before the async-proxy reads
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      for (int tt = 0; tt < min(n_tiles, 2); ++tt) issue(tt);
-    }
+    const uint4* Kg = reinterpret_cast<const uint4*>(w.kc + head_off * D);
+    const uint4* Vg = reinterpret_cast<const uint4*>(w.vc + head_off * D);
     for (int i = tid; i < G * D; i += kConsumerThreads)
-      q_s[i] = a.q[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i];
+      q_s[i] = __ldcg(a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i);
     if (tid < G) {
       m_run[tid] = -INFINITY;
       l_run[tid] = 0.f;
@@ -284,23 +268,21 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, u
 #pragma unroll
     for (int i = 0; i < kMaxSlots; ++i) acc0[i] = acc1[i] = 0.f;
     for (int tt = 0; tt < n_tiles; ++tt) {
-      const int slot = tt & 1;
-      int ok = 1;
-      if (tid == 0) {
-        ok = mbar_wait(&tfull[slot], tcount[slot] & 1, abort_cta, a.err, kErrWaitFull) ? 1 : 0;
-        if (!ok) atomicExch(a.abort_all, 1);
+      const int j0 = k0 + tt * kAttnTile;
+      const int nk = min(kAttnTile, k1 - j0);
+      const int n16 = nk * kRowChunks;
+      for (int i = tid; i < 2 * n16; i += kConsumerThreads) {
+        const bool is_v = i >= n16;
+        const int c = is_v ? i - n16 : i;
+        tile[(is_v ? kAttnTile * kRowChunks : 0) + c] =
+            __ldcg((is_v ? Vg : Kg) + static_cast<size_t>(j0) * kRowChunks + c);
       }
-      tcount[slot] += 1;
-      if (consumers_barrier_or(!ok)) return false;
-      const int nk = min(kAttnTile, k1 - (k0 + tt * kAttnTile));
-      const uint4* Ks = reinterpret_cast<const uint4*>(tiles + static_cast<size_t>(slot) * 2 * kTileBytes);
-      const uint32_t* Vs =
-          reinterpret_cast<const uint32_t*>(tiles + static_cast<size_t>(slot) * 2 * kTileBytes + kTileBytes);
-      attn_tile_math<D>(Ks, Vs, nk, G, a.attn_scale, q_s, s_s, m_run, l_run, corr, acc0, acc1);
       asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (tid == 0 && tt + 2 < n_tiles) issue(tt + 2);
+      attn_tile_math<D>(tile, reinterpret_cast<const uint32_t*>(tile + kAttnTile * kRowChunks), nk, G, a.attn_scale,
+                        q_s, s_s, m_run, l_run, corr, acc0, acc1);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
     }
-    attn_finish<D>(t, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last, reinterpret_cast<float*>(tiles));
+    attn_finish<D>(t, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last, reinterpret_cast<float*>(tile));
     asm volatile("bar.sync 1, 256;" ::: "memory");
   }
   return true;
@@ -311,7 +293,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint64_t* tfull = empty + kMaxStages;                                   // 2 attention tile barriers
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + 512);
   int* is_last = reinterpret_cast<int*>(smem + 516);
   float* red = reinterpret_cast<float*>(smem + 576);                      // 8 floats
@@ -328,8 +309,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
-    mbar_init(&tfull[0], 1);
-    mbar_init(&tfull[1], 1);
     *abort_cta = 0;
     fence_mbar_init();
   }
@@ -357,7 +336,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
 
   // --------------------------------------------------------------- consumer warps
   int sg = 0;
-  int tcount[2] = {0, 0};
   float best_v[BT];
   uint32_t best_i[BT];
   bool ok = true;
@@ -384,7 +362,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
                                      is_last) &&
          grid_sync(a, abort_cta);
     if (!ok) break;
-    ok = attention_phase<D>(a, l, attn_area, tfull, tcount, abort_cta, is_last) && grid_sync(a, abort_cta);
+    ok = attention_phase<D>(a, l, attn_area, is_last) && grid_sync(a, abort_cta);
     if (!ok) break;
     // r += Wo o
     io.x = a.o;
