@@ -522,8 +522,6 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   a->off_ring = align_up(a->off_attn + attn_bytes, 128);
   if (a->off_ring + 2 * kStepSlotBytes > kSmemMax) return false;
   a->n_slots = std::min<int>(4, static_cast<int>((kSmemMax - a->off_ring) / kStepSlotBytes));
-  // the log-sum-exp merge uses the tile area as scratch
-  if (2u * (static_cast<uint32_t>(w.n_split) * (Hq / Hkv) + Hq / Hkv) * 4u > 2u * kAttnTile * D * 2u) return false;
   *smem = a->off_ring + static_cast<uint32_t>(a->n_slots) * kStepSlotBytes;
   a->L = m->n_layers;
   a->H = H;

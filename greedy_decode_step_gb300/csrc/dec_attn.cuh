@@ -20,6 +20,7 @@ constexpr int kAttnTile = 64;       // keys per stage
 constexpr int kAttnChunkMin = 32;   // fewest keys a split is given
 constexpr int kAttnMaxGroup = 16;   // query heads per KV head
 constexpr int kAttnSlots = 2;
+constexpr int kAttnMergeBatch = 20;  // splits folded per batch of loads in the merge
 constexpr int kAttnWarps = 8;        // consumer warps
 constexpr int kAttnConsumers = 256;
 
@@ -138,12 +139,11 @@ __device__ __forceinline__ void attn_tile_math(const uint4* Ks, const uint32_t* 
 // After the last tile: with one split the output is final; otherwise the
 // split's partial (unnormalised accumulator, running max and sum) goes to
 // global memory and the last split of the group to finish (atomic ticket)
-// merges all of them by log-sum-exp weights.  `scratch` is shared memory the
-// merge may use (at least 2*(n_split*G + G) floats).  256 consumer threads.
+// merges all of them by log-sum-exp weights.  256 consumer threads.
 template <int D>
 __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int split, int n_active, int G,
                                             const float (&acc0)[attn_slots<D>()], const float (&acc1)[attn_slots<D>()],
-                                            const float* m_run, const float* l_run, int* is_last, float* scratch) {
+                                            const float* m_run, const float* l_run, int* is_last) {
   constexpr int kPairsPerHead = D / 2;
   constexpr int kMaxSlots = attn_slots<D>();
   const int tid = threadIdx.x;
@@ -186,46 +186,53 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
   asm volatile("bar.sync 1, 256;" ::: "memory");
   if (!*is_last) return;
   __threadfence();
-  // Merge by log-sum-exp weights: o = sum_s w_s acc_s with
-  // w_s = exp(m_s - M) / sum_s' exp(m_s' - M) l_s'.  The split maxima and
-  // sums are staged in shared memory (the ring is free now) in one parallel
-  // pass, and each thread issues its accumulator loads together.
+  // Merge by log-sum-exp weights, o = sum_s exp(m_s - M) acc_s / sum_s exp(m_s - M) l_s,
+  // one thread per (head, dimension pair), folding the splits in batches
+  // whose loads (maximum, sum and the two accumulator entries of each split)
+  // are all in flight together; M is carried as a running maximum.
   const float* base = a.part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
-  float* ms = scratch;          // [n_active][G] split maxima, then weights
-  float* ls = ms + a.n_split * G;                      // [n_active][G] split sums
-  float* mh = ls + a.n_split * G;                      // [G] overall max, [G] 1 / overall sum
-  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
-    const int sp = i / G, h = i - sp * G;
-    ms[i] = __ldcg(base + sp * stride + G * D + h);
-    ls[i] = __ldcg(base + sp * stride + G * D + G + h);
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < n_active; ++sp) M = fmaxf(M, ms[sp * G + tid]);
-    float L = 0.f;
-    for (int sp = 0; sp < n_active; ++sp) L = fmaf(expf(ms[sp * G + tid] - M), ls[sp * G + tid], L);
-    mh[tid] = M;
-    mh[G + tid] = 1.0f / L;
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  for (int i = tid; i < n_active * G; i += kAttnConsumers) {
-    const int h = i % G;
-    ms[i] = expf(ms[i] - mh[h]) * mh[G + h];
-  }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  for (int idx = tid; idx < G * D; idx += kAttnConsumers) {
-    const int h = idx / D, d = idx - h * D;
-    float num = 0.f;
-    for (int s0 = 0; s0 < n_active; s0 += 8) {
-      float v[8];
+  for (int pr = tid; pr < n_pairs; pr += kAttnConsumers) {
+    const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+    float M = -INFINITY, L = 0.f, n0 = 0.f, n1 = 0.f;
+    for (int s0 = 0; s0 < n_active; s0 += kAttnMergeBatch) {
+      float mv[kAttnMergeBatch], lv[kAttnMergeBatch];
+      float2 av[kAttnMergeBatch];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = s0 + j < n_active ? __ldcg(base + (s0 + j) * stride + h * D + d) : 0.f;
+      for (int j = 0; j < kAttnMergeBatch; ++j) {
+        const int sp = s0 + j;
+        if (sp < n_active) {
+          const float* ps = base + sp * stride;
+          mv[j] = __ldcg(ps + G * D + h);
+          lv[j] = __ldcg(ps + G * D + G + h);
+          av[j] = __ldcg(reinterpret_cast<const float2*>(ps + h * D + 2 * dp));
+        } else {
+          mv[j] = -INFINITY;
+          lv[j] = 0.f;
+          av[j] = make_float2(0.f, 0.f);
+        }
+      }
+      float bm = M;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (s0 + j < n_active) num = fmaf(ms[(s0 + j) * G + h], v[j], num);
+      for (int j = 0; j < kAttnMergeBatch; ++j) bm = fmaxf(bm, mv[j]);
+      const float c = (M == -INFINITY) ? 0.f : expf(M - bm);
+      L *= c;
+      n0 *= c;
+      n1 *= c;
+#pragma unroll
+      for (int j = 0; j < kAttnMergeBatch; ++j) {
+        if (s0 + j < n_active) {
+          const float w = expf(mv[j] - bm);
+          L = fmaf(w, lv[j], L);
+          n0 = fmaf(w, av[j].x, n0);
+          n1 = fmaf(w, av[j].y, n1);
+        }
+      }
+      M = bm;
     }
-    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] = num;
+    const float inv = 1.0f / L;
+    float* dst = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + 2 * dp;
+    dst[0] = n0 * inv;
+    dst[1] = n1 * inv;
   }
   if (tid == 0) atomicExch(ticket, 0u);
 }
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
   asm volatile("bar.sync 2, 288;" ::: "memory");
   if (!ok) return;
 
-  attn_finish<D>(a, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last, reinterpret_cast<float*>(ring));
+  attn_finish<D>(a, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last);
 }
 
 }  // namespace dec

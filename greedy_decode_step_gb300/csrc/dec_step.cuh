@@ -26,6 +26,7 @@ namespace dec {
 
 constexpr int kStepMaxLayers = 64;
 constexpr uint32_t kStepSlotBytes = 40 * 1024;
+constexpr int kAttnLoads = 9;  // 16-byte loads in flight per thread in the attention phase
 constexpr uint32_t kStepHeaderBytes = 2048;
 
 enum StepPhase : int { kPhQKV = 0, kPhO = 1, kPhGLU = 2, kPhDown = 3, kPhHead = 4, kNumPhases = 5 };
@@ -211,7 +212,7 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
 // weight copies), runs the same tile math as the single-op attention kernel
 // and finishes the same way (partials + last-split merge).
 template <int D>
-__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, int* is_last) {
+__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, const int* pos_s, int* is_last) {
   constexpr int kRowChunks = D / 8;  // 16-byte chunks per cache row
   constexpr int kMaxSlots = attn_slots<D>();
   float* m_run = reinterpret_cast<float*>(area);
@@ -220,6 +221,7 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, i
   float* q_s = reinterpret_cast<float*>(area + 256);
   float* s_s = q_s + kAttnMaxGroup * D;
   uint4* tile = reinterpret_cast<uint4*>(s_s + kAttnMaxGroup * kAttnTile);  // K rows then V rows
+  uint4* q_s4 = reinterpret_cast<uint4*>(q_s);
   const int tid = threadIdx.x;
   const int G = a.Hq / a.Hkv;
   const StepLayer& w = a.layers[l];
@@ -244,7 +246,7 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, i
     const int rem = it - b * a.Hkv * a.n_split;
     const int g = rem / a.n_split;
     const int split = rem - g * a.n_split;
-    const int p = __ldcg(a.pos + b);
+    const int p = pos_s[b];
     if (p < 0 || p >= a.S_max) {
       if (split == 0 && g == 0 && tid == 0) atomicOr(a.err, kErrPosRange);
       continue;
@@ -258,8 +260,7 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, i
     const size_t head_off = (static_cast<size_t>(b) * a.Hkv + g) * a.S_max;
     const uint4* Kg = reinterpret_cast<const uint4*>(w.kc + head_off * D);
     const uint4* Vg = reinterpret_cast<const uint4*>(w.vc + head_off * D);
-    for (int i = tid; i < G * D; i += kConsumerThreads)
-      q_s[i] = __ldcg(a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i);
+    const uint4* Qg = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D);
     if (tid < G) {
       m_run[tid] = -INFINITY;
       l_run[tid] = 0.f;
@@ -271,18 +272,37 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, i
       const int j0 = k0 + tt * kAttnTile;
       const int nk = min(kAttnTile, k1 - j0);
       const int n16 = nk * kRowChunks;
-      for (int i = tid; i < 2 * n16; i += kConsumerThreads) {
-        const bool is_v = i >= n16;
-        const int c = is_v ? i - n16 : i;
-        tile[(is_v ? kAttnTile * kRowChunks : 0) + c] =
-            __ldcg((is_v ? Vg : Kg) + static_cast<size_t>(j0) * kRowChunks + c);
+      // the tile's key and value rows (with the group's queries on the first
+      // tile), every load of a thread in flight before the first store
+      const int nq = tt == 0 ? G * D / 4 : 0;
+      const int total = nq + 2 * n16;
+      for (int i0 = 0; i0 < total; i0 += kAttnLoads * kConsumerThreads) {
+        uint4 v[kAttnLoads];
+#pragma unroll
+        for (int j = 0; j < kAttnLoads; ++j) {
+          const int i = i0 + tid + j * kConsumerThreads;
+          if (i < nq) {
+            v[j] = __ldcg(Qg + i);
+          } else if (i < nq + n16) {
+            v[j] = __ldcg(Kg + static_cast<size_t>(j0) * kRowChunks + (i - nq));
+          } else if (i < total) {
+            v[j] = __ldcg(Vg + static_cast<size_t>(j0) * kRowChunks + (i - nq - n16));
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kAttnLoads; ++j) {
+          const int i = i0 + tid + j * kConsumerThreads;
+          if (i < nq) q_s4[i] = v[j];
+          else if (i < nq + n16) tile[i - nq] = v[j];
+          else if (i < total) tile[kAttnTile * kRowChunks + (i - nq - n16)] = v[j];
+        }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
       attn_tile_math<D>(tile, reinterpret_cast<const uint32_t*>(tile + kAttnTile * kRowChunks), nk, G, a.attn_scale,
                         q_s, s_s, m_run, l_run, corr, acc0, acc1);
       asm volatile("bar.sync 1, 256;" ::: "memory");
     }
-    attn_finish<D>(t, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last, reinterpret_cast<float*>(tile));
+    attn_finish<D>(t, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last);
     asm volatile("bar.sync 1, 256;" ::: "memory");
   }
   return true;
@@ -298,6 +318,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   float* red = reinterpret_cast<float*>(smem + 576);                      // 8 floats
   float* head_val = reinterpret_cast<float*>(smem + 640);                 // [8][kMaxBatch]
   uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 640 + 4 * kConsumerWarps * kMaxBatch);
+  int* pos_s = reinterpret_cast<int*>(smem + 1792);                     // [kMaxBatch] positions of this step
   float* xs = reinterpret_cast<float*>(smem + a.off_x);
   float* part = reinterpret_cast<float*>(smem + a.off_part);
   unsigned char* attn_area = smem + a.off_attn;
@@ -312,6 +333,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     *abort_cta = 0;
     fence_mbar_init();
   }
+  if (threadIdx.x < a.B) pos_s[threadIdx.x] = a.pos[threadIdx.x];
   __syncthreads();
 
   if (warp == kConsumerWarps) {
@@ -362,7 +384,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
                                      is_last) &&
          grid_sync(a, abort_cta);
     if (!ok) break;
-    ok = attention_phase<D>(a, l, attn_area, is_last) && grid_sync(a, abort_cta);
+    ok = attention_phase<D>(a, l, attn_area, pos_s, is_last) && grid_sync(a, abort_cta);
     if (!ok) break;
     // r += Wo o
     io.x = a.o;
