@@ -515,11 +515,14 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
     part = std::max(part, pb);
   }
   const uint32_t x_bytes = static_cast<uint32_t>(*BT) * H * 4u;
-  const uint32_t attn_bytes = 256u + kAttnMaxGroup * D * 4u + kAttnMaxGroup * kAttnTile * 4u + 2u * kAttnTile * D * 2u;
+  const uint32_t G = static_cast<uint32_t>(Hq / Hkv);
+  const uint32_t attn_bytes = 256u + G * D * 4u + G * kAttnTile * 4u + 2u * kAttnTile * D * 2u;
+  if (H % 8 != 0) return false;  // the norm gains travel as 16-byte bulk copies
   a->off_x = kStepHeaderBytes;
   a->off_part = align_up(a->off_x + x_bytes, 16);
   a->off_attn = align_up(a->off_part + part, 128);
-  a->off_ring = align_up(a->off_attn + attn_bytes, 128);
+  a->off_gamma = align_up(a->off_attn + attn_bytes, 128);
+  a->off_ring = align_up(a->off_gamma + 2u * static_cast<uint32_t>(H) * 2u, 128);
   if (a->off_ring + 2 * kStepSlotBytes > kSmemMax) return false;
   a->n_slots = std::min<int>(4, static_cast<int>((kSmemMax - a->off_ring) / kStepSlotBytes));
   *smem = a->off_ring + static_cast<uint32_t>(a->n_slots) * kStepSlotBytes;

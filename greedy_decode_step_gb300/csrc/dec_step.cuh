@@ -74,7 +74,7 @@ struct StepArgs {
   int* abort_all;              // raised when any CTA gives up
   uint32_t* err;
   int n_slots;
-  uint32_t off_x, off_part, off_attn, off_ring;
+  uint32_t off_x, off_part, off_attn, off_gamma, off_ring;
   StepPlan plan[kNumPhases];
   double inv_freq[64];
   StepLayer layers[kStepMaxLayers];
@@ -172,17 +172,51 @@ __device__ __forceinline__ bool produce_phase(const StepArgs& a, int ph, int l, 
   return produce_stages<KIND>(sh, u0, n, R, sg, policy);
 }
 
+// Norm gains into shared memory: the producer copies each gain vector (the
+// layer's attention and MLP norms, then the final norm) into one of two
+// buffers as it starts the phase's weights, so the phase's prologue reads
+// them on chip instead of from DRAM behind the weight stream.  Copy j uses
+// buffer j % 2 (phase j / 2 of its barriers).
+struct GammaRing {
+  uint64_t* full;
+  uint64_t* empty;
+  unsigned char* base;
+  uint32_t bytes;  // H * 2
+};
+
+__device__ __forceinline__ bool produce_gamma(const GammaRing& G, const uint16_t* src, int& gq, const Ring& R) {
+  const int slot = gq & 1;
+  if (gq >= 2 && !mbar_wait(&G.empty[slot], ((gq >> 1) - 1) & 1, R.abort, R.err, kErrWaitEmpty)) return false;
+  mbar_arrive_expect_tx(&G.full[slot], G.bytes);
+  bulk_copy_g2s(G.base + static_cast<size_t>(slot) * G.bytes, src, G.bytes, &G.full[slot], l2_policy_evict_last());
+  ++gq;
+  return true;
+}
+
+// Consumer side: the gains of copy gq (bounded wait, warp-uniform verdict).
+__device__ __forceinline__ const uint16_t* consume_gamma(const GammaRing& G, int gq, const Ring& R) {
+  const int slot = gq & 1;
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(&G.full[slot], (gq >> 1) & 1, R.abort, R.err, kErrWaitFull) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return nullptr;
+  (void)mbar_try_wait(&G.full[slot], (gq >> 1) & 1);
+  return reinterpret_cast<const uint16_t*>(G.base + static_cast<size_t>(slot) * G.bytes);
+}
+
 // One GEMV phase on the consumer side: activations, the stage stream, the
 // epilogue.  Returns false on abort.
 template <int KIND, int BT>
 __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io, const Ring& R, int& sg, float* xs,
                               float* red, float* part, float (&best_v)[BT], uint32_t (&best_i)[BT], float* head_val,
-                              uint32_t* head_idx, int* is_last) {
+                              uint32_t* head_idx, int* is_last, uint64_t* gamma_empty = nullptr) {
   const GemvShape sh = phase_shape(a, ph, l);
   int u0, n;
   cta_units(sh.n_units, blockIdx.x, gridDim.x, &u0, &n);
   const int K = sh.K;
-  if (io.x_smem) stage_activations<BT>(io, K, xs, red);
+  if (io.x_smem) stage_activations<BT>(io, K, xs, red);  // ends with a consumer barrier
+  if (gamma_empty != nullptr && threadIdx.x == 0) mbar_arrive(gamma_empty);
   const int warp = threadIdx.x >> 5;
   const int C = K / kChunkElems;
   const int cb = (warp % sh.parts) * sh.chunks_per_part;
@@ -218,12 +252,12 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
   float* m_run = reinterpret_cast<float*>(area);
   float* l_run = m_run + kAttnMaxGroup;
   float* corr = l_run + kAttnMaxGroup;
+  const int G = a.Hq / a.Hkv;
   float* q_s = reinterpret_cast<float*>(area + 256);
-  float* s_s = q_s + kAttnMaxGroup * D;
-  uint4* tile = reinterpret_cast<uint4*>(s_s + kAttnMaxGroup * kAttnTile);  // K rows then V rows
+  float* s_s = q_s + G * D;
+  uint4* tile = reinterpret_cast<uint4*>(s_s + G * kAttnTile);  // K rows then V rows
   uint4* q_s4 = reinterpret_cast<uint4*>(q_s);
   const int tid = threadIdx.x;
-  const int G = a.Hq / a.Hkv;
   const StepLayer& w = a.layers[l];
   AttnArgs t{};
   t.q = a.q;
@@ -319,6 +353,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   float* head_val = reinterpret_cast<float*>(smem + 640);                 // [8][kMaxBatch]
   uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 640 + 4 * kConsumerWarps * kMaxBatch);
   int* pos_s = reinterpret_cast<int*>(smem + 1792);                     // [kMaxBatch] positions of this step
+  const GammaRing GR{reinterpret_cast<uint64_t*>(smem + 256), reinterpret_cast<uint64_t*>(smem + 272),
+                     smem + a.off_gamma, static_cast<uint32_t>(a.H) * 2u};
   float* xs = reinterpret_cast<float*>(smem + a.off_x);
   float* part = reinterpret_cast<float*>(smem + a.off_part);
   unsigned char* attn_area = smem + a.off_attn;
@@ -330,6 +366,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&GR.full[i], 1);
+      mbar_init(&GR.empty[i], 1);
+    }
     *abort_cta = 0;
     fence_mbar_init();
   }
@@ -338,26 +378,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer warp
-    int sg = 0;
+    int sg = 0, gq = 0;
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
       bool ok = true;
       for (int l = 0; l < a.L && ok; ++l) {
-        ok = produce_phase<kKindQKV>(a, kPhQKV, l, R, sg, policy) &&
+        ok = produce_gamma(GR, a.layers[l].attn_norm, gq, R) &&
+             produce_phase<kKindQKV>(a, kPhQKV, l, R, sg, policy) &&
              produce_phase<kKindResid>(a, kPhO, l, R, sg, policy) &&
+             produce_gamma(GR, a.layers[l].mlp_norm, gq, R) &&
              produce_phase<kKindGLU>(a, kPhGLU, l, R, sg, policy) &&
              produce_phase<kKindResid>(a, kPhDown, l, R, sg, policy);
       }
-      if (ok && a.lm_head) produce_phase<kKindHead>(a, kPhHead, 0, R, sg, policy);
+      if (ok && a.lm_head) ok = produce_gamma(GR, a.final_norm, gq, R) && produce_phase<kKindHead>(a, kPhHead, 0, R, sg, policy);
     }
     __syncwarp();
     asm volatile("bar.sync 2, 288;" ::: "memory");
-    if (lane == 0) drain_ring(R, sg);
+    if (lane == 0) {
+      drain_ring(R, sg);
+      const Ring GRing{GR.full, GR.empty, GR.base, 2, GR.bytes, abort_cta, a.err};
+      drain_ring(GRing, gq);
+    }
     return;
   }
 
   // --------------------------------------------------------------- consumer warps
-  int sg = 0;
+  int sg = 0, gq = 0;
   float best_v[BT];
   uint32_t best_i[BT];
   bool ok = true;
@@ -371,7 +417,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     const StepLayer& w = a.layers[l];
     // q, k, v with RoPE; k, v into the cache
     io.x = a.resid;
-    io.norm_gamma = w.attn_norm;
+    io.norm_gamma = consume_gamma(GR, gq, R);
+    if (io.norm_gamma == nullptr) {
+      ok = false;
+      break;
+    }
     io.tokens = (l == 0 && a.embed) ? a.token : nullptr;
     io.embed = a.embed;
     io.vocab = a.V;
@@ -381,7 +431,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.k_cache = w.kc;
     io.v_cache = w.vc;
     ok = consume_phase<kKindQKV, BT>(a, kPhQKV, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
-                                     is_last) &&
+                                     is_last, &GR.empty[gq & 1]) &&
          grid_sync(a, abort_cta);
     if (!ok) break;
     ok = attention_phase<D>(a, l, attn_area, pos_s, is_last) && grid_sync(a, abort_cta);
@@ -398,12 +448,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
          grid_sync(a, abort_cta);
     if (!ok) break;
     // h = silu(Wg y) * (Wu y), y = norm(r)
+    ++gq;
     io.x = a.resid;
-    io.norm_gamma = w.mlp_norm;
+    io.norm_gamma = consume_gamma(GR, gq, R);
+    if (io.norm_gamma == nullptr) {
+      ok = false;
+      break;
+    }
     io.x_smem = 1;
     io.out = a.h;
     ok = consume_phase<kKindGLU, BT>(a, kPhGLU, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
-                                     is_last) &&
+                                     is_last, &GR.empty[gq & 1]) &&
          grid_sync(a, abort_cta);
     if (!ok) break;
     // r += Wd h
@@ -414,11 +469,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     ok = consume_phase<kKindResid, BT>(a, kPhDown, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                        is_last) &&
          grid_sync(a, abort_cta);
+    ++gq;
   }
   if (ok) {
     if (a.lm_head) {
       io.x = a.resid;
-      io.norm_gamma = a.final_norm;
+      io.norm_gamma = consume_gamma(GR, gq, R);
       io.x_smem = 1;
       io.out = nullptr;
       io.logits = nullptr;
@@ -426,8 +482,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
       io.ticket = a.head_ticket;
       io.token_out = nullptr;
       io.book = a.book;
-      consume_phase<kKindHead, BT>(a, kPhHead, 0, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
-                                   is_last);
+      if (io.norm_gamma != nullptr)
+        consume_phase<kKindHead, BT>(a, kPhHead, 0, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
+                                     is_last, &GR.empty[gq & 1]);
     } else if (blockIdx.x == 0 && threadIdx.x < a.B) {
       a.pos[threadIdx.x] += 1;
     }
