@@ -86,19 +86,21 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
-// Grid-wide barrier over the consumer warps of all CTAs (sense-reversing: the
-// word's top bit flips once per barrier and the word returns to its start
-// value, so it needs no reset).  Bounded: returns false when the grid aborts.
-__device__ inline bool grid_sync(const StepArgs& a, volatile int* abort_cta) {
+// Grid-wide barrier over the consumer warps of all CTAs, sense-reversing: CTA
+// 0 adds 2^31 - (n - 1) and the others 1, so the word's low bits return to
+// zero and its top bit flips once all n CTAs have arrived.  Thread 0 of each
+// CTA read the top bit before its first arrival (`sense`) and flips its copy
+// per barrier, so the arrival is a release reduction with no reply to wait
+// for.  Bounded: returns false when the grid aborts.
+__device__ inline bool grid_sync(const StepArgs& a, volatile int* abort_cta, uint32_t& sense) {
   asm volatile("bar.sync 1, 256;" ::: "memory");
   int bad = 0;
   if (threadIdx.x == 0) {
-    __threadfence();
     const unsigned int inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
-    const unsigned int old = atomicAdd(a.grid_bar, inc);
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.grid_bar), "r"(inc) : "memory");
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
-      if ((ld_acquire_u32(a.grid_bar) ^ old) & 0x80000000u) break;
+      if ((ld_acquire_u32(a.grid_bar) >> 31) != sense) break;
       if ((i & 31u) == 31u) {
         if (*reinterpret_cast<volatile int*>(a.abort_all)) {
           bad = 1;
@@ -112,7 +114,7 @@ __device__ inline bool grid_sync(const StepArgs& a, volatile int* abort_cta) {
         }
       }
     }
-    __threadfence();
+    sense ^= 1u;
     if (bad) *abort_cta = 1;
   }
   return !consumers_barrier_or(bad != 0);
@@ -404,6 +406,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
 
   // --------------------------------------------------------------- consumer warps
   int sg = 0, gq = 0;
+  uint32_t sense = 0;  // thread 0: top bit of the barrier word before this CTA's first arrival
+  if (threadIdx.x == 0) sense = ld_acquire_u32(a.grid_bar) >> 31;
   float best_v[BT];
   uint32_t best_i[BT];
   bool ok = true;
@@ -432,9 +436,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.v_cache = w.vc;
     ok = consume_phase<kKindQKV, BT>(a, kPhQKV, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                      is_last, &GR.empty[gq & 1]) &&
-         grid_sync(a, abort_cta);
+         grid_sync(a, abort_cta, sense);
     if (!ok) break;
-    ok = attention_phase<D>(a, l, attn_area, pos_s, is_last) && grid_sync(a, abort_cta);
+    ok = attention_phase<D>(a, l, attn_area, pos_s, is_last) && grid_sync(a, abort_cta, sense);
     if (!ok) break;
     // r += Wo o
     io.x = a.o;
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.out = a.resid;
     ok = consume_phase<kKindResid, BT>(a, kPhO, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                        is_last) &&
-         grid_sync(a, abort_cta);
+         grid_sync(a, abort_cta, sense);
     if (!ok) break;
     // h = silu(Wg y) * (Wu y), y = norm(r)
     ++gq;
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.out = a.h;
     ok = consume_phase<kKindGLU, BT>(a, kPhGLU, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                      is_last, &GR.empty[gq & 1]) &&
-         grid_sync(a, abort_cta);
+         grid_sync(a, abort_cta, sense);
     if (!ok) break;
     // r += Wd h
     io.x = a.h;
@@ -468,7 +472,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.out = a.resid;
     ok = consume_phase<kKindResid, BT>(a, kPhDown, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                        is_last) &&
-         grid_sync(a, abort_cta);
+         grid_sync(a, abort_cta, sense);
     ++gq;
   }
   if (ok) {
