@@ -70,6 +70,7 @@ _SIGNATURES = {
     "dec_state_init": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P]),
     "dec_state_release": (_I, [ctypes.POINTER(DecState)]),
     "dec_step": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P]),
+    "dec_step_launches": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), ctypes.POINTER(_I)]),
     "dec_prefill": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P, _I, _P]),
     "dec_decode": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _I, _I, _P, ctypes.POINTER(_I), _P]),
     "dec_generate": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P, _I, _I, _I, _P,
@@ -281,6 +282,13 @@ class State:
 
 def dec_step(model: Model, state: State, stream=None):
     _check(lib().dec_step(ctypes.byref(model.c), ctypes.byref(state.c), _stream(stream)))
+
+
+def dec_step_launches(model: Model, state: State) -> int:
+    """Kernel launches one dec_step makes for this model and state (1: the persistent step kernel)."""
+    n = ctypes.c_int(0)
+    _check(lib().dec_step_launches(ctypes.byref(model.c), ctypes.byref(state.c), ctypes.byref(n)))
+    return n.value
 
 
 def dec_prefill(model: Model, state: State, prompt, stream=None):

@@ -495,8 +495,9 @@ bool step_phase_plan(int K, int n_units, int RU, int BT, int sms, StepPlan* out,
 
 // Fills the step kernel's arguments; false if the model / batch is outside
 // what it handles (then the step runs as single-op kernels).
-bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, StepArgs* a,
-               uint32_t* smem, int* BT) {
+bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
+               StepArgs* a, uint32_t* smem, int* BT) {
+  const bool with_head = head && m->lm_head != nullptr;
   const int B = s->batch;
   if (B > 2 || m->n_layers > kStepMaxLayers) return false;
   *BT = bt_bucket(B);
@@ -510,7 +511,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   part = std::max(part, pb);
   if (!step_phase_plan(I, H, 1, *BT, dv->sms, &a->plan[kPhDown], &pb)) return false;
   part = std::max(part, pb);
-  if (m->lm_head) {
+  if (with_head) {
     if (!step_phase_plan(H, m->vocab, 1, *BT, dv->sms, &a->plan[kPhHead], &pb)) return false;
     part = std::max(part, pb);
   }
@@ -538,7 +539,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   a->eps = m->rms_eps;
   a->embed = static_cast<const uint16_t*>(m->embed);
   a->final_norm = static_cast<const uint16_t*>(m->final_norm);
-  a->lm_head = static_cast<const uint16_t*>(m->lm_head);
+  a->lm_head = with_head ? static_cast<const uint16_t*>(m->lm_head) : nullptr;
   a->token = s->token;
   a->pos = s->pos;
   a->resid = s->residual;
@@ -581,12 +582,12 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
 // Layers of one step; with `head`, also the LM head and the bookkeeping.
 int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
                  cudaStream_t st) {
-  if (head || !m->lm_head) {
-    // b <= 2: the whole step is one persistent kernel
+  {
+    // b <= 2: the whole step (with or without the head) is one persistent kernel
     static thread_local StepArgs sa;  // ~6 KB: kept off the stack
     uint32_t smem = 0;
     int BT = 1;
-    if (plan_step(m, s, dv, w, &sa, &smem, &BT)) {
+    if (plan_step(m, s, dv, w, head, &sa, &smem, &BT)) {
       cudaError_t e = launch_step(BT, sa, dv->sms, smem, st);
       DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "step kernel launch: %s", cudaGetErrorString(e));
       return DEC_OK;
@@ -978,6 +979,26 @@ int dec_step(const dec_model* m, dec_state* s, void* stream) {
   StateWs w;
   DEC_TRY(state_views(m, s, dv, &w));
   return enqueue_step(m, s, dv, w, true, static_cast<cudaStream_t>(stream));
+}
+
+int dec_step_launches(const dec_model* m, const dec_state* s, int* launches) {
+  DEC_TRY(check_model(m));
+  DEC_TRY(check_state(m, s, false));
+  DEC_CHECK(launches != nullptr, DEC_EINVAL, "launches must be non-null");
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  StateWs w;
+  DEC_TRY(state_views(m, const_cast<dec_state*>(s), dv, &w));
+  static thread_local StepArgs sa;
+  uint32_t smem = 0;
+  int BT = 1;
+  if (plan_step(m, s, dv, w, true, &sa, &smem, &BT)) {
+    *launches = 1;
+    return DEC_OK;
+  }
+  const bool fuse = norm_fusable(s->batch, m->hidden);
+  *launches = m->n_layers * (fuse ? 5 : 7) + (m->lm_head ? (fuse ? 1 : 2) : 1);
+  return DEC_OK;
 }
 
 int dec_prefill(const dec_model* m, dec_state* s, const int32_t* prompt, int P, void* stream) {

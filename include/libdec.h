@@ -224,6 +224,14 @@ int dec_state_release(dec_state* s);
 int dec_step(const dec_model* m, dec_state* s, void* stream);
 
 /*
+ * Number of kernel launches one dec_step (with the LM head) makes for this
+ * model and state on the current device: 1 when the whole step runs as the
+ * persistent kernel (B <= 2 and the model fits its plan), otherwise the
+ * count of single-op launches.  Validates like dec_step; launches nothing.
+ */
+int dec_step_launches(const dec_model* m, const dec_state* s, int* launches);
+
+/*
  * Teacher-forced prompt pass: for i = 0 .. P-2 runs the layers on prompt
  * token i at position pos[b] + i (filling the cache) and moves on to prompt
  * token i+1 without the LM head; leaves token[b] = prompt[b][P-1] and

@@ -245,3 +245,12 @@ def test_decode_rejects_bad_arguments():
     with pytest.raises(gd.DecError, match="n_steps"):
         gd.dec_decode(p.model, p.state, -1, 0, None)
     assert gd.dec_decode(p.model, p.state, 0, 0, None) == 0
+
+
+def test_step_launch_count():
+    """One launch per step while the persistent kernel applies (b <= 2), the
+    single-op sequence above that."""
+    m = synth.workload("tiny", n_layers=2).model
+    for B, want in ((1, {1}), (2, {1}), (3, {5 * 2 + 1, 7 * 2 + 2})):
+        p = _fresh(m, B, 64)
+        assert gd.dec_step_launches(p.model, p.state) in want
