@@ -352,6 +352,7 @@ struct StateWs {
   float* o;
   float* h;
   float* y;
+  float* kraw;
   float* attn_part;
   unsigned int* grid_bar;
   int* abort_all;
@@ -376,6 +377,7 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   const size_t o_part = c.take(attn_part_bytes(B, m->n_heads, m->n_kv_heads, m->head_dim, w.n_split));
   const size_t o_gbar = c.take(sizeof(unsigned int));
   const size_t o_abort = c.take(sizeof(int));
+  const size_t o_kraw = c.take(sizeof(float) * B * m->n_kv_heads * m->head_dim);
   w.bytes = c.off;
   if (base) {
     w.ctrl = reinterpret_cast<Ctrl*>(base + o_ctrl);
@@ -390,6 +392,7 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
     w.attn_part = reinterpret_cast<float*>(base + o_part);
     w.grid_bar = reinterpret_cast<unsigned int*>(base + o_gbar);
     w.abort_all = reinterpret_cast<int*>(base + o_abort);
+    w.kraw = reinterpret_cast<float*>(base + o_kraw);
   }
   return w;
 }
@@ -503,7 +506,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   *BT = bt_bucket(B);
   const int H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
   uint32_t part = 0, pb = 0;
-  if (!step_phase_plan(H, (Hq + 2 * Hkv) * (D / 2), 2, *BT, dv->sms, &a->plan[kPhQKV], &pb)) return false;
+  if (!step_phase_plan(H, (Hq + 2 * Hkv) * D, 1, *BT, dv->sms, &a->plan[kPhQKV], &pb)) return false;
   part = std::max(part, pb);
   if (!step_phase_plan(Hq * D, H, 1, *BT, dv->sms, &a->plan[kPhO], &pb)) return false;
   part = std::max(part, pb);
@@ -544,6 +547,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   a->pos = s->pos;
   a->resid = s->residual;
   a->q = w.q;
+  a->kraw = w.kraw;
   a->o = w.o;
   a->h = w.h;
   a->attn_part = w.attn_part;

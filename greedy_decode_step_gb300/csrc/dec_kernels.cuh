@@ -9,6 +9,10 @@
 //               token's position; k, v stored (bf16) into the static cache
 //   kKindGLU    h = silu(Wg y) * (Wu y)
 //   kKindResid  r <- r + W x          (o_proj and down projection)
+//   kKindQKVRows  the rows of [Wq; Wk; Wv] as plain units (no pairing):
+//               q and k unrotated to fp32 buffers, v straight into the
+//               cache (the persistent step kernel rotates q and k after
+//               the next grid barrier)
 //   kKindHead   logits = W_lm f, greedy argmax (lowest index on ties), and in
 //               step mode the token / position / EOS bookkeeping
 //
@@ -37,7 +41,7 @@ constexpr int kXregIt = 5;                           // chunks per lane of a war
 constexpr int kXregRows = 2;                         // rows per warp per stage (register path)
 constexpr uint32_t kGemvHeaderBytes = 1536;          // barriers, flags and reduction scratch
 
-enum GemvKind : int { kKindQKV = 0, kKindGLU = 1, kKindResid = 2, kKindHead = 3 };
+enum GemvKind : int { kKindQKV = 0, kKindGLU = 1, kKindResid = 2, kKindHead = 3, kKindQKVRows = 4 };
 
 // Device control block of a decode state (lives in the state workspace).
 struct Ctrl {
@@ -87,6 +91,7 @@ struct GemvIO {
   const int32_t* pos;     // QKV: [B]
   int S_max;
   float* logits;          // Head: optional [B][V]
+  float* k_raw;           // QKVRows: unrotated k [B][Hkv*D]
   unsigned long long* argmax_keys;  // Head: [B], zero between launches
   unsigned int* ticket;             // Head: zero between launches
   int32_t* token_out;               // Head: optional [B]
@@ -160,6 +165,13 @@ __device__ __forceinline__ void rope_cos_sin(int p, double inv_freq, float* c, f
   sincosf(static_cast<float>(red), s, c);
 }
 
+// Rotate-half RoPE of one pair (x_i, x_{i+D/2}) by the angle with cosine cs
+// and sine sn; roundings pinned so every path gives the same bits.
+__device__ __forceinline__ void rope_rotate(float lo, float hi, float cs, float sn, float* l2, float* h2) {
+  *l2 = __fmaf_rn(lo, cs, -__fmul_rn(hi, sn));
+  *h2 = __fmaf_rn(hi, cs, __fmul_rn(lo, sn));
+}
+
 // ----------------------------------------------------------------------------- GEMV: stages
 // A CTA owns the units [u0, u0 + n).  Its rows are streamed as a sequence of
 // stages; each stage is ONE bulk copy of up to rows_per_stage consecutive rows
@@ -188,6 +200,11 @@ __device__ __forceinline__ const uint16_t* unit_row(const GemvShape& sh, int u, 
     return sh.w2 + (static_cast<size_t>(hh) * sh.D + row_in_head) * K;
   } else if constexpr (KIND == kKindGLU) {
     return (r == 0 ? sh.w0 : sh.w1) + static_cast<size_t>(u) * K;
+  } else if constexpr (KIND == kKindQKVRows) {
+    const int nq = sh.Hq * sh.D, nk = sh.Hkv * sh.D;
+    if (u < nq) return sh.w0 + static_cast<size_t>(u) * K;
+    if (u < nq + nk) return sh.w1 + static_cast<size_t>(u - nq) * K;
+    return sh.w2 + static_cast<size_t>(u - nq - nk) * K;
   } else {
     return sh.w0 + static_cast<size_t>(u) * K;
   }
@@ -207,6 +224,15 @@ __device__ __forceinline__ void for_each_run(const GemvShape& sh, int u0, int n,
   } else if constexpr (KIND == kKindGLU) {
     if (f(0, n, 0)) return;
     f(0, n, 1);
+  } else if constexpr (KIND == kKindQKVRows) {
+    const int b1 = sh.Hq * sh.D, b2 = b1 + sh.Hkv * sh.D;
+    for (int ul = 0; ul < n;) {
+      const int u = u0 + ul;
+      const int lim = u < b1 ? b1 : (u < b2 ? b2 : u0 + n);
+      const int end = min(n, lim - u0);
+      if (f(ul, end - ul, 0)) return;
+      ul = end;
+    }
   } else {
     f(0, n, 0);
   }
@@ -469,7 +495,22 @@ __device__ void gemv_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int
       for (int p = 0; p < P; ++p) sum += part[((static_cast<size_t>(ul) * RU + r) * P + p) * BT + b];
       v[r] = sum;
     }
-    if constexpr (KIND == kKindResid) {
+    if constexpr (KIND == kKindQKVRows) {
+      const int nq = sh.Hq * sh.D, nk = sh.Hkv * sh.D;
+      if (u < nq) {
+        io.out[static_cast<size_t>(b) * nq + u] = v[0];
+      } else if (u < nq + nk) {
+        io.k_raw[static_cast<size_t>(b) * nk + (u - nq)] = v[0];
+      } else {
+        const int p = __ldcg(io.pos + b);
+        if (p < 0 || p >= io.S_max) {
+          atomicOr(io.err, kErrPosRange);
+          continue;
+        }
+        const int e = u - nq - nk, g = e / sh.D, d = e - g * sh.D;
+        io.v_cache[((static_cast<size_t>(b) * sh.Hkv + g) * io.S_max + p) * sh.D + d] = f32_to_bf16(v[0]);
+      }
+    } else if constexpr (KIND == kKindResid) {
       float* dst = io.out + static_cast<size_t>(b) * sh.n_units + u;
       *dst = __ldcg(dst) + v[0];
     } else if constexpr (KIND == kKindGLU) {
@@ -481,10 +522,9 @@ __device__ void gemv_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int
       const int p = __ldcg(io.pos + b);
       float lo = v[0], hi = v[1];
       if (hh < sh.Hq + sh.Hkv) {
-        float cs, sn;
+        float cs, sn, l2, h2;
         rope_cos_sin(p, inv_freq[j], &cs, &sn);
-        const float l2 = lo * cs - hi * sn;
-        const float h2 = hi * cs + lo * sn;
+        rope_rotate(lo, hi, cs, sn, &l2, &h2);
         lo = l2;
         hi = h2;
       }

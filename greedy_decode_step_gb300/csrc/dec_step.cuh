@@ -27,7 +27,7 @@ namespace dec {
 constexpr int kStepMaxLayers = 64;
 constexpr uint32_t kStepSlotBytes = 40 * 1024;
 constexpr int kAttnLoads = 9;  // 16-byte loads in flight per thread in the attention phase
-constexpr uint32_t kStepHeaderBytes = 2048;
+constexpr uint32_t kStepHeaderBytes = 3072;
 
 enum StepPhase : int { kPhQKV = 0, kPhO = 1, kPhGLU = 2, kPhDown = 3, kPhHead = 4, kNumPhases = 5 };
 
@@ -60,7 +60,8 @@ struct StepArgs {
   int32_t* token;
   int32_t* pos;
   float* resid;
-  float* q;
+  float* q;                    // unrotated q of the step [B][Hq*D]
+  float* kraw;                 // unrotated k of the step [B][Hkv*D]
   float* o;
   float* h;
   float* attn_part;
@@ -138,12 +139,12 @@ __device__ __forceinline__ GemvShape phase_shape(const StepArgs& a, int ph, int 
   }
   const StepLayer& w = a.layers[l];
   switch (ph) {
-    case kPhQKV:
+    case kPhQKV:  // rows of [Wq; Wk; Wv] (kKindQKVRows)
       sh.w0 = w.wq;
       sh.w1 = w.wk;
       sh.w2 = w.wv;
       sh.K = a.H;
-      sh.n_units = (a.Hq + 2 * a.Hkv) * (a.D / 2);
+      sh.n_units = (a.Hq + 2 * a.Hkv) * a.D;
       break;
     case kPhO:
       sh.w0 = w.wo;
@@ -248,7 +249,8 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
 // weight copies), runs the same tile math as the single-op attention kernel
 // and finishes the same way (partials + last-split merge).
 template <int D>
-__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, const int* pos_s, int* is_last) {
+__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, const int* pos_s, const float* rope_s,
+                                int* is_last) {
   constexpr int kRowChunks = D / 8;  // 16-byte chunks per cache row
   constexpr int kMaxSlots = attn_slots<D>();
   float* m_run = reinterpret_cast<float*>(area);
@@ -258,7 +260,6 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
   float* q_s = reinterpret_cast<float*>(area + 256);
   float* s_s = q_s + G * D;
   uint4* tile = reinterpret_cast<uint4*>(s_s + G * kAttnTile);  // K rows then V rows
-  uint4* q_s4 = reinterpret_cast<uint4*>(q_s);
   const int tid = threadIdx.x;
   const StepLayer& w = a.layers[l];
   AttnArgs t{};
@@ -296,7 +297,10 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
     const size_t head_off = (static_cast<size_t>(b) * a.Hkv + g) * a.S_max;
     const uint4* Kg = reinterpret_cast<const uint4*>(w.kc + head_off * D);
     const uint4* Vg = reinterpret_cast<const uint4*>(w.vc + head_off * D);
-    const uint4* Qg = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D);
+    const float* Qg = a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
+    const float* Kn = a.kraw + (static_cast<size_t>(b) * a.Hkv + g) * D;
+    const float* cs_b = rope_s + b * (D / 2);
+    const float* sn_b = rope_s + a.B * (D / 2) + b * (D / 2);
     if (tid < G) {
       m_run[tid] = -INFINITY;
       l_run[tid] = 0.f;
@@ -308,30 +312,74 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
       const int j0 = k0 + tt * kAttnTile;
       const int nk = min(kAttnTile, k1 - j0);
       const int n16 = nk * kRowChunks;
-      // the tile's key and value rows (with the group's queries on the first
-      // tile), every load of a thread in flight before the first store
-      const int nq = tt == 0 ? G * D / 4 : 0;
-      const int total = nq + 2 * n16;
+      const int newest = (j0 + nk == p + 1) ? p - j0 : -1;  // tile row of the step's own key
+      // first tile: this thread's query pairs and (for the item holding key p)
+      // the new key's pair, unrotated from L2, loaded with the tile's rows
+      constexpr int kQP = (kAttnMaxGroup * (D / 2) + kConsumerThreads - 1) / kConsumerThreads;
+      float qa[kQP], qb[kQP], ka = 0.f, kb = 0.f;
+      if (tt == 0) {
+#pragma unroll
+        for (int i = 0; i < kQP; ++i) {
+          const int pr = tid + i * kConsumerThreads;
+          qa[i] = qb[i] = 0.f;
+          if (pr < G * (D / 2)) {
+            const int h = pr / (D / 2), j = pr - h * (D / 2);
+            qa[i] = __ldcg(Qg + h * D + j);
+            qb[i] = __ldcg(Qg + h * D + j + D / 2);
+          }
+        }
+      }
+      if (newest >= 0 && tid < D / 2) {
+        ka = __ldcg(Kn + tid);
+        kb = __ldcg(Kn + tid + D / 2);
+      }
+      // the tile's key and value rows (the new key's row comes from the
+      // rotation below), every load of a thread in flight before the first store
+      const int total = 2 * n16;
       for (int i0 = 0; i0 < total; i0 += kAttnLoads * kConsumerThreads) {
         uint4 v[kAttnLoads];
 #pragma unroll
         for (int j = 0; j < kAttnLoads; ++j) {
           const int i = i0 + tid + j * kConsumerThreads;
-          if (i < nq) {
-            v[j] = __ldcg(Qg + i);
-          } else if (i < nq + n16) {
-            v[j] = __ldcg(Kg + static_cast<size_t>(j0) * kRowChunks + (i - nq));
+          if (i < n16) {
+            if (i / kRowChunks != newest) v[j] = __ldcg(Kg + static_cast<size_t>(j0) * kRowChunks + i);
           } else if (i < total) {
-            v[j] = __ldcg(Vg + static_cast<size_t>(j0) * kRowChunks + (i - nq - n16));
+            v[j] = __ldcg(Vg + static_cast<size_t>(j0) * kRowChunks + (i - n16));
           }
         }
 #pragma unroll
         for (int j = 0; j < kAttnLoads; ++j) {
           const int i = i0 + tid + j * kConsumerThreads;
-          if (i < nq) q_s4[i] = v[j];
-          else if (i < nq + n16) tile[i - nq] = v[j];
-          else if (i < total) tile[kAttnTile * kRowChunks + (i - nq - n16)] = v[j];
+          if (i < n16) {
+            if (i / kRowChunks != newest) tile[i] = v[j];
+          } else if (i < total) {
+            tile[kAttnTile * kRowChunks + (i - n16)] = v[j];
+          }
         }
+      }
+      if (tt == 0) {
+#pragma unroll
+        for (int i = 0; i < kQP; ++i) {
+          const int pr = tid + i * kConsumerThreads;
+          if (pr < G * (D / 2)) {
+            const int h = pr / (D / 2), j = pr - h * (D / 2);
+            float l2, h2;
+            rope_rotate(qa[i], qb[i], cs_b[j], sn_b[j], &l2, &h2);
+            q_s[h * D + j] = l2;
+            q_s[h * D + j + D / 2] = h2;
+          }
+        }
+      }
+      if (newest >= 0 && tid < D / 2) {
+        float l2, h2;
+        rope_rotate(ka, kb, cs_b[tid], sn_b[tid], &l2, &h2);
+        const uint16_t lo16 = f32_to_bf16(l2), hi16 = f32_to_bf16(h2);
+        uint16_t* row = reinterpret_cast<uint16_t*>(tile) + static_cast<size_t>(newest) * D;
+        row[tid] = lo16;
+        row[tid + D / 2] = hi16;
+        uint16_t* dst = w.kc + (head_off + p) * D;
+        dst[tid] = lo16;
+        dst[tid + D / 2] = hi16;
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
       attn_tile_math<D>(tile, reinterpret_cast<const uint32_t*>(tile + kAttnTile * kRowChunks), nk, G, a.attn_scale,
@@ -355,6 +403,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   float* head_val = reinterpret_cast<float*>(smem + 640);                 // [8][kMaxBatch]
   uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 640 + 4 * kConsumerWarps * kMaxBatch);
   int* pos_s = reinterpret_cast<int*>(smem + 1792);                     // [kMaxBatch] positions of this step
+  float* rope_s = reinterpret_cast<float*>(smem + 2048);                // [B][D/2] cos, then [B][D/2] sin
   const GammaRing GR{reinterpret_cast<uint64_t*>(smem + 256), reinterpret_cast<uint64_t*>(smem + 272),
                      smem + a.off_gamma, static_cast<uint32_t>(a.H) * 2u};
   float* xs = reinterpret_cast<float*>(smem + a.off_x);
@@ -386,7 +435,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
       bool ok = true;
       for (int l = 0; l < a.L && ok; ++l) {
         ok = produce_gamma(GR, a.layers[l].attn_norm, gq, R) &&
-             produce_phase<kKindQKV>(a, kPhQKV, l, R, sg, policy) &&
+             produce_phase<kKindQKVRows>(a, kPhQKV, l, R, sg, policy) &&
              produce_phase<kKindResid>(a, kPhO, l, R, sg, policy) &&
              produce_gamma(GR, a.layers[l].mlp_norm, gq, R) &&
              produce_phase<kKindGLU>(a, kPhGLU, l, R, sg, policy) &&
@@ -408,6 +457,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   int sg = 0, gq = 0;
   uint32_t sense = 0;  // thread 0: top bit of the barrier word before this CTA's first arrival
   if (threadIdx.x == 0) sense = ld_acquire_u32(a.grid_bar) >> 31;
+  // RoPE angles of this step's positions (used by the attention phases; the
+  // first phase's prologue barrier publishes them)
+  for (int t = threadIdx.x; t < a.B * (a.D / 2); t += kConsumerThreads) {
+    const int b = t / (a.D / 2), i = t - b * (a.D / 2);
+    rope_cos_sin(pos_s[b], a.inv_freq[i], &rope_s[t], &rope_s[a.B * (a.D / 2) + t]);
+  }
   float best_v[BT];
   uint32_t best_i[BT];
   bool ok = true;
@@ -432,13 +487,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.resid_store = a.resid;
     io.x_smem = 1;
     io.out = a.q;
+    io.k_raw = a.kraw;
     io.k_cache = w.kc;
     io.v_cache = w.vc;
-    ok = consume_phase<kKindQKV, BT>(a, kPhQKV, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
+    ok = consume_phase<kKindQKVRows, BT>(a, kPhQKV, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                      is_last, &GR.empty[gq & 1]) &&
          grid_sync(a, abort_cta, sense);
     if (!ok) break;
-    ok = attention_phase<D>(a, l, attn_area, pos_s, is_last) && grid_sync(a, abort_cta, sense);
+    ok = attention_phase<D>(a, l, attn_area, pos_s, rope_s, is_last) && grid_sync(a, abort_cta, sense);
     if (!ok) break;
     // r += Wo o
     io.x = a.o;
