@@ -318,14 +318,19 @@ __device__ __forceinline__ void drain_ring(const Ring& R, int sg_issued) {
 
 // Consumer wait for stage sg: lane 0 polls (bounded), the verdict is
 // warp-uniform, then every lane acquires the completed phase.
-__device__ __forceinline__ bool consumer_wait(const Ring& R, int sg) {
+__device__ __forceinline__ bool consumer_wait_at(const Ring& R, int slot, uint32_t parity) {
+  // common case: the stage is there -- one test by the whole warp
+  if (__all_sync(0xffffffffu, mbar_test_wait(&R.full[slot], parity))) return true;
   const int lane = threadIdx.x & 31;
-  const int slot = sg % R.ns;
   int ok = 1;
-  if (lane == 0) ok = mbar_wait(&R.full[slot], (sg / R.ns) & 1, R.abort, R.err, kErrWaitFull) ? 1 : 0;
+  if (lane == 0) ok = mbar_wait(&R.full[slot], parity, R.abort, R.err, kErrWaitFull) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) (void)mbar_try_wait(&R.full[slot], (sg / R.ns) & 1);
+  if (ok) (void)mbar_try_wait(&R.full[slot], parity);
   return ok != 0;
+}
+
+__device__ __forceinline__ bool consumer_wait(const Ring& R, int sg) {
+  return consumer_wait_at(R, sg % R.ns, static_cast<uint32_t>(sg / R.ns) & 1u);
 }
 
 // ----------------------------------------------------------------------------- GEMV: consumer pieces
@@ -405,13 +410,21 @@ __device__ bool consume_xreg(const GemvShape& sh, int u0, int n, const Ring& R, 
   const int NSLOT = kConsumerWarps / P;
   const int my_p = warp % P, my_slot = warp / P;
   const uint32_t row_bytes = static_cast<uint32_t>(sh.K) * 2u;
-  const int total = count_stages<KIND>(sh, u0, n);
-  for (int s = 0; s < total; ++s, ++sg) {
-    if (!consumer_wait(R, sg)) return false;
-    const int slot = sg % R.ns;
-    const StageDesc d = nth_stage<KIND>(sh, u0, n, s);
-    const int rot = (s * sh.rows_per_stage) % NSLOT;
-    const int first = (my_slot - rot + NSLOT) % NSLOT;
+  const int rps = sh.rows_per_stage;
+  const int rstep = rps % NSLOT;
+  // stage bookkeeping carried from stage to stage (no divisions in the loop):
+  // ring slot and phase, and this warp's first row of the stage
+  int slot = sg % R.ns;
+  uint32_t parity = static_cast<uint32_t>(sg / R.ns) & 1u;
+  int first = my_slot;
+  bool ok = true;
+  for_each_run<KIND>(sh, u0, n, [&](int run_ul0, int run_len, int run_r) {
+   for (int off = 0; off < run_len; off += rps) {
+    const StageDesc d{run_ul0 + off, min(rps, run_len - off), run_r};
+    if (!consumer_wait_at(R, slot, parity)) {
+      ok = false;
+      return true;
+    }
     uint4 wv[kXregRows][kXregIt];
     int nmine = 0;
 #pragma unroll
@@ -472,8 +485,17 @@ __device__ bool consume_xreg(const GemvShape& sh, int u0, int n, const Ring& R, 
         for (int b = 0; b < BT; ++b) part[((static_cast<size_t>(ul) * RU + d.r) * P + my_p) * BT + b] = sum[0][b];
       }
     }
-  }
-  return true;
+    ++sg;
+    if (++slot == R.ns) {
+      slot = 0;
+      parity ^= 1u;
+    }
+    first -= rstep;
+    if (first < 0) first += NSLOT;
+   }
+   return false;
+  });
+  return ok;
 }
 
 // Output of unit u for row b from its partial sums (QKV, GLU, residual).
