@@ -136,6 +136,71 @@ __device__ __forceinline__ void attn_tile_math(const uint4* Ks, const uint32_t* 
     }
 }
 
+// One merged output o[h][d] of a (row, KV head) from its n_active split
+// partials at `base` (stride floats apart; accumulator [G][D], maxima [G],
+// sums [G]): o = sum_s exp(m_s - M) acc_s[h][d] / sum_s exp(m_s - M) l_s[h]
+// with M the largest m_s, summed in split order.  Shared by every path.
+template <int D>
+__device__ __forceinline__ float attn_merge_one(const float* base, size_t stride, int n_active, int G, int h, int d) {
+  float M = -INFINITY, L = 0.f, num = 0.f;
+  if (n_active <= kAttnMergeBatch) {
+    float mv[kAttnMergeBatch], lv[kAttnMergeBatch], av[kAttnMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kAttnMergeBatch; ++j) {
+      mv[j] = -INFINITY;
+      lv[j] = av[j] = 0.f;
+      if (j < n_active) {
+        const float* ps = base + j * stride;
+        mv[j] = __ldcg(ps + G * D + h);
+        lv[j] = __ldcg(ps + G * D + G + h);
+        av[j] = __ldcg(ps + h * D + d);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kAttnMergeBatch; ++j) M = fmaxf(M, mv[j]);
+#pragma unroll
+    for (int j = 0; j < kAttnMergeBatch; ++j) {
+      if (j < n_active) {
+        const float w = expf(mv[j] - M);
+        L = fmaf(w, lv[j], L);
+        num = fmaf(w, av[j], num);
+      }
+    }
+  } else {
+    for (int j = 0; j < n_active; ++j) M = fmaxf(M, __ldcg(base + j * stride + G * D + h));
+    for (int j = 0; j < n_active; ++j) {
+      const float* ps = base + j * stride;
+      const float w = expf(__ldcg(ps + G * D + h) - M);
+      L = fmaf(w, __ldcg(ps + G * D + G + h), L);
+      num = fmaf(w, __ldcg(ps + h * D + d), num);
+    }
+  }
+  return num / L;
+}
+
+// This split's partial (unnormalised accumulator, running max and sum) to
+// its slot of the partial buffer.  256 consumer threads.
+template <int D>
+__device__ __forceinline__ void attn_store_partial(float* mine, int G, const float (&acc0)[attn_slots<D>()],
+                                                   const float (&acc1)[attn_slots<D>()], const float* m_run,
+                                                   const float* l_run) {
+  constexpr int kPairsPerHead = D / 2;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < attn_slots<D>(); ++i) {
+    const int pr = tid + i * kAttnConsumers;
+    if (pr < G * kPairsPerHead) {
+      const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+      mine[h * D + 2 * dp] = acc0[i];
+      mine[h * D + 2 * dp + 1] = acc1[i];
+    }
+  }
+  if (tid < G) {
+    mine[G * D + tid] = m_run[tid];
+    mine[G * D + G + tid] = l_run[tid];
+  }
+}
+
 // After the last tile: with one split the output is final; otherwise the
 // split's partial (unnormalised accumulator, running max and sum) goes to
 // global memory and the last split of the group to finish (atomic ticket)
@@ -166,19 +231,7 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
   // partial of this split, then the last split of the group merges
   const size_t stride = static_cast<size_t>(G) * (D + 2);
   float* mine = a.part + ((static_cast<size_t>(b) * a.Hkv + g) * a.n_split + split) * stride;
-#pragma unroll
-  for (int i = 0; i < kMaxSlots; ++i) {
-    const int pr = tid + i * kAttnConsumers;
-    if (pr < n_pairs) {
-      const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
-      mine[h * D + 2 * dp] = acc0[i];
-      mine[h * D + 2 * dp + 1] = acc1[i];
-    }
-  }
-  if (tid < G) {
-    mine[G * D + tid] = m_run[tid];
-    mine[G * D + G + tid] = l_run[tid];
-  }
+  attn_store_partial<D>(mine, G, acc0, acc1, m_run, l_run);
   __threadfence();
   asm volatile("bar.sync 1, 256;" ::: "memory");
   unsigned int* ticket = a.tickets + static_cast<size_t>(b) * a.Hkv + g;
@@ -186,53 +239,11 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
   asm volatile("bar.sync 1, 256;" ::: "memory");
   if (!*is_last) return;
   __threadfence();
-  // Merge by log-sum-exp weights, o = sum_s exp(m_s - M) acc_s / sum_s exp(m_s - M) l_s,
-  // one thread per (head, dimension pair), folding the splits in batches
-  // whose loads (maximum, sum and the two accumulator entries of each split)
-  // are all in flight together; M is carried as a running maximum.
   const float* base = a.part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
-  for (int pr = tid; pr < n_pairs; pr += kAttnConsumers) {
-    const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
-    float M = -INFINITY, L = 0.f, n0 = 0.f, n1 = 0.f;
-    for (int s0 = 0; s0 < n_active; s0 += kAttnMergeBatch) {
-      float mv[kAttnMergeBatch], lv[kAttnMergeBatch];
-      float2 av[kAttnMergeBatch];
-#pragma unroll
-      for (int j = 0; j < kAttnMergeBatch; ++j) {
-        const int sp = s0 + j;
-        if (sp < n_active) {
-          const float* ps = base + sp * stride;
-          mv[j] = __ldcg(ps + G * D + h);
-          lv[j] = __ldcg(ps + G * D + G + h);
-          av[j] = __ldcg(reinterpret_cast<const float2*>(ps + h * D + 2 * dp));
-        } else {
-          mv[j] = -INFINITY;
-          lv[j] = 0.f;
-          av[j] = make_float2(0.f, 0.f);
-        }
-      }
-      float bm = M;
-#pragma unroll
-      for (int j = 0; j < kAttnMergeBatch; ++j) bm = fmaxf(bm, mv[j]);
-      const float c = (M == -INFINITY) ? 0.f : expf(M - bm);
-      L *= c;
-      n0 *= c;
-      n1 *= c;
-#pragma unroll
-      for (int j = 0; j < kAttnMergeBatch; ++j) {
-        if (s0 + j < n_active) {
-          const float w = expf(mv[j] - bm);
-          L = fmaf(w, lv[j], L);
-          n0 = fmaf(w, av[j].x, n0);
-          n1 = fmaf(w, av[j].y, n1);
-        }
-      }
-      M = bm;
-    }
-    const float inv = 1.0f / L;
-    float* dst = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + 2 * dp;
-    dst[0] = n0 * inv;
-    dst[1] = n1 * inv;
+  for (int e = tid; e < G * D; e += kAttnConsumers) {
+    const int h = e / D, d = e - h * D;
+    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] =
+        attn_merge_one<D>(base, stride, n_active, G, h, d);
   }
   if (tid == 0) atomicExch(ticket, 0u);
 }

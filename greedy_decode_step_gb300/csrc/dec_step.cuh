@@ -27,7 +27,7 @@ namespace dec {
 constexpr int kStepMaxLayers = 64;
 constexpr uint32_t kStepSlotBytes = 40 * 1024;
 constexpr int kAttnLoads = 9;  // 16-byte loads in flight per thread in the attention phase
-constexpr uint32_t kStepHeaderBytes = 3072;
+constexpr uint32_t kStepHeaderBytes = 3328;
 
 enum StepPhase : int { kPhQKV = 0, kPhO = 1, kPhGLU = 2, kPhDown = 3, kPhHead = 4, kNumPhases = 5 };
 
@@ -65,7 +65,7 @@ struct StepArgs {
   float* o;
   float* h;
   float* attn_part;
-  unsigned int* attn_tickets;
+  unsigned int* attn_tickets;  // [B][Hkv] monotonic count of finished splits
   int n_split;
   float attn_scale;
   unsigned long long* argmax_keys;
@@ -250,7 +250,7 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
 // and finishes the same way (partials + last-split merge).
 template <int D>
 __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, const int* pos_s, const float* rope_s,
-                                int* is_last) {
+                                const unsigned int* tick0, volatile int* abort_cta, int* is_last) {
   constexpr int kRowChunks = D / 8;  // 16-byte chunks per cache row
   constexpr int kMaxSlots = attn_slots<D>();
   float* m_run = reinterpret_cast<float*>(area);
@@ -386,7 +386,51 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
                         q_s, s_s, m_run, l_run, corr, acc0, acc1);
       asm volatile("bar.sync 1, 256;" ::: "memory");
     }
-    attn_finish<D>(t, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last);
+    if (n_active == 1 || items > static_cast<int>(gridDim.x)) {
+      // one split, or more items than CTAs (a CTA may hold two splits of one
+      // group, so none may wait for the others): the last split merges alone
+      attn_finish<D>(t, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      continue;
+    }
+    // Split-K: this split's partial, a count of finished splits, and -- once
+    // all n_active splits of (b, g) are in -- the merge of one slice of the
+    // group's outputs by each split (no CTA merges alone).
+    const size_t stride = static_cast<size_t>(G) * (D + 2);
+    const float* base = a.attn_part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
+    attn_store_partial<D>(const_cast<float*>(base) + split * stride, G, acc0, acc1, m_run, l_run);
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    unsigned int* ticket = a.attn_tickets + static_cast<size_t>(b) * a.Hkv + g;
+    int bad = 0;
+    if (tid == 0) {
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ticket) : "memory");
+      const unsigned int target = tick0[b * a.Hkv + g] + static_cast<unsigned int>((l + 1) * n_active);
+      const uint64_t t0 = globaltimer_ns();
+      for (uint32_t i = 0;; ++i) {
+        if (static_cast<int>(ld_acquire_u32(ticket) - target) >= 0) break;
+        if ((i & 31u) == 31u) {
+          if (*reinterpret_cast<volatile int*>(a.abort_all)) {
+            bad = 1;
+            break;
+          }
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(a.err, kErrGridWait);
+            atomicExch(a.abort_all, 1);
+            bad = 1;
+            break;
+          }
+        }
+      }
+      if (bad) *abort_cta = 1;
+    }
+    if (consumers_barrier_or(bad != 0)) return false;
+    const int per = (G * D + n_active - 1) / n_active;
+    const int e0 = split * per;
+    for (int e = e0 + tid; e < min(G * D, e0 + per); e += kConsumerThreads) {
+      const int h = e / D, d = e - h * D;
+      a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] =
+          attn_merge_one<D>(base, stride, n_active, G, h, d);
+    }
     asm volatile("bar.sync 1, 256;" ::: "memory");
   }
   return true;
@@ -404,6 +448,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 640 + 4 * kConsumerWarps * kMaxBatch);
   int* pos_s = reinterpret_cast<int*>(smem + 1792);                     // [kMaxBatch] positions of this step
   float* rope_s = reinterpret_cast<float*>(smem + 2048);                // [B][D/2] cos, then [B][D/2] sin
+  unsigned int* tick0 = reinterpret_cast<unsigned int*>(smem + 3072);   // [B][Hkv] split counters at launch
   const GammaRing GR{reinterpret_cast<uint64_t*>(smem + 256), reinterpret_cast<uint64_t*>(smem + 272),
                      smem + a.off_gamma, static_cast<uint32_t>(a.H) * 2u};
   float* xs = reinterpret_cast<float*>(smem + a.off_x);
@@ -425,6 +470,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     fence_mbar_init();
   }
   if (threadIdx.x < a.B) pos_s[threadIdx.x] = a.pos[threadIdx.x];
+  // the split counters before any CTA of this launch can add to them (the
+  // first additions come after the first grid barrier)
+  for (int i = threadIdx.x; i < a.B * a.Hkv; i += blockDim.x) tick0[i] = ld_acquire_u32(a.attn_tickets + i);
   __syncthreads();
 
   if (warp == kConsumerWarps) {
@@ -494,7 +542,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
                                      is_last, &GR.empty[gq & 1]) &&
          grid_sync(a, abort_cta, sense);
     if (!ok) break;
-    ok = attention_phase<D>(a, l, attn_area, pos_s, rope_s, is_last) && grid_sync(a, abort_cta, sense);
+    ok = attention_phase<D>(a, l, attn_area, pos_s, rope_s, tick0, abort_cta, is_last) && grid_sync(a, abort_cta, sense);
     if (!ok) break;
     // r += Wo o
     io.x = a.o;
