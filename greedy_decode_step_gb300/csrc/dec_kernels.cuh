@@ -89,6 +89,8 @@ struct GemvIO {
   uint16_t* k_cache;      // QKV: [B][Hkv][S_max][D]
   uint16_t* v_cache;
   const int32_t* pos;     // QKV: [B]
+  const int* pos_s;       // optional: the same positions already in shared memory
+  int have_pre;           // Resid: the calling thread holds out[b][u0 + i] for idx = i * B + b = threadIdx.x in `pre`
   int S_max;
   float* logits;          // Head: optional [B][V]
   float* k_raw;           // QKVRows: unrotated k [B][Hkv*D]
@@ -501,7 +503,7 @@ __device__ bool consume_xreg(const GemvShape& sh, int u0, int n, const Ring& R, 
 // Output of unit u for row b from its partial sums (QKV, GLU, residual).
 template <int KIND, int BT>
 __device__ void gemv_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int n, const float* part,
-                              const double* inv_freq) {
+                              const double* inv_freq, float pre = 0.f) {
   constexpr int RU = (KIND == kKindQKV || KIND == kKindGLU) ? 2 : 1;
   const int P = sh.parts;
   const int B = io.B;
@@ -524,7 +526,7 @@ __device__ void gemv_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int
       } else if (u < nq + nk) {
         io.k_raw[static_cast<size_t>(b) * nk + (u - nq)] = v[0];
       } else {
-        const int p = __ldcg(io.pos + b);
+        const int p = io.pos_s ? io.pos_s[b] : __ldcg(io.pos + b);
         if (p < 0 || p >= io.S_max) {
           atomicOr(io.err, kErrPosRange);
           continue;
@@ -534,7 +536,7 @@ __device__ void gemv_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int
       }
     } else if constexpr (KIND == kKindResid) {
       float* dst = io.out + static_cast<size_t>(b) * sh.n_units + u;
-      *dst = __ldcg(dst) + v[0];
+      *dst = ((io.have_pre && idx == static_cast<int>(threadIdx.x)) ? pre : __ldcg(dst)) + v[0];
     } else if constexpr (KIND == kKindGLU) {
       io.out[static_cast<size_t>(b) * sh.n_units + u] = silu_f32(v[0]) * v[1];
     } else if constexpr (KIND == kKindQKV) {

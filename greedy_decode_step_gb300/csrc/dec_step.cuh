@@ -218,6 +218,17 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
   int u0, n;
   cta_units(sh.n_units, blockIdx.x, gridDim.x, &u0, &n);
   const int K = sh.K;
+  GemvIO iox = io;
+  float pre = 0.f;
+  if constexpr (KIND == kKindResid) {
+    // the residual entry this thread's epilogue adds to is read now, so that
+    // the load completes while the stages stream (kept in a register)
+    const int i = threadIdx.x;
+    if (i < n * io.B) {
+      pre = __ldcg(io.out + static_cast<size_t>(i % io.B) * sh.n_units + u0 + i / io.B);
+      iox.have_pre = 1;
+    }
+  }
   if (io.x_smem) stage_activations<BT>(io, K, xs, red);  // ends with a consumer barrier
   if (gamma_empty != nullptr && threadIdx.x == 0) mbar_arrive(gamma_empty);
   const int warp = threadIdx.x >> 5;
@@ -237,7 +248,7 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
     }
     head_epilogue<BT>(sh, io, u0, n, part, true, best_v, best_i, head_val, head_idx, is_last);
   } else {
-    gemv_epilogue<KIND, BT>(sh, io, u0, n, part, a.inv_freq);
+    gemv_epilogue<KIND, BT>(sh, iox, u0, n, part, a.inv_freq, pre);
   }
   return true;
 }
@@ -520,6 +531,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   io.err = a.err;
   io.S_max = a.S_max;
   io.pos = a.pos;
+  io.pos_s = pos_s;
   for (int l = 0; l < a.L && ok; ++l) {
     const StepLayer& w = a.layers[l];
     // q, k, v with RoPE; k, v into the cache
