@@ -333,7 +333,7 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic (seeded Philox N(0,0.02) weights, uniform prompt tokens)",
         "config": {
             "workload": "dense4b: 36 layers, H=2560, Hq=32, Hkv=8, D=128, I=9728, V=151936 tied; b=1; "
-                        "512-token prompt (teacher-forced, untimed); 256 greedy decode positions (511..766) "
+                        "512-token prompt (batched prompt pass on tensor-core GEMMs, untimed); 256 greedy decode positions (511..766) "
                         "per pass through the CUDA-graph decode loop, EOS id 0 checked every 16 steps",
             "batch": B, "prompt_len": P, "decode_positions": [positions[0], positions[-1]] if positions else None,
             "accumulate": "fp32", "weights": "bf16", "kv_cache": "bf16", "activations": "fp32",

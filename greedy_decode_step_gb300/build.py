@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdec.so")
-UNITS = ["api.cu", "gemv_qkv.cu", "gemv_glu.cu", "gemv_resid.cu", "gemv_head.cu", "attn.cu", "step.cu"]
+UNITS = ["api.cu", "gemv_qkv.cu", "gemv_glu.cu", "gemv_resid.cu", "gemv_head.cu", "attn.cu", "step.cu", "prefill.cu"]
 HEADERS = ["dec_common.cuh", "dec_kernels.cuh", "dec_attn.cuh", "dec_step.cuh", "dec_launch.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
-        run([nvcc(), ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+        run([nvcc(), ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcublas",
              "-Xlinker", f"-rpath,{cuda_lib}"])
         os.replace(tmp, LIB)
     return LIB

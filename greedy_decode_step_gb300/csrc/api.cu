@@ -2,6 +2,7 @@
 // and the native decode loop (graph capture + replay, EOS check every 16
 // steps).  Declarations and the contract of every entry point are in
 // include/libdec.h.
+#include <cublas_v2.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -357,8 +358,22 @@ struct StateWs {
   unsigned int* grid_bar;
   int* abort_all;
   int n_split;
+  // batched prompt pass: rows of up to pf_rows positions (all sequences)
+  int pf_rows;
+  float* pf_r;          // [rows][H] residual
+  float* pf_big;        // [rows][max((Hq + 2 Hkv) D, 2 I)] GEMM outputs (q|k|v, then gate|up)
+  float* pf_q;          // [rows][Hq D] rotated queries
+  float* pf_o;          // [rows][Hq D] attention output
+  uint16_t* pf_bf;      // [rows][max(H, Hq D, I)] bf16 GEMM operand (hi part)
+  uint16_t* pf_bf_lo;   // the same, lo part
+  void* pf_blas_ws;     // cuBLAS workspace
+  size_t pf_blas_bytes;
   size_t bytes;
 };
+
+// Positions per chunk of the batched prompt pass (times the batch).
+constexpr int kPrefillRows = 512;
+constexpr size_t kBlasWorkspace = 32u << 20;
 
 StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char* base) {
   Carve c;
@@ -378,6 +393,19 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   const size_t o_gbar = c.take(sizeof(unsigned int));
   const size_t o_abort = c.take(sizeof(int));
   const size_t o_kraw = c.take(sizeof(float) * B * m->n_kv_heads * m->head_dim);
+  const int pf_pos = std::max(1, kPrefillRows / std::max(1, B));
+  w.pf_rows = B * pf_pos;
+  const size_t R = static_cast<size_t>(w.pf_rows);
+  const size_t H = m->hidden, QD = static_cast<size_t>(m->n_heads) * m->head_dim;
+  const size_t QKV = static_cast<size_t>(m->n_heads + 2 * m->n_kv_heads) * m->head_dim, I = m->intermediate;
+  const size_t o_pf_r = c.take(sizeof(float) * R * H);
+  const size_t o_pf_big = c.take(sizeof(float) * R * std::max(QKV, 2 * I));
+  const size_t o_pf_q = c.take(sizeof(float) * R * QD);
+  const size_t o_pf_o = c.take(sizeof(float) * R * QD);
+  const size_t o_pf_bf = c.take(sizeof(uint16_t) * R * std::max(H, std::max(QD, I)));
+  const size_t o_pf_bf_lo = c.take(sizeof(uint16_t) * R * std::max(H, std::max(QD, I)));
+  w.pf_blas_bytes = kBlasWorkspace;
+  const size_t o_pf_ws = c.take(kBlasWorkspace);
   w.bytes = c.off;
   if (base) {
     w.ctrl = reinterpret_cast<Ctrl*>(base + o_ctrl);
@@ -393,12 +421,20 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
     w.grid_bar = reinterpret_cast<unsigned int*>(base + o_gbar);
     w.abort_all = reinterpret_cast<int*>(base + o_abort);
     w.kraw = reinterpret_cast<float*>(base + o_kraw);
+    w.pf_r = reinterpret_cast<float*>(base + o_pf_r);
+    w.pf_big = reinterpret_cast<float*>(base + o_pf_big);
+    w.pf_q = reinterpret_cast<float*>(base + o_pf_q);
+    w.pf_o = reinterpret_cast<float*>(base + o_pf_o);
+    w.pf_bf = reinterpret_cast<uint16_t*>(base + o_pf_bf);
+    w.pf_bf_lo = reinterpret_cast<uint16_t*>(base + o_pf_bf_lo);
+    w.pf_blas_ws = base + o_pf_ws;
   }
   return w;
 }
 
 struct StateInternal {
   int device = -1;
+  cublasHandle_t blas = nullptr;  // the prompt pass's GEMMs (workspace inside the state's workspace)
   int* pinned_word = nullptr;
   cudaStream_t own_stream = nullptr;
   cudaEvent_t ev_in = nullptr, ev_out = nullptr;
@@ -958,6 +994,12 @@ int dec_state_init(const dec_model* m, dec_state* s, void* stream) {
     dec_state_release(s);
     return fail(DEC_ECUDA, "state set-up: %s", cudaGetErrorString(e));
   }
+  cublasStatus_t bs = cublasCreate(&in->blas);
+  if (bs == CUBLAS_STATUS_SUCCESS) bs = cublasSetWorkspace(in->blas, w.pf_blas_ws, w.pf_blas_bytes);
+  if (bs != CUBLAS_STATUS_SUCCESS) {
+    dec_state_release(s);
+    return fail(DEC_ECUDA, "state set-up: cuBLAS handle (status %d)", static_cast<int>(bs));
+  }
   return DEC_OK;
 }
 
@@ -965,6 +1007,7 @@ int dec_state_release(dec_state* s) {
   DEC_CHECK(s != nullptr, DEC_EINVAL, "state is NULL");
   auto* in = static_cast<StateInternal*>(s->internal);
   if (!in) return DEC_OK;
+  if (in->blas) cublasDestroy(in->blas);
   if (in->exec) cudaGraphExecDestroy(in->exec);
   if (in->ev_in) cudaEventDestroy(in->ev_in);
   if (in->ev_out) cudaEventDestroy(in->ev_out);
@@ -1005,6 +1048,92 @@ int dec_step_launches(const dec_model* m, const dec_state* s, int* launches) {
   return DEC_OK;
 }
 
+// ------------------------------------------------------------------------------- batched prompt pass
+
+// C[rows][N] (leading dimension ldc) = beta * C + Y[rows][K] . W[N][K]^T with
+// bf16 operands and fp32 accumulation and output (cuBLAS is column-major: it
+// computes C^T = W . Y^T).
+// The activation operand comes as hi and lo bf16 parts: C = beta C + W.hi + W.lo.
+int gemm_rows(cublasHandle_t h, const void* W, int N, int K, const uint16_t* Y, const uint16_t* Y_lo, int rows,
+              float* C, int ldc, float beta) {
+  const float alpha = 1.0f, one = 1.0f;
+  for (int part = 0; part < 2; ++part) {
+    const cublasStatus_t bs = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, rows, K, &alpha, W, CUDA_R_16BF, K,
+                                           part == 0 ? Y : Y_lo, CUDA_R_16BF, K, part == 0 ? &beta : &one, C,
+                                           CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS GEMM (%d x %d x %d) failed with status %d", N, rows,
+              K, static_cast<int>(bs));
+  }
+  return DEC_OK;
+}
+
+__global__ void prefill_finish_kernel(int32_t* token, int32_t* pos, int B, const int32_t* prompt, int P) {
+  const int b = threadIdx.x;
+  if (b < B) {
+    token[b] = prompt[static_cast<size_t>(b) * P + (P - 1)];
+    pos[b] += P - 1;
+  }
+}
+
+// The prompt's positions 0 .. P-2 of every sequence as rows of GEMMs, in
+// chunks of w.pf_rows / B positions (a chunk attends to the cache, which
+// holds every earlier position and its own); then token = prompt[b][P-1] and
+// pos advanced by P-1, as the step-by-step pass leaves them.
+int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
+                    const int32_t* prompt, int P, cudaStream_t st) {
+  const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
+  const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D, WB = std::max(QKV, 2 * I);
+  const int per = w.pf_rows / B;
+  const cublasStatus_t bs = cublasSetStream(h, st);
+  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS stream (status %d)", static_cast<int>(bs));
+  for (int i0 = 0; i0 < P - 1; i0 += per) {
+    const int n = std::min(per, P - 1 - i0);
+    const int R = B * n;
+    DEC_CUDA(launch_prefill_embed(prompt, P, i0, n, R, H, static_cast<const uint16_t*>(m->embed), m->vocab, w.pf_r,
+                                  dv->err, st));
+    for (int l = 0; l < m->n_layers; ++l) {
+      const dec_layer_weights& lw = m->layers[l];
+      uint16_t* kc = static_cast<uint16_t*>(s->k_cache[l]);
+      uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
+      DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, w.pf_bf,
+                                   w.pf_bf_lo, R, st));
+      DEC_TRY(gemm_rows(h, lw.wq, QD, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, QKV, 0.f));
+      DEC_TRY(gemm_rows(h, lw.wk, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD, QKV, 0.f));
+      DEC_TRY(gemm_rows(h, lw.wv, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD + Hkv * D, QKV, 0.f));
+      DEC_CUDA(launch_prefill_rope_store(w.pf_big, w.pf_q, s->pos, kc, vc, n, i0, R, Hq, Hkv, D, s->max_seq,
+                                         m->rope_theta, dv->err, st));
+      AttnArgs t{};
+      t.q = w.pf_q;
+      t.k_cache = kc;
+      t.v_cache = vc;
+      t.pos = s->pos;
+      t.o = w.pf_o;
+      t.part = w.attn_part;
+      t.tickets = w.attn_tickets;
+      t.Hq = Hq;
+      t.Hkv = Hkv;
+      t.D = D;
+      t.S_max = s->max_seq;
+      t.n_split = 1;
+      t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+      t.rows_per_seq = n;
+      t.row_pos0 = i0;
+      DEC_TRY(run_attn(t, R, dv, st, false));
+      DEC_CUDA(launch_prefill_cast(w.pf_o, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R) * QD, dv->sms, st));
+      DEC_TRY(gemm_rows(h, lw.wo, H, QD, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
+      DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, w.pf_bf,
+                                   w.pf_bf_lo, R, st));
+      DEC_TRY(gemm_rows(h, lw.wg, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, 2 * I, 0.f));
+      DEC_TRY(gemm_rows(h, lw.wu, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + I, 2 * I, 0.f));
+      DEC_CUDA(launch_prefill_glu(w.pf_big, I, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R), dv->sms, st));
+      DEC_TRY(gemm_rows(h, lw.wd, H, I, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
+    }
+  }
+  (void)WB;
+  DEC_CUDA(launch(prefill_finish_kernel, dim3(1), dim3(32), 0, st, false, s->token, s->pos, B, prompt, P));
+  return DEC_OK;
+}
+
 int dec_prefill(const dec_model* m, dec_state* s, const int32_t* prompt, int P, void* stream) {
   DEC_TRY(check_model(m));
   DEC_TRY(check_state(m, s, false));
@@ -1016,6 +1145,8 @@ int dec_prefill(const dec_model* m, dec_state* s, const int32_t* prompt, int P, 
   DEC_TRY(state_views(m, s, dv, &w));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int B = s->batch;
+  auto* in = static_cast<StateInternal*>(s->internal);
+  if (in && in->blas) return prefill_batched(m, s, dv, w, in->blas, prompt, P, st);
   DEC_CUDA(launch(set_tokens_kernel, dim3(1), dim3(32), 0, st, false, s->token, B, prompt, P, 0));
   for (int i = 0; i + 1 < P; ++i) {
     DEC_TRY(enqueue_step(m, s, dv, w, false, st));

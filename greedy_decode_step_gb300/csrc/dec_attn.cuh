@@ -35,6 +35,10 @@ struct AttnArgs {
   int Hq, Hkv, D, S_max, n_split;
   float scale;                // 1/sqrt(D)
   uint32_t* err;
+  // prompt pass: query row r is position pos[r / rows_per_seq] + row_pos0 +
+  // r % rows_per_seq of sequence r / rows_per_seq (0: row r is sequence r at pos[r])
+  int rows_per_seq;
+  int row_pos0;
 };
 
 // (head, dim-pair) slots per consumer thread for P.V
@@ -281,7 +285,8 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
     const int i = threadIdx.x + j * 288;
     qv[j] = i < G * D ? a.q[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i] : 0.f;
   }
-  const int p = a.pos[b];
+  const int seq = a.rows_per_seq ? b / a.rows_per_seq : b;
+  const int p = a.rows_per_seq ? a.pos[seq] + a.row_pos0 + b % a.rows_per_seq : a.pos[b];
   if (p < 0 || p >= a.S_max) {
     if (split == 0 && g == 0 && threadIdx.x == 0) atomicOr(a.err, kErrPosRange);
     return;
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
   const int k1 = min(len, k0 + chunk);
   const int n_tiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
 
-  const size_t head_off = (static_cast<size_t>(b) * a.Hkv + g) * a.S_max;
+  const size_t head_off = (static_cast<size_t>(seq) * a.Hkv + g) * a.S_max;
   const uint16_t* Kg = a.k_cache + head_off * D;
   const uint16_t* Vg = a.v_cache + head_off * D;
 

@@ -58,6 +58,18 @@ cudaError_t launch_gemv_head(int BT, bool xreg, const GemvArgs& a, int grid, uin
                              bool pdl);
 cudaError_t launch_attn(const AttnArgs& a, int B, uint32_t smem, cudaStream_t st, bool pdl);
 
+// Batched prompt pass (prefill.cu): rows are (sequence, position) pairs.
+cudaError_t launch_prefill_embed(const int32_t* prompt, int P, int i0, int n, int rows, int H, const uint16_t* embed,
+                                 int vocab, float* r, uint32_t* err, cudaStream_t st);
+cudaError_t launch_prefill_norm(const float* r, const uint16_t* gamma, float eps, int H, uint16_t* y, uint16_t* y_lo,
+                                int rows, cudaStream_t st);
+cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int32_t* pos, uint16_t* k_cache,
+                                      uint16_t* v_cache, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
+                                      float theta, uint32_t* err, cudaStream_t st);
+cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st);
+cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
+                               cudaStream_t st);
+
 // Raise the dynamic shared-memory limit of every kernel of a unit (once per device).
 cudaError_t allow_smem_qkv();
 cudaError_t allow_smem_glu();

@@ -1,0 +1,178 @@
+// The batched prompt pass: the prompt's positions go through the layers as
+// rows of dense GEMMs (tensor cores, through cuBLAS: bf16 operands, fp32
+// accumulation and output) instead of one decode step per token.  Every fp32
+// activation operand is split into two bf16 parts, hi = bf16(x) and lo =
+// bf16(x - hi), and each GEMM runs on both (W.hi + W.lo), which keeps about
+// 16 bits of the activations -- the decode step's fp32 activations are the
+// reference, and a single bf16 rounding of them moves attention scores far
+// enough to show in the logits.  The
+// elementwise work between the GEMMs -- the embedding gather, RMSNorm,
+// rotate-half RoPE with the K/V store, SiLU*mul -- and the causal attention
+// (the decode attention kernel with one query row per position) are kernels
+// of this library.  Rows are laid out sequence-major: row r is position
+// pos[b] + i0 + i of sequence b = r / n, i = r % n, for a chunk of n
+// positions starting at i0.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "dec_launch.cuh"
+
+namespace dec {
+
+namespace {
+
+// r[row] = embedding row of the row's prompt token (fp32).
+__global__ void prefill_embed_kernel(const int32_t* prompt, int P, int i0, int n, int H, const uint16_t* embed,
+                                     int vocab, float* r, uint32_t* err) {
+  const int row = blockIdx.x;
+  const int b = row / n, i = row - b * n;
+  const int tok = prompt[static_cast<size_t>(b) * P + i0 + i];
+  const bool ok = tok >= 0 && tok < vocab;
+  if (!ok && threadIdx.x == 0) atomicOr(err, kErrTokenRange);
+  const uint16_t* e = embed + static_cast<size_t>(ok ? tok : 0) * H;
+  float* dst = r + static_cast<size_t>(row) * H;
+  for (int k = threadIdx.x; k < H; k += blockDim.x)
+    dst[k] = ok ? __uint_as_float(static_cast<uint32_t>(e[k]) << 16) : 0.f;
+}
+
+// x as two bf16 parts, hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split_bf16(float x, uint16_t* hi, uint16_t* lo) {
+  const uint16_t h = f32_to_bf16(x);
+  *hi = h;
+  *lo = f32_to_bf16(x - __uint_as_float(static_cast<uint32_t>(h) << 16));
+}
+
+// y = r / sqrt(mean(r^2) + eps) * gamma as hi/lo bf16 parts; one CTA of 256 per row.
+__global__ void prefill_norm_kernel(const float* r, const uint16_t* gamma, float eps, int H, uint16_t* y,
+                                    uint16_t* y_lo) {
+  __shared__ float red[8];
+  const float* x = r + static_cast<size_t>(blockIdx.x) * H;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < H; k += 256) ss = fmaf(x[k], x[k], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
+  uint16_t* out = y + static_cast<size_t>(blockIdx.x) * H;
+  uint16_t* out_lo = y_lo + static_cast<size_t>(blockIdx.x) * H;
+  for (int k = threadIdx.x; k < H; k += 256)
+    split_bf16((x[k] * inv) * __uint_as_float(static_cast<uint32_t>(gamma[k]) << 16), &out[k], &out_lo[k]);
+}
+
+struct RopeArgs {
+  const float* qkv;     // [rows][(Hq + 2 Hkv) * D]
+  float* q_out;         // [rows][Hq * D] rotated queries
+  const int32_t* pos;   // [B]
+  uint16_t* k_cache;    // [B][Hkv][S_max][D]
+  uint16_t* v_cache;
+  int n, i0, Hq, Hkv, D, S_max;
+  uint32_t* err;
+  double inv_freq[64];
+};
+
+// Rotate-half RoPE of q (to q_out) and k at the row's position, k and v to
+// the cache.  One CTA per row; thread t takes pair t of each head.
+__global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
+  const int row = blockIdx.x;
+  const int b = row / a.n, i = row - b * a.n;
+  const int p = a.pos[b] + a.i0 + i;
+  if (p < 0 || p >= a.S_max) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrPosRange);
+    return;
+  }
+  const int half = a.D / 2;
+  const int width = (a.Hq + 2 * a.Hkv) * a.D;
+  const float* x = a.qkv + static_cast<size_t>(row) * width;
+  for (int t = threadIdx.x; t < (a.Hq + a.Hkv) * half; t += blockDim.x) {
+    const int hh = t / half, j = t - hh * half;
+    float cs, sn, l2, h2;
+    rope_cos_sin(p, a.inv_freq[j], &cs, &sn);
+    const float* v = x + hh * a.D;
+    rope_rotate(v[j], v[j + half], cs, sn, &l2, &h2);
+    if (hh < a.Hq) {
+      float* q = a.q_out + static_cast<size_t>(row) * a.Hq * a.D + hh * a.D;
+      q[j] = l2;
+      q[j + half] = h2;
+    } else {
+      uint16_t* dst = a.k_cache + ((static_cast<size_t>(b) * a.Hkv + (hh - a.Hq)) * a.S_max + p) * a.D;
+      dst[j] = f32_to_bf16(l2);
+      dst[j + half] = f32_to_bf16(h2);
+    }
+  }
+  const float* vv = x + (a.Hq + a.Hkv) * a.D;
+  for (int t = threadIdx.x; t < a.Hkv * a.D; t += blockDim.x) {
+    const int g = t / a.D, d = t - g * a.D;
+    a.v_cache[((static_cast<size_t>(b) * a.Hkv + g) * a.S_max + p) * a.D + d] = f32_to_bf16(vv[t]);
+  }
+}
+
+// hi/lo bf16 parts of an fp32 array.
+__global__ void prefill_cast_kernel(const float* x, uint16_t* y, uint16_t* y_lo, size_t n) {
+  for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<size_t>(gridDim.x) * blockDim.x)
+    split_bf16(x[k], &y[k], &y_lo[k]);
+}
+
+// h = silu(g) * u as hi/lo bf16 parts, from gu = [rows][2 I] (gate columns, then up).
+__global__ void prefill_glu_kernel(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows) {
+  const size_t n = rows * I;
+  for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t row = k / I, c = k - row * I;
+    const float* x = gu + row * 2 * I;
+    split_bf16(silu_f32(x[c]) * x[I + c], &h[k], &h_lo[k]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_embed(const int32_t* prompt, int P, int i0, int n, int rows, int H, const uint16_t* embed,
+                                 int vocab, float* r, uint32_t* err, cudaStream_t st) {
+  prefill_embed_kernel<<<rows, 256, 0, st>>>(prompt, P, i0, n, H, embed, vocab, r, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_norm(const float* r, const uint16_t* gamma, float eps, int H, uint16_t* y, uint16_t* y_lo,
+                                int rows, cudaStream_t st) {
+  prefill_norm_kernel<<<rows, 256, 0, st>>>(r, gamma, eps, H, y, y_lo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int32_t* pos, uint16_t* k_cache,
+                                      uint16_t* v_cache, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
+                                      float theta, uint32_t* err, cudaStream_t st) {
+  RopeArgs a{};
+  a.qkv = qkv;
+  a.q_out = q_out;
+  a.pos = pos;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.n = n;
+  a.i0 = i0;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.S_max = S_max;
+  a.err = err;
+  for (int j = 0; j < D / 2; ++j)
+    a.inv_freq[j] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(D));
+  prefill_rope_store_kernel<<<rows, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st) {
+  prefill_cast_kernel<<<sms * 4, 256, 0, st>>>(x, y, y_lo, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
+                               cudaStream_t st) {
+  prefill_glu_kernel<<<sms * 4, 256, 0, st>>>(gu, I, h, h_lo, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace dec
