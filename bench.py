@@ -3,8 +3,8 @@
 Workload (default ``dense4b``): a 36-layer 4B-class dense GQA decoder
 (H=2560, Hq=32, Hkv=8, D=128, I=9728, V=151936, tied embeddings, bf16
 weights N(0, 0.02), norm gains 1 + N(0, 0.02), seeded synthetic data), batch
-1, a 512-token uniform-random prompt through the teacher-forced prompt pass
-(untimed), then greedy decode steps through the native loop (CUDA-graph
+1, a 512-token uniform-random prompt through the batched prompt pass
+(tensor-core GEMMs; untimed), then greedy decode steps through the native loop (CUDA-graph
 replays, EOS id 0 checked every 16 steps).  A "step" is one decode step of
 the whole model; the timed steps cycle over the workload's 256 decode
 positions 511..766 (the cache slots are rewritten on each pass).

@@ -204,13 +204,14 @@ size_t dec_state_workspace_size(const dec_model* m, int B, int S_max);
 
 /*
  * Validates model and state, zeroes the workspace (on `stream`) and creates
- * the library-owned part of the state (pinned host word, graph cache).  Call
+ * the library-owned part of the state (pinned host word, graph cache, a
+ * cuBLAS handle whose workspace lies inside the state's workspace).  Call
  * once before dec_step / dec_prefill / dec_decode; the workspace keeps its
  * counters at zero between calls.
  */
 int dec_state_init(const dec_model* m, dec_state* s, void* stream);
 
-/* Frees what dec_state_init created (graphs, pinned word).  Caller memory is untouched. */
+/* Frees what dec_state_init created (graphs, pinned word, cuBLAS handle).  Caller memory is untouched. */
 int dec_state_release(dec_state* s);
 
 /*
@@ -232,11 +233,16 @@ int dec_step(const dec_model* m, dec_state* s, void* stream);
 int dec_step_launches(const dec_model* m, const dec_state* s, int* launches);
 
 /*
- * Teacher-forced prompt pass: for i = 0 .. P-2 runs the layers on prompt
- * token i at position pos[b] + i (filling the cache) and moves on to prompt
- * token i+1 without the LM head; leaves token[b] = prompt[b][P-1] and
- * pos[b] advanced by P-1, so that the next dec_step processes the last prompt
- * token.  prompt: device int32 [B][P].  pos must hold the start positions.
+ * Prompt pass: runs the layers over prompt tokens 0 .. P-2 of every row at
+ * positions pos[b] + i (filling the cache, no LM head); leaves token[b] =
+ * prompt[b][P-1] and pos[b] advanced by P-1, so that the next dec_step
+ * processes the last prompt token.  prompt: device int32 [B][P].  pos must
+ * hold the start positions.  On an initialised state the positions run as
+ * rows of dense GEMMs (chunks of up to 512 rows over all B sequences) on the
+ * tensor cores through cuBLAS: bf16 weights, activations split into two bf16
+ * parts (about 16 bits kept), fp32 accumulation; attention per position over
+ * the cache (causal by construction).  Without dec_state_init it runs one
+ * decode step per position instead.  Stream-ordered; asynchronous.
  */
 int dec_prefill(const dec_model* m, dec_state* s, const int32_t* prompt, int P, void* stream);
 
