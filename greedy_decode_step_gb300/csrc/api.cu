@@ -620,6 +620,9 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
 }
 
 // Layers of one step; with `head`, also the LM head and the bookkeeping.
+int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
+              bool head, cudaStream_t st);
+
 int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
                  cudaStream_t st) {
   {
@@ -632,6 +635,16 @@ int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, c
       DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "step kernel launch: %s", cudaGetErrorString(e));
       return DEC_OK;
     }
+  }
+  {
+    // batch > 2: the weight GEMVs as tensor-core GEMMs with the batch as rows
+    auto* in = static_cast<StateInternal*>(s->internal);
+    const size_t need = 2ull * s->batch * std::max<size_t>(static_cast<size_t>(m->vocab), 1);
+    const size_t have = static_cast<size_t>(w.pf_rows) *
+                        std::max<size_t>(static_cast<size_t>(m->n_heads + 2 * m->n_kv_heads) * m->head_dim,
+                                         2ull * m->intermediate);
+    if (in && in->blas && 2 * s->batch <= w.pf_rows && (!m->lm_head || need <= have))
+      return step_gemm(m, s, dv, w, in->blas, head, st);
   }
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
   const bool fuse = norm_fusable(B, H);
@@ -759,6 +772,180 @@ int state_views(const dec_model* m, dec_state* s, const DeviceInfo* dv, StateWs*
   *w = carve_state(m, s->batch, s->max_seq, dv->sms, static_cast<unsigned char*>(s->workspace));
   DEC_CHECK(s->workspace_bytes >= w->bytes, DEC_EINVAL, "workspace has %zu bytes, needs %zu", s->workspace_bytes,
             w->bytes);
+  return DEC_OK;
+}
+
+// ------------------------------------------------------------------------------- batched prompt pass
+
+// C[rows][N] (leading dimension ldc) = beta * C + Y[rows][K] . W[N][K]^T with
+// bf16 operands and fp32 accumulation and output (cuBLAS is column-major: it
+// computes C^T = W . Y^T).
+// The activation operand comes as hi and lo bf16 parts: C = beta C + W.hi + W.lo.
+int gemm_rows(cublasHandle_t h, const void* W, int N, int K, const uint16_t* Y, const uint16_t* Y_lo, int rows,
+              float* C, int ldc, float beta) {
+  const float alpha = 1.0f, one = 1.0f;
+  for (int part = 0; part < 2; ++part) {
+    const cublasStatus_t bs = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, rows, K, &alpha, W, CUDA_R_16BF, K,
+                                           part == 0 ? Y : Y_lo, CUDA_R_16BF, K, part == 0 ? &beta : &one, C,
+                                           CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS GEMM (%d x %d x %d) failed with status %d", N, rows,
+              K, static_cast<int>(bs));
+  }
+  return DEC_OK;
+}
+
+__global__ void prefill_finish_kernel(int32_t* token, int32_t* pos, int B, const int32_t* prompt, int P) {
+  const int b = threadIdx.x;
+  if (b < B) {
+    token[b] = prompt[static_cast<size_t>(b) * P + (P - 1)];
+    pos[b] += P - 1;
+  }
+}
+
+// The prompt's positions 0 .. P-2 of every sequence as rows of GEMMs, in
+// chunks of w.pf_rows / B positions (a chunk attends to the cache, which
+// holds every earlier position and its own); then token = prompt[b][P-1] and
+// pos advanced by P-1, as the step-by-step pass leaves them.
+int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
+                    const int32_t* prompt, int P, cudaStream_t st) {
+  const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
+  const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D, WB = std::max(QKV, 2 * I);
+  const int per = w.pf_rows / B;
+  const cublasStatus_t bs = cublasSetStream(h, st);
+  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS stream (status %d)", static_cast<int>(bs));
+  for (int i0 = 0; i0 < P - 1; i0 += per) {
+    const int n = std::min(per, P - 1 - i0);
+    const int R = B * n;
+    DEC_CUDA(launch_prefill_embed(prompt, P, i0, n, R, H, static_cast<const uint16_t*>(m->embed), m->vocab, w.pf_r,
+                                  dv->err, st));
+    for (int l = 0; l < m->n_layers; ++l) {
+      const dec_layer_weights& lw = m->layers[l];
+      uint16_t* kc = static_cast<uint16_t*>(s->k_cache[l]);
+      uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
+      DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, w.pf_bf,
+                                   w.pf_bf_lo, R, st));
+      DEC_TRY(gemm_rows(h, lw.wq, QD, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, QKV, 0.f));
+      DEC_TRY(gemm_rows(h, lw.wk, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD, QKV, 0.f));
+      DEC_TRY(gemm_rows(h, lw.wv, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD + Hkv * D, QKV, 0.f));
+      DEC_CUDA(launch_prefill_rope_store(w.pf_big, w.pf_q, s->pos, kc, vc, n, i0, R, Hq, Hkv, D, s->max_seq,
+                                         m->rope_theta, dv->err, st));
+      AttnArgs t{};
+      t.q = w.pf_q;
+      t.k_cache = kc;
+      t.v_cache = vc;
+      t.pos = s->pos;
+      t.o = w.pf_o;
+      t.part = w.attn_part;
+      t.tickets = w.attn_tickets;
+      t.Hq = Hq;
+      t.Hkv = Hkv;
+      t.D = D;
+      t.S_max = s->max_seq;
+      t.n_split = 1;
+      t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+      t.rows_per_seq = n;
+      t.row_pos0 = i0;
+      DEC_TRY(run_attn(t, R, dv, st, false));
+      DEC_CUDA(launch_prefill_cast(w.pf_o, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R) * QD, dv->sms, st));
+      DEC_TRY(gemm_rows(h, lw.wo, H, QD, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
+      DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, w.pf_bf,
+                                   w.pf_bf_lo, R, st));
+      DEC_TRY(gemm_rows(h, lw.wg, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, 2 * I, 0.f));
+      DEC_TRY(gemm_rows(h, lw.wu, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + I, 2 * I, 0.f));
+      DEC_CUDA(launch_prefill_glu(w.pf_big, I, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R), dv->sms, st));
+      DEC_TRY(gemm_rows(h, lw.wd, H, I, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
+    }
+  }
+  (void)WB;
+  DEC_CUDA(launch(prefill_finish_kernel, dim3(1), dim3(32), 0, st, false, s->token, s->pos, B, prompt, P));
+  return DEC_OK;
+}
+
+// C[rows][N] = Y[rows][K] . W[N][K]^T, one GEMM (bf16 operands, fp32 out).
+int gemm_stacked(cublasHandle_t h, const void* W, int N, int K, const uint16_t* Y, int rows, float* C, int ldc) {
+  const float alpha = 1.0f, beta = 0.0f;
+  const cublasStatus_t bs = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, rows, K, &alpha, W, CUDA_R_16BF, K, Y,
+                                         CUDA_R_16BF, K, &beta, C, CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F,
+                                         CUBLAS_GEMM_DEFAULT);
+  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS GEMM (%d x %d x %d) failed with status %d", N, rows, K,
+            static_cast<int>(bs));
+  return DEC_OK;
+}
+
+// One decode step for batch > 2 (dec_step semantics): the weight GEMVs run as
+// GEMMs whose rows are the B sequences' activations, split into hi and lo
+// bf16 parts and stacked (2B rows, the weights read once); the kernels after
+// each GEMM add the halves.  Attention is the split-K decode kernel, and the
+// LM head ends in a row argmax and the same bookkeeping as the GEMV path.
+int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
+              bool head, cudaStream_t st) {
+  const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
+  const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D;
+  const int B2 = 2 * B;
+  const cublasStatus_t bs = cublasSetStream(h, st);
+  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS stream (status %d)", static_cast<int>(bs));
+  float* r = s->residual;
+  uint16_t* xs = w.pf_bf;   // [2B][K]: hi rows, then lo rows
+  float* c2 = w.pf_big;     // [2B][N] stacked GEMM output
+  if (m->embed) DEC_CUDA(launch_prefill_embed(s->token, 1, 0, 1, B, H, static_cast<const uint16_t*>(m->embed),
+                                              m->vocab, r, dv->err, st));
+  for (int l = 0; l < m->n_layers; ++l) {
+    const dec_layer_weights& lw = m->layers[l];
+    uint16_t* kc = static_cast<uint16_t*>(s->k_cache[l]);
+    uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
+    DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, xs,
+                                 xs + static_cast<size_t>(B) * H, B, st));
+    DEC_TRY(gemm_stacked(h, lw.wq, QD, H, xs, B2, c2, QKV));
+    DEC_TRY(gemm_stacked(h, lw.wk, Hkv * D, H, xs, B2, c2 + QD, QKV));
+    DEC_TRY(gemm_stacked(h, lw.wv, Hkv * D, H, xs, B2, c2 + QD + Hkv * D, QKV));
+    DEC_CUDA(launch_prefill_rope_store(c2, w.q, s->pos, kc, vc, 1, 0, B, Hq, Hkv, D, s->max_seq, m->rope_theta,
+                                       dv->err, st, B));
+    AttnArgs t{};
+    t.q = w.q;
+    t.k_cache = kc;
+    t.v_cache = vc;
+    t.pos = s->pos;
+    t.o = w.o;
+    t.part = w.attn_part;
+    t.tickets = w.attn_tickets;
+    t.Hq = Hq;
+    t.Hkv = Hkv;
+    t.D = D;
+    t.S_max = s->max_seq;
+    t.n_split = w.n_split;
+    t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+    DEC_TRY(run_attn(t, B, dv, st, false));
+    DEC_CUDA(launch_prefill_cast(w.o, xs, xs + static_cast<size_t>(B) * QD, static_cast<size_t>(B) * QD, dv->sms,
+                                 st));
+    DEC_TRY(gemm_stacked(h, lw.wo, H, QD, xs, B2, c2, H));
+    DEC_CUDA(launch_rows_resid_add(c2, B, H, r, dv->sms, st));
+    DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, xs,
+                                 xs + static_cast<size_t>(B) * H, B, st));
+    DEC_TRY(gemm_stacked(h, lw.wg, I, H, xs, B2, c2, 2 * I));
+    DEC_TRY(gemm_stacked(h, lw.wu, I, H, xs, B2, c2 + I, 2 * I));
+    DEC_CUDA(launch_prefill_glu(c2, I, xs, xs + static_cast<size_t>(B) * I, static_cast<size_t>(B), dv->sms, st, B));
+    DEC_TRY(gemm_stacked(h, lw.wd, H, I, xs, B2, c2, H));
+    DEC_CUDA(launch_rows_resid_add(c2, B, H, r, dv->sms, st));
+  }
+  if (head && m->lm_head) {
+    DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(m->final_norm), m->rms_eps, H, xs,
+                                 xs + static_cast<size_t>(B) * H, B, st));
+    DEC_TRY(gemm_stacked(h, m->lm_head, m->vocab, H, xs, B2, c2, m->vocab));
+    DEC_CUDA(launch_rows_argmax(c2, B, m->vocab, w.keys, dv->sms, st));
+    GemvIO io{};
+    io.B = B;
+    io.argmax_keys = w.keys;
+    io.err = dv->err;
+    io.book.enabled = 1;
+    io.book.token = s->token;
+    io.book.pos = s->pos;
+    io.book.done = w.done;
+    io.book.ctrl = w.ctrl;
+    DEC_CUDA(launch_rows_finish(io, st));
+  } else {
+    DEC_CUDA(launch(advance_kernel, dim3(1), dim3(32), 0, st, false, s->token, s->pos, B,
+                    static_cast<const int32_t*>(nullptr), 0, 0));
+  }
   return DEC_OK;
 }
 
@@ -1043,94 +1230,14 @@ int dec_step_launches(const dec_model* m, const dec_state* s, int* launches) {
     *launches = 1;
     return DEC_OK;
   }
+  auto* in = static_cast<StateInternal*>(s->internal);
+  if (in && in->blas && 2 * s->batch <= w.pf_rows) {
+    // the GEMM path: this library's kernels around the cuBLAS GEMMs
+    *launches = (m->embed ? 1 : 0) + 8 * m->n_layers + (m->lm_head ? 3 : 1);
+    return DEC_OK;
+  }
   const bool fuse = norm_fusable(s->batch, m->hidden);
   *launches = m->n_layers * (fuse ? 5 : 7) + (m->lm_head ? (fuse ? 1 : 2) : 1);
-  return DEC_OK;
-}
-
-// ------------------------------------------------------------------------------- batched prompt pass
-
-// C[rows][N] (leading dimension ldc) = beta * C + Y[rows][K] . W[N][K]^T with
-// bf16 operands and fp32 accumulation and output (cuBLAS is column-major: it
-// computes C^T = W . Y^T).
-// The activation operand comes as hi and lo bf16 parts: C = beta C + W.hi + W.lo.
-int gemm_rows(cublasHandle_t h, const void* W, int N, int K, const uint16_t* Y, const uint16_t* Y_lo, int rows,
-              float* C, int ldc, float beta) {
-  const float alpha = 1.0f, one = 1.0f;
-  for (int part = 0; part < 2; ++part) {
-    const cublasStatus_t bs = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, rows, K, &alpha, W, CUDA_R_16BF, K,
-                                           part == 0 ? Y : Y_lo, CUDA_R_16BF, K, part == 0 ? &beta : &one, C,
-                                           CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS GEMM (%d x %d x %d) failed with status %d", N, rows,
-              K, static_cast<int>(bs));
-  }
-  return DEC_OK;
-}
-
-__global__ void prefill_finish_kernel(int32_t* token, int32_t* pos, int B, const int32_t* prompt, int P) {
-  const int b = threadIdx.x;
-  if (b < B) {
-    token[b] = prompt[static_cast<size_t>(b) * P + (P - 1)];
-    pos[b] += P - 1;
-  }
-}
-
-// The prompt's positions 0 .. P-2 of every sequence as rows of GEMMs, in
-// chunks of w.pf_rows / B positions (a chunk attends to the cache, which
-// holds every earlier position and its own); then token = prompt[b][P-1] and
-// pos advanced by P-1, as the step-by-step pass leaves them.
-int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
-                    const int32_t* prompt, int P, cudaStream_t st) {
-  const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
-  const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D, WB = std::max(QKV, 2 * I);
-  const int per = w.pf_rows / B;
-  const cublasStatus_t bs = cublasSetStream(h, st);
-  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS stream (status %d)", static_cast<int>(bs));
-  for (int i0 = 0; i0 < P - 1; i0 += per) {
-    const int n = std::min(per, P - 1 - i0);
-    const int R = B * n;
-    DEC_CUDA(launch_prefill_embed(prompt, P, i0, n, R, H, static_cast<const uint16_t*>(m->embed), m->vocab, w.pf_r,
-                                  dv->err, st));
-    for (int l = 0; l < m->n_layers; ++l) {
-      const dec_layer_weights& lw = m->layers[l];
-      uint16_t* kc = static_cast<uint16_t*>(s->k_cache[l]);
-      uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
-      DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, w.pf_bf,
-                                   w.pf_bf_lo, R, st));
-      DEC_TRY(gemm_rows(h, lw.wq, QD, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, QKV, 0.f));
-      DEC_TRY(gemm_rows(h, lw.wk, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD, QKV, 0.f));
-      DEC_TRY(gemm_rows(h, lw.wv, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD + Hkv * D, QKV, 0.f));
-      DEC_CUDA(launch_prefill_rope_store(w.pf_big, w.pf_q, s->pos, kc, vc, n, i0, R, Hq, Hkv, D, s->max_seq,
-                                         m->rope_theta, dv->err, st));
-      AttnArgs t{};
-      t.q = w.pf_q;
-      t.k_cache = kc;
-      t.v_cache = vc;
-      t.pos = s->pos;
-      t.o = w.pf_o;
-      t.part = w.attn_part;
-      t.tickets = w.attn_tickets;
-      t.Hq = Hq;
-      t.Hkv = Hkv;
-      t.D = D;
-      t.S_max = s->max_seq;
-      t.n_split = 1;
-      t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
-      t.rows_per_seq = n;
-      t.row_pos0 = i0;
-      DEC_TRY(run_attn(t, R, dv, st, false));
-      DEC_CUDA(launch_prefill_cast(w.pf_o, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R) * QD, dv->sms, st));
-      DEC_TRY(gemm_rows(h, lw.wo, H, QD, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
-      DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, w.pf_bf,
-                                   w.pf_bf_lo, R, st));
-      DEC_TRY(gemm_rows(h, lw.wg, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, 2 * I, 0.f));
-      DEC_TRY(gemm_rows(h, lw.wu, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + I, 2 * I, 0.f));
-      DEC_CUDA(launch_prefill_glu(w.pf_big, I, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R), dv->sms, st));
-      DEC_TRY(gemm_rows(h, lw.wd, H, I, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
-    }
-  }
-  (void)WB;
-  DEC_CUDA(launch(prefill_finish_kernel, dim3(1), dim3(32), 0, st, false, s->token, s->pos, B, prompt, P));
   return DEC_OK;
 }
 

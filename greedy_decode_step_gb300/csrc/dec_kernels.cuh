@@ -585,6 +585,43 @@ __device__ __forceinline__ void better(float& bv, uint32_t& bi, float v, uint32_
 // the bookkeeping (token, position, output column, EOS state).  When
 // `from_part` is set the CTA's logits are first assembled from the partial
 // sums of the register path.  head_val/head_idx: [8][kMaxBatch] shared.
+// Step bookkeeping once every row's argmax key is in (one warp, lane b = row
+// b): token[b] <- the argmax (or eos once the row has ended), the emitted
+// token into the output buffer, pos[b] + 1, the all-done word and the step
+// count; the keys go back to zero.
+__device__ __forceinline__ void finish_rows(const GemvIO& io, int B) {
+  const int lane = threadIdx.x & 31;
+  int32_t emit = 0;
+  bool row_done = true;
+  const int b = lane;
+  if (b < B) {
+    const unsigned long long key = atomicExch(&io.argmax_keys[b], 0ull);
+    const int32_t tok = static_cast<int32_t>(argmax_key_index(key));
+    if (io.token_out) io.token_out[b] = tok;
+    if (io.book.enabled) {
+      Ctrl* c = io.book.ctrl;
+      const int eos = c->eos_id;
+      emit = io.book.done[b] ? eos : tok;
+      if (eos >= 0 && emit == eos) io.book.done[b] = 1;
+      row_done = io.book.done[b] != 0;
+      const int step = c->step;
+      if (c->out_tokens) {
+        if (step < c->out_cap)
+          c->out_tokens[static_cast<size_t>(b) * c->out_cap + step] = emit;
+        else
+          atomicOr(io.err, kErrOutRange);
+      }
+      io.book.token[b] = emit;
+      io.book.pos[b] += 1;
+    }
+  }
+  const unsigned all = __all_sync(0xffffffffu, row_done);
+  if (lane == 0 && io.book.enabled) {
+    io.book.ctrl->all_done = all ? 1 : 0;
+    io.book.ctrl->step += 1;
+  }
+}
+
 template <int BT>
 __device__ void head_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int n, const float* part,
                               bool from_part, float (&best_v)[BT], uint32_t (&best_i)[BT], float* head_val,
@@ -641,38 +678,8 @@ __device__ void head_epilogue(const GemvShape& sh, const GemvIO& io, int u0, int
   asm volatile("bar.sync 1, 256;" ::: "memory");
   if (*is_last && warp == 0) {
     __threadfence();
-    int32_t emit = 0;
-    bool row_done = true;
-    const int b = lane;
-    if (b < B) {
-      const unsigned long long key = atomicExch(&io.argmax_keys[b], 0ull);
-      const int32_t tok = static_cast<int32_t>(argmax_key_index(key));
-      if (io.token_out) io.token_out[b] = tok;
-      if (io.book.enabled) {
-        Ctrl* c = io.book.ctrl;
-        const int eos = c->eos_id;
-        emit = io.book.done[b] ? eos : tok;
-        if (eos >= 0 && emit == eos) io.book.done[b] = 1;
-        row_done = io.book.done[b] != 0;
-        const int step = c->step;
-        if (c->out_tokens) {
-          if (step < c->out_cap)
-            c->out_tokens[static_cast<size_t>(b) * c->out_cap + step] = emit;
-          else
-            atomicOr(io.err, kErrOutRange);
-        }
-        io.book.token[b] = emit;
-        io.book.pos[b] += 1;
-      }
-    }
-    const unsigned all = __all_sync(0xffffffffu, row_done);
-    if (lane == 0) {
-      if (io.book.enabled) {
-        io.book.ctrl->all_done = all ? 1 : 0;
-        io.book.ctrl->step += 1;
-      }
-      atomicExch(io.ticket, 0u);
-    }
+    finish_rows(io, B);
+    if (lane == 0) atomicExch(io.ticket, 0u);
   }
 }
 

@@ -65,10 +65,14 @@ cudaError_t launch_prefill_norm(const float* r, const uint16_t* gamma, float eps
                                 int rows, cudaStream_t st);
 cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int32_t* pos, uint16_t* k_cache,
                                       uint16_t* v_cache, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
-                                      float theta, uint32_t* err, cudaStream_t st);
+                                      float theta, uint32_t* err, cudaStream_t st, int half_rows = 0);
 cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st);
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
-                               cudaStream_t st);
+                               cudaStream_t st, int half_rows = 0);
+// Decode step at batch > 2 on the same GEMM path (halves of stacked GEMMs added).
+cudaError_t launch_rows_resid_add(const float* C, int B, int H, float* r, int sms, cudaStream_t st);
+cudaError_t launch_rows_argmax(const float* C, int B, int V, unsigned long long* keys, int sms, cudaStream_t st);
+cudaError_t launch_rows_finish(const GemvIO& io, cudaStream_t st);
 
 // Raise the dynamic shared-memory limit of every kernel of a unit (once per device).
 cudaError_t allow_smem_qkv();

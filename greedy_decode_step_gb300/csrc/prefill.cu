@@ -12,8 +12,13 @@
 // of this library.  Rows are laid out sequence-major: row r is position
 // pos[b] + i0 + i of sequence b = r / n, i = r % n, for a chunk of n
 // positions starting at i0.
+//
+// The same kernels serve the decode step at batch > 2 (one row per sequence,
+// n = 1): there the hi and lo parts are stacked as 2B rows of ONE GEMM (the
+// weights are read once) and the kernels after it add the two halves.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "dec_launch.cuh"
@@ -70,6 +75,7 @@ struct RopeArgs {
   uint16_t* k_cache;    // [B][Hkv][S_max][D]
   uint16_t* v_cache;
   int n, i0, Hq, Hkv, D, S_max;
+  int half_rows;        // > 0: row r of the GEMM output is rows r and r + half_rows added
   uint32_t* err;
   double inv_freq[64];
 };
@@ -87,12 +93,15 @@ __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
   const int half = a.D / 2;
   const int width = (a.Hq + 2 * a.Hkv) * a.D;
   const float* x = a.qkv + static_cast<size_t>(row) * width;
+  const float* x2 = a.half_rows ? x + static_cast<size_t>(a.half_rows) * width : nullptr;
   for (int t = threadIdx.x; t < (a.Hq + a.Hkv) * half; t += blockDim.x) {
     const int hh = t / half, j = t - hh * half;
     float cs, sn, l2, h2;
     rope_cos_sin(p, a.inv_freq[j], &cs, &sn);
-    const float* v = x + hh * a.D;
-    rope_rotate(v[j], v[j + half], cs, sn, &l2, &h2);
+    const int e = hh * a.D + j;
+    const float lo = x2 ? x[e] + x2[e] : x[e];
+    const float hi = x2 ? x[e + half] + x2[e + half] : x[e + half];
+    rope_rotate(lo, hi, cs, sn, &l2, &h2);
     if (hh < a.Hq) {
       float* q = a.q_out + static_cast<size_t>(row) * a.Hq * a.D + hh * a.D;
       q[j] = l2;
@@ -103,10 +112,11 @@ __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
       dst[j + half] = f32_to_bf16(h2);
     }
   }
-  const float* vv = x + (a.Hq + a.Hkv) * a.D;
+  const int vo = (a.Hq + a.Hkv) * a.D;
   for (int t = threadIdx.x; t < a.Hkv * a.D; t += blockDim.x) {
     const int g = t / a.D, d = t - g * a.D;
-    a.v_cache[((static_cast<size_t>(b) * a.Hkv + g) * a.S_max + p) * a.D + d] = f32_to_bf16(vv[t]);
+    const float v = x2 ? x[vo + t] + x2[vo + t] : x[vo + t];
+    a.v_cache[((static_cast<size_t>(b) * a.Hkv + g) * a.S_max + p) * a.D + d] = f32_to_bf16(v);
   }
 }
 
@@ -117,16 +127,64 @@ __global__ void prefill_cast_kernel(const float* x, uint16_t* y, uint16_t* y_lo,
     split_bf16(x[k], &y[k], &y_lo[k]);
 }
 
-// h = silu(g) * u as hi/lo bf16 parts, from gu = [rows][2 I] (gate columns, then up).
-__global__ void prefill_glu_kernel(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows) {
+// h = silu(g) * u as hi/lo bf16 parts, from gu = [rows][2 I] (gate columns,
+// then up; with half_rows > 0 rows r and r + half_rows added).
+__global__ void prefill_glu_kernel(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int half_rows) {
   const size_t n = rows * I;
   for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
        k += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const size_t row = k / I, c = k - row * I;
     const float* x = gu + row * 2 * I;
-    split_bf16(silu_f32(x[c]) * x[I + c], &h[k], &h_lo[k]);
+    float g = x[c], u = x[I + c];
+    if (half_rows) {
+      const float* x2 = x + static_cast<size_t>(half_rows) * 2 * I;
+      g += x2[c];
+      u += x2[I + c];
+    }
+    split_bf16(silu_f32(g) * u, &h[k], &h_lo[k]);
   }
 }
+
+// r[b] += C[b] + C[B + b] (the two halves of a stacked GEMM).
+__global__ void rows_resid_add_kernel(const float* C, int B, int H, float* r) {
+  const size_t n = static_cast<size_t>(B) * H;
+  for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<size_t>(gridDim.x) * blockDim.x)
+    r[k] += C[k] + C[n + k];
+}
+
+// Greedy argmax of row b of the logits C[b] + C[B + b] over a slice of the
+// vocabulary per CTA (ties to the lower index), folded into keys[b].
+__global__ void rows_argmax_kernel(const float* C, int B, int V, unsigned long long* keys) {
+  __shared__ float bv_s[8];
+  __shared__ uint32_t bi_s[8];
+  const int b = blockIdx.y;
+  const int per = (V + gridDim.x - 1) / gridDim.x;
+  const int v0 = blockIdx.x * per, v1 = min(V, v0 + per);
+  const float* lo = C + static_cast<size_t>(b) * V;
+  const float* hi = C + static_cast<size_t>(B + b) * V;
+  float bv = -INFINITY;
+  uint32_t bi = 0xFFFFFFFFu;
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) better(bv, bi, lo[v] + hi[v], static_cast<uint32_t>(v));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const uint32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    better(bv, bi, ov, oi);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    bv_s[threadIdx.x >> 5] = bv;
+    bi_s[threadIdx.x >> 5] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) better(bv, bi, bv_s[w], bi_s[w]);
+    if (bi != 0xFFFFFFFFu) atomicMax(&keys[b], argmax_key(bv, bi));
+  }
+}
+
+// The step's bookkeeping (one warp) once every row's key is in.
+__global__ void rows_finish_kernel(const GemvIO io) { finish_rows(io, io.B); }
 
 }  // namespace
 
@@ -144,8 +202,9 @@ cudaError_t launch_prefill_norm(const float* r, const uint16_t* gamma, float eps
 
 cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int32_t* pos, uint16_t* k_cache,
                                       uint16_t* v_cache, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
-                                      float theta, uint32_t* err, cudaStream_t st) {
+                                      float theta, uint32_t* err, cudaStream_t st, int half_rows) {
   RopeArgs a{};
+  a.half_rows = half_rows;
   a.qkv = qkv;
   a.q_out = q_out;
   a.pos = pos;
@@ -170,8 +229,24 @@ cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, siz
 }
 
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
-                               cudaStream_t st) {
-  prefill_glu_kernel<<<sms * 4, 256, 0, st>>>(gu, I, h, h_lo, rows);
+                               cudaStream_t st, int half_rows) {
+  prefill_glu_kernel<<<sms * 4, 256, 0, st>>>(gu, I, h, h_lo, rows, half_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_resid_add(const float* C, int B, int H, float* r, int sms, cudaStream_t st) {
+  rows_resid_add_kernel<<<sms, 256, 0, st>>>(C, B, H, r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_argmax(const float* C, int B, int V, unsigned long long* keys, int sms, cudaStream_t st) {
+  const dim3 grid(std::max(1, (sms * 2 + B - 1) / B), B);
+  rows_argmax_kernel<<<grid, 256, 0, st>>>(C, B, V, keys);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_finish(const GemvIO& io, cudaStream_t st) {
+  rows_finish_kernel<<<1, 32, 0, st>>>(io);
   return cudaGetLastError();
 }
 

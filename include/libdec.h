@@ -221,14 +221,21 @@ int dec_state_release(dec_state* s);
  * and the bookkeeping: token[b] <- argmax (or eos_id once the row has ended),
  * pos[b] <- pos[b] + 1, and the token is written to the decode output buffer
  * set by dec_decode (if any).  Without an LM head only pos advances.
+ * B <= 2: one persistent kernel (fp32 activations, bf16 weights streamed by
+ * TMA).  B > 2 on an initialised state: the weight GEMVs run as tensor-core
+ * GEMMs over the batch (cuBLAS; activations split into hi/lo bf16 parts,
+ * fp32 accumulation) around this library's norm, RoPE, attention, SiLU and
+ * argmax kernels.
  */
 int dec_step(const dec_model* m, dec_state* s, void* stream);
 
 /*
- * Number of kernel launches one dec_step (with the LM head) makes for this
- * model and state on the current device: 1 when the whole step runs as the
- * persistent kernel (B <= 2 and the model fits its plan), otherwise the
- * count of single-op launches.  Validates like dec_step; launches nothing.
+ * Number of this library's kernel launches one dec_step (with the LM head)
+ * makes for this model and state on the current device: 1 when the whole
+ * step runs as the persistent kernel (B <= 2 and the model fits its plan);
+ * for B > 2 on an initialised state, the kernels around the step's cuBLAS
+ * GEMMs (which are not counted); otherwise the count of single-op launches.
+ * Validates like dec_step; launches nothing.
  */
 int dec_step_launches(const dec_model* m, const dec_state* s, int* launches);
 

@@ -106,9 +106,11 @@ def _compose(p: Pair, r, K, V, pos, tokens=None):
     return tok
 
 
-@pytest.mark.parametrize("case", ["tiny2", "4b1", "gqa12x3_b5"])
-def test_fused_step_equals_composed_calls_bitwise(case):
-    if case == "tiny2":
+def _fused_vs_composed(case):
+    if case == "tiny2_b2":
+        m = synth.workload("tiny", n_layers=2).model
+        B, kv = 2, [128, 60]
+    elif case == "tiny2_b3":
         m = synth.workload("tiny", n_layers=2).model
         B, kv = 3, [128, 5, 60]
     elif case == "4b1":
@@ -128,10 +130,45 @@ def test_fused_step_equals_composed_calls_bitwise(case):
     gd.dec_step(p.model, p.state)
     tok2 = _compose(p, r2, K2, V2, pos2, tokens=dev_i32(tokens))
     torch.cuda.synchronize()
+    return p, m, B, kv, r2, tok2, K2, V2, pos2
+
+
+@pytest.mark.parametrize("case", ["tiny2_b2", "4b1"])
+def test_fused_step_equals_composed_calls_bitwise(case):
+    """b <= 2: the persistent step kernel computes exactly (bit for bit) what
+    the single-op entry points compute one after the other."""
+    p, m, B, kv, r2, tok2, K2, V2, pos2 = _fused_vs_composed(case)
+    assert p.model is not None and gd.dec_step_launches(p.model, p.state) == 1
     assert torch.equal(p.state.residual, r2)
     assert torch.equal(p.state.token, tok2)
     for a, b in zip(p.state.k_cache + p.state.v_cache, K2 + V2):
         assert torch.equal(a, b)
+    assert torch.equal(p.state.pos, pos2 + 1)
+
+
+@pytest.mark.parametrize("case", ["tiny2_b3", "gqa12x3_b5"])
+def test_gemm_step_matches_composed_calls(case):
+    """b > 2: the step's weight GEMVs run as tensor-core GEMMs over the batch
+    (activations split into hi/lo bf16 parts); it agrees with the single-op
+    entry points within the tolerance, token for token where the logit
+    margin is clear, and touches the same cache slots."""
+    p, m, B, kv, r2, tok2, K2, V2, pos2 = _fused_vs_composed(case)
+    assert_close(p.state.residual.cpu().numpy(), r2.cpu().numpy(), TOL, "residual")
+    for l in range(m.n_layers):
+        for a, b, what in ((p.state.k_cache[l], K2[l], "K"), (p.state.v_cache[l], V2[l], "V")):
+            ga, gb = host_bits(a), host_bits(b)
+            for row in range(B):
+                pp = kv[row]
+                assert np.array_equal(np.delete(ga[row], pp, axis=1), np.delete(gb[row], pp, axis=1)), what
+                assert_close(synth.bf16_to_f64(ga[row][:, pp]), synth.bf16_to_f64(gb[row][:, pp]), TOL, what)
+    logits = torch.empty((B, m.vocab), dtype=torch.float32, device="cuda")
+    t3 = torch.empty(B, dtype=torch.int32, device="cuda")
+    gd.dec_lmhead_argmax(r2, p.model.final_norm, m.rms_eps, p.model.lm_head, t3, logits)
+    lg = logits.cpu().numpy()
+    got, ref = p.state.token.cpu().numpy(), tok2.cpu().numpy()
+    for row in range(B):
+        if oracle.top2_margin(lg[row]) > MARGIN:
+            assert got[row] == ref[row], row
     assert torch.equal(p.state.pos, pos2 + 1)
 
 
@@ -250,10 +287,10 @@ def test_decode_rejects_bad_arguments():
 
 
 def test_step_launch_count():
-    """One launch per step while the persistent kernel applies (b <= 2), the
-    single-op sequence above that."""
+    """One launch per step while the persistent kernel applies (b <= 2); above
+    that the kernels around the step's GEMMs (1 gather + 8 per layer + 3)."""
     m = synth.workload("tiny", n_layers=2).model
-    for B, want in ((1, {1}), (2, {1}), (3, {5 * 2 + 1, 7 * 2 + 2})):
+    for B, want in ((1, {1}), (2, {1}), (3, {1 + 8 * 2 + 3})):
         p = _fresh(m, B, 64)
         assert gd.dec_step_launches(p.model, p.state) in want
 
