@@ -308,10 +308,10 @@ void fill_inv_freq(GemvArgs& a, int D, float theta) {
 // Key splits per (row, KV head): one wave of work items (one per SM) while
 // the cache is short, more splits once a split would cover over ~1024 keys on
 // average (long or batched caches, where balance matters more than latency).
-int attn_splits(int B, int Hkv, int S_max, int sms, int requested) {
+int attn_splits(int B, int Hkv, int S_max, int sms, int requested, int waves = 1) {
   const int cap = std::max(1, (S_max + kAttnChunkMin - 1) / kAttnChunkMin);
   if (requested > 0) return std::min(requested, cap);
-  const int one_wave = std::max(1, sms / (B * Hkv));
+  const int one_wave = std::max(1, waves * sms / (B * Hkv));
   const int by_len = static_cast<int>(static_cast<long long>(S_max) * B * Hkv / (static_cast<long long>(sms) * 1024)) + 1;
   return std::max(1, std::min(std::max(one_wave, by_len), cap));
 }
@@ -321,7 +321,7 @@ size_t attn_part_bytes(int B, int Hq, int Hkv, int D, int n_split) {
 }
 
 uint32_t attn_smem(int D) {
-  return 512u + static_cast<uint32_t>(kAttnMaxGroup * D * 4 + kAttnMaxGroup * kAttnTile * 4) +
+  return 512u + static_cast<uint32_t>(kAttnMaxGroup * (D + D / 8) * 4 + kAttnMaxGroup * kAttnTile * 4) +
          static_cast<uint32_t>(kAttnSlots * 2 * kAttnTile * D * 2);
 }
 
@@ -388,7 +388,9 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   const size_t o_o = c.take(sizeof(float) * B * Hq_D);
   const size_t o_h = c.take(sizeof(float) * B * m->intermediate);
   const size_t o_y = c.take(sizeof(float) * B * m->hidden);
-  w.n_split = attn_splits(B, m->n_kv_heads, S_max, sms, 0);
+  // the persistent step kernel (b <= 2) wants one item per CTA; the
+  // single-op attention kernel holds two CTAs per SM
+  w.n_split = attn_splits(B, m->n_kv_heads, S_max, sms, 0, B > 2 ? 2 : 1);
   const size_t o_part = c.take(attn_part_bytes(B, m->n_heads, m->n_kv_heads, m->head_dim, w.n_split));
   const size_t o_gbar = c.take(sizeof(unsigned int));
   const size_t o_abort = c.take(sizeof(int));
@@ -556,7 +558,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   }
   const uint32_t x_bytes = static_cast<uint32_t>(*BT) * H * 4u;
   const uint32_t G = static_cast<uint32_t>(Hq / Hkv);
-  const uint32_t attn_bytes = 256u + G * D * 4u + G * kAttnTile * 4u + 2u * kAttnTile * D * 2u;
+  const uint32_t attn_bytes = 256u + G * (D + D / 8u) * 4u + G * kAttnTile * 4u + 2u * kAttnTile * D * 2u;
   if (H % 8 != 0) return false;  // the norm gains travel as 16-byte bulk copies
   a->off_x = kStepHeaderBytes;
   a->off_part = align_up(a->off_x + x_bytes, 16);

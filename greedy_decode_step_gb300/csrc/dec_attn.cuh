@@ -19,7 +19,7 @@ namespace dec {
 constexpr int kAttnTile = 64;       // keys per stage
 constexpr int kAttnChunkMin = 32;   // fewest keys a split is given
 constexpr int kAttnMaxGroup = 16;   // query heads per KV head
-constexpr int kAttnSlots = 2;
+constexpr int kAttnSlots = 3;
 constexpr int kAttnMergeBatch = 20;  // splits folded per batch of loads in the merge
 constexpr int kAttnWarps = 8;        // consumer warps
 constexpr int kAttnConsumers = 256;
@@ -40,6 +40,16 @@ struct AttnArgs {
   int rows_per_seq;
   int row_pos0;
 };
+
+// Queries in shared memory: head h at q_s + h * attn_qstride<D>(), element e
+// at attn_qoff(e).  Every fourth chunk of 8 floats starts 4 floats further
+// on, so the 16 chunks that the lanes of a warp read at once (chunk order
+// rotated by key) fall on each 16-byte bank group exactly twice.
+template <int D>
+__host__ __device__ constexpr int attn_qstride() {
+  return D + D / 8;
+}
+__host__ __device__ __forceinline__ int attn_qoff(int e) { return e + ((e >> 5) << 2); }
 
 // (head, dim-pair) slots per consumer thread for P.V
 template <int D>
@@ -77,14 +87,14 @@ __device__ __forceinline__ void attn_tile_math(const uint4* Ks, const uint32_t* 
       float sc = -INFINITY;
       if (j < nk) {
         const uint4* kr = Ks + j * kChunks;
-        const float* qh = q_s + h * D;
+        const float* qh = q_s + h * attn_qstride<D>();
         float accs = 0.f;
 #pragma unroll 4
         for (int cc = 0; cc < kChunks; ++cc) {
           const int c = (cc + j) & (kChunks - 1);
           const uint4 w = kr[c];
-          const float4 q0 = reinterpret_cast<const float4*>(qh)[2 * c];
-          const float4 q1 = reinterpret_cast<const float4*>(qh)[2 * c + 1];
+          const float4 q0 = reinterpret_cast<const float4*>(qh + attn_qoff(8 * c))[0];
+          const float4 q1 = reinterpret_cast<const float4*>(qh + attn_qoff(8 * c))[1];
           accs = fmaf(bf16lo(w.x), q0.x, accs);
           accs = fmaf(bf16hi(w.x), q0.y, accs);
           accs = fmaf(bf16lo(w.y), q0.z, accs);
@@ -119,23 +129,32 @@ __device__ __forceinline__ void attn_tile_math(const uint4* Ks, const uint32_t* 
       }
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
-    // P.V: thread slot (head h, dims 2dp, 2dp+1)
+    // P.V: thread slot (head h, dims 2dp, 2dp+1); keys in fours into two
+    // accumulator pairs (even and odd keys), then the rescaled old value
 #pragma unroll
     for (int i = 0; i < kMaxSlots; ++i) {
       const int pr = tid + i * kAttnConsumers;
       if (pr < n_pairs) {
         const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
         const float c = corr[h];
-        float x0 = acc0[i] * c, x1 = acc1[i] * c;
         const float* ph = s_s + h * kAttnTile;
-        for (int j = 0; j < nk; ++j) {
-          const uint32_t v = Vs[j * kPairsPerHead + dp];
-          const float pj = ph[j];
-          x0 = fmaf(pj, bf16lo(v), x0);
-          x1 = fmaf(pj, bf16hi(v), x1);
+        float2 e = make_float2(0.f, 0.f), o = e;
+        int j = 0;
+        for (; j + 4 <= nk; j += 4) {
+          const uint32_t v0 = Vs[(j + 0) * kPairsPerHead + dp], v1 = Vs[(j + 1) * kPairsPerHead + dp];
+          const uint32_t v2 = Vs[(j + 2) * kPairsPerHead + dp], v3 = Vs[(j + 3) * kPairsPerHead + dp];
+          const float4 pj = *reinterpret_cast<const float4*>(ph + j);
+          e = __ffma2_rn(make_float2(pj.x, pj.x), make_float2(bf16lo(v0), bf16hi(v0)), e);
+          o = __ffma2_rn(make_float2(pj.y, pj.y), make_float2(bf16lo(v1), bf16hi(v1)), o);
+          e = __ffma2_rn(make_float2(pj.z, pj.z), make_float2(bf16lo(v2), bf16hi(v2)), e);
+          o = __ffma2_rn(make_float2(pj.w, pj.w), make_float2(bf16lo(v3), bf16hi(v3)), o);
         }
-        acc0[i] = x0;
-        acc1[i] = x1;
+        for (; j < nk; ++j) {
+          const uint32_t v = Vs[j * kPairsPerHead + dp];
+          e = __ffma2_rn(make_float2(ph[j], ph[j]), make_float2(bf16lo(v), bf16hi(v)), e);
+        }
+        acc0[i] = fmaf(acc0[i], c, e.x + o.x);
+        acc1[i] = fmaf(acc1[i], c, e.y + o.y);
       }
     }
 }
@@ -253,7 +272,7 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(288, 2) attn_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kAttnSlots;
@@ -262,8 +281,8 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
   float* m_run = reinterpret_cast<float*>(smem + 128);                 // [G]
   float* l_run = m_run + kAttnMaxGroup;                                 // [G]
   float* corr = l_run + kAttnMaxGroup;                                  // [G]
-  float* q_s = reinterpret_cast<float*>(smem + 512);                    // [G][D]
-  float* s_s = q_s + kAttnMaxGroup * D;                                 // [G][kAttnTile]
+  float* q_s = reinterpret_cast<float*>(smem + 512);                    // [G][attn_qstride]
+  float* s_s = q_s + kAttnMaxGroup * attn_qstride<D>();                 // [G][kAttnTile]
   unsigned char* ring = reinterpret_cast<unsigned char*>(s_s + kAttnMaxGroup * kAttnTile);
   constexpr uint32_t kRowBytes = D * 2;
   constexpr uint32_t kTileBytes = kAttnTile * kRowBytes;   // one of K or V
@@ -327,7 +346,7 @@ __global__ void __launch_bounds__(288, 1) attn_kernel(const __grid_constant__ At
 #pragma unroll
   for (int j = 0; j < kQPerThread; ++j) {
     const int i = threadIdx.x + j * 288;
-    if (i < G * D) q_s[i] = qv[j];
+    if (i < G * D) q_s[(i / D) * attn_qstride<D>() + attn_qoff(i % D)] = qv[j];
   }
   if (threadIdx.x < G) {
     m_run[threadIdx.x] = -INFINITY;

@@ -269,7 +269,7 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
   float* corr = l_run + kAttnMaxGroup;
   const int G = a.Hq / a.Hkv;
   float* q_s = reinterpret_cast<float*>(area + 256);
-  float* s_s = q_s + G * D;
+  float* s_s = q_s + G * attn_qstride<D>();
   uint4* tile = reinterpret_cast<uint4*>(s_s + G * kAttnTile);  // K rows then V rows
   const int tid = threadIdx.x;
   const StepLayer& w = a.layers[l];
@@ -376,8 +376,8 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
             const int h = pr / (D / 2), j = pr - h * (D / 2);
             float l2, h2;
             rope_rotate(qa[i], qb[i], cs_b[j], sn_b[j], &l2, &h2);
-            q_s[h * D + j] = l2;
-            q_s[h * D + j + D / 2] = h2;
+            q_s[h * attn_qstride<D>() + attn_qoff(j)] = l2;
+            q_s[h * attn_qstride<D>() + attn_qoff(j + D / 2)] = h2;
           }
         }
       }
