@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gemv", choices=["gemv", "reference"])
-    ap.add_argument("--workload", default="dense4b", choices=["dense4b", "layer4b"])
+    ap.add_argument("--workload", default="dense4b", choices=["dense4b", "layer4b", "dense4b_b8", "gqa12x3_b16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--prompt", type=int, default=None, help="prompt length (default: the workload's 512)")
@@ -206,6 +206,79 @@ def run_layer(args, world, rank, local):
                       "step_hbm_frac_of_measured": round(gbs / peaks()[0], 4)},
            "roofline": glu_roofline(gd, torch, model, m, dev, stream, reps=20),
            "gpu_launches": gd.dec_step_launches(model, st) * args.steps, "clocks": clk.summary()}
+    return res, None
+
+
+def run_batched(args, world, rank, local):
+    """The batched configurations (not the headline): b=8 on the 36-layer
+    4B-class model with cache lengths U{1024..32768}, or b=16 on the 24-layer
+    H=1536 12/3-head model with 8192-token caches; decode steps through
+    dec_decode.  Weights bf16 N(0, 0.02), gains 1 + N(0, 0.02), caches bf16
+    N(0, 1), drawn on the device from a seeded torch generator (the same
+    recipe as the parity tests' Philox inputs, not the same numbers)."""
+    import torch
+    import greedy_decode_step_gb300 as gd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.workload == "dense4b_b8":
+        L, H, Hq, Hkv, D, I, V, B = 36, 2560, 32, 8, 128, 9728, 151936, 8
+        kv = [int(x) for x in np.random.default_rng(0).integers(1024, 32769, B)]
+        steps = min(args.steps, 64)
+    else:
+        L, H, Hq, Hkv, D, I, V, B = 24, 1536, 12, 3, 128, 8960, 151936, 16
+        kv = [8192] * B
+        steps = min(args.steps, 128)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    bf = torch.bfloat16
+
+    def w(*sh):
+        return (torch.randn(*sh, device=dev, generator=g) * 0.02).to(bf)
+
+    def gam(n):
+        return (1 + 0.02 * torch.randn(n, device=dev, generator=g)).to(bf)
+
+    layers = [dict(attn_norm=gam(H), wq=w(Hq * D, H), wk=w(Hkv * D, H), wv=w(Hkv * D, H), wo=w(H, Hq * D),
+                   mlp_norm=gam(H), wg=w(I, H), wu=w(I, H), wd=w(H, I)) for _ in range(L)]
+    E = w(V, H)
+    model = gd.Model(L, H, Hq, Hkv, D, I, V, 1e-6, 1e6, layers, embed=E, final_norm=gam(H), lm_head=E)
+    S_max = max(kv) + steps + max(16, args.warmup) + 8
+    st = gd.State(model, B, S_max, device=dev).init()
+    for l in range(L):
+        st.k_cache[l].normal_(generator=g)
+        st.v_cache[l].normal_(generator=g)
+    p0 = torch.tensor(kv, dtype=torch.int32, device=dev)
+    t0 = torch.randint(0, V, (B,), dtype=torch.int32, device=dev, generator=g)
+    out = torch.empty((B, steps), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st.pos.copy_(p0)
+    st.token.copy_(t0)
+    gd.dec_decode(model, st, max(16, args.warmup), -1, out)
+    torch.cuda.synchronize(dev)
+    st.pos.copy_(p0)
+    st.token.copy_(t0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        n = gd.dec_decode(model, st, steps, -1, out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    assert gd.device_error(clear=True) == 0
+    ms = e0.elapsed_time(e1) / n
+    w_bytes = L * 2 * (2 * Hq * D * H + 2 * Hkv * D * H + 3 * I * H) + 2 * V * H + L * 2 * 2 * H + 2 * H
+    kv_bytes = sum(2 * L * Hkv * D * 2 * (p + (steps - 1) / 2 + 1) for p in kv)
+    gbs = (w_bytes + kv_bytes) / (ms / 1e3) / 1e9
+    peak, src = peaks()
+    res = {"metric": f"greedy decode tok/s at b={B} ({args.workload}); HBM GB/s", "value": round(B / (ms / 1e3), 2),
+           "unit": "tok/s", "n_gpus": 1, "steps": n, "warmup": max(16, args.warmup), "ms_per_step": round(ms, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded torch N(0,0.02) weights, N(0,1) caches)",
+           "config": {"workload": args.workload, "batch": B, "layers": L, "kv_lens": kv,
+                      "step_bytes": int(w_bytes + kv_bytes), "step_hbm_gbs": round(gbs, 1),
+                      "step_hbm_frac_of_measured": round(gbs / peak, 4),
+                      "path": "weight GEMMs on tensor cores (cuBLAS, hi/lo bf16 activations), split-K attention"},
+           "gpu_launches": gd.dec_step_launches(model, st) * n + 2, "clocks": clk.summary()}
     return res, None
 
 
@@ -478,6 +551,8 @@ def main():
         dist.init_process_group("nccl")
     if args.workload == "layer4b":
         res, host = run_layer(args, world, rank, local)
+    elif args.workload in ("dense4b_b8", "gqa12x3_b16"):
+        res, host = run_batched(args, world, rank, local)
     else:
         res, host = run_gpu(args, world, rank, local)
     if rank == 0 and host is not None and not args.no_cpu_baseline:
