@@ -32,6 +32,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "greedy decode tok/s at b=1 (36-layer 4B-class); HBM GB/s vs 8 TB/s peak"
 POSITIONS_PER_PASS = 256
+WORKLOAD_DESC = ("dense4b: 36 layers, H=2560, Hq=32, Hkv=8, D=128, I=9728, V=151936 tied; b=1; 512-token prompt "
+                 "(batched prompt pass on tensor-core GEMMs, untimed); 256 greedy decode positions (511..766) per "
+                 "pass through the CUDA-graph decode loop, EOS id 0 checked every 16 steps")
 
 
 def parse():
@@ -405,9 +408,7 @@ def run_gpu(args, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic (seeded Philox N(0,0.02) weights, uniform prompt tokens)",
         "config": {
-            "workload": "dense4b: 36 layers, H=2560, Hq=32, Hkv=8, D=128, I=9728, V=151936 tied; b=1; "
-                        "512-token prompt (batched prompt pass on tensor-core GEMMs, untimed); 256 greedy decode positions (511..766) "
-                        "per pass through the CUDA-graph decode loop, EOS id 0 checked every 16 steps",
+            "workload": WORKLOAD_DESC,
             "batch": B, "prompt_len": P, "decode_positions": [positions[0], positions[-1]] if positions else None,
             "accumulate": "fp32", "weights": "bf16", "kv_cache": "bf16", "activations": "fp32",
             "l2": "inputs larger than L2: every step streams 8.0 GB of weights (L2 129 MB)",
@@ -535,8 +536,9 @@ def main():
         line = {"metric": METRIC, "value": round(v, 5), "unit": "tok/s", "n_gpus": args.gpus, "steps": done,
                 "warmup": 0, "ms_per_step": round(el / done * 1e3, 1), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-                "config": {"workload": "dense4b (as the GPU arm), decode steps at positions 511.. over a "
-                                       "511-token N(0,1) cache prefix"},
+                "config": {"workload": WORKLOAD_DESC,
+                           "reference_sample": "the fp64 oracle's decode steps at positions 511.. over a 511-token "
+                                               "N(0,1) cache prefix (bounded sample of the same workload)"},
                 "cpu_baseline": {"value": round(v, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
                                  "sample": f"{done} full decode steps (36 layers + LM head) of the fp64 oracle, "
                                            f"single thread, {cpu_model()}"},
