@@ -50,6 +50,23 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (the whole job's time) of the timed region."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def dist_setup(n):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -358,19 +375,14 @@ def run_gpu(args, world, rank, local):
             positions += list(range(int(pos0[0]), int(pos0[0]) + n))
         torch.cuda.synchronize(dev)
     ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(passes)))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        dist.barrier()
+    ms = max_over_ranks(ms, world, dev)
     tokens_out = out.cpu().numpy()
     assert gd.device_error(clear=True) == 0
 
     w_bytes, kv_bytes = bytes_per_step(m, positions, B)
     step_bytes = w_bytes + kv_bytes / max(1, len(positions))
     ms_per_step = ms / executed
-    tok_s = executed * B * world / (ms / 1e3)
+    tok_s = job_rate(executed * B, world, ms)
 
     # dominant kernel: the persistent step kernel (one launch is one whole
     # step); its average launch time is the timed region over the steps run,
