@@ -524,8 +524,13 @@ bool step_phase_plan(int K, int n_units, int RU, int BT, int sms, StepPlan* out,
   while (p < kConsumerWarps && (C + p - 1) / p > 32 * kXregIt) p *= 2;
   if ((C + p - 1) / p > 32 * kXregIt) return false;
   const int nslot = kConsumerWarps / p;
-  const int rps = std::min<int>(static_cast<int>(kStepSlotBytes / row_bytes), kXregRows * nslot);
-  if (rps < 1) return false;
+  const int rps_max = std::min<int>(static_cast<int>(kStepSlotBytes / row_bytes), kXregRows * nslot);
+  if (rps_max < 1) return false;
+  // the fewest rows per stage that keep the largest CTA's stage count, so
+  // that CTAs one unit short of it do not finish a stage earlier
+  const int upc_max = (n_units + sms - 1) / sms;
+  const int n_st = std::max(1, (upc_max + rps_max - 1) / rps_max);
+  const int rps = std::max(1, std::min(rps_max, (upc_max + n_st - 1) / n_st));
   out->parts = p;
   out->chunks_per_part = (C + p - 1) / p;
   out->rows_per_stage = rps;
