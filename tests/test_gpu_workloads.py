@@ -105,6 +105,46 @@ def test_dense4b_full_generation_is_deterministic_and_consistent(dense4b):
         assert int(st.token[0]) == toks[0, s]
 
 
+def test_dense4b_full_prompt_sampled_outputs_match_oracle(dense4b):
+    """The benchmark's exact configuration (512-token prompt through the
+    prompt pass, then graph-replayed decode steps), checked on the outputs
+    the oracle can compute one by one at full size: layer 0's K and V at
+    sampled prompt positions (they depend on that position's token alone),
+    and the LM head's greedy token at full vocabulary from the GPU's own
+    final residual after the first decode step."""
+    w, hm, model = dense4b
+    m = w.model
+    P = w.prompt_len
+    prompt_h = synth.make_tokens(w.seed, "prompt", (1, P), m.vocab)
+    st = _state(model, m, 1, P + 40)
+    gd.dec_prefill(model, st, dev_i32(prompt_h))
+    out = torch.empty((1, 16), dtype=torch.int32, device="cuda")
+    gd.dec_decode(model, st, 16, -1, out)
+    torch.cuda.synchronize()
+    K0 = st.k_cache[0][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    V0 = st.v_cache[0][0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    L0 = hm.layers[0]
+    D, Hkv = m.head_dim, m.n_kv_heads
+    for i in (0, 1, 137, 255, 400, P - 2):
+        x = synth.bf16_to_f64(hm.embed[int(prompt_h[0, i])])
+        _, y = oracle.rmsnorm(x, L0["attn_norm"], m.rms_eps)
+        k = oracle.rope(oracle.linear(L0["wk"], y).reshape(Hkv, D), i, m.rope_theta)
+        v = oracle.linear(L0["wv"], y).reshape(Hkv, D)
+        kg, vg = synth.bf16_to_f64(K0[:, i]), synth.bf16_to_f64(V0[:, i])
+        assert rel_err(kg, k) < TOL, i
+        assert rel_err(vg, v) < TOL, i
+    # the greedy token of the step that follows, from the GPU's final residual
+    st2 = _state(model, m, 1, P + 40)
+    gd.dec_prefill(model, st2, dev_i32(prompt_h))
+    gd.dec_step(model, st2)
+    torch.cuda.synchronize()
+    r = st2.residual[0].cpu().numpy().astype(np.float64)
+    t_ref, logits = oracle.head(r, hm.final_norm, hm.lm_head, m.rms_eps)
+    if oracle.top2_margin(logits) > MARGIN:
+        assert int(st2.token[0]) == t_ref
+    assert int(st2.token[0]) == int(out[0, 0])
+
+
 # ----------------------------------------------------------------------------- batched, ragged
 
 def _oracle_rows(args):
