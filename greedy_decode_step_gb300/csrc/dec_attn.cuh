@@ -286,7 +286,6 @@ __global__ void __launch_bounds__(288, 2) attn_kernel(const __grid_constant__ At
   unsigned char* ring = reinterpret_cast<unsigned char*>(s_s + kAttnMaxGroup * kAttnTile);
   constexpr uint32_t kRowBytes = D * 2;
   constexpr uint32_t kTileBytes = kAttnTile * kRowBytes;   // one of K or V
-  constexpr int kChunks = D / 8;
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv;
@@ -386,7 +385,6 @@ __global__ void __launch_bounds__(288, 2) attn_kernel(const __grid_constant__ At
   }
 
   // ------------------------------------------------------------- consumer warps
-  const int tid = threadIdx.x;  // 0..255
   constexpr int kMaxSlots = attn_slots<D>();
   float acc0[kMaxSlots], acc1[kMaxSlots];
 #pragma unroll
