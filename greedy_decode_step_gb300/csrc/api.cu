@@ -305,13 +305,15 @@ void fill_inv_freq(GemvArgs& a, int D, float theta) {
 
 // ------------------------------------------------------------------------------- attention planning
 
-// Key splits per (row, KV head): one wave of work items (one per SM) while
-// the cache is short, more splits once a split would cover over ~1024 keys on
-// average (long or batched caches, where balance matters more than latency).
+// Key splits per (row, KV head): up to one wave of work items (one per SM,
+// but no more splits than 64-key tiles in the cache: a split's time is
+// nearly that of its first tile, and fewer splits make the merge cheaper)
+// while the cache is short, more splits once a split would cover over ~1024
+// keys on average (long or batched caches, where balance matters more).
 int attn_splits(int B, int Hkv, int S_max, int sms, int requested, int waves = 1) {
   const int cap = std::max(1, (S_max + kAttnChunkMin - 1) / kAttnChunkMin);
   if (requested > 0) return std::min(requested, cap);
-  const int one_wave = std::max(1, waves * sms / (B * Hkv));
+  const int one_wave = std::max(1, std::min(waves * sms / (B * Hkv), (S_max + kAttnTile - 1) / kAttnTile));
   const int by_len = static_cast<int>(static_cast<long long>(S_max) * B * Hkv / (static_cast<long long>(sms) * 1024)) + 1;
   return std::max(1, std::min(std::max(one_wave, by_len), cap));
 }
