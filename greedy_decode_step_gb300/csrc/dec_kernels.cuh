@@ -318,8 +318,9 @@ __device__ __forceinline__ void drain_ring(const Ring& R, int sg_issued) {
   }
 }
 
-// Consumer wait for stage sg: lane 0 polls (bounded), the verdict is
-// warp-uniform, then every lane acquires the completed phase.
+// Consumer wait for the stage in `slot` (phase `parity`): one warp-wide test
+// when it has landed (the common case); otherwise lane 0 polls (bounded),
+// the verdict is made warp-uniform and every lane acquires the phase.
 __device__ __forceinline__ bool consumer_wait_at(const Ring& R, int slot, uint32_t parity) {
   // common case: the stage is there -- one test by the whole warp
   if (__all_sync(0xffffffffu, mbar_test_wait(&R.full[slot], parity))) return true;
