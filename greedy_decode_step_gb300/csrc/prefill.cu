@@ -52,9 +52,19 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t* hi, uint16_t* lo) 
 __global__ void prefill_norm_kernel(const float* r, const uint16_t* gamma, float eps, int H, uint16_t* y,
                                     uint16_t* y_lo) {
   __shared__ float red[8];
+  constexpr int kKeep = 16;  // values per thread kept in registers between the two passes
   const float* x = r + static_cast<size_t>(blockIdx.x) * H;
+  float v[kKeep], g[kKeep];
+#pragma unroll
+  for (int i = 0; i < kKeep; ++i) {
+    const int k = threadIdx.x + i * 256;
+    v[i] = k < H ? x[k] : 0.f;
+    g[i] = k < H ? __uint_as_float(static_cast<uint32_t>(gamma[k]) << 16) : 0.f;
+  }
   float ss = 0.f;
-  for (int k = threadIdx.x; k < H; k += 256) ss = fmaf(x[k], x[k], ss);
+#pragma unroll
+  for (int i = 0; i < kKeep; ++i) ss = fmaf(v[i], v[i], ss);
+  for (int k = threadIdx.x + kKeep * 256; k < H; k += 256) ss = fmaf(x[k], x[k], ss);
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
@@ -64,7 +74,12 @@ __global__ void prefill_norm_kernel(const float* r, const uint16_t* gamma, float
   const float inv = 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
   uint16_t* out = y + static_cast<size_t>(blockIdx.x) * H;
   uint16_t* out_lo = y_lo + static_cast<size_t>(blockIdx.x) * H;
-  for (int k = threadIdx.x; k < H; k += 256)
+#pragma unroll
+  for (int i = 0; i < kKeep; ++i) {
+    const int k = threadIdx.x + i * 256;
+    if (k < H) split_bf16((v[i] * inv) * g[i], &out[k], &out_lo[k]);
+  }
+  for (int k = threadIdx.x + kKeep * 256; k < H; k += 256)
     split_bf16((x[k] * inv) * __uint_as_float(static_cast<uint32_t>(gamma[k]) << 16), &out[k], &out_lo[k]);
 }
 
@@ -94,10 +109,14 @@ __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
   const int width = (a.Hq + 2 * a.Hkv) * a.D;
   const float* x = a.qkv + static_cast<size_t>(row) * width;
   const float* x2 = a.half_rows ? x + static_cast<size_t>(a.half_rows) * width : nullptr;
+  // the row's angles once (double-precision reduction), then every head
+  __shared__ float cs_s[64], sn_s[64];
+  for (int j = threadIdx.x; j < half; j += blockDim.x) rope_cos_sin(p, a.inv_freq[j], &cs_s[j], &sn_s[j]);
+  __syncthreads();
   for (int t = threadIdx.x; t < (a.Hq + a.Hkv) * half; t += blockDim.x) {
     const int hh = t / half, j = t - hh * half;
-    float cs, sn, l2, h2;
-    rope_cos_sin(p, a.inv_freq[j], &cs, &sn);
+    const float cs = cs_s[j], sn = sn_s[j];
+    float l2, h2;
     const int e = hh * a.D + j;
     const float lo = x2 ? x[e] + x2[e] : x[e];
     const float hi = x2 ? x[e + half] + x2[e + half] : x[e + half];
