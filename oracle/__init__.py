@@ -66,6 +66,7 @@ def lib():
             "orc_layer": (None, [ctypes.POINTER(Dims)] + [_P] * 11 + [_I, _P, ctypes.POINTER(Taps)]),
             "orc_head": (_I, [_P, _P, _P, _I, _I, _D, _P]),
             "orc_step": (_I, [ctypes.POINTER(Dims), _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P]),
+            "orc_select": (_I, [_P, _I, _P, _I, _D, _D, _I, _D, _D, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -262,6 +263,25 @@ class Model:
                              self.lm_head.ctypes.data if has_head else None, m.vocab,
                              _ptr(logits), r_out.ctypes.data)
         return int(tok), logits, r_out
+
+
+# ----------------------------------------------------------------------------- token selection
+
+def select_token(logits, prev=None, penalty: float = 1.0, temperature: float = 0.0, top_k: int = 0,
+                 top_p: float = 1.0, u: float = 0.0):
+    """Token chosen from one float32 logits row (repetition penalty, temperature,
+    top-k, top-p, then the draw ``u`` in [0, 1)); ``temperature == 0`` is greedy.
+
+    Returns ``(token, margin_p, margin_u)``: the relative distances of the
+    top-p cut and of ``u * M`` from the nearest cumulative boundary.
+    """
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    assert z.ndim == 1
+    pv = np.ascontiguousarray(prev if prev is not None else np.zeros(0), dtype=np.int32)
+    mg = np.empty(2)
+    t = lib().orc_select(z.ctypes.data, z.size, pv.ctypes.data if pv.size else None, pv.size, float(penalty),
+                         float(temperature), int(top_k), float(top_p), float(u), mg.ctypes.data)
+    return int(t), float(mg[0]), float(mg[1])
 
 
 def top2_margin(logits) -> float:

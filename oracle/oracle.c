@@ -322,3 +322,145 @@ int64_t orc_step(const orc_dims* d, int64_t L, const bf16_t* const* layer_w, bf1
   free(r);
   return tok;
 }
+
+/* ---------------------------------------------------------------- token selection */
+
+typedef struct {
+  float z;
+  int64_t i;
+} orc_zi;
+
+/* Larger logit first; equal logits in index order. */
+static int by_logit_desc(const void* a, const void* b) {
+  const orc_zi* x = (const orc_zi*)a;
+  const orc_zi* y = (const orc_zi*)b;
+  if (x->z > y->z) return -1;
+  if (x->z < y->z) return 1;
+  return (x->i > y->i) - (x->i < y->i);
+}
+
+/*
+ * Token selection from one row of float32 logits: the sampled counterpart of
+ * the greedy argmax.  The rollout engine's sampling path (the "do_sample /
+ * temperature / top_p" arguments of its generate fallback; the repetition
+ * penalty applied before the token selector, token selection run after the
+ * captured step) leaves the definitions to Hugging Face generate's logits
+ * processors, which are taken here as written in their documentation:
+ *   1. repetition penalty theta on each id in prev[0 .. n_prev): a negative
+ *      logit is multiplied by theta, any other divided by it; an id listed
+ *      twice counts once; ids outside [0, V) are ignored.  The penalised logit
+ *      is rounded to float32, the precision the tokens are ordered in.
+ *   2. temperature == 0: greedy, the smallest index attaining the maximum.
+ *   3. weights w_v = exp((z_v - z_max) / temperature).
+ *   4. top-k (0 < top_k < V): v survives iff fewer than top_k tokens have a
+ *      strictly larger logit (every token tied at the cut survives).
+ *   5. top-p (top_p < 1): a survivor v stays iff the weight of the survivors
+ *      with a strictly larger logit is below top_p times the survivors' total.
+ *   6. the draw: with M the weight of the kept set, the token is the first kept
+ *      v in index order whose running kept weight exceeds u * M.
+ * margins (may be NULL) gets two relative distances: [0] from top_p * Z to the
+ * nearest cumulative weight at a logit boundary (Z the survivors' total;
+ * infinity without top-p), [1] from u * M to the chosen token's cumulative
+ * bounds (infinity for greedy).
+ */
+int64_t orc_select(const float* logits, int64_t V, const int32_t* prev, int64_t n_prev, double penalty,
+                   double temperature, int64_t top_k, double top_p, double u, double* margins) {
+  float* z = (float*)malloc(sizeof(float) * (size_t)V);
+  unsigned char* seen = (unsigned char*)calloc((size_t)V, 1);
+  for (int64_t i = 0; i < n_prev; ++i)
+    if (prev[i] >= 0 && prev[i] < V) seen[prev[i]] = 1;
+  for (int64_t v = 0; v < V; ++v) {
+    double d = (double)logits[v];
+    z[v] = seen[v] ? (float)(d < 0.0 ? d * penalty : d / penalty) : logits[v];
+  }
+  free(seen);
+  if (margins) margins[0] = margins[1] = INFINITY;
+  if (temperature == 0.0) {
+    int64_t best = 0;
+    for (int64_t v = 1; v < V; ++v)
+      if (z[v] > z[best]) best = v;
+    free(z);
+    return best;
+  }
+
+  orc_zi* order = (orc_zi*)malloc(sizeof(orc_zi) * (size_t)V);
+  for (int64_t v = 0; v < V; ++v) {
+    order[v].z = z[v];
+    order[v].i = v;
+  }
+  qsort(order, (size_t)V, sizeof(orc_zi), by_logit_desc);
+  double zmax = (double)order[0].z;
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  unsigned char* keep = (unsigned char*)malloc((size_t)V);
+  for (int64_t v = 0; v < V; ++v) {
+    w[v] = exp(((double)z[v] - zmax) / temperature);
+    keep[v] = 1;
+  }
+
+  /* top-k: walk the groups of equal logits from the largest down. */
+  if (top_k > 0 && top_k < V) {
+    for (int64_t s = 0; s < V;) {
+      int64_t e = s;
+      while (e < V && order[e].z == order[s].z) ++e;
+      if (s >= top_k)
+        for (int64_t j = s; j < e; ++j) keep[order[j].i] = 0;
+      s = e;
+    }
+  }
+
+  /* top-p over the survivors, group by group. */
+  if (top_p < 1.0) {
+    double Z = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+      if (keep[v]) Z += w[v];
+    double target = top_p * Z;
+    double before = 0.0;
+    double margin = INFINITY;
+    for (int64_t s = 0; s < V;) {
+      int64_t e = s;
+      while (e < V && order[e].z == order[s].z) ++e;
+      if (keep[order[s].i]) {
+        double g = 0.0;
+        for (int64_t j = s; j < e; ++j) g += w[order[j].i];
+        if (before < target) {
+          double a = target - before, b = before + g - target;
+          margin = (a < b ? a : b) / Z;
+        } else {
+          for (int64_t j = s; j < e; ++j) keep[order[j].i] = 0;
+        }
+        before += g;
+      }
+      s = e;
+    }
+    if (margins) margins[0] = margin;
+  }
+
+  double M = 0.0;
+  for (int64_t v = 0; v < V; ++v)
+    if (keep[v]) M += w[v];
+  double target = u * M;
+  double cum = 0.0;
+  int64_t tok = -1, last = 0;
+  for (int64_t v = 0; v < V; ++v) {
+    if (!keep[v]) continue;
+    if (w[v] > 0.0) last = v;
+    if (cum + w[v] > target) {
+      tok = v;
+      if (margins) {
+        double a = target - cum, b = cum + w[v] - target;
+        margins[1] = (a < b ? a : b) / M;
+      }
+      break;
+    }
+    cum += w[v];
+  }
+  if (tok < 0) {
+    tok = last;
+    if (margins) margins[1] = 0.0;
+  }
+  free(order);
+  free(w);
+  free(keep);
+  free(z);
+  return tok;
+}
