@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gemv", choices=["gemv", "reference"])
-    ap.add_argument("--workload", default="dense4b", choices=["dense4b", "layer4b", "dense4b_b8", "gqa12x3_b16"])
+    ap.add_argument("--workload", default="dense4b",
+                    choices=["dense4b", "layer4b", "dense4b_b8", "gqa12x3_b16", "select_b16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--prompt", type=int, default=None, help="prompt length (default: the workload's 512)")
@@ -299,6 +300,84 @@ def run_batched(args, world, rank, local):
                       "step_hbm_frac_of_measured": round(gbs / peak, 4),
                       "path": "weight GEMMs on tensor cores (cuBLAS, hi/lo bf16 activations), split-K attention"},
            "gpu_launches": gd.dec_step_launches(model, st) * n + 2, "clocks": clk.summary()}
+    return res, None
+
+
+def run_select(args, world, rank, local):
+    """Token selection (not the headline): dec_select_tokens on b=16 rows of
+    V=151936 float32 logits (synth draws, std 4) with a repetition penalty
+    over 512 listed ids per row, temperature 0.7, top-k 50 and top-p 0.9, so
+    that every phase of the kernel runs.  L2 is flushed (a 256 MB write)
+    before every timed call; each call is timed by its own CUDA events."""
+    import torch
+    import greedy_decode_step_gb300 as gd
+    import oracle
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, V, n_prev = 16, 151936, 512
+    kw = dict(repetition_penalty=1.1, temperature=0.7, top_k=50, top_p=0.9)
+    z = synth.make_logits(0, "bench.select", B, V, 4.0, True)
+    u = synth.make_uniforms(0, "bench.select.u", B)
+    prev = synth.uniform_int(0, "bench.select.prev", (B, n_prev), 0, V - 1)
+    zd, ud, pd = (torch.from_numpy(x).to(dev) for x in (z, u, prev))
+    out = torch.empty(B, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        gd.dec_select_tokens(zd, out, u=ud, prev_tokens=pd, **kw)
+    torch.cuda.synchronize(dev)
+    steps = max(1, min(args.steps, 200))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(local) as clk:
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            gd.dec_select_tokens(zd, out, u=ud, prev_tokens=pd, **kw)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+    assert gd.device_error(clear=True) == 0
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    # end to end from pinned host buffers: logits, draws and ids in, tokens out
+    zh, uh, ph = (torch.from_numpy(x).pin_memory() for x in (z, u, prev))
+    oh = torch.empty(B, dtype=torch.int32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        zd.copy_(zh, non_blocking=True)
+        ud.copy_(uh, non_blocking=True)
+        pd.copy_(ph, non_blocking=True)
+        gd.dec_select_tokens(zd, out, u=ud, prev_tokens=pd, **kw)
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / steps
+    algo = B * V * 4 + B * n_prev * 4 + B * 4 + B * 4
+    peak, src = peaks()
+    gbs = algo / (ms / 1e3) / 1e9
+    t0 = time.perf_counter()
+    ref = [oracle.select_token(z[b], prev=prev[b], penalty=float(np.float32(1.1)), temperature=float(np.float32(0.7)),
+                               top_k=50, top_p=float(np.float32(0.9)), u=float(u[b]))[0] for b in range(B)]
+    cpu_ms = (time.perf_counter() - t0) * 1e3
+    agree = int(sum(int(a == b) for a, b in zip(out.cpu().tolist(), ref)))
+    res = {"metric": "token selection us per call (b=16, V=151936; penalty, temperature, top-k 50, top-p 0.9)",
+           "value": round(ms * 1e3, 2), "unit": "us/call", "n_gpus": 1, "steps": steps,
+           "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": False,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (synth logits, std 4)",
+           "config": {"workload": "select_b16: 16 rows x 151936 fp32 logits, 512 penalised ids per row, T=0.7, "
+                                  "top_k=50, top_p=0.9; L2 flushed before each call",
+                      "tokens_equal_to_oracle": f"{agree}/{B}"},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "traffic": None, "peak_source": src,
+                        "note": "one cluster of 8 CTAs per row; 34 cluster-barrier rounds bound the call, "
+                                "not DRAM"},
+           "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "us/call", "h2d_bytes_per_step": int(algo - B * 4),
+                   "d2h_bytes_per_step": B * 4},
+           "cpu_baseline": {"value": round(cpu_ms * 1e3, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+                            "sample": f"the fp64 oracle's selection of the same {B} rows, single thread, "
+                                      f"{cpu_model()}"},
+           "gpu_launches": steps, "clocks": clk.summary()}
     return res, None
 
 
@@ -567,6 +646,8 @@ def main():
         res, host = run_layer(args, world, rank, local)
     elif args.workload in ("dense4b_b8", "gqa12x3_b16"):
         res, host = run_batched(args, world, rank, local)
+    elif args.workload == "select_b16":
+        res, host = run_select(args, world, rank, local)
     else:
         res, host = run_gpu(args, world, rank, local)
     if rank == 0 and host is not None and not args.no_cpu_baseline:

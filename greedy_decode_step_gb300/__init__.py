@@ -66,6 +66,7 @@ _SIGNATURES = {
     "dec_down_gemv": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "dec_lmhead_workspace_size": (_S, [_I]),
     "dec_lmhead_argmax": (_I, [_P, _P, _F, _P, _P, _P, _P, _S, _I, _I, _I, _P]),
+    "dec_select_tokens": (_I, [_P, _P, _I, _F, _F, _I, _F, _P, _P, _I, _I, _P]),
     "dec_state_workspace_size": (_S, [ctypes.POINTER(DecModel), _I, _I]),
     "dec_state_init": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P]),
     "dec_state_release": (_I, [ctypes.POINTER(DecState)]),
@@ -205,6 +206,18 @@ def dec_lmhead_argmax(residual, final_norm, eps: float, W_lm, token_out, logits_
                                    _ptr(W_lm, _bf16, "W_lm"), _ptr(token_out, _i32, "token_out"),
                                    _ptr(logits_out, _f32, "logits_out"), _ptr(ws, None, "ws"),
                                    ws.numel() * ws.element_size(), B, H, V, _stream(stream)))
+
+
+def dec_select_tokens(logits, token_out, u=None, prev_tokens=None, repetition_penalty: float = 1.0,
+                      temperature: float = 0.0, top_k: int = 0, top_p: float = 1.0, stream=None):
+    """Token per row of fp32 ``logits`` [B, V]: repetition penalty over ``prev_tokens``
+    (int32 [B, n_prev]), then greedy (``temperature == 0``) or a draw by ``u``
+    (fp32 [B] in [0, 1)) from the top-k / top-p filtered softmax."""
+    B, V = logits.shape
+    n_prev = 0 if prev_tokens is None else prev_tokens.shape[1]
+    _check(lib().dec_select_tokens(_ptr(logits, _f32, "logits"), _ptr(prev_tokens, _i32, "prev_tokens"), n_prev,
+                                   repetition_penalty, temperature, top_k, top_p, _ptr(u, _f32, "u"),
+                                   _ptr(token_out, _i32, "token_out"), B, V, _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- model / state

@@ -13,7 +13,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdec.so")
-UNITS = ["api.cu", "gemv_qkv.cu", "gemv_glu.cu", "gemv_resid.cu", "gemv_head.cu", "attn.cu", "step.cu", "prefill.cu"]
+UNITS = ["api.cu", "gemv_qkv.cu", "gemv_glu.cu", "gemv_resid.cu", "gemv_head.cu", "attn.cu", "step.cu", "prefill.cu",
+         "select.cu"]
 HEADERS = ["dec_common.cuh", "dec_kernels.cuh", "dec_attn.cuh", "dec_step.cuh", "dec_launch.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -158,6 +158,7 @@ int device_info(DeviceInfo** out) {
     DEC_CUDA(allow_smem_head());
     DEC_CUDA(allow_smem_attn());
     DEC_CUDA(allow_smem_step());
+    DEC_CUDA(allow_smem_select());
     DEC_CUDA(prefer_max_carveout(add_rmsnorm_kernel));
     DEC_CUDA(prefer_max_carveout(advance_kernel));
     DEC_CUDA(prefer_max_carveout(set_tokens_kernel));
@@ -1156,6 +1157,43 @@ int dec_lmhead_argmax(const float* residual, const void* final_norm, float eps, 
   a.io.ticket = reinterpret_cast<unsigned int*>(base + 256);
   a.io.token_out = token_out;
   return run_gemv(kKindHead, a, B, dv, true, st, false);
+}
+
+int dec_select_tokens(const float* logits, const int32_t* prev_tokens, int n_prev, float repetition_penalty,
+                      float temperature, int top_k, float top_p, const float* u, int32_t* token_out, int B, int V,
+                      void* stream) {
+  DEC_CHECK(B >= 1 && B <= kSelectMaxBatch, DEC_EUNSUPPORTED, "batch %d outside 1..%d", B, kSelectMaxBatch);
+  DEC_TRY(check_row(V, "V"));
+  DEC_PTR(logits);
+  DEC_CHECK(token_out != nullptr, DEC_EINVAL, "token_out is NULL");
+  DEC_CHECK(n_prev >= 0, DEC_EINVAL, "n_prev must be >= 0");
+  DEC_CHECK(n_prev == 0 || prev_tokens != nullptr, DEC_EINVAL, "prev_tokens is NULL with n_prev = %d", n_prev);
+  DEC_CHECK(repetition_penalty > 0.f && std::isfinite(repetition_penalty), DEC_EINVAL,
+            "repetition_penalty must be finite and > 0");
+  DEC_CHECK(temperature >= 0.f && std::isfinite(temperature), DEC_EINVAL, "temperature must be finite and >= 0");
+  DEC_CHECK(top_k >= 0, DEC_EINVAL, "top_k must be >= 0");
+  DEC_CHECK(top_p > 0.f && top_p <= 1.f, DEC_EINVAL, "top_p must lie in (0, 1]");
+  DEC_CHECK(temperature == 0.f || u != nullptr, DEC_EINVAL, "u is NULL with temperature > 0");
+  DEC_CHECK(select_smem_bytes(V) <= select_smem_limit(), DEC_EUNSUPPORTED,
+            "V = %d needs %u bytes of shared memory per CTA (limit %u)", V, select_smem_bytes(V),
+            select_smem_limit());
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  DEC_CHECK(select_max_active_clusters(V) >= 1, DEC_EUNSUPPORTED, "a cluster of 8 CTAs does not fit for V = %d", V);
+  SelectArgs a{};
+  a.logits = logits;
+  a.prev = prev_tokens;
+  a.u = u;
+  a.token_out = token_out;
+  a.V = V;
+  a.chunk = static_cast<int>(select_chunk(V));
+  a.n_prev = n_prev;
+  a.top_k = top_k;
+  a.penalty = repetition_penalty;
+  a.temperature = temperature;
+  a.top_p = top_p;
+  DEC_CUDA(launch_select(a, B, static_cast<cudaStream_t>(stream)));
+  return DEC_OK;
 }
 
 size_t dec_state_workspace_size(const dec_model* m, int B, int S_max) {

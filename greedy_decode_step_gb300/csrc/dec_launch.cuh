@@ -85,4 +85,21 @@ cudaError_t allow_smem_step();
 // One persistent whole-step launch (cooperative: all CTAs resident).
 cudaError_t launch_step(int BT, const StepArgs& a, int grid, uint32_t smem, cudaStream_t st);
 
+// Token selection (select.cu): one cluster of 8 CTAs per row of logits.
+constexpr int kSelectMaxBatch = 4096;
+struct SelectArgs {
+  const float* logits;    // [B][V]
+  const int32_t* prev;    // [B][n_prev] ids for the repetition penalty
+  const float* u;         // [B] uniform draws
+  int32_t* token_out;     // [B]
+  int V, chunk, n_prev, top_k;
+  float penalty, temperature, top_p;
+};
+uint32_t select_chunk(int V);            // logits per CTA
+uint32_t select_smem_bytes(int V);       // dynamic shared memory per CTA
+uint32_t select_smem_limit();            // the most dynamic shared memory a CTA may take
+cudaError_t allow_smem_select();
+int select_max_active_clusters(int V);   // 0: the cluster does not fit this device
+cudaError_t launch_select(const SelectArgs& a, int B, cudaStream_t st);
+
 }  // namespace dec

@@ -163,6 +163,37 @@ size_t dec_lmhead_workspace_size(int B);
 int dec_lmhead_argmax(const float* residual, const void* final_norm, float eps, const void* W_lm, int32_t* token_out,
                       float* logits_out, void* ws, size_t ws_bytes, int B, int H, int V, void* stream);
 
+/*
+ * Token selection from logits: the sampled counterpart of the greedy choice.
+ * The rollout engine of the segment-KI pull request samples with do_sample /
+ * temperature / top_p after the captured step and applies a repetition
+ * penalty before its token selector; the definitions are those of Hugging
+ * Face generate's logits processors.  For each row b < B, with z = logits[b]:
+ *   1. every id of prev_tokens[b][0 .. n_prev) inside [0, V) (an id listed
+ *      twice counts once): z_v <- z_v * penalty if z_v < 0, else z_v / penalty,
+ *      rounded to float32;
+ *   2. temperature == 0: token_out[b] = smallest v with z_v maximal (top_k,
+ *      top_p and u are then unused);
+ *   3. w_v = exp((z_v - max z) / temperature);
+ *   4. top_k > 0: v survives iff fewer than top_k tokens have a strictly
+ *      larger z (every token tied at the cut survives); top_k = 0 or >= V: all;
+ *   5. top_p < 1: a survivor v is kept iff the survivors with a strictly
+ *      larger z weigh less than top_p times the survivors' total weight;
+ *   6. token_out[b] = the first kept v in index order whose running kept
+ *      weight exceeds u[b] * M, M the kept weight (u[b] is clamped to [0, 1)).
+ * logits fp32 [B][V] (e.g. the logits_out of dec_lmhead_argmax), read only;
+ * prev_tokens int32 [B][n_prev] (NULL when n_prev == 0); u fp32 [B], the
+ * caller's uniform draws (NULL allowed when temperature == 0); token_out
+ * int32 [B].  repetition_penalty > 0 (1: none); temperature >= 0; top_k >= 0;
+ * top_p in (0, 1].  B is 1..4096 here; V a multiple of 8 up to about 220,000
+ * (one eighth of a row fits one SM's shared memory).  The kernel orders
+ * tokens by their float32 logits exactly and sums weights in a fixed order,
+ * so a row's token is reproducible; logits must be finite or -infinity.
+ */
+int dec_select_tokens(const float* logits, const int32_t* prev_tokens, int n_prev, float repetition_penalty,
+                      float temperature, int top_k, float top_p, const float* u, int32_t* token_out, int B, int V,
+                      void* stream);
+
 /* ------------------------------------------------------------------ whole step */
 
 typedef struct dec_layer_weights {

@@ -229,3 +229,18 @@ def make_residual(seed: int, batch: int, hidden: int) -> np.ndarray:
 
 def make_tokens(seed: int, name: str, shape, vocab: int) -> np.ndarray:
     return uniform_int(seed, name, shape, 0, vocab - 1)
+
+
+def make_logits(seed: int, name: str, batch: int, vocab: int, std: float = 1.0, fine: bool = True) -> np.ndarray:
+    """float32 logits [batch, vocab]: a bf16 draw of std * N(0,1) plus, with
+    ``fine``, a second bf16 draw of std/256 * N(0,1), so that values rarely tie
+    (without it, bf16-valued logits tie in large groups)."""
+    a = bf16_to_f32(normal_bf16(seed, name, (batch, vocab), 0.0, std))
+    if fine:
+        a = a + bf16_to_f32(normal_bf16(seed, name + ".fine", (batch, vocab), 0.0, std / 256.0))
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def make_uniforms(seed: int, name: str, n: int) -> np.ndarray:
+    """float32 draws k / 2^24 on [0, 1), k uniform integers."""
+    return (uniform_int(seed, name, (n,), 0, (1 << 24) - 1).astype(np.float64) / float(1 << 24)).astype(np.float32)

@@ -91,3 +91,32 @@ def test_missing_library_fails_loudly(monkeypatch, gd):
     monkeypatch.setattr(gd, "LIB_PATH", "/nonexistent/libdec.so")
     with pytest.raises(RuntimeError, match="not built"):
         gd.lib()
+
+
+def test_token_selection_arguments_are_checked_on_the_host(gd):
+    p = 0x1000
+    rc, msg = _call(gd, "dec_select_tokens", None, None, 0, 1.0, 0.0, 0, 1.0, None, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "logits" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.5, 0, 1.5, p, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "top_p" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.5, 0, 0.0, p, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "top_p" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 3, 1.0, 0.5, 0, 1.0, p, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "prev_tokens" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.5, 0, 1.0, None, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "u is NULL" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 0.0, 0.5, 0, 1.0, p, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "repetition_penalty" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, -1.0, 0, 1.0, p, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "temperature" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.5, -1, 1.0, p, p, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "top_k" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.5, 0, 1.0, p, p, 1, 1 << 19, None)
+    assert rc == gd.DEC_EUNSUPPORTED and "shared memory" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.5, 0, 1.0, p, p, 1, 1020, None)
+    assert rc == gd.DEC_EUNSUPPORTED and "multiple of 8" in msg
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.5, 0, 1.0, p, p, 0, 1024, None)
+    assert rc == gd.DEC_EUNSUPPORTED and "batch" in msg
+    # greedy needs no draws
+    rc, msg = _call(gd, "dec_select_tokens", p, None, 0, 1.0, 0.0, 0, 1.0, None, None, 1, 1024, None)
+    assert rc == gd.DEC_EINVAL and "token_out" in msg

@@ -1,0 +1,193 @@
+"""Token selection on the GPU (dec_select_tokens) against the fp64 oracle.
+
+Greedy choices, the order of tokens and the top-k cut are decided on float32
+logits on both sides, so they must agree exactly.  The top-p cut and the draw
+compare weights that the kernel sums in float32: a row must agree wherever
+the oracle's distance from each decision boundary (relative to the total
+weight) is at least AMBIG; nearer a boundary the GPU's token must be one that
+the oracle picks for a draw or a p within that distance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import dev_f32, dev_i32
+
+pytestmark = pytest.mark.gpu
+
+# Relative error bound of the kernel's weight sums: expf (a few ulp), the
+# float32 (z - max) / T, per-thread float32 partial sums of ~40 terms and a
+# warp butterfly -- under 1e-5 together; the bar keeps a margin above that.
+AMBIG = 2e-5
+VOCAB = 151936
+
+
+@pytest.fixture(scope="module")
+def gd():
+    import greedy_decode_step_gb300 as gd
+    gd.build()
+    return gd
+
+
+def run(gd, z, u=None, prev=None, **kw):
+    B = z.shape[0]
+    out = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    gd.dec_select_tokens(dev_f32(z), out, u=None if u is None else dev_f32(u),
+                         prev_tokens=None if prev is None else dev_i32(prev), **kw)
+    torch.cuda.synchronize()
+    assert gd.device_error(clear=True) == 0
+    return out.cpu().numpy()
+
+
+def oracle_rows(z, u, prev, penalty, temperature, top_k, top_p):
+    res = []
+    for b in range(z.shape[0]):
+        res.append(oracle.select_token(z[b], prev=None if prev is None else prev[b], penalty=penalty,
+                                       temperature=temperature, top_k=top_k, top_p=top_p,
+                                       u=0.0 if u is None else float(u[b])))
+    return res
+
+
+def nearby_tokens(zb, ub, prevb, penalty, temperature, top_k, top_p):
+    """Oracle tokens for draws and p within AMBIG of the given ones."""
+    out = set()
+    for du in (-AMBIG, 0.0, AMBIG):
+        for dp in (-AMBIG, 0.0, AMBIG):
+            uu = min(max(ub + du, 0.0), np.nextafter(1.0, 0.0))
+            pp = min(top_p + dp, 1.0) if top_p < 1.0 else 1.0
+            out.add(oracle.select_token(zb, prev=prevb, penalty=penalty, temperature=temperature, top_k=top_k,
+                                        top_p=pp, u=uu)[0])
+    return out
+
+
+def check_rows(got, z, u, prev, penalty, temperature, top_k, top_p, min_exact=0.5):
+    ref = oracle_rows(z, u, prev, penalty, temperature, top_k, top_p)
+    exact = 0
+    for b, (t, mp, mu) in enumerate(ref):
+        assert 0 <= got[b] < z.shape[1]
+        if min(mp, mu) >= AMBIG:
+            assert got[b] == t, f"row {b}: gpu {got[b]} oracle {t} (margins {mp:.2e}, {mu:.2e})"
+            exact += 1
+        else:
+            near = nearby_tokens(z[b], float(u[b]), None if prev is None else prev[b], penalty, temperature, top_k,
+                                 top_p)
+            assert got[b] in near, f"row {b}: gpu {got[b]} not among {sorted(near)} near a boundary"
+    assert exact >= min_exact * len(ref), f"only {exact} of {len(ref)} rows away from every boundary"
+
+
+# ----------------------------------------------------------------------------- greedy
+
+@pytest.mark.parametrize("V,fine,penalty", [(1024, True, 1.0), (VOCAB, True, 1.0), (VOCAB, False, 1.0),
+                                            (VOCAB, True, 1.3), (8, False, 1.3)])
+def test_greedy_is_bit_exact(gd, V, fine, penalty):
+    B = 4
+    z = synth.make_logits(11, f"sel.greedy.{V}", B, V, 2.0, fine)
+    prev = synth.uniform_int(11, f"sel.prev.{V}", (B, 64), -3, V + 3)
+    # make the penalty decide: list each row's current maximum
+    prev[:, 0] = np.argmax(z, axis=1)
+    got = run(gd, z, prev=prev, repetition_penalty=penalty)
+    for b in range(B):
+        assert got[b] == oracle.select_token(z[b], prev=prev[b], penalty=penalty)[0]
+
+
+def test_greedy_ties_take_the_lowest_index_across_cluster_slices(gd):
+    V = VOCAB
+    z = np.full((3, V), -5.0, dtype=np.float32)
+    z[0, [100_000, 20, 150_000]] = 3.0
+    z[1, [151_935, 151_934]] = 1.0
+    z[2, :] = -0.0
+    z[2, 77] = 0.0  # +0 and -0 tie: index 0 is the first maximum
+    got = run(gd, z)
+    assert list(got) == [20, 151_934, 0]
+
+
+# ----------------------------------------------------------------------------- sampling
+
+CASES = [
+    # V,     std, fine, T,   top_k, top_p, penalty, share of rows that must match exactly
+    (1024, 2.0, True, 1.0, 0, 1.0, 1.0, 0.5),
+    (1024, 2.0, True, 0.7, 50, 0.9, 1.2, 0.5),
+    # flat: each of the 151,936 tokens holds ~1e-5 of the weight, so every draw
+    # lies within AMBIG of a boundary; the rows are checked against their neighbours
+    (VOCAB, 1.0, True, 1.0, 0, 1.0, 1.0, 0.0),
+    (VOCAB, 4.0, True, 0.7, 0, 0.9, 1.0, 0.5),
+    (VOCAB, 4.0, True, 0.7, 50, 0.9, 1.1, 0.5),
+    (VOCAB, 3.0, False, 1.0, 40, 0.8, 1.0, 0.5),   # bf16-valued logits: large tie groups
+    (VOCAB, 6.0, True, 1.5, 0, 0.5, 1.0, 0.5),
+    (VOCAB, 2.0, True, 1.0, 1, 1.0, 1.0, 0.5),
+    (VOCAB, 8.0, True, 0.6, 0, 0.95, 1.3, 0.5),
+    (4104, 2.0, True, 1.0, 5000, 0.3, 1.0, 0.5),   # top_k >= V: no cut
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"V{c[0]}_T{c[3]}_k{c[4]}_p{c[5]}_pen{c[6]}_{'f' if c[2] else 'b'}"
+                                              for c in CASES])
+def test_sampling_matches_oracle(gd, case):
+    V, std, fine, T, K, P, pen, share = case
+    B = 6
+    tag = f"sel.{V}.{std}.{fine}.{T}.{K}.{P}.{pen}"
+    z = synth.make_logits(12, tag, B, V, std, fine)
+    u = synth.make_uniforms(12, tag + ".u", B)
+    prev = synth.uniform_int(12, tag + ".prev", (B, 256), 0, V - 1) if pen != 1.0 else None
+    got = run(gd, z, u=u, prev=prev, repetition_penalty=pen, temperature=T, top_k=K, top_p=P)
+    check_rows(got, z, u, prev, pen, T, K, float(np.float32(P)), min_exact=share)
+
+
+def test_many_draws_over_one_row(gd):
+    # one row repeated with a grid of draws: every inverse-CDF interval is hit
+    V, B = 64, 512
+    z1 = synth.make_logits(13, "sel.grid", 1, V, 1.5, True)
+    z = np.repeat(z1, B, axis=0)
+    u = ((np.arange(B) + 0.5) / B).astype(np.float32)
+    for K, P in ((0, 1.0), (10, 0.9), (0, 0.6)):
+        got = run(gd, z, u=u, temperature=0.8, top_k=K, top_p=P)
+        check_rows(got, z, u, None, 1.0, 0.8, K, float(np.float32(P)), min_exact=0.9)
+
+
+def test_draw_edges_and_masked_logits(gd):
+    V = 4104
+    z = synth.make_logits(14, "sel.edges", 4, V, 1.0, True)
+    z[2, :] = -np.inf
+    z[2, 4000] = 0.5          # one finite logit: always chosen
+    z[3, ::2] = -np.inf       # half the vocabulary masked
+    u = np.array([0.0, np.nextafter(np.float32(1), np.float32(0)), 0.3, 0.7], dtype=np.float32)
+    got = run(gd, z, u=u, temperature=1.0)
+    ref = oracle_rows(z, u, None, 1.0, 1.0, 0, 1.0)
+    assert got[0] == ref[0][0] == 0           # u = 0: the first token with weight
+    assert got[2] == 4000
+    assert got[3] % 2 == 1
+    check_rows(got, z, u, None, 1.0, 1.0, 0, 1.0)
+
+
+def test_small_vocabulary_uses_one_slice(gd):
+    z = np.array([[0.0, 1.0, 2.0, 3.0, -1.0, 0.5, 2.5, 1.5]] * 3, dtype=np.float32)
+    u = np.array([0.01, 0.5, 0.99], dtype=np.float32)
+    got = run(gd, z, u=u, temperature=1.0, top_k=3)
+    check_rows(got, z, u, None, 1.0, 1.0, 3, 1.0, min_exact=1.0)
+
+
+def test_selection_is_reproducible(gd):
+    B, V = 8, VOCAB
+    z = synth.make_logits(15, "sel.repro", B, V, 3.0, True)
+    u = synth.make_uniforms(15, "sel.repro.u", B)
+    kw = dict(temperature=0.9, top_k=100, top_p=0.9)
+    a = run(gd, z, u=u, **kw)
+    b = run(gd, z, u=u, **kw)
+    assert np.array_equal(a, b)
+
+
+def test_greedy_selection_of_lmhead_logits_equals_its_argmax(gd):
+    B, H, V = 3, 256, 1024
+    W = synth.normal_bf16(16, "sel.lm", (V, H), 0.0, 0.05)
+    g = synth.normal_bf16(16, "sel.gain", (H,), 1.0, 0.1)
+    r = synth.make_residual(16, B, H)
+    from helpers import dev_bf16
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    logits = torch.empty(B, V, dtype=torch.float32, device="cuda")
+    gd.dec_lmhead_argmax(dev_f32(r), dev_bf16(g), 1e-6, dev_bf16(W), tok, logits_out=logits)
+    out = torch.empty(B, dtype=torch.int32, device="cuda")
+    gd.dec_select_tokens(logits, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, tok)
