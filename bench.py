@@ -339,6 +339,16 @@ def run_select(args, world, rank, local):
         torch.cuda.synchronize(dev)
     assert gd.device_error(clear=True) == 0
     ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    # one row alone (one cluster): the latency of a row, without other clusters beside it
+    out1 = torch.empty(1, dtype=torch.int32, device=dev)
+    ev1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for e0, e1 in ev1:
+        flush.zero_()
+        e0.record(stream)
+        gd.dec_select_tokens(zd[:1], out1, u=ud[:1], prev_tokens=pd[:1], **kw)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms1 = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev1)
     # end to end from pinned host buffers: logits, draws and ids in, tokens out
     zh, uh, ph = (torch.from_numpy(x).pin_memory() for x in (z, u, prev))
     oh = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -367,11 +377,11 @@ def run_select(args, world, rank, local):
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (synth logits, std 4)",
            "config": {"workload": "select_b16: 16 rows x 151936 fp32 logits, 512 penalised ids per row, T=0.7, "
                                   "top_k=50, top_p=0.9; L2 flushed before each call",
-                      "tokens_equal_to_oracle": f"{agree}/{B}"},
+                      "tokens_equal_to_oracle": f"{agree}/{B}", "one_row_us": round(ms1 * 1e3, 2)},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(gbs / peak, 4), "traffic": None, "peak_source": src,
-                        "note": "one cluster of 8 CTAs per row; 34 cluster-barrier rounds bound the call, "
-                                "not DRAM"},
+                        "note": "one cluster of 8 CTAs per row; 34 cluster-barrier rounds, not DRAM, "
+                                "bound the call"},
            "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "us/call", "h2d_bytes_per_step": int(algo - B * 4),
                    "d2h_bytes_per_step": B * 4},
            "cpu_baseline": {"value": round(cpu_ms * 1e3, 1), "unit": "us/call", "cores": 1, "kind": "oracle",

@@ -14,15 +14,19 @@
 //   * the token is the first kept v (index order) whose running kept weight
 //     exceeds u * M, M the kept weight, u the caller's uniform draw.
 //
-// GB300 layout: one cluster of 8 CTAs per row.  Each CTA holds 1/8 of the
-// row in shared memory as (order key, weight) pairs, so the searches never go
-// back to L2.  Both cuts are thresholds on the 32-bit order key of the
-// penalised logit (a monotone map of the float), found by a most-significant
-// first search that settles 2 bits per round: every round each CTA counts (or
-// weighs) its keys against 3 candidates, the CTA totals meet through
-// distributed shared memory behind one cluster barrier, and every CTA takes
-// the same decision.  All sums run in a fixed order, so a row's result is
-// reproducible run to run.
+// GB300 layout: one cluster of 8 CTAs per row.  Each CTA keeps 1/8 of the
+// row in shared memory as 32-bit order keys of the penalised logits (a
+// monotone map of the float), so the searches never go back to L2.  Both cuts
+// are thresholds on that key, found by a most-significant-first search that
+// settles 2 bits per round: each CTA counts (or weighs) its keys against 3
+// candidates, the CTA totals meet through distributed shared memory behind
+// one cluster barrier, and every CTA takes the same decision.  A thread only
+// revisits its keys that still lie in the search range: keys below it leave,
+// keys above it are folded into one running total.  Weights are fixed point,
+// w * 2^40 in 64-bit integers (exact for w >= 2^-16, truncated below), so
+// every sum is exact and independent of order: the cuts, the kept weight and
+// the draw are reproducible, and the draw lands in exactly one token.  No
+// step uses double precision.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -40,15 +44,18 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelPhases = 40;  // 1 (max) + 16 (top-k) + 16 (top-p) + 1 (draw), rounded up
 constexpr int kSelVals = 4;     // values one CTA publishes per phase
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+using u64 = unsigned long long;
 
 struct SelShared {
-  double warp_part[kSelWarps][kSelVals];
-  double slot[kSelPhases][kSelVals];  // read by the other CTAs of the cluster
-  double bcast[kSelVals];
-  double cta_mass[kSelCluster];
-  unsigned long long warp_max[kSelWarps];
-  unsigned long long max_slot;
-  unsigned long long max_bcast;
+  u64 warp_part[kSelWarps][kSelVals];
+  u64 slot[kSelPhases][kSelVals];  // read by the other CTAs of the cluster
+  u64 bcast[kSelVals];
+  u64 cta_mass[kSelCluster];
+  u64 warp_max[kSelWarps];
+  u64 max_slot;
+  u64 max_bcast;
 };
 
 // Monotone map of a float to an unsigned key (larger float, larger key); -0
@@ -62,37 +69,81 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__device__ __forceinline__ float warp_sum_f(float v) {
+// w = exp((z - z_max) / T) as w * 2^40 truncated to an integer.
+__device__ __forceinline__ u64 weight_fixed(uint32_t key, float zmax, float T) {
+  const float w = expf(__fdiv_rn(__fsub_rn(key_value(key), zmax), T));
+  return __float2ull_rz(__fmul_rn(w, 1099511627776.0f));
+}
+
+// floor(f * X) (or the ceiling) for a float f in [0, 1] and X < 2^63, exact:
+// the 24-bit significand times X in 128 bits, shifted down.
+__device__ __forceinline__ u64 scale_fixed(float f, u64 X, bool round_up) {
+  const uint32_t b = __float_as_uint(f);
+  const int E = static_cast<int>((b >> 23) & 0xFFu);
+  if (E == 0) return 0ull;  // zero or subnormal
+  const u64 m = (b & 0x7FFFFFu) | 0x800000u;
+  const int s = 150 - E;    // f = m * 2^-s, s >= 23 for f <= 1
+  const u64 lo = m * X, hi = __umul64hi(m, X);
+  u64 q;
+  bool rem;
+  if (s >= 128) {
+    q = 0ull;
+    rem = (lo | hi) != 0ull;
+  } else if (s >= 64) {
+    const int r = s - 64;
+    q = r == 0 ? hi : (hi >> r);
+    rem = lo != 0ull || (r != 0 && (hi & ((1ull << r) - 1ull)) != 0ull);
+  } else {
+    q = (hi << (64 - s)) | (lo >> s);
+    rem = (lo & ((1ull << s) - 1ull)) != 0ull;
+  }
+  return (round_up && rem) ? q + 1ull : q;
+}
+
+__device__ __forceinline__ u64 warp_sum(u64 v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ u64 warp_max(u64 v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const u64 w = __shfl_xor_sync(kFull, v, o);
+    v = w > v ? w : v;
+  }
   return v;
 }
 
 // Cluster totals of kSelVals values whose per-warp parts lane 0 of every warp
-// has written to warp_part: CTA sums in warp order, cluster sums in rank
-// order, all in double.  Every thread of the cluster returns the same totals.
-// The phase's slot is written once and never reused, so one cluster barrier
-// orders the exchange.
-__device__ void cluster_totals(SelShared& sh, cg::cluster_group& cl, int phase, double* out) {
+// has written to warp_part.  Warp 0 adds the 16 warp parts, publishes the CTA
+// total in this phase's slot, and after the cluster barrier its lanes 0..7
+// read the 8 CTAs' slots side by side.  Every thread of the cluster returns
+// the same totals.  A phase's slot is written once and never reused, so one
+// cluster barrier orders the exchange.
+__device__ void cluster_totals(SelShared& sh, cg::cluster_group& cl, int phase, u64* out) {
+  const int tid = threadIdx.x;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (tid < 32) {
 #pragma unroll
     for (int j = 0; j < kSelVals; ++j) {
-      double s = 0.0;
-      for (int w = 0; w < kSelWarps; ++w) s += sh.warp_part[w][j];
-      sh.slot[phase][j] = s;
+      const u64 v = warp_sum(tid < kSelWarps ? sh.warp_part[tid][j] : 0ull);
+      if (tid == 0) sh.slot[phase][j] = v;
     }
   }
   cl.sync();
-  if (threadIdx.x == 0) {
-    double t[kSelVals] = {0.0, 0.0, 0.0, 0.0};
-    for (int r = 0; r < kSelCluster; ++r) {
-      const double* rs = cl.map_shared_rank(&sh.slot[phase][0], r);
+  if (tid < 32) {
+    u64 r[kSelVals] = {0ull, 0ull, 0ull, 0ull};
+    if (tid < kSelCluster) {
+      const u64* rs = cl.map_shared_rank(&sh.slot[phase][0], tid);
 #pragma unroll
-      for (int j = 0; j < kSelVals; ++j) t[j] += rs[j];
+      for (int j = 0; j < kSelVals; ++j) r[j] = rs[j];
     }
 #pragma unroll
-    for (int j = 0; j < kSelVals; ++j) sh.bcast[j] = t[j];
+    for (int j = 0; j < kSelVals; ++j) {
+      const u64 v = warp_sum(r[j]);
+      if (tid == 0) sh.bcast[j] = v;
+    }
   }
   __syncthreads();
 #pragma unroll
@@ -109,9 +160,10 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int lo = rank * a.chunk;
   const int n = max(0, min(a.chunk, a.V - lo));
+  const int cap = (a.chunk + kSelThreads - 1) / kSelThreads;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  float* wts = reinterpret_cast<float*>(smem + static_cast<size_t>(a.chunk) * 4);
-  uint32_t* seen = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(a.chunk) * 8);
+  uint32_t* seen = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(a.chunk) * 4);
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(a.chunk) * 4 + a.chunk / 8) + tid * cap;
   const int seen_words = a.chunk / 32;
   int phase = 0;
 
@@ -129,7 +181,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   }
 
   // ---- phase 0: keys of the penalised logits and the row maximum (smallest index on ties)
-  unsigned long long best = 0ull;
+  u64 best = 0ull;
   {
     const float4* src = reinterpret_cast<const float4*>(a.logits + static_cast<size_t>(row) * a.V + lo);
     for (int i4 = tid; i4 < n / 4; i4 += kSelThreads) {
@@ -143,31 +195,21 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
           z = z < 0.f ? __fmul_rn(z, a.penalty) : __fdiv_rn(z, a.penalty);
         const uint32_t k = order_key(z);
         keys[i] = k;
-        const unsigned long long packed =
-            (static_cast<unsigned long long>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(lo + i));
+        const u64 packed = (static_cast<u64>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(lo + i));
         best = packed > best ? packed : best;
       }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      best = other > best ? other : best;
-    }
+    best = warp_max(best);
     if (lane == 0) sh.warp_max[warp] = best;
     __syncthreads();
-    if (tid == 0) {
-      unsigned long long m = 0ull;
-      for (int w = 0; w < kSelWarps; ++w) m = sh.warp_max[w] > m ? sh.warp_max[w] : m;
-      sh.max_slot = m;
+    if (tid < 32) {
+      const u64 v = warp_max(tid < kSelWarps ? sh.warp_max[tid] : 0ull);
+      if (tid == 0) sh.max_slot = v;
     }
     cl.sync();
-    if (tid == 0) {
-      unsigned long long m = 0ull;
-      for (int r = 0; r < kSelCluster; ++r) {
-        const unsigned long long v = *cl.map_shared_rank(&sh.max_slot, r);
-        m = v > m ? v : m;
-      }
-      sh.max_bcast = m;
+    if (tid < 32) {
+      const u64 v = warp_max(tid < kSelCluster ? *cl.map_shared_rank(&sh.max_slot, tid) : 0ull);
+      if (tid == 0) sh.max_bcast = v;
     }
     __syncthreads();
     best = sh.max_bcast;
@@ -180,160 +222,193 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     cl.sync();  // no CTA leaves while a peer may still read its shared memory
     return;
   }
-
-  // ---- weights w = exp((z - z_max) / T)
   const float zmax = key_value(static_cast<uint32_t>(best >> 32));
-  for (int i = tid; i < n; i += kSelThreads)
-    wts[i] = expf(__fdiv_rn(__fsub_rn(key_value(keys[i]), zmax), a.temperature));
-  __syncthreads();  // the draw reads the slice by warp segments
+  const float T = a.temperature;
 
   // ---- top-k: largest key k with count(key >= k) >= top_k
   uint32_t kcut = 0u;
   if (a.top_k > 0 && a.top_k < a.V) {
+    uint32_t k = 0u, above = 0u;
+    u64 kend = 1ull << 32;
+    int cnt = 0;
     for (int shift = 30; shift >= 0; shift -= 2) {
-      const uint32_t c1 = kcut | (1u << shift), c2 = kcut | (2u << shift), c3 = kcut | (3u << shift);
-      uint32_t n1 = 0, n2 = 0, n3 = 0;
-      for (int i = tid; i < n; i += kSelThreads) {
-        const uint32_t k = keys[i];
-        n1 += k >= c1;
-        n2 += k >= c2;
-        n3 += k >= c3;
+      const uint32_t c1 = k | (1u << shift), c2 = k | (2u << shift), c3 = k | (3u << shift);
+      uint32_t n1 = 0u, n2 = 0u, n3 = 0u;
+      int kept = 0;
+      if (shift == 30) {
+        for (int i = tid; i < n; i += kSelThreads) {
+          const uint32_t key = keys[i];
+          n1 += key >= c1;
+          n2 += key >= c2;
+          n3 += key >= c3;
+          list[kept++] = static_cast<uint16_t>(i);
+        }
+      } else {
+        for (int j = 0; j < cnt; ++j) {
+          const int i = list[j];
+          const uint32_t key = keys[i];
+          if (key < k) continue;
+          if (static_cast<u64>(key) >= kend) {
+            ++above;
+            continue;
+          }
+          n1 += key >= c1;
+          n2 += key >= c2;
+          n3 += key >= c3;
+          list[kept++] = static_cast<uint16_t>(i);
+        }
       }
-      n1 = __reduce_add_sync(0xFFFFFFFFu, n1);
-      n2 = __reduce_add_sync(0xFFFFFFFFu, n2);
-      n3 = __reduce_add_sync(0xFFFFFFFFu, n3);
+      cnt = kept;
+      n1 = __reduce_add_sync(kFull, n1 + above);
+      n2 = __reduce_add_sync(kFull, n2 + above);
+      n3 = __reduce_add_sync(kFull, n3 + above);
       if (lane == 0) {
-        sh.warp_part[warp][0] = 0.0;
+        sh.warp_part[warp][0] = 0ull;
         sh.warp_part[warp][1] = n1;
         sh.warp_part[warp][2] = n2;
         sh.warp_part[warp][3] = n3;
       }
-      double t[kSelVals];
+      u64 t[kSelVals];
       cluster_totals(sh, cl, phase++, t);
-      const double K = a.top_k;
-      kcut = t[3] >= K ? c3 : t[2] >= K ? c2 : t[1] >= K ? c1 : kcut;
+      const u64 K = static_cast<u64>(a.top_k);
+      k = t[3] >= K ? c3 : t[2] >= K ? c2 : t[1] >= K ? c1 : k;
+      kend = static_cast<u64>(k) + (1ull << shift);
     }
+    kcut = k;
   }
 
   // ---- top-p over the survivors: largest key k with weight(key >= k) >= p * weight(key >= kcut)
   if (a.top_p < 1.0f) {
-    double target = 0.0;
     uint32_t k = 0u;
+    u64 kend = 1ull << 32, above = 0ull, target = 1ull;
+    int cnt = 0;
     for (int shift = 30; shift >= 0; shift -= 2) {
       const uint32_t c1 = k | (1u << shift), c2 = k | (2u << shift), c3 = k | (3u << shift);
-      const bool first = shift == 30;
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      for (int i = tid; i < n; i += kSelThreads) {
-        const uint32_t kk = keys[i];
-        const float w = wts[i];
-        if (first) s0 += kk >= kcut ? w : 0.f;
-        s1 += kk >= c1 ? w : 0.f;
-        s2 += kk >= c2 ? w : 0.f;
-        s3 += kk >= c3 ? w : 0.f;
+      u64 s0 = 0ull, s1 = 0ull, s2 = 0ull, s3 = 0ull;
+      int kept = 0;
+      if (shift == 30) {
+        for (int i = tid; i < n; i += kSelThreads) {
+          const uint32_t key = keys[i];
+          if (key < kcut) continue;
+          const u64 w = weight_fixed(key, zmax, T);
+          s0 += w;
+          s1 += key >= c1 ? w : 0ull;
+          s2 += key >= c2 ? w : 0ull;
+          s3 += key >= c3 ? w : 0ull;
+          list[kept++] = static_cast<uint16_t>(i);
+        }
+      } else {
+        for (int j = 0; j < cnt; ++j) {
+          const int i = list[j];
+          const uint32_t key = keys[i];
+          if (key < k) continue;
+          const u64 w = weight_fixed(key, zmax, T);
+          if (static_cast<u64>(key) >= kend) {
+            above += w;
+            continue;
+          }
+          s1 += key >= c1 ? w : 0ull;
+          s2 += key >= c2 ? w : 0ull;
+          s3 += key >= c3 ? w : 0ull;
+          list[kept++] = static_cast<uint16_t>(i);
+        }
       }
-      s0 = warp_sum_f(s0);
-      s1 = warp_sum_f(s1);
-      s2 = warp_sum_f(s2);
-      s3 = warp_sum_f(s3);
+      cnt = kept;
+      s0 = warp_sum(s0);
+      s1 = warp_sum(s1 + above);
+      s2 = warp_sum(s2 + above);
+      s3 = warp_sum(s3 + above);
       if (lane == 0) {
         sh.warp_part[warp][0] = s0;
         sh.warp_part[warp][1] = s1;
         sh.warp_part[warp][2] = s2;
         sh.warp_part[warp][3] = s3;
       }
-      double t[kSelVals];
+      u64 t[kSelVals];
       cluster_totals(sh, cl, phase++, t);
-      if (first) target = static_cast<double>(a.top_p) * t[0];
+      if (shift == 30) {
+        target = scale_fixed(a.top_p, t[0], true);
+        target = target > 0ull ? target : 1ull;
+      }
       k = t[3] >= target ? c3 : t[2] >= target ? c2 : t[1] >= target ? c1 : k;
+      kend = static_cast<u64>(k) + (1ull << shift);
     }
     kcut = k > kcut ? k : kcut;
   }
 
-  // ---- the draw: kept weight per warp segment, per CTA, per cluster
+  // ---- the draw: kept weight per warp segment, per CTA, per cluster (exact integers)
   const int seg = ((a.chunk + kSelWarps - 1) / kSelWarps + 31) / 32 * 32;
   const int seg_lo = min(n, warp * seg), seg_hi = min(n, seg_lo + seg);
   {
-    float m = 0.f;
-    for (int i = seg_lo + lane; i < seg_hi; i += 32) m += keys[i] >= kcut ? wts[i] : 0.f;
-    m = warp_sum_f(m);
-    if (lane == 0) {
-      sh.warp_part[warp][0] = m;
-      sh.warp_part[warp][1] = 0.0;
-      sh.warp_part[warp][2] = 0.0;
-      sh.warp_part[warp][3] = 0.0;
+    u64 m = 0ull;
+    for (int i = seg_lo + lane; i < seg_hi; i += 32) {
+      const uint32_t key = keys[i];
+      if (key >= kcut) m += weight_fixed(key, zmax, T);
     }
+    m = warp_sum(m);
+    if (lane == 0) sh.warp_part[warp][0] = m;
   }
   __syncthreads();
-  if (tid == 0) {
-    double s = 0.0;
-    for (int w = 0; w < kSelWarps; ++w) s += sh.warp_part[w][0];
-    sh.slot[phase][0] = s;
+  if (tid < 32) {
+    const u64 v = warp_sum(tid < kSelWarps ? sh.warp_part[tid][0] : 0ull);
+    if (tid == 0) sh.slot[phase][0] = v;
   }
   cl.sync();
-  if (tid == 0) {
-    for (int r = 0; r < kSelCluster; ++r) sh.cta_mass[r] = *cl.map_shared_rank(&sh.slot[phase][0], r);
-  }
+  if (tid < kSelCluster) sh.cta_mass[tid] = *cl.map_shared_rank(&sh.slot[phase][0], tid);
   __syncthreads();
   ++phase;
 
-  double M = 0.0, base_c = 0.0;
-  int last_c = -1;
+  u64 M = 0ull, base_c = 0ull;
   for (int r = 0; r < kSelCluster; ++r) {
     if (r == rank) base_c = M;
     M += sh.cta_mass[r];
-    if (sh.cta_mass[r] > 0.0) last_c = r;
   }
   float uu = a.u[row];
   uu = uu >= 0.f ? uu : 0.f;  // also maps NaN to 0
   uu = uu < 1.f ? uu : 0x1.fffffep-1f;
-  const double target = static_cast<double>(uu) * M;
-  const bool sane = M > 0.0 && M <= 1.0e300;
+  const u64 t = scale_fixed(uu, M, false);  // t < M whenever M > 0
 
-  if (!sane) {
-    if (rank == 0 && tid == 0) a.token_out[row] = greedy;
+  if (M == 0ull) {
+    if (rank == 0 && tid == 0) a.token_out[row] = greedy;  // no finite logit
   } else {
-    const double my_mass = sh.cta_mass[rank];
-    const bool cta_claims = my_mass > 0.0 && target >= base_c && (target < base_c + my_mass || rank == last_c);
-    if (cta_claims) {
-      // the warp whose segment holds the target (the last warp with weight takes any rounding overflow)
-      double wb = base_c;
-      int claim_w = -1, last_w = -1;
-      double claim_base = 0.0;
+    const u64 my_mass = sh.cta_mass[rank];
+    if (t >= base_c && t - base_c < my_mass) {
+      // the warp whose segment holds t
+      u64 wb = base_c;
+      int claim_w = -1;
+      u64 claim_base = 0ull;
       for (int w = 0; w < kSelWarps; ++w) {
-        const double mw = sh.warp_part[w][0];
-        if (mw > 0.0) last_w = w;
-        if (mw > 0.0 && claim_w < 0 && target >= wb && target < wb + mw) {
+        const u64 mw = sh.warp_part[w][0];
+        if (claim_w < 0 && t >= wb && t - wb < mw) {
           claim_w = w;
           claim_base = wb;
         }
         wb += mw;
       }
-      if (claim_w < 0) {
-        claim_w = last_w;
-        wb = base_c;
-        for (int w = 0; w < last_w; ++w) wb += sh.warp_part[w][0];
-        claim_base = wb;
-      }
       if (warp == claim_w) {
-        double run = claim_base;
-        int chosen = -1, last_pos = -1;
-        for (int i0 = seg_lo; i0 < seg_hi && chosen < 0; i0 += 32) {
+        u64 run = claim_base;
+        int chosen = -1;
+        for (int i0 = seg_lo; i0 < seg_hi; i0 += 32) {
           const int i = i0 + lane;
-          const float x = (i < seg_hi && keys[i] >= kcut) ? wts[i] : 0.f;
-          float incl = x;
+          u64 x = 0ull;
+          if (i < seg_hi) {
+            const uint32_t key = keys[i];
+            if (key >= kcut) x = weight_fixed(key, zmax, T);
+          }
+          u64 incl = x;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            const u64 y = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += y;
           }
-          const unsigned hit = __ballot_sync(0xFFFFFFFFu, x > 0.f && run + static_cast<double>(incl) > target);
-          const unsigned pos = __ballot_sync(0xFFFFFFFFu, x > 0.f);
-          if (pos) last_pos = i0 + 31 - __clz(pos);
-          if (hit) chosen = i0 + __ffs(hit) - 1;
-          run += static_cast<double>(__shfl_sync(0xFFFFFFFFu, incl, 31));
+          const unsigned hit = __ballot_sync(kFull, x > 0ull && run + incl > t);
+          if (hit) {
+            chosen = i0 + __ffs(hit) - 1;
+            break;
+          }
+          run += __shfl_sync(kFull, incl, 31);
         }
-        if (chosen < 0) chosen = last_pos;
-        if (lane == 0 && chosen >= 0) a.token_out[row] = lo + chosen;
+        if (lane == 0) a.token_out[row] = chosen >= 0 ? lo + chosen : greedy;
       }
     }
   }
@@ -349,7 +424,8 @@ uint32_t select_chunk(int V) {
 
 uint32_t select_smem_bytes(int V) {
   const uint32_t chunk = select_chunk(V);
-  return chunk * 8u + chunk / 8u;
+  const uint32_t cap = (chunk + kSelThreads - 1) / kSelThreads;
+  return chunk * 4u + chunk / 8u + cap * kSelThreads * 2u;
 }
 
 uint32_t select_smem_limit() { return kSmemMax - static_cast<uint32_t>(sizeof(SelShared)) - 1024u; }

@@ -185,10 +185,12 @@ int dec_lmhead_argmax(const float* residual, const void* final_norm, float eps, 
  * prev_tokens int32 [B][n_prev] (NULL when n_prev == 0); u fp32 [B], the
  * caller's uniform draws (NULL allowed when temperature == 0); token_out
  * int32 [B].  repetition_penalty > 0 (1: none); temperature >= 0; top_k >= 0;
- * top_p in (0, 1].  B is 1..4096 here; V a multiple of 8 up to about 220,000
- * (one eighth of a row fits one SM's shared memory).  The kernel orders
- * tokens by their float32 logits exactly and sums weights in a fixed order,
- * so a row's token is reproducible; logits must be finite or -infinity.
+ * top_p in (0, 1].  B is 1..4096 here; V a multiple of 8 up to 299,008 (one
+ * eighth of a row fits one SM's shared memory).  The kernel orders tokens by
+ * their float32 logits exactly and adds weights as fixed-point integers
+ * (w * 2^40, w from float32 expf), so every sum is exact and a row's token is
+ * reproducible.  Logits must be finite or -infinity; a row with no finite
+ * logit gets the greedy index.
  */
 int dec_select_tokens(const float* logits, const int32_t* prev_tokens, int n_prev, float repetition_penalty,
                       float temperature, int top_k, float top_p, const float* u, int32_t* token_out, int B, int V,
