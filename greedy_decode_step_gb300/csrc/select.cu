@@ -20,9 +20,11 @@
 // are thresholds on that key, found by a most-significant-first search that
 // settles 2 bits per round: each CTA counts (or weighs) its keys against 3
 // candidates, the CTA totals meet through distributed shared memory behind
-// one cluster barrier, and every CTA takes the same decision.  A thread only
-// revisits its keys that still lie in the search range: keys below it leave,
-// keys above it are folded into one running total.  Weights are fixed point,
+// one cluster barrier, and every CTA takes the same decision.  Once few of a
+// thread's keys remain in the search range it lists them and revisits only
+// those: keys below the range leave, keys above it are folded into one
+// running total.  About 4.1 bytes of shared memory per logit plus 16 KB, so
+// two CTAs share an SM at a 151,936-token vocabulary.  Weights are fixed point,
 // w * 2^40 in 64-bit integers (exact for w >= 2^-16, truncated below), so
 // every sum is exact and independent of order: the cuts, the kept weight and
 // the draw are reproducible, and the draw lands in exactly one token.  No
@@ -44,6 +46,7 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelPhases = 40;  // 1 (max) + 16 (top-k) + 16 (top-p) + 1 (draw), rounded up
 constexpr int kSelVals = 4;     // values one CTA publishes per phase
+constexpr int kSelListCap = 16; // keys a thread keeps listed between search rounds
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 using u64 = unsigned long long;
@@ -150,7 +153,87 @@ __device__ void cluster_totals(SelShared& sh, cg::cluster_group& cl, int phase, 
   for (int j = 0; j < kSelVals; ++j) out[j] = sh.bcast[j];
 }
 
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 1)
+// Most-significant-first search, 2 bits per round, for the largest key k with
+// total(key >= k) >= goal over the cluster's keys >= floor_key, where total
+// counts keys (kMass false) or adds their fixed-point weights (kMass true;
+// the goal is then ceil(top_p * Z), Z the weight of the keys >= floor_key,
+// taken in the first round).  A thread lists the keys of its slice that lie
+// in the current range [k, kend) once they number at most kSelListCap, and
+// from then on visits only those: keys that fall below the range leave, keys
+// above it join `above`, which counts for every later candidate.  While the
+// range holds more of its keys than the list takes, it rescans the slice.
+template <bool kMass>
+__device__ uint32_t key_search(SelShared& sh, cg::cluster_group& cl, int& phase, const uint32_t* keys, int n,
+                               uint16_t* list, uint32_t floor_key, u64 goal, float top_p, float zmax, float T) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t k = 0u;
+  u64 kend = 1ull << 32, above = 0ull, target = goal;
+  int cnt = 0;
+  bool rescan = true;
+  for (int shift = 30; shift >= 0; shift -= 2) {
+    const uint32_t c1 = k | (1u << shift), c2 = k | (2u << shift), c3 = k | (3u << shift);
+    u64 s0 = 0ull, s1 = 0ull, s2 = 0ull, s3 = 0ull;
+    int kept = 0;
+    if (rescan) {
+      u64 above_now = 0ull;
+      for (int i = tid; i < n; i += kSelThreads) {
+        const uint32_t key = keys[i];
+        if (key < floor_key || key < k) continue;
+        const u64 w = kMass ? weight_fixed(key, zmax, T) : 1ull;
+        s0 += w;
+        if (static_cast<u64>(key) >= kend) {
+          above_now += w;
+          continue;
+        }
+        s1 += key >= c1 ? w : 0ull;
+        s2 += key >= c2 ? w : 0ull;
+        s3 += key >= c3 ? w : 0ull;
+        if (kept < kSelListCap) list[kept] = static_cast<uint16_t>(i);
+        ++kept;
+      }
+      above = above_now;
+      rescan = kept > kSelListCap;
+      cnt = rescan ? 0 : kept;
+    } else {
+      for (int j = 0; j < cnt; ++j) {
+        const int i = list[j];
+        const uint32_t key = keys[i];
+        if (key < k) continue;
+        const u64 w = kMass ? weight_fixed(key, zmax, T) : 1ull;
+        if (static_cast<u64>(key) >= kend) {
+          above += w;
+          continue;
+        }
+        s1 += key >= c1 ? w : 0ull;
+        s2 += key >= c2 ? w : 0ull;
+        s3 += key >= c3 ? w : 0ull;
+        list[kept++] = static_cast<uint16_t>(i);
+      }
+      cnt = kept;
+    }
+    s0 = warp_sum(s0);
+    s1 = warp_sum(s1 + above);
+    s2 = warp_sum(s2 + above);
+    s3 = warp_sum(s3 + above);
+    if (lane == 0) {
+      sh.warp_part[warp][0] = s0;
+      sh.warp_part[warp][1] = s1;
+      sh.warp_part[warp][2] = s2;
+      sh.warp_part[warp][3] = s3;
+    }
+    u64 t[kSelVals];
+    cluster_totals(sh, cl, phase++, t);
+    if (kMass && shift == 30) {
+      target = scale_fixed(top_p, t[0], true);
+      target = target > 0ull ? target : 1ull;
+    }
+    k = t[3] >= target ? c3 : t[2] >= target ? c2 : t[1] >= target ? c1 : k;
+    kend = static_cast<u64>(k) + (1ull << shift);
+  }
+  return k;
+}
+
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
     select_kernel(const __grid_constant__ SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ SelShared sh;
@@ -160,10 +243,10 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int lo = rank * a.chunk;
   const int n = max(0, min(a.chunk, a.V - lo));
-  const int cap = (a.chunk + kSelThreads - 1) / kSelThreads;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
   uint32_t* seen = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(a.chunk) * 4);
-  uint16_t* list = reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(a.chunk) * 4 + a.chunk / 8) + tid * cap;
+  uint16_t* list =
+      reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(a.chunk) * 4 + a.chunk / 8) + tid * kSelListCap;
   const int seen_words = a.chunk / 32;
   int phase = 0;
 
@@ -227,112 +310,12 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 
   // ---- top-k: largest key k with count(key >= k) >= top_k
   uint32_t kcut = 0u;
-  if (a.top_k > 0 && a.top_k < a.V) {
-    uint32_t k = 0u, above = 0u;
-    u64 kend = 1ull << 32;
-    int cnt = 0;
-    for (int shift = 30; shift >= 0; shift -= 2) {
-      const uint32_t c1 = k | (1u << shift), c2 = k | (2u << shift), c3 = k | (3u << shift);
-      uint32_t n1 = 0u, n2 = 0u, n3 = 0u;
-      int kept = 0;
-      if (shift == 30) {
-        for (int i = tid; i < n; i += kSelThreads) {
-          const uint32_t key = keys[i];
-          n1 += key >= c1;
-          n2 += key >= c2;
-          n3 += key >= c3;
-          list[kept++] = static_cast<uint16_t>(i);
-        }
-      } else {
-        for (int j = 0; j < cnt; ++j) {
-          const int i = list[j];
-          const uint32_t key = keys[i];
-          if (key < k) continue;
-          if (static_cast<u64>(key) >= kend) {
-            ++above;
-            continue;
-          }
-          n1 += key >= c1;
-          n2 += key >= c2;
-          n3 += key >= c3;
-          list[kept++] = static_cast<uint16_t>(i);
-        }
-      }
-      cnt = kept;
-      n1 = __reduce_add_sync(kFull, n1 + above);
-      n2 = __reduce_add_sync(kFull, n2 + above);
-      n3 = __reduce_add_sync(kFull, n3 + above);
-      if (lane == 0) {
-        sh.warp_part[warp][0] = 0ull;
-        sh.warp_part[warp][1] = n1;
-        sh.warp_part[warp][2] = n2;
-        sh.warp_part[warp][3] = n3;
-      }
-      u64 t[kSelVals];
-      cluster_totals(sh, cl, phase++, t);
-      const u64 K = static_cast<u64>(a.top_k);
-      k = t[3] >= K ? c3 : t[2] >= K ? c2 : t[1] >= K ? c1 : k;
-      kend = static_cast<u64>(k) + (1ull << shift);
-    }
-    kcut = k;
-  }
+  if (a.top_k > 0 && a.top_k < a.V)
+    kcut = key_search<false>(sh, cl, phase, keys, n, list, 0u, static_cast<u64>(a.top_k), 1.f, zmax, T);
 
   // ---- top-p over the survivors: largest key k with weight(key >= k) >= p * weight(key >= kcut)
   if (a.top_p < 1.0f) {
-    uint32_t k = 0u;
-    u64 kend = 1ull << 32, above = 0ull, target = 1ull;
-    int cnt = 0;
-    for (int shift = 30; shift >= 0; shift -= 2) {
-      const uint32_t c1 = k | (1u << shift), c2 = k | (2u << shift), c3 = k | (3u << shift);
-      u64 s0 = 0ull, s1 = 0ull, s2 = 0ull, s3 = 0ull;
-      int kept = 0;
-      if (shift == 30) {
-        for (int i = tid; i < n; i += kSelThreads) {
-          const uint32_t key = keys[i];
-          if (key < kcut) continue;
-          const u64 w = weight_fixed(key, zmax, T);
-          s0 += w;
-          s1 += key >= c1 ? w : 0ull;
-          s2 += key >= c2 ? w : 0ull;
-          s3 += key >= c3 ? w : 0ull;
-          list[kept++] = static_cast<uint16_t>(i);
-        }
-      } else {
-        for (int j = 0; j < cnt; ++j) {
-          const int i = list[j];
-          const uint32_t key = keys[i];
-          if (key < k) continue;
-          const u64 w = weight_fixed(key, zmax, T);
-          if (static_cast<u64>(key) >= kend) {
-            above += w;
-            continue;
-          }
-          s1 += key >= c1 ? w : 0ull;
-          s2 += key >= c2 ? w : 0ull;
-          s3 += key >= c3 ? w : 0ull;
-          list[kept++] = static_cast<uint16_t>(i);
-        }
-      }
-      cnt = kept;
-      s0 = warp_sum(s0);
-      s1 = warp_sum(s1 + above);
-      s2 = warp_sum(s2 + above);
-      s3 = warp_sum(s3 + above);
-      if (lane == 0) {
-        sh.warp_part[warp][0] = s0;
-        sh.warp_part[warp][1] = s1;
-        sh.warp_part[warp][2] = s2;
-        sh.warp_part[warp][3] = s3;
-      }
-      u64 t[kSelVals];
-      cluster_totals(sh, cl, phase++, t);
-      if (shift == 30) {
-        target = scale_fixed(a.top_p, t[0], true);
-        target = target > 0ull ? target : 1ull;
-      }
-      k = t[3] >= target ? c3 : t[2] >= target ? c2 : t[1] >= target ? c1 : k;
-      kend = static_cast<u64>(k) + (1ull << shift);
-    }
+    const uint32_t k = key_search<true>(sh, cl, phase, keys, n, list, kcut, 1ull, a.top_p, zmax, T);
     kcut = k > kcut ? k : kcut;
   }
 
@@ -424,8 +407,7 @@ uint32_t select_chunk(int V) {
 
 uint32_t select_smem_bytes(int V) {
   const uint32_t chunk = select_chunk(V);
-  const uint32_t cap = (chunk + kSelThreads - 1) / kSelThreads;
-  return chunk * 4u + chunk / 8u + cap * kSelThreads * 2u;
+  return chunk * 4u + chunk / 8u + kSelListCap * kSelThreads * 2u;
 }
 
 uint32_t select_smem_limit() { return kSmemMax - static_cast<uint32_t>(sizeof(SelShared)) - 1024u; }
