@@ -1174,12 +1174,20 @@ int dec_select_tokens(const float* logits, const int32_t* prev_tokens, int n_pre
   DEC_CHECK(top_k >= 0, DEC_EINVAL, "top_k must be >= 0");
   DEC_CHECK(top_p > 0.f && top_p <= 1.f, DEC_EINVAL, "top_p must lie in (0, 1]");
   DEC_CHECK(temperature == 0.f || u != nullptr, DEC_EINVAL, "u is NULL with temperature > 0");
-  DEC_CHECK(select_smem_bytes(V) <= select_smem_limit(), DEC_EUNSUPPORTED,
-            "V = %d needs %u bytes of shared memory per CTA (limit %u)", V, select_smem_bytes(V),
-            select_smem_limit());
+  DEC_CHECK(select_smem_bytes(V, kSelectSmallListCap) <= select_smem_limit(), DEC_EUNSUPPORTED,
+            "V = %d needs %u bytes of shared memory per CTA (limit %u)", V,
+            select_smem_bytes(V, kSelectSmallListCap), select_smem_limit());
   DeviceInfo* dv;
   DEC_TRY(device_info(&dv));
-  DEC_CHECK(select_max_active_clusters(V) >= 1, DEC_EUNSUPPORTED, "a cluster of 8 CTAs does not fit for V = %d", V);
+  // Full-length search lists when every row's cluster is resident at once with
+  // them; else short lists, which let two CTAs share an SM.
+  int cap = kSelectSmallListCap;
+  const int cap_full = select_full_list_cap(V);
+  if (cap_full > cap && select_smem_bytes(V, cap_full) <= select_smem_limit() &&
+      select_max_active_clusters(V, cap_full) >= B)
+    cap = cap_full;
+  DEC_CHECK(select_max_active_clusters(V, cap) >= 1, DEC_EUNSUPPORTED, "a cluster of 8 CTAs does not fit for V = %d",
+            V);
   SelectArgs a{};
   a.logits = logits;
   a.prev = prev_tokens;
@@ -1189,6 +1197,7 @@ int dec_select_tokens(const float* logits, const int32_t* prev_tokens, int n_pre
   a.chunk = static_cast<int>(select_chunk(V));
   a.n_prev = n_prev;
   a.top_k = top_k;
+  a.list_cap = cap;
   a.penalty = repetition_penalty;
   a.temperature = temperature;
   a.top_p = top_p;

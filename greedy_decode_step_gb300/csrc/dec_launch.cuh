@@ -93,13 +93,16 @@ struct SelectArgs {
   const float* u;         // [B] uniform draws
   int32_t* token_out;     // [B]
   int V, chunk, n_prev, top_k;
+  int list_cap;           // keys a thread may list between search rounds
   float penalty, temperature, top_p;
 };
+constexpr int kSelectSmallListCap = 16;
 uint32_t select_chunk(int V);            // logits per CTA
-uint32_t select_smem_bytes(int V);       // dynamic shared memory per CTA
+int select_full_list_cap(int V);         // a list that holds every key of a thread
+uint32_t select_smem_bytes(int V, int list_cap);  // dynamic shared memory per CTA
 uint32_t select_smem_limit();            // the most dynamic shared memory a CTA may take
 cudaError_t allow_smem_select();
-int select_max_active_clusters(int V);   // 0: the cluster does not fit this device
+int select_max_active_clusters(int V, int list_cap);  // 0: the cluster does not fit this device
 cudaError_t launch_select(const SelectArgs& a, int B, cudaStream_t st);
 
 }  // namespace dec

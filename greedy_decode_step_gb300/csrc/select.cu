@@ -23,8 +23,10 @@
 // one cluster barrier, and every CTA takes the same decision.  Once few of a
 // thread's keys remain in the search range it lists them and revisits only
 // those: keys below the range leave, keys above it are folded into one
-// running total.  About 4.1 bytes of shared memory per logit plus 16 KB, so
-// two CTAs share an SM at a 151,936-token vocabulary.  Weights are fixed point,
+// running total.  The list holds every key of the thread (about 6.1 bytes of
+// shared memory per logit) when the clusters of all rows fit the GPU at once,
+// else 16 keys (about 4.1 bytes per logit plus 16 KB), so that two CTAs share
+// an SM and more rows run side by side.  Weights are fixed point,
 // w * 2^40 in 64-bit integers (exact for w >= 2^-16, truncated below), so
 // every sum is exact and independent of order: the cuts, the kept weight and
 // the draw are reproducible, and the draw lands in exactly one token.  No
@@ -46,7 +48,6 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelPhases = 40;  // 1 (max) + 16 (top-k) + 16 (top-p) + 1 (draw), rounded up
 constexpr int kSelVals = 4;     // values one CTA publishes per phase
-constexpr int kSelListCap = 16; // keys a thread keeps listed between search rounds
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 using u64 = unsigned long long;
@@ -158,13 +159,14 @@ __device__ void cluster_totals(SelShared& sh, cg::cluster_group& cl, int phase, 
 // counts keys (kMass false) or adds their fixed-point weights (kMass true;
 // the goal is then ceil(top_p * Z), Z the weight of the keys >= floor_key,
 // taken in the first round).  A thread lists the keys of its slice that lie
-// in the current range [k, kend) once they number at most kSelListCap, and
-// from then on visits only those: keys that fall below the range leave, keys
-// above it join `above`, which counts for every later candidate.  While the
-// range holds more of its keys than the list takes, it rescans the slice.
+// in the current range [k, kend) once they number at most `cap`, and from
+// then on visits only those: keys that fall below the range leave, keys above
+// it join `above`, which counts for every later candidate.  While the range
+// holds more of its keys than the list takes, it rescans the slice.
 template <bool kMass>
 __device__ uint32_t key_search(SelShared& sh, cg::cluster_group& cl, int& phase, const uint32_t* keys, int n,
-                               uint16_t* list, uint32_t floor_key, u64 goal, float top_p, float zmax, float T) {
+                               uint16_t* list, int cap, uint32_t floor_key, u64 goal, float top_p, float zmax,
+                               float T) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t k = 0u;
   u64 kend = 1ull << 32, above = 0ull, target = goal;
@@ -188,11 +190,11 @@ __device__ uint32_t key_search(SelShared& sh, cg::cluster_group& cl, int& phase,
         s1 += key >= c1 ? w : 0ull;
         s2 += key >= c2 ? w : 0ull;
         s3 += key >= c3 ? w : 0ull;
-        if (kept < kSelListCap) list[kept] = static_cast<uint16_t>(i);
+        if (kept < cap) list[kept] = static_cast<uint16_t>(i);
         ++kept;
       }
       above = above_now;
-      rescan = kept > kSelListCap;
+      rescan = kept > cap;
       cnt = rescan ? 0 : kept;
     } else {
       for (int j = 0; j < cnt; ++j) {
@@ -246,7 +248,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
   uint32_t* seen = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(a.chunk) * 4);
   uint16_t* list =
-      reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(a.chunk) * 4 + a.chunk / 8) + tid * kSelListCap;
+      reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(a.chunk) * 4 + a.chunk / 8) + tid * a.list_cap;
   const int seen_words = a.chunk / 32;
   int phase = 0;
 
@@ -311,11 +313,11 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   // ---- top-k: largest key k with count(key >= k) >= top_k
   uint32_t kcut = 0u;
   if (a.top_k > 0 && a.top_k < a.V)
-    kcut = key_search<false>(sh, cl, phase, keys, n, list, 0u, static_cast<u64>(a.top_k), 1.f, zmax, T);
+    kcut = key_search<false>(sh, cl, phase, keys, n, list, a.list_cap, 0u, static_cast<u64>(a.top_k), 1.f, zmax, T);
 
   // ---- top-p over the survivors: largest key k with weight(key >= k) >= p * weight(key >= kcut)
   if (a.top_p < 1.0f) {
-    const uint32_t k = key_search<true>(sh, cl, phase, keys, n, list, kcut, 1ull, a.top_p, zmax, T);
+    const uint32_t k = key_search<true>(sh, cl, phase, keys, n, list, a.list_cap, kcut, 1ull, a.top_p, zmax, T);
     kcut = k > kcut ? k : kcut;
   }
 
@@ -405,9 +407,11 @@ uint32_t select_chunk(int V) {
   return (per + 63u) / 64u * 64u;
 }
 
-uint32_t select_smem_bytes(int V) {
+int select_full_list_cap(int V) { return static_cast<int>((select_chunk(V) + kSelThreads - 1) / kSelThreads); }
+
+uint32_t select_smem_bytes(int V, int list_cap) {
   const uint32_t chunk = select_chunk(V);
-  return chunk * 4u + chunk / 8u + kSelListCap * kSelThreads * 2u;
+  return chunk * 4u + chunk / 8u + static_cast<uint32_t>(list_cap) * kSelThreads * 2u;
 }
 
 uint32_t select_smem_limit() { return kSmemMax - static_cast<uint32_t>(sizeof(SelShared)) - 1024u; }
@@ -417,18 +421,18 @@ cudaError_t allow_smem_select() {
                               static_cast<int>(select_smem_limit()));
 }
 
-int select_max_active_clusters(int V) {
+int select_max_active_clusters(int V, int list_cap) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kSelCluster);
   cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = select_smem_bytes(V);
+  cfg.dynamicSmemBytes = select_smem_bytes(V, list_cap);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, select_kernel, &cfg) != cudaSuccess) return 0;
   return n;
 }
 
 cudaError_t launch_select(const SelectArgs& a, int B, cudaStream_t st) {
-  select_kernel<<<B * kSelCluster, kSelThreads, select_smem_bytes(a.V), st>>>(a);
+  select_kernel<<<B * kSelCluster, kSelThreads, select_smem_bytes(a.V, a.list_cap), st>>>(a);
   return cudaGetLastError();
 }
 

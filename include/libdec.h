@@ -185,7 +185,7 @@ int dec_lmhead_argmax(const float* residual, const void* final_norm, float eps, 
  * prev_tokens int32 [B][n_prev] (NULL when n_prev == 0); u fp32 [B], the
  * caller's uniform draws (NULL allowed when temperature == 0); token_out
  * int32 [B].  repetition_penalty > 0 (1: none); temperature >= 0; top_k >= 0;
- * top_p in (0, 1].  B is 1..4096 here; V a multiple of 8 up to 299,008 (one
+ * top_p in (0, 1].  B is 1..4096 here; V a multiple of 8 up to 412,672 (one
  * eighth of a row fits one SM's shared memory).  The kernel orders tokens by
  * their float32 logits exactly and adds weights as fixed-point integers
  * (w * 2^40, w from float32 expf), so every sum is exact and a row's token is

@@ -137,6 +137,19 @@ def test_sampling_matches_oracle(gd, case):
     check_rows(got, z, u, prev, pen, T, K, float(np.float32(P)), min_exact=share)
 
 
+def test_many_rows_and_a_large_vocabulary(gd):
+    # 40 rows are more clusters than fit the GPU at once with full-length
+    # search lists, so the kernel takes the short lists; 400,000 logits put
+    # 50,000 in each CTA
+    for B, V, K, P in ((40, VOCAB, 50, 0.9), (3, 400_000, 0, 0.8)):
+        tag = f"sel.rows.{B}.{V}"
+        z = synth.make_logits(17, tag, B, V, 4.0, True)
+        u = synth.make_uniforms(17, tag + ".u", B)
+        got = run(gd, z, u=u, temperature=0.8, top_k=K, top_p=P)
+        check_rows(got, z, u, None, 1.0, 0.8, K, float(np.float32(P)))
+        assert np.array_equal(run(gd, z), np.argmax(z, axis=1))
+
+
 def test_many_draws_over_one_row(gd):
     # one row repeated with a grid of draws: every inverse-CDF interval is hit
     V, B = 64, 512
