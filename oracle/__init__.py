@@ -34,6 +34,10 @@ class Taps(ctypes.Structure):
     _fields_ = [(n, _P) for n in ("y_attn", "q", "k", "v", "o", "y_mlp", "h")]
 
 
+class AttnVariant(ctypes.Structure):
+    _fields_ = [("rot_dim", _I), ("q_norm", _P), ("k_norm", _P), ("Wgate", _P)]
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle (plain -O2, no fast-math) into ``liboracle.so``."""
     src = os.path.join(_HERE, "oracle.c")
@@ -64,6 +68,11 @@ def lib():
             "orc_glu": (None, [_P, _P, _P, _I, _I, _P]),
             "orc_argmax": (_I, [_P, _I]),
             "orc_layer": (None, [ctypes.POINTER(Dims)] + [_P] * 11 + [_I, _P, ctypes.POINTER(Taps)]),
+            "orc_layer_ex": (None, [ctypes.POINTER(Dims), ctypes.POINTER(AttnVariant)] + [_P] * 11
+                             + [_I, _P, ctypes.POINTER(Taps)]),
+            "orc_rope_partial": (None, [_P, _I, _I, _I, _D]),
+            "orc_head_rmsnorm": (None, [_P, _I, _I, _P, _D]),
+            "orc_sigmoid": (_D, [_D]),
             "orc_head": (_I, [_P, _P, _P, _I, _I, _D, _P]),
             "orc_step": (_I, [ctypes.POINTER(Dims), _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P]),
             "orc_select": (_I, [_P, _I, _P, _I, _D, _D, _I, _D, _D, _P]),
@@ -145,6 +154,31 @@ def rope(v, p: int, theta: float):
     return flat.reshape(v.shape)
 
 
+def rope_partial(v, rot_dim: int, p: int, theta: float):
+    """RoPE of the first rot_dim dims of head vectors v[..., D] at position p; the rest unchanged."""
+    v = _f64(v).copy()
+    D = v.shape[-1]
+    flat = v.reshape(-1, D)
+    for i in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[i])
+        lib().orc_rope_partial(row.ctypes.data, D, int(rot_dim), int(p), float(theta))
+        flat[i] = row
+    return flat.reshape(v.shape)
+
+
+def head_rmsnorm(v, gain, eps: float):
+    """RMSNorm of each head vector v[..., D] with the shared effective gain [D] (bf16 bits)."""
+    v = _f64(v).copy()
+    D = v.shape[-1]
+    flat = np.ascontiguousarray(v.reshape(-1, D))
+    lib().orc_head_rmsnorm(flat.ctypes.data, flat.shape[0], D, _u16(gain).ctypes.data, float(eps))
+    return flat.reshape(v.shape)
+
+
+def sigmoid(z: float) -> float:
+    return float(lib().orc_sigmoid(float(z)))
+
+
 def kv_head(h: int, Hq: int, Hkv: int) -> int:
     return int(lib().orc_kv_head(h, Hq, Hkv))
 
@@ -205,9 +239,13 @@ def dims(m, S_max: int) -> Dims:
     return Dims(m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.intermediate, S_max, m.rms_eps, m.rope_theta)
 
 
-def layer(m, w: dict, Kc, Vc, p: int, r, taps: bool = False):
+def layer(m, w: dict, Kc, Vc, p: int, r, taps: bool = False, variant: dict | None = None):
     """One layer of one sequence at position p.  Kc/Vc ([Hkv, S_max, D] bf16, this
-    sequence's slice) are updated in place.  Returns (r_new, taps dict or None)."""
+    sequence's slice) are updated in place.  Returns (r_new, taps dict or None).
+
+    variant (the gated attention layer): optional keys ``rot_dim`` (rotary dims
+    per head), ``q_norm`` / ``k_norm`` (per-head RMSNorm gains [D], bf16 bits)
+    and ``wgate`` (output-gate projection [Hq*D, H], bf16 bits)."""
     Kc, Vc = _u16(Kc), _u16(Vc)
     d = dims(m, Kc.shape[1])
     r = _f64(r).copy()
@@ -219,8 +257,15 @@ def layer(m, w: dict, Kc, Vc, p: int, r, taps: bool = False):
              "o": np.empty(Hq * D), "y_mlp": np.empty(H), "h": np.empty(I)}
         tp = Taps(*[t[n].ctypes.data for n in ("y_attn", "q", "k", "v", "o", "y_mlp", "h")])
     ws = [_u16(w[k]) for k in LAYER_KEYS]
-    lib().orc_layer(ctypes.byref(d), *[a.ctypes.data for a in ws], Kc.ctypes.data, Vc.ctypes.data, int(p),
-                    r.ctypes.data, ctypes.byref(tp) if tp is not None else None)
+    if variant is None:
+        lib().orc_layer(ctypes.byref(d), *[a.ctypes.data for a in ws], Kc.ctypes.data, Vc.ctypes.data, int(p),
+                        r.ctypes.data, ctypes.byref(tp) if tp is not None else None)
+        return r, t
+    keep = {k: _u16(variant[k]) for k in ("q_norm", "k_norm", "wgate") if variant.get(k) is not None}
+    var = AttnVariant(int(variant.get("rot_dim", 0)), *[keep[k].ctypes.data if k in keep else None
+                                                        for k in ("q_norm", "k_norm", "wgate")])
+    lib().orc_layer_ex(ctypes.byref(d), ctypes.byref(var), *[a.ctypes.data for a in ws], Kc.ctypes.data,
+                       Vc.ctypes.data, int(p), r.ctypes.data, ctypes.byref(tp) if tp is not None else None)
     return r, t
 
 

@@ -111,6 +111,25 @@ void orc_rope(double* v, int64_t D, int64_t p, double theta) {
   }
 }
 
+/* Partial rotary ("partial NeoX RoPE" of the decode-path review "Two more
+ * decode-path suggestions"): the rotate-half RoPE above applied to the first
+ * r dims of a D-vector as if they were the whole head (angles
+ * p * theta^(-2i/r), pairs (i, i + r/2)); dims r .. D-1 are left as they are. */
+void orc_rope_partial(double* v, int64_t D, int64_t r, int64_t p, double theta) {
+  (void)D;
+  orc_rope(v, r, p, theta);
+}
+
+/* Per-head RMSNorm ("q/k RMSNorm(1+w)" of the same review): each of the
+ * n_heads consecutive D-vectors is normalised on its own and scaled by the
+ * effective gain g[0..D) shared by the heads. */
+void orc_head_rmsnorm(double* v, int64_t n_heads, int64_t D, const bf16_t* g, double eps) {
+  for (int64_t h = 0; h < n_heads; ++h) orc_rmsnorm(v + h * D, g, D, eps, v + h * D);
+}
+
+/* The output gate's squashing function ("* sigmoid(gate)" in the same review). */
+double orc_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
 /* GQA: query head h reads KV head floor(h / (Hq / Hkv)) -- contiguous groups. */
 int64_t orc_kv_head(int64_t h, int64_t Hq, int64_t Hkv) { return h / (Hq / Hkv); }
 
@@ -240,14 +259,32 @@ typedef struct {
 } orc_taps;
 
 /*
+ * The gated attention variant of the decode-path review "Two more decode-path
+ * suggestions" (item 1): q/k RMSNorm per head, partial NeoX RoPE, and the
+ * attention output multiplied by sigmoid(gate) before o_proj.  The review
+ * does not say where the gate comes from; here it is a projection of the
+ * layer's normed input, gate = Wgate y, one value per attention-output
+ * element.  A NULL field (or rot_dim 0) leaves that part as in the plain layer.
+ */
+typedef struct {
+  int64_t rot_dim;       /* rotary dims per head, even, 0 < rot_dim <= D (0: all D) */
+  const bf16_t* q_norm;  /* [D] effective gain of the per-head query RMSNorm */
+  const bf16_t* k_norm;  /* [D] effective gain of the per-head key RMSNorm */
+  const bf16_t* Wgate;   /* [Hq*D][H] output-gate projection */
+} orc_attn_variant;
+
+/*
  * One decoder layer for the token at position p of one sequence.
  * r: [H] residual stream, updated in place.  Kc/Vc: this sequence's
  * [Hkv][S_max][D] bf16 caches; slot p is written, then keys 0..p are read.
+ * var may be NULL (the plain dense layer).
  */
-void orc_layer(const orc_dims* d, const bf16_t* attn_norm, const bf16_t* Wq, const bf16_t* Wk, const bf16_t* Wv,
-               const bf16_t* Wo, const bf16_t* mlp_norm, const bf16_t* Wg, const bf16_t* Wu, const bf16_t* Wd,
-               bf16_t* Kc, bf16_t* Vc, int64_t p, double* r, orc_taps* taps) {
+void orc_layer_ex(const orc_dims* d, const orc_attn_variant* var, const bf16_t* attn_norm, const bf16_t* Wq,
+                  const bf16_t* Wk, const bf16_t* Wv, const bf16_t* Wo, const bf16_t* mlp_norm, const bf16_t* Wg,
+                  const bf16_t* Wu, const bf16_t* Wd, bf16_t* Kc, bf16_t* Vc, int64_t p, double* r,
+                  orc_taps* taps) {
   int64_t H = d->H, Hq = d->Hq, Hkv = d->Hkv, D = d->D, I = d->I;
+  int64_t rot = (var && var->rot_dim > 0) ? var->rot_dim : D;
   double* y = (double*)malloc(sizeof(double) * (size_t)H);
   double* q = (double*)malloc(sizeof(double) * (size_t)(Hq * D));
   double* k = (double*)malloc(sizeof(double) * (size_t)(Hkv * D));
@@ -262,8 +299,10 @@ void orc_layer(const orc_dims* d, const bf16_t* attn_norm, const bf16_t* Wq, con
   orc_linear(Wq, y, Hq * D, H, q);
   orc_linear(Wk, y, Hkv * D, H, k);
   orc_linear(Wv, y, Hkv * D, H, v);
-  for (int64_t h = 0; h < Hq; ++h) orc_rope(q + h * D, D, p, d->theta);
-  for (int64_t g = 0; g < Hkv; ++g) orc_rope(k + g * D, D, p, d->theta);
+  if (var && var->q_norm) orc_head_rmsnorm(q, Hq, D, var->q_norm, d->eps);
+  if (var && var->k_norm) orc_head_rmsnorm(k, Hkv, D, var->k_norm, d->eps);
+  for (int64_t h = 0; h < Hq; ++h) orc_rope_partial(q + h * D, D, rot, p, d->theta);
+  for (int64_t g = 0; g < Hkv; ++g) orc_rope_partial(k + g * D, D, rot, p, d->theta);
   if (taps && taps->q) memcpy(taps->q, q, sizeof(double) * (size_t)(Hq * D));
   if (taps && taps->k) memcpy(taps->k, k, sizeof(double) * (size_t)(Hkv * D));
   if (taps && taps->v) memcpy(taps->v, v, sizeof(double) * (size_t)(Hkv * D));
@@ -273,6 +312,12 @@ void orc_layer(const orc_dims* d, const bf16_t* attn_norm, const bf16_t* Wq, con
       Vc[(g * d->S_max + p) * D + e] = orc_f64_to_bf16(v[g * D + e]);
     }
   orc_attention(q, Kc, Vc, p + 1, Hq, Hkv, D, d->S_max, o);
+  if (var && var->Wgate) {
+    double* gate = (double*)malloc(sizeof(double) * (size_t)(Hq * D));
+    orc_linear(var->Wgate, y, Hq * D, H, gate);
+    for (int64_t i = 0; i < Hq * D; ++i) o[i] *= orc_sigmoid(gate[i]);
+    free(gate);
+  }
   if (taps && taps->o) memcpy(taps->o, o, sizeof(double) * (size_t)(Hq * D));
   orc_linear(Wo, o, H, Hq * D, a);
   for (int64_t i = 0; i < H; ++i) r[i] += a[i];
@@ -286,6 +331,13 @@ void orc_layer(const orc_dims* d, const bf16_t* attn_norm, const bf16_t* Wq, con
   for (int64_t i = 0; i < H; ++i) r[i] += a[i];
 
   free(y); free(q); free(k); free(v); free(o); free(a); free(hh);
+}
+
+/* The plain dense layer. */
+void orc_layer(const orc_dims* d, const bf16_t* attn_norm, const bf16_t* Wq, const bf16_t* Wk, const bf16_t* Wv,
+               const bf16_t* Wo, const bf16_t* mlp_norm, const bf16_t* Wg, const bf16_t* Wu, const bf16_t* Wd,
+               bf16_t* Kc, bf16_t* Vc, int64_t p, double* r, orc_taps* taps) {
+  orc_layer_ex(d, 0, attn_norm, Wq, Wk, Wv, Wo, mlp_norm, Wg, Wu, Wd, Kc, Vc, p, r, taps);
 }
 
 /* Final norm, LM-head logits and the greedy token. */
