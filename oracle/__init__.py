@@ -75,6 +75,7 @@ def lib():
             "orc_sigmoid": (_D, [_D]),
             "orc_head": (_I, [_P, _P, _P, _I, _I, _D, _P]),
             "orc_step": (_I, [ctypes.POINTER(Dims), _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P]),
+            "orc_step_ex": (_I, [ctypes.POINTER(Dims), _I, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P]),
             "orc_select": (_I, [_P, _I, _P, _I, _D, _D, _I, _D, _D, _P]),
         }
         for name, (res, args) in sig.items():
@@ -273,10 +274,11 @@ class Model:
     """Host-side model for the oracle: lists of bf16 weight arrays and per-sequence caches.
 
     layers: list of dicts (LAYER_KEYS -> uint16 arrays); kcache/vcache: per layer
-    arrays [B, Hkv, S_max, D] (uint16), owned and updated by the oracle only.
+    arrays [B, Hkv, S_max, D] (uint16), owned and updated by the oracle only;
+    variants: None, or one gated-attention dict per layer (see ``layer``).
     """
 
-    def __init__(self, m, layers, embed, final_norm, lm_head, kcache, vcache):
+    def __init__(self, m, layers, embed, final_norm, lm_head, kcache, vcache, variants=None):
         self.m = m
         self.layers = layers
         self.embed = embed
@@ -286,6 +288,15 @@ class Model:
         self.vcache = vcache
         self._wptr = (ctypes.c_void_p * (9 * len(layers)))(
             *[_u16(l[k]).ctypes.data for l in layers for k in LAYER_KEYS])
+        self._var = None
+        if variants is not None:
+            assert len(variants) == len(layers)
+            self._keep = [{k: _u16(v[k]) for k in ("q_norm", "k_norm", "wgate") if v.get(k) is not None}
+                          for v in variants]
+            self._var = (AttnVariant * len(layers))(
+                *[AttnVariant(int(v.get("rot_dim", 0)), *[kp[k].ctypes.data if k in kp else None
+                                                          for k in ("q_norm", "k_norm", "wgate")])
+                  for v, kp in zip(variants, self._keep)])
 
     def step(self, b: int, p: int, token: int | None = None, x_in=None):
         """One decode step of sequence b at position p.  Returns (token, logits, r_final)."""
@@ -301,12 +312,12 @@ class Model:
         has_head = self.lm_head is not None
         logits = np.empty(m.vocab) if has_head else None
         x = None if x_in is None else _f64(x_in)
-        tok = lib().orc_step(ctypes.byref(d), L, self._wptr, kc, vc,
-                             None if self.embed is None else self.embed.ctypes.data,
-                             _ptr(x), -1 if token is None else int(token), int(p),
-                             None if self.final_norm is None else self.final_norm.ctypes.data,
-                             self.lm_head.ctypes.data if has_head else None, m.vocab,
-                             _ptr(logits), r_out.ctypes.data)
+        tok = lib().orc_step_ex(ctypes.byref(d), L, self._wptr, self._var, kc, vc,
+                                None if self.embed is None else self.embed.ctypes.data,
+                                _ptr(x), -1 if token is None else int(token), int(p),
+                                None if self.final_norm is None else self.final_norm.ctypes.data,
+                                self.lm_head.ctypes.data if has_head else None, m.vocab,
+                                _ptr(logits), r_out.ctypes.data)
         return int(tok), logits, r_out
 
 

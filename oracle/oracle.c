@@ -356,23 +356,33 @@ int64_t orc_head(const double* r, const bf16_t* final_norm, const bf16_t* lm_hea
  * layers at position p, and ends in logits and the greedy token.
  * layer_w: L*9 pointers in the order attn_norm, Wq, Wk, Wv, Wo, mlp_norm, Wg, Wu, Wd.
  * kc, vc: L pointers to this sequence's caches.  lm_head may be NULL (no head:
- * returns -1 and only r_out is written).
+ * returns -1 and only r_out is written).  variants: NULL, or L per-layer
+ * gated-attention settings (orc_layer_ex).
  */
-int64_t orc_step(const orc_dims* d, int64_t L, const bf16_t* const* layer_w, bf16_t* const* kc, bf16_t* const* vc,
-                 const bf16_t* embed, const double* x_in, int64_t token, int64_t p, const bf16_t* final_norm,
-                 const bf16_t* lm_head, int64_t V, double* logits, double* r_out) {
+int64_t orc_step_ex(const orc_dims* d, int64_t L, const bf16_t* const* layer_w, const orc_attn_variant* variants,
+                    bf16_t* const* kc, bf16_t* const* vc, const bf16_t* embed, const double* x_in, int64_t token,
+                    int64_t p, const bf16_t* final_norm, const bf16_t* lm_head, int64_t V, double* logits,
+                    double* r_out) {
   int64_t H = d->H;
   double* r = (double*)malloc(sizeof(double) * (size_t)H);
   for (int64_t i = 0; i < H; ++i) r[i] = x_in ? x_in[i] : widen(embed[token * H + i]);
   for (int64_t l = 0; l < L; ++l) {
     const bf16_t* const* w = layer_w + 9 * l;
-    orc_layer(d, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7], w[8], kc[l], vc[l], p, r, 0);
+    orc_layer_ex(d, variants ? variants + l : 0, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7], w[8], kc[l], vc[l],
+                 p, r, 0);
   }
   if (r_out) memcpy(r_out, r, sizeof(double) * (size_t)H);
   int64_t tok = -1;
   if (lm_head) tok = orc_head(r, final_norm, lm_head, H, V, d->eps, logits);
   free(r);
   return tok;
+}
+
+/* The plain dense step (no layer uses the gated variant). */
+int64_t orc_step(const orc_dims* d, int64_t L, const bf16_t* const* layer_w, bf16_t* const* kc, bf16_t* const* vc,
+                 const bf16_t* embed, const double* x_in, int64_t token, int64_t p, const bf16_t* final_norm,
+                 const bf16_t* lm_head, int64_t V, double* logits, double* r_out) {
+  return orc_step_ex(d, L, layer_w, 0, kc, vc, embed, x_in, token, p, final_norm, lm_head, V, logits, r_out);
 }
 
 /* ---------------------------------------------------------------- token selection */

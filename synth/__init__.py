@@ -206,6 +206,17 @@ def make_layer(seed: int, m: ModelShape, layer: int, alloc=None) -> dict:
     return out
 
 
+def make_gated_attention(seed: int, m: ModelShape, layer: int, rot_dim: int) -> dict:
+    """bf16 bits of one layer's gated-attention parts: per-head q/k RMSNorm gains
+    [D] of 1 + N(0, gain_std) and the output-gate projection [Hq*D, H] of
+    N(0, weight_std), with the rotary width ``rot_dim``."""
+    D = m.head_dim
+    return {"rot_dim": int(rot_dim),
+            "q_norm": normal_bf16(seed, f"L{layer}.q_norm", (D,), 1.0, m.gain_std),
+            "k_norm": normal_bf16(seed, f"L{layer}.k_norm", (D,), 1.0, m.gain_std),
+            "wgate": normal_bf16(seed, f"L{layer}.wgate", (m.n_heads * D, m.hidden), 0.0, m.weight_std)}
+
+
 def make_embedding(seed: int, m: ModelShape, alloc=None) -> np.ndarray:
     shape = (m.vocab, m.hidden)
     return normal_bf16(seed, "embed", shape, 0.0, m.weight_std, out=alloc(shape) if alloc else None)

@@ -190,3 +190,41 @@ def test_gated_layer_equals_composition_of_pinned_primitives():
     np.testing.assert_array_equal(V1, V2)
     np.testing.assert_allclose(taps["o"], o, rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(r1, r, rtol=1e-14, atol=1e-14)
+
+
+def test_gated_step_equals_its_layers_then_the_head():
+    m = synth.workload("tiny").model
+    m = dataclasses.replace(m, n_layers=2)
+    S_max, p = 24, 9
+    lays = [synth.make_layer(0, m, l) for l in range(2)]
+    vars_ = [synth.make_gated_attention(0, m, l, 16) for l in range(2)]
+    E = synth.make_embedding(0, m)
+    fn = synth.make_final_norm(0, m)
+    Ks = [np.zeros((1, m.n_kv_heads, S_max, m.head_dim), np.uint16) for _ in range(2)]
+    Vs = [np.zeros_like(k) for k in Ks]
+    for l in range(2):
+        synth.make_kv_prefix(0, m, l, 0, p, "k", Ks[l][0])
+        synth.make_kv_prefix(0, m, l, 0, p, "v", Vs[l][0])
+    Ka, Va = [k.copy() for k in Ks], [v.copy() for v in Vs]
+    model = oracle.Model(m, lays, E, fn, E, Ka, Va, variants=vars_)
+    tok, logits, r_out = model.step(0, p, token=123)
+
+    r = synth.bf16_to_f64(E[123])
+    Kb, Vb = [k[0].copy() for k in Ks], [v[0].copy() for v in Vs]
+    for l in range(2):
+        r, _ = oracle.layer(m, lays[l], Kb[l], Vb[l], p, r, variant=vars_[l])
+    t2, logits2 = oracle.head(r, fn, E, m.rms_eps)
+    np.testing.assert_array_equal(r_out, r)
+    np.testing.assert_array_equal(logits, logits2)
+    assert tok == t2
+    for l in range(2):
+        np.testing.assert_array_equal(Ka[l][0], Kb[l])
+    # without variants the model is the plain dense step
+    plain = oracle.Model(m, lays, E, fn, E, [k.copy() for k in Ks], [v.copy() for v in Vs])
+    _, _, r_plain = plain.step(0, p, token=123)
+    r = synth.bf16_to_f64(E[123])
+    Kc, Vc = [k[0].copy() for k in Ks], [v[0].copy() for v in Vs]
+    for l in range(2):
+        r, _ = oracle.layer(m, lays[l], Kc[l], Vc[l], p, r)
+    np.testing.assert_array_equal(r_plain, r)
+    assert not np.array_equal(r_plain, r_out)
