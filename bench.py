@@ -264,7 +264,7 @@ def run_batched(args, world, rank, local):
                    mlp_norm=gam(H), wg=w(I, H), wu=w(I, H), wd=w(H, I)) for _ in range(L)]
     E = w(V, H)
     model = gd.Model(L, H, Hq, Hkv, D, I, V, 1e-6, 1e6, layers, embed=E, final_norm=gam(H), lm_head=E)
-    S_max = max(kv) + steps + max(16, args.warmup) + 8
+    S_max = max(kv) + steps + 16 + args.warmup + 8
     st = gd.State(model, B, S_max, device=dev).init()
     for l in range(L):
         st.k_cache[l].normal_(generator=g)
@@ -275,7 +275,12 @@ def run_batched(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     st.pos.copy_(p0)
     st.token.copy_(t0)
-    gd.dec_decode(model, st, max(16, args.warmup), -1, out)
+    # the first 16-step call captures the decode graph (set-up), then W warm-up steps
+    gd.dec_decode(model, st, 16, -1, torch.empty((B, 16), dtype=torch.int32, device=dev))
+    if args.warmup > 0:
+        st.pos.copy_(p0)
+        st.token.copy_(t0)
+        gd.dec_decode(model, st, args.warmup, -1, torch.empty((B, args.warmup), dtype=torch.int32, device=dev))
     torch.cuda.synchronize(dev)
     st.pos.copy_(p0)
     st.token.copy_(t0)
@@ -292,7 +297,7 @@ def run_batched(args, world, rank, local):
     gbs = (w_bytes + kv_bytes) / (ms / 1e3) / 1e9
     peak, src = peaks()
     res = {"metric": f"greedy decode tok/s at b={B} ({args.workload}); HBM GB/s", "value": round(B / (ms / 1e3), 2),
-           "unit": "tok/s", "n_gpus": 1, "steps": n, "warmup": max(16, args.warmup), "ms_per_step": round(ms, 5),
+           "unit": "tok/s", "n_gpus": 1, "steps": n, "warmup": args.warmup, "ms_per_step": round(ms, 5),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
            "data": "synthetic (seeded torch N(0,0.02) weights, N(0,1) caches)",
            "config": {"workload": args.workload, "batch": B, "layers": L, "kv_lens": kv,
@@ -429,18 +434,22 @@ def run_gpu(args, world, rank, local):
     pos0 = st.pos.clone()
     tok0 = st.token.clone()
 
-    out = torch.empty((B, POSITIONS_PER_PASS), dtype=torch.int32, device=dev)
-
     def restart():
         st.pos.copy_(pos0)
         st.token.copy_(tok0)
 
-    # warm-up: the first call also captures the 16-step graph
+    # set-up: the first 16-step call captures the decode graph (not counted
+    # as warm-up); then exactly W untimed warm-up steps
     t_cap = time.time()
     restart()
-    gd.dec_decode(model, st, max(16, args.warmup), w.eos_id, out)
+    cap_out = torch.empty((B, 16), dtype=torch.int32, device=dev)
+    gd.dec_decode(model, st, 16, w.eos_id, cap_out)
     torch.cuda.synchronize(dev)
-    capture_and_warmup_s = time.time() - t_cap
+    capture_s = time.time() - t_cap
+    if args.warmup > 0:
+        restart()
+        gd.dec_decode(model, st, args.warmup, w.eos_id, torch.empty((B, args.warmup), dtype=torch.int32, device=dev))
+        torch.cuda.synchronize(dev)
 
     # timed: exactly K steps, in passes over the workload's decode positions
     passes = []
@@ -454,18 +463,29 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize(dev)
     executed = 0
     positions = []
+    outs = [torch.empty((B, n), dtype=torch.int32, device=dev) for n in passes]
+    done_per_pass = []
     with ClockSampler(local) as clk:
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(passes))]
         for i, n in enumerate(passes):
             restart()
             ev[2 * i].record(stream)
-            executed += gd.dec_decode(model, st, n, w.eos_id, out)
+            d = gd.dec_decode(model, st, n, w.eos_id, outs[i])
             ev[2 * i + 1].record(stream)
+            executed += d
+            done_per_pass.append(d)
             positions += list(range(int(pos0[0]), int(pos0[0]) + n))
         torch.cuda.synchronize(dev)
     ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(passes)))
     ms = max_over_ranks(ms, world, dev)
-    tokens_out = out.cpu().numpy()
+    # end-of-sequence tokens actually emitted in the executed columns (the
+    # columns after a row's first EOS are padding and not counted)
+    eos_emitted = 0
+    for o, d in zip(outs, done_per_pass):
+        t = o.cpu().numpy()[:, :d]
+        for row in t:
+            hit = np.nonzero(row == w.eos_id)[0]
+            eos_emitted += 1 if hit.size else 0
     assert gd.device_error(clear=True) == 0
 
     w_bytes, kv_bytes = bytes_per_step(m, positions, B)
@@ -501,7 +521,7 @@ def run_gpu(args, world, rank, local):
         "unit": "tok/s",
         "n_gpus": world,
         "steps": executed,
-        "warmup": max(16, args.warmup),
+        "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True,
         "scaling": "weak",
@@ -514,13 +534,14 @@ def run_gpu(args, world, rank, local):
             "accumulate": "fp32", "weights": "bf16", "kv_cache": "bf16", "activations": "fp32",
             "l2": "inputs larger than L2: every step streams 8.0 GB of weights (L2 129 MB)",
             "parallelism": f"replicas x{world} (no collective)",
-            "prefill_ms": round(prefill_ms, 2), "capture_and_warmup_s": round(capture_and_warmup_s, 3),
+            "prefill_ms": round(prefill_ms, 2), "graph_capture_s": round(capture_s, 3),
+            "graph_capture_steps": 16,
             "setup_s": round(setup_s, 2),
             "step_bytes": int(step_bytes), "step_weight_bytes": int(w_bytes),
             "step_hbm_gbs": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
             "step_hbm_frac_of_measured": round(step_bytes / (ms_per_step / 1e3) / 1e9 / peaks()[0], 4),
             "step_hbm_frac_of_8tbs": round(step_bytes / (ms_per_step / 1e3) / 8e12, 4),
-            "eos_hits": int(np.sum(tokens_out == w.eos_id)),
+            "rows_that_emitted_eos": eos_emitted,
         },
         "roofline": roof,
         "glu_alone": glu_alone,

@@ -70,6 +70,7 @@ _SIGNATURES = {
     "dec_state_workspace_size": (_S, [ctypes.POINTER(DecModel), _I, _I]),
     "dec_state_init": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P]),
     "dec_state_release": (_I, [ctypes.POINTER(DecState)]),
+    "dec_state_set_wait": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), ctypes.c_ulonglong, _I, _P]),
     "dec_step": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P]),
     "dec_step_launches": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), ctypes.POINTER(_I)]),
     "dec_prefill": (_I, [ctypes.POINTER(DecModel), ctypes.POINTER(DecState), _P, _I, _P]),
@@ -310,7 +311,28 @@ def dec_prefill(model: Model, state: State, prompt, stream=None):
                              _stream(stream)))
 
 
+def _check_out(out_tokens, state: State, n_steps: int):
+    """out_tokens must hold the packed [B][n_steps] int32 block the library
+    writes (row b at offset b * n_steps): contiguous, at least B * n_steps
+    elements."""
+    if out_tokens is None:
+        return
+    if out_tokens.dtype != _i32 or not out_tokens.is_contiguous():
+        raise DecError(DEC_EINVAL, "out_tokens must be a contiguous int32 tensor")
+    if out_tokens.numel() < state.batch * n_steps:
+        raise DecError(DEC_EINVAL, f"out_tokens holds {out_tokens.numel()} elements; the [B][n_steps] block "
+                                   f"needs {state.batch * n_steps}")
+
+
+def dec_state_set_wait(model: Model, state: State, limit_ns: int = 0, hold: bool = False, stream=None):
+    """Limit (ns, 0 = default) of the step kernel's waits for other CTAs; ``hold``
+    adds a wait nothing ends, to exercise the bounded-wait path."""
+    _check(lib().dec_state_set_wait(ctypes.byref(model.c), ctypes.byref(state.c), int(limit_ns), int(bool(hold)),
+                                    _stream(stream)))
+
+
 def dec_decode(model: Model, state: State, n_steps: int, eos_id: int, out_tokens=None, stream=None) -> int:
+    _check_out(out_tokens, state, n_steps)
     done = ctypes.c_int(0)
     _check(lib().dec_decode(ctypes.byref(model.c), ctypes.byref(state.c), n_steps, eos_id,
                             _ptr(out_tokens, _i32, "out_tokens"), ctypes.byref(done), _stream(stream)))
@@ -318,6 +340,7 @@ def dec_decode(model: Model, state: State, n_steps: int, eos_id: int, out_tokens
 
 
 def dec_generate(model: Model, state: State, prompt, n_steps: int, eos_id: int, out_tokens, stream=None) -> int:
+    _check_out(out_tokens, state, n_steps)
     B, P = prompt.shape
     done = ctypes.c_int(0)
     _check(lib().dec_generate(ctypes.byref(model.c), ctypes.byref(state.c), _ptr(prompt, _i32, "prompt"), P,

@@ -118,6 +118,13 @@ __global__ void ctrl_detach_kernel(Ctrl* c) {
   }
 }
 
+__global__ void set_wait_kernel(Ctrl* c, unsigned long long ns, int hold) {
+  if (threadIdx.x == 0) {
+    c->wait_ns = ns;
+    c->hold = hold;
+  }
+}
+
 __global__ void pad_kernel(int32_t* out, int B, int cap, int from, int value) {
   const int n = cap - from;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * n; i += gridDim.x * blockDim.x) {
@@ -360,6 +367,7 @@ struct StateWs {
   float* attn_part;
   unsigned int* grid_bar;
   int* abort_all;
+  unsigned int* exit_count;
   int n_split;
   // batched prompt pass: rows of up to pf_rows positions (all sequences)
   int pf_rows;
@@ -397,6 +405,7 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   const size_t o_part = c.take(attn_part_bytes(B, m->n_heads, m->n_kv_heads, m->head_dim, w.n_split));
   const size_t o_gbar = c.take(sizeof(unsigned int));
   const size_t o_abort = c.take(sizeof(int));
+  const size_t o_exit = c.take(sizeof(unsigned int));
   const size_t o_kraw = c.take(sizeof(float) * B * m->n_kv_heads * m->head_dim);
   const int pf_pos = std::max(1, kPrefillRows / std::max(1, B));
   w.pf_rows = B * pf_pos;
@@ -425,6 +434,7 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
     w.attn_part = reinterpret_cast<float*>(base + o_part);
     w.grid_bar = reinterpret_cast<unsigned int*>(base + o_gbar);
     w.abort_all = reinterpret_cast<int*>(base + o_abort);
+    w.exit_count = reinterpret_cast<unsigned int*>(base + o_exit);
     w.kraw = reinterpret_cast<float*>(base + o_kraw);
     w.pf_r = reinterpret_cast<float*>(base + o_pf_r);
     w.pf_big = reinterpret_cast<float*>(base + o_pf_big);
@@ -609,6 +619,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   a->book.ctrl = w.ctrl;
   a->grid_bar = w.grid_bar;
   a->abort_all = w.abort_all;
+  a->exit_count = w.exit_count;
   a->err = dv->err;
   for (int i = 0; i < D / 2; ++i) a->inv_freq[i] = std::pow(static_cast<double>(m->rope_theta), -2.0 * i / D);
   for (int l = 0; l < m->n_layers; ++l) {
@@ -1246,6 +1257,18 @@ int dec_state_init(const dec_model* m, dec_state* s, void* stream) {
   return DEC_OK;
 }
 
+int dec_state_set_wait(const dec_model* m, dec_state* s, unsigned long long limit_ns, int hold, void* stream) {
+  DEC_TRY(check_model(m));
+  DEC_TRY(check_state(m, s, false));
+  DeviceInfo* dv;
+  DEC_TRY(device_info(&dv));
+  StateWs w;
+  DEC_TRY(state_views(m, s, dv, &w));
+  DEC_CUDA(launch(set_wait_kernel, dim3(1), dim3(32), 0, static_cast<cudaStream_t>(stream), false, w.ctrl, limit_ns,
+                  hold ? 1 : 0));
+  return DEC_OK;
+}
+
 int dec_state_release(dec_state* s) {
   DEC_CHECK(s != nullptr, DEC_EINVAL, "state is NULL");
   auto* in = static_cast<StateInternal*>(s->internal);
@@ -1392,8 +1415,11 @@ int dec_decode(const dec_model* m, dec_state* s, int n_steps, int eos_id, int32_
     DEC_CUDA(cudaEventRecord(in->ev_out, st));
     DEC_CUDA(cudaStreamWaitEvent(user, in->ev_out, 0));
   }
+  DEC_CUDA(cudaMemcpyAsync(in->pinned_word, dv->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
   DEC_CUDA(cudaStreamSynchronize(st));
   if (steps_done) *steps_done = done;
+  const uint32_t bits = static_cast<uint32_t>(*in->pinned_word);
+  DEC_CHECK(bits == 0, DEC_EDEVICE, "the GPU set error bits 0x%x during the decode loop (see dec_device_error)", bits);
   return DEC_OK;
 }
 

@@ -20,7 +20,7 @@ enum DeviceError : uint32_t {
   kErrTokenRange = 1u << 3,    // a token id outside [0, V) reached the embedding gather
   kErrOutRange = 1u << 4,      // more steps than the output buffer holds
   kErrDrain = 1u << 5,         // copies still in flight after the drain limit
-  kErrGridWait = 1u << 6,      // a grid-wide barrier of the step kernel ran past the limit
+  kErrGridWait = 1u << 6,      // a wait of the step kernel for other CTAs ran past its limit
 };
 
 // Wall-clock limit of any single wait inside a kernel.

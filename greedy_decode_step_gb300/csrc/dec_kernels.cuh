@@ -50,6 +50,8 @@ struct Ctrl {
   int32_t all_done;    // every row has emitted eos_id
   int32_t out_cap;     // columns of out_tokens
   int32_t* out_tokens; // [B][out_cap] or null
+  uint64_t wait_ns;    // limit of one cross-CTA wait of the step kernel (0: kWaitLimitNs)
+  int32_t hold;        // non-zero: the step kernel first waits for this word to clear (nothing clears it)
 };
 
 struct StepBook {

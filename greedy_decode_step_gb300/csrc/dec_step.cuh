@@ -73,6 +73,7 @@ struct StepArgs {
   StepBook book;
   unsigned int* grid_bar;      // sense-reversing grid barrier word (zero at rest)
   int* abort_all;              // raised when any CTA gives up
+  unsigned int* exit_count;    // CTAs that have left this launch (zero at rest)
   uint32_t* err;
   int n_slots;
   uint32_t off_x, off_part, off_attn, off_gamma, off_ring;
@@ -93,7 +94,7 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
 // CTA read the top bit before its first arrival (`sense`) and flips its copy
 // per barrier, so the arrival is a release reduction with no reply to wait
 // for.  Bounded: returns false when the grid aborts.
-__device__ inline bool grid_sync(const StepArgs& a, volatile int* abort_cta, uint32_t& sense) {
+__device__ inline bool grid_sync(const StepArgs& a, volatile int* abort_cta, uint32_t& sense, uint64_t limit) {
   asm volatile("bar.sync 1, 256;" ::: "memory");
   int bad = 0;
   if (threadIdx.x == 0) {
@@ -107,7 +108,7 @@ __device__ inline bool grid_sync(const StepArgs& a, volatile int* abort_cta, uin
           bad = 1;
           break;
         }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
           atomicOr(a.err, kErrGridWait);
           atomicExch(a.abort_all, 1);
           bad = 1;
@@ -261,7 +262,7 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
 // and finishes the same way (partials + last-split merge).
 template <int D>
 __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, const int* pos_s, const float* rope_s,
-                                const unsigned int* tick0, volatile int* abort_cta, int* is_last) {
+                                const unsigned int* tick0, volatile int* abort_cta, int* is_last, uint64_t limit) {
   constexpr int kRowChunks = D / 8;  // 16-byte chunks per cache row
   constexpr int kMaxSlots = attn_slots<D>();
   float* m_run = reinterpret_cast<float*>(area);
@@ -424,7 +425,7 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
             bad = 1;
             break;
           }
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          if (globaltimer_ns() - t0 > limit) {
             atomicOr(a.err, kErrGridWait);
             atomicExch(a.abort_all, 1);
             bad = 1;
@@ -454,6 +455,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   uint64_t* empty = full + kMaxStages;
   volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + 512);
   int* is_last = reinterpret_cast<int*>(smem + 516);
+  uint64_t* limit_s = reinterpret_cast<uint64_t*>(smem + 520);          // limit of a cross-CTA wait (ns)
   float* red = reinterpret_cast<float*>(smem + 576);                      // 8 floats
   float* head_val = reinterpret_cast<float*>(smem + 640);                 // [8][kMaxBatch]
   uint32_t* head_idx = reinterpret_cast<uint32_t*>(smem + 640 + 4 * kConsumerWarps * kMaxBatch);
@@ -478,6 +480,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
       mbar_init(&GR.empty[i], 1);
     }
     *abort_cta = 0;
+    const uint64_t lim = *reinterpret_cast<volatile uint64_t*>(&a.book.ctrl->wait_ns);
+    *limit_s = lim ? lim : kWaitLimitNs;
     fence_mbar_init();
   }
   if (threadIdx.x < a.B) pos_s[threadIdx.x] = a.pos[threadIdx.x];
@@ -516,6 +520,19 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
   int sg = 0, gq = 0;
   uint32_t sense = 0;  // thread 0: top bit of the barrier word before this CTA's first arrival
   if (threadIdx.x == 0) sense = ld_acquire_u32(a.grid_bar) >> 31;
+  const uint64_t limit = *limit_s;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && *reinterpret_cast<volatile int32_t*>(&a.book.ctrl->hold)) {
+    // a hold word that nothing clears: this wait runs out and the grid aborts
+    const uint64_t t0 = globaltimer_ns();
+    while (*reinterpret_cast<volatile int32_t*>(&a.book.ctrl->hold)) {
+      if (globaltimer_ns() - t0 > limit) {
+        atomicOr(a.err, kErrGridWait);
+        atomicExch(a.abort_all, 1);
+        *abort_cta = 1;
+        break;
+      }
+    }
+  }
   // RoPE angles of this step's positions (used by the attention phases; the
   // first phase's prologue barrier publishes them)
   for (int t = threadIdx.x; t < a.B * (a.D / 2); t += kConsumerThreads) {
@@ -552,9 +569,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.v_cache = w.vc;
     ok = consume_phase<kKindQKVRows, BT>(a, kPhQKV, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                      is_last, &GR.empty[gq & 1]) &&
-         grid_sync(a, abort_cta, sense);
+         grid_sync(a, abort_cta, sense, limit);
     if (!ok) break;
-    ok = attention_phase<D>(a, l, attn_area, pos_s, rope_s, tick0, abort_cta, is_last) && grid_sync(a, abort_cta, sense);
+    ok = attention_phase<D>(a, l, attn_area, pos_s, rope_s, tick0, abort_cta, is_last, limit) &&
+         grid_sync(a, abort_cta, sense, limit);
     if (!ok) break;
     // r += Wo o
     io.x = a.o;
@@ -565,7 +583,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.out = a.resid;
     ok = consume_phase<kKindResid, BT>(a, kPhO, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                        is_last) &&
-         grid_sync(a, abort_cta, sense);
+         grid_sync(a, abort_cta, sense, limit);
     if (!ok) break;
     // h = silu(Wg y) * (Wu y), y = norm(r)
     ++gq;
@@ -579,7 +597,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.out = a.h;
     ok = consume_phase<kKindGLU, BT>(a, kPhGLU, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                      is_last, &GR.empty[gq & 1]) &&
-         grid_sync(a, abort_cta, sense);
+         grid_sync(a, abort_cta, sense, limit);
     if (!ok) break;
     // r += Wd h
     io.x = a.h;
@@ -588,7 +606,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
     io.out = a.resid;
     ok = consume_phase<kKindResid, BT>(a, kPhDown, l, io, R, sg, xs, red, part, best_v, best_i, head_val, head_idx,
                                        is_last) &&
-         grid_sync(a, abort_cta, sense);
+         grid_sync(a, abort_cta, sense, limit);
     ++gq;
   }
   if (ok) {
@@ -609,7 +627,25 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
       a.pos[threadIdx.x] += 1;
     }
   }
+  if (!ok && threadIdx.x == 0) *abort_cta = 1;
   asm volatile("bar.sync 2, 288;" ::: "memory");  // the producer may drain and leave
+  if (threadIdx.x == 0) {
+    // the last CTA to leave an aborted launch puts the barrier word and the
+    // counters back to rest, so that the next launch starts clean
+    __threadfence();
+    const unsigned int t = atomicAdd(a.exit_count, 1u);
+    if (t == gridDim.x - 1) {
+      __threadfence();
+      if (*reinterpret_cast<volatile int*>(a.abort_all)) {
+        *a.grid_bar = 0u;
+        *a.head_ticket = 0u;
+        for (int b = 0; b < a.B; ++b) a.argmax_keys[b] = 0ull;
+        *a.abort_all = 0;
+      }
+      *a.exit_count = 0u;
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace dec

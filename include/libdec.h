@@ -62,7 +62,9 @@ const char* dec_version(void);
  * Bits: 1 wait for a copy ran past its limit, 2 wait for a free stage ran past
  * its limit, 4 a position outside [0, S_max), 8 a token id outside [0, V),
  * 16 more steps than the output buffer has columns, 32 copies still in flight
- * at a kernel's exit.  Synchronises the device.
+ * at a kernel's exit, 64 a wait of the persistent step kernel for other CTAs
+ * (its grid barrier, the attention merge) ran past its limit (see
+ * dec_state_set_wait).  Synchronises the device.
  */
 int dec_device_error(uint32_t* bits, int clear);
 
@@ -248,6 +250,23 @@ int dec_state_init(const dec_model* m, dec_state* s, void* stream);
 int dec_state_release(dec_state* s);
 
 /*
+ * Failure handling of the persistent step kernel (the pages' spin-off on a
+ * bounded-spin handshake, quoted in the review thread of #8602, asks that no
+ * wait for another party be unbounded).  Every wait of that kernel for other
+ * CTAs (its grid barrier and the attention merge) gives up after limit_ns
+ * nanoseconds (0: the default, 1.5 s); the CTA then sets error bit 64,
+ * raises a grid-wide abort word that every other CTA reads at its next
+ * wait, and the launch ends without hanging.  hold != 0 adds, at the start
+ * of every later step, a wait for a word that nothing clears -- a host-made
+ * failure that exercises that path on a live GPU without faulting it;
+ * hold = 0 removes it.  The next launch after an aborted one starts clean
+ * (the last CTA to leave resets the barrier and the counters), but the
+ * state's residual and cache slots of the aborted step are undefined.
+ * Stream-ordered.
+ */
+int dec_state_set_wait(const dec_model* m, dec_state* s, unsigned long long limit_ns, int hold, void* stream);
+
+/*
  * One decode step for all B rows: x = embed[token] (or the caller's residual
  * when embed is NULL), the n_layers layers at positions pos[b] (each writes
  * its K/V slot), then -- with an LM head -- final norm, logits, greedy token
@@ -255,8 +274,8 @@ int dec_state_release(dec_state* s);
  * pos[b] <- pos[b] + 1, and the token is written to the decode output buffer
  * set by dec_decode (if any).  Without an LM head only pos advances.
  * B <= 2: one persistent kernel (fp32 activations, bf16 weights streamed by
- * TMA).  B > 2 on an initialised state: the weight GEMVs run as tensor-core
- * GEMMs over the batch (cuBLAS; activations split into hi/lo bf16 parts,
+ * TMA; bounded waits, see dec_state_set_wait).  B > 2 on an initialised
+ * state: the weight GEMVs run as tensor-core GEMMs over the batch (cuBLAS; activations split into hi/lo bf16 parts,
  * fp32 accumulation) around this library's norm, RoPE, attention, SiLU and
  * argmax kernels.
  */
@@ -289,11 +308,15 @@ int dec_prefill(const dec_model* m, dec_state* s, const int32_t* prompt, int P, 
 /*
  * Native decode loop: runs n_steps steps as replays of a captured CUDA graph
  * (16 steps per replay), writing the emitted tokens to out_tokens (device
- * int32 [B][n_steps]); every 16 steps it reads one word from the device and
+ * int32, packed [B][n_steps]: row b starts at element b * n_steps; the caller
+ * owns at least B * n_steps elements -- the call cannot check the size of
+ * device memory, and a smaller buffer is written out of bounds; NULL: no
+ * output); every 16 steps it reads one word from the device and
  * stops once every row has emitted eos_id (-1: never stop).  Tokens after a
  * row's first eos_id are eos_id, and columns past the last executed step are
  * filled with eos_id on the device.  *steps_done (host) receives the number
- * of steps executed.  Blocks until the loop ends.  The caller must ensure
+ * of steps executed.  Blocks until the loop ends; returns DEC_EDEVICE if the
+ * device error word is non-zero then (it is not cleared: dec_device_error).  The caller must ensure
  * pos[b] + n_steps <= S_max.
  */
 int dec_decode(const dec_model* m, dec_state* s, int n_steps, int eos_id, int32_t* out_tokens, int* steps_done,

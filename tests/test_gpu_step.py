@@ -330,3 +330,46 @@ def test_batched_prompt_pass_matches_oracle_cache(case):
             # slots before the prompt and after it are untouched
             assert np.array_equal(kg[b][:, :kv[b]], before_k[l][b][:, :kv[b]])
             assert np.array_equal(kg[b][:, kv[b] + P - 1:], before_k[l][b][:, kv[b] + P - 1:])
+
+
+# ----------------------------------------------------------------------------- bounded waits
+
+def test_step_kernel_wait_runs_out_and_the_next_step_is_clean():
+    """A hold word that nothing clears (dec_state_set_wait) makes the step
+    kernel's first wait for other CTAs run out after 1 ms: error bit 64 is
+    set, the launch ends instead of hanging, and the decode loop reports
+    DEC_EDEVICE.  With the hold removed and the inputs restored, the next
+    step is bit for bit the step of a state that never failed."""
+    m = synth.workload("tiny", n_layers=2).model
+    p = Pair(m, 1, [128], 160)
+    ref = Pair(m, 1, [128], 160)
+    assert gd.dec_step_launches(p.model, p.state) == 1
+    tokens = dev_i32(synth.make_tokens(3, "t", (1,), m.vocab))
+    K0 = [k.clone() for k in p.state.k_cache]
+    V0 = [v.clone() for v in p.state.v_cache]
+    p.state.token.copy_(tokens)
+    gd.dec_state_set_wait(p.model, p.state, 1_000_000, hold=True)
+    gd.dec_step(p.model, p.state)
+    torch.cuda.synchronize()
+    assert gd.device_error(clear=True) & 64
+    # the decode loop reports the error (and its steps also end)
+    out = torch.empty((1, 16), dtype=torch.int32, device="cuda")
+    with pytest.raises(gd.DecError) as exc:
+        gd.dec_decode(p.model, p.state, 16, -1, out)
+    assert exc.value.code == gd.DEC_EDEVICE
+    assert gd.device_error(clear=True) & 64
+    # hold removed, inputs back: the same step as a state that never failed
+    gd.dec_state_set_wait(p.model, p.state, 0, hold=False)
+    for a, b in zip(p.state.k_cache + p.state.v_cache, K0 + V0):
+        a.copy_(b)
+    p.state.pos.fill_(128)
+    p.state.token.copy_(tokens)
+    ref.state.token.copy_(tokens)
+    gd.dec_step(p.model, p.state)
+    gd.dec_step(ref.model, ref.state)
+    torch.cuda.synchronize()
+    assert torch.equal(p.state.residual, ref.state.residual)
+    assert torch.equal(p.state.token, ref.state.token)
+    assert torch.equal(p.state.pos, ref.state.pos)
+    for a, b in zip(p.state.k_cache + p.state.v_cache, ref.state.k_cache + ref.state.v_cache):
+        assert torch.equal(a, b)
