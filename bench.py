@@ -303,7 +303,8 @@ def run_batched(args, world, rank, local):
            "config": {"workload": args.workload, "batch": B, "layers": L, "kv_lens": kv,
                       "step_bytes": int(w_bytes + kv_bytes), "step_hbm_gbs": round(gbs, 1),
                       "step_hbm_frac_of_measured": round(gbs / peak, 4),
-                      "path": "weight GEMMs on tensor cores (cuBLAS, hi/lo bf16 activations), split-K attention"},
+                      "path": "weight GEMMs on this library's tcgen05 tensor-core GEMM (hi/lo bf16 activations "
+                                   "into one fp32 accumulator), split-K attention"},
            "gpu_launches": gd.dec_step_launches(model, st) * n + 2, "clocks": clk.summary()}
     return res, None
 

@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdec.so")
 UNITS = ["api.cu", "gemv_qkv.cu", "gemv_glu.cu", "gemv_resid.cu", "gemv_head.cu", "attn.cu", "step.cu", "prefill.cu",
-         "select.cu"]
+         "select.cu", "tcgemm.cu"]
 HEADERS = ["dec_common.cuh", "dec_kernels.cuh", "dec_attn.cuh", "dec_step.cuh", "dec_launch.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -62,8 +62,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
-        run([nvcc(), ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcublas",
-             "-Xlinker", f"-rpath,{cuda_lib}"])
+        run([nvcc(), ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-Xlinker", f"-rpath,{cuda_lib}"])
         os.replace(tmp, LIB)
     return LIB
 

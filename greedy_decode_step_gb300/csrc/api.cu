@@ -2,13 +2,13 @@
 // and the native decode loop (graph capture + replay, EOS check every 16
 // steps).  Declarations and the contract of every entry point are in
 // include/libdec.h.
-#include <cublas_v2.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <initializer_list>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -165,6 +165,7 @@ int device_info(DeviceInfo** out) {
     DEC_CUDA(allow_smem_head());
     DEC_CUDA(allow_smem_attn());
     DEC_CUDA(allow_smem_step());
+    DEC_CUDA(allow_smem_tcgemm());
     DEC_CUDA(allow_smem_select());
     DEC_CUDA(prefer_max_carveout(add_rmsnorm_kernel));
     DEC_CUDA(prefer_max_carveout(advance_kernel));
@@ -377,14 +378,14 @@ struct StateWs {
   float* pf_o;          // [rows][Hq D] attention output
   uint16_t* pf_bf;      // [rows][max(H, Hq D, I)] bf16 GEMM operand (hi part)
   uint16_t* pf_bf_lo;   // the same, lo part
-  void* pf_blas_ws;     // cuBLAS workspace
-  size_t pf_blas_bytes;
+  float* gemm_part;     // split-K partial sums of the tensor-core GEMM
+  size_t gemm_part_bytes;
   size_t bytes;
 };
 
 // Positions per chunk of the batched prompt pass (times the batch).
 constexpr int kPrefillRows = 512;
-constexpr size_t kBlasWorkspace = 32u << 20;
+constexpr size_t kGemmPartBytes = 32u << 20;
 
 StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char* base) {
   Carve c;
@@ -418,8 +419,8 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   const size_t o_pf_o = c.take(sizeof(float) * R * QD);
   const size_t o_pf_bf = c.take(sizeof(uint16_t) * R * std::max(H, std::max(QD, I)));
   const size_t o_pf_bf_lo = c.take(sizeof(uint16_t) * R * std::max(H, std::max(QD, I)));
-  w.pf_blas_bytes = kBlasWorkspace;
-  const size_t o_pf_ws = c.take(kBlasWorkspace);
+  w.gemm_part_bytes = kGemmPartBytes;
+  const size_t o_pf_ws = c.take(kGemmPartBytes);
   w.bytes = c.off;
   if (base) {
     w.ctrl = reinterpret_cast<Ctrl*>(base + o_ctrl);
@@ -442,14 +443,13 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
     w.pf_o = reinterpret_cast<float*>(base + o_pf_o);
     w.pf_bf = reinterpret_cast<uint16_t*>(base + o_pf_bf);
     w.pf_bf_lo = reinterpret_cast<uint16_t*>(base + o_pf_bf_lo);
-    w.pf_blas_ws = base + o_pf_ws;
+    w.gemm_part = reinterpret_cast<float*>(base + o_pf_ws);
   }
   return w;
 }
 
 struct StateInternal {
   int device = -1;
-  cublasHandle_t blas = nullptr;  // the prompt pass's GEMMs (workspace inside the state's workspace)
   int* pinned_word = nullptr;
   cudaStream_t own_stream = nullptr;
   cudaEvent_t ev_in = nullptr, ev_out = nullptr;
@@ -641,8 +641,8 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
 }
 
 // Layers of one step; with `head`, also the LM head and the bookkeeping.
-int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
-              bool head, cudaStream_t st);
+int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
+              cudaStream_t st);
 
 int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
                  cudaStream_t st) {
@@ -664,8 +664,8 @@ int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, c
     const size_t have = static_cast<size_t>(w.pf_rows) *
                         std::max<size_t>(static_cast<size_t>(m->n_heads + 2 * m->n_kv_heads) * m->head_dim,
                                          2ull * m->intermediate);
-    if (in && in->blas && 2 * s->batch <= w.pf_rows && (!m->lm_head || need <= have))
-      return step_gemm(m, s, dv, w, in->blas, head, st);
+    if (in && 2 * s->batch <= w.pf_rows && (!m->lm_head || need <= have))
+      return step_gemm(m, s, dv, w, head, st);
   }
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
   const bool fuse = norm_fusable(B, H);
@@ -798,20 +798,17 @@ int state_views(const dec_model* m, dec_state* s, const DeviceInfo* dv, StateWs*
 
 // ------------------------------------------------------------------------------- batched prompt pass
 
-// C[rows][N] (leading dimension ldc) = beta * C + Y[rows][K] . W[N][K]^T with
-// bf16 operands and fp32 accumulation and output (cuBLAS is column-major: it
-// computes C^T = W . Y^T).
-// The activation operand comes as hi and lo bf16 parts: C = beta C + W.hi + W.lo.
-int gemm_rows(cublasHandle_t h, const void* W, int N, int K, const uint16_t* Y, const uint16_t* Y_lo, int rows,
-              float* C, int ldc, float beta) {
-  const float alpha = 1.0f, one = 1.0f;
-  for (int part = 0; part < 2; ++part) {
-    const cublasStatus_t bs = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, rows, K, &alpha, W, CUDA_R_16BF, K,
-                                           part == 0 ? Y : Y_lo, CUDA_R_16BF, K, part == 0 ? &beta : &one, C,
-                                           CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS GEMM (%d x %d x %d) failed with status %d", N, rows,
-              K, static_cast<int>(bs));
-  }
+// The weight products of the batched rows on the tensor cores (this
+// library's tcgen05 GEMM): for each segment, C[r][n] (leading dimension ldc)
+// = beta * C + (Y[r] + Y_lo[r]) . W[n] with bf16 operands, fp32 accumulation
+// and output.
+int gemm_rows(const DeviceInfo* dv, const StateWs& w, std::initializer_list<TcSeg> segs, int K, const uint16_t* Y,
+              const uint16_t* Y_lo, int rows, int ldc, float beta, cudaStream_t st) {
+  const char* why = nullptr;
+  const int rc = tc_gemm(segs.begin(), static_cast<int>(segs.size()), Y, Y_lo, rows, K, ldc, beta, w.gemm_part,
+                         w.gemm_part_bytes, dv->sms, dv->err, st, &why);
+  DEC_CHECK(rc == 0, rc == 1 ? DEC_EUNSUPPORTED : DEC_ECUDA, "tensor-core GEMM (%d rows, K %d): %s", rows, K,
+            why ? why : "failed");
   return DEC_OK;
 }
 
@@ -827,13 +824,11 @@ __global__ void prefill_finish_kernel(int32_t* token, int32_t* pos, int B, const
 // chunks of w.pf_rows / B positions (a chunk attends to the cache, which
 // holds every earlier position and its own); then token = prompt[b][P-1] and
 // pos advanced by P-1, as the step-by-step pass leaves them.
-int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
-                    const int32_t* prompt, int P, cudaStream_t st) {
+int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, const StateWs& w, const int32_t* prompt,
+                    int P, cudaStream_t st) {
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
   const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D, WB = std::max(QKV, 2 * I);
   const int per = w.pf_rows / B;
-  const cublasStatus_t bs = cublasSetStream(h, st);
-  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS stream (status %d)", static_cast<int>(bs));
   for (int i0 = 0; i0 < P - 1; i0 += per) {
     const int n = std::min(per, P - 1 - i0);
     const int R = B * n;
@@ -845,9 +840,8 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
       uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
       DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, w.pf_bf,
                                    w.pf_bf_lo, R, st));
-      DEC_TRY(gemm_rows(h, lw.wq, QD, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, QKV, 0.f));
-      DEC_TRY(gemm_rows(h, lw.wk, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD, QKV, 0.f));
-      DEC_TRY(gemm_rows(h, lw.wv, Hkv * D, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + QD + Hkv * D, QKV, 0.f));
+      DEC_TRY(gemm_rows(dv, w, {{lw.wq, QD, w.pf_big}, {lw.wk, Hkv * D, w.pf_big + QD}, {lw.wv, Hkv * D,
+                        w.pf_big + QD + Hkv * D}}, H, w.pf_bf, w.pf_bf_lo, R, QKV, 0.f, st));
       DEC_CUDA(launch_prefill_rope_store(w.pf_big, w.pf_q, s->pos, kc, vc, n, i0, R, Hq, Hkv, D, s->max_seq,
                                          m->rope_theta, dv->err, st));
       AttnArgs t{};
@@ -868,13 +862,13 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
       t.row_pos0 = i0;
       DEC_TRY(run_attn(t, R, dv, st, false));
       DEC_CUDA(launch_prefill_cast(w.pf_o, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R) * QD, dv->sms, st));
-      DEC_TRY(gemm_rows(h, lw.wo, H, QD, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
+      DEC_TRY(gemm_rows(dv, w, {{lw.wo, H, w.pf_r}}, QD, w.pf_bf, w.pf_bf_lo, R, H, 1.f, st));
       DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, w.pf_bf,
                                    w.pf_bf_lo, R, st));
-      DEC_TRY(gemm_rows(h, lw.wg, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big, 2 * I, 0.f));
-      DEC_TRY(gemm_rows(h, lw.wu, I, H, w.pf_bf, w.pf_bf_lo, R, w.pf_big + I, 2 * I, 0.f));
+      DEC_TRY(gemm_rows(dv, w, {{lw.wg, I, w.pf_big}, {lw.wu, I, w.pf_big + I}}, H, w.pf_bf, w.pf_bf_lo, R, 2 * I, 0.f,
+                        st));
       DEC_CUDA(launch_prefill_glu(w.pf_big, I, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R), dv->sms, st));
-      DEC_TRY(gemm_rows(h, lw.wd, H, I, w.pf_bf, w.pf_bf_lo, R, w.pf_r, H, 1.f));
+      DEC_TRY(gemm_rows(dv, w, {{lw.wd, H, w.pf_r}}, I, w.pf_bf, w.pf_bf_lo, R, H, 1.f, st));
     }
   }
   (void)WB;
@@ -882,32 +876,19 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
   return DEC_OK;
 }
 
-// C[rows][N] = Y[rows][K] . W[N][K]^T, one GEMM (bf16 operands, fp32 out).
-int gemm_stacked(cublasHandle_t h, const void* W, int N, int K, const uint16_t* Y, int rows, float* C, int ldc) {
-  const float alpha = 1.0f, beta = 0.0f;
-  const cublasStatus_t bs = cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, rows, K, &alpha, W, CUDA_R_16BF, K, Y,
-                                         CUDA_R_16BF, K, &beta, C, CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F,
-                                         CUBLAS_GEMM_DEFAULT);
-  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS GEMM (%d x %d x %d) failed with status %d", N, rows, K,
-            static_cast<int>(bs));
-  return DEC_OK;
-}
-
 // One decode step for batch > 2 (dec_step semantics): the weight GEMVs run as
-// GEMMs whose rows are the B sequences' activations, split into hi and lo
-// bf16 parts and stacked (2B rows, the weights read once); the kernels after
-// each GEMM add the halves.  Attention is the split-K decode kernel, and the
-// LM head ends in a row argmax and the same bookkeeping as the GEMV path.
-int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, cublasHandle_t h,
-              bool head, cudaStream_t st) {
+// tensor-core GEMMs whose rows are the B sequences' activations (split into
+// hi and lo bf16 parts that accumulate into one fp32 result; the weights are
+// read once), o_proj and down add into the residual in their epilogue.
+// Attention is the split-K decode kernel, and the LM head ends in a row
+// argmax and the same bookkeeping as the GEMV path.
+int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
+              cudaStream_t st) {
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
   const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D;
-  const int B2 = 2 * B;
-  const cublasStatus_t bs = cublasSetStream(h, st);
-  DEC_CHECK(bs == CUBLAS_STATUS_SUCCESS, DEC_ECUDA, "cuBLAS stream (status %d)", static_cast<int>(bs));
   float* r = s->residual;
-  uint16_t* xs = w.pf_bf;   // [2B][K]: hi rows, then lo rows
-  float* c2 = w.pf_big;     // [2B][N] stacked GEMM output
+  uint16_t* xs = w.pf_bf;   // [B][K] hi parts, then [B][K] lo parts
+  float* c2 = w.pf_big;     // [B][N] GEMM output
   if (m->embed) DEC_CUDA(launch_prefill_embed(s->token, 1, 0, 1, B, H, static_cast<const uint16_t*>(m->embed),
                                               m->vocab, r, dv->err, st));
   for (int l = 0; l < m->n_layers; ++l) {
@@ -916,11 +897,10 @@ int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, cons
     uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
     DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, xs,
                                  xs + static_cast<size_t>(B) * H, B, st));
-    DEC_TRY(gemm_stacked(h, lw.wq, QD, H, xs, B2, c2, QKV));
-    DEC_TRY(gemm_stacked(h, lw.wk, Hkv * D, H, xs, B2, c2 + QD, QKV));
-    DEC_TRY(gemm_stacked(h, lw.wv, Hkv * D, H, xs, B2, c2 + QD + Hkv * D, QKV));
+    DEC_TRY(gemm_rows(dv, w, {{lw.wq, QD, c2}, {lw.wk, Hkv * D, c2 + QD}, {lw.wv, Hkv * D, c2 + QD + Hkv * D}}, H, xs,
+                      xs + static_cast<size_t>(B) * H, B, QKV, 0.f, st));
     DEC_CUDA(launch_prefill_rope_store(c2, w.q, s->pos, kc, vc, 1, 0, B, Hq, Hkv, D, s->max_seq, m->rope_theta,
-                                       dv->err, st, B));
+                                       dv->err, st));
     AttnArgs t{};
     t.q = w.q;
     t.k_cache = kc;
@@ -938,20 +918,19 @@ int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, cons
     DEC_TRY(run_attn(t, B, dv, st, false));
     DEC_CUDA(launch_prefill_cast(w.o, xs, xs + static_cast<size_t>(B) * QD, static_cast<size_t>(B) * QD, dv->sms,
                                  st));
-    DEC_TRY(gemm_stacked(h, lw.wo, H, QD, xs, B2, c2, H));
-    DEC_CUDA(launch_rows_resid_add(c2, B, H, r, dv->sms, st));
+    DEC_TRY(gemm_rows(dv, w, {{lw.wo, H, r}}, QD, xs, xs + static_cast<size_t>(B) * QD, B, H, 1.f, st));
     DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, xs,
                                  xs + static_cast<size_t>(B) * H, B, st));
-    DEC_TRY(gemm_stacked(h, lw.wg, I, H, xs, B2, c2, 2 * I));
-    DEC_TRY(gemm_stacked(h, lw.wu, I, H, xs, B2, c2 + I, 2 * I));
-    DEC_CUDA(launch_prefill_glu(c2, I, xs, xs + static_cast<size_t>(B) * I, static_cast<size_t>(B), dv->sms, st, B));
-    DEC_TRY(gemm_stacked(h, lw.wd, H, I, xs, B2, c2, H));
-    DEC_CUDA(launch_rows_resid_add(c2, B, H, r, dv->sms, st));
+    DEC_TRY(gemm_rows(dv, w, {{lw.wg, I, c2}, {lw.wu, I, c2 + I}}, H, xs, xs + static_cast<size_t>(B) * H, B, 2 * I,
+                      0.f, st));
+    DEC_CUDA(launch_prefill_glu(c2, I, xs, xs + static_cast<size_t>(B) * I, static_cast<size_t>(B), dv->sms, st));
+    DEC_TRY(gemm_rows(dv, w, {{lw.wd, H, r}}, I, xs, xs + static_cast<size_t>(B) * I, B, H, 1.f, st));
   }
   if (head && m->lm_head) {
     DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(m->final_norm), m->rms_eps, H, xs,
                                  xs + static_cast<size_t>(B) * H, B, st));
-    DEC_TRY(gemm_stacked(h, m->lm_head, m->vocab, H, xs, B2, c2, m->vocab));
+    DEC_TRY(gemm_rows(dv, w, {{m->lm_head, m->vocab, c2}}, H, xs, xs + static_cast<size_t>(B) * H, B, m->vocab, 0.f,
+                      st));
     DEC_CUDA(launch_rows_argmax(c2, B, m->vocab, w.keys, dv->sms, st));
     GemvIO io{};
     io.B = B;
@@ -1248,12 +1227,6 @@ int dec_state_init(const dec_model* m, dec_state* s, void* stream) {
     dec_state_release(s);
     return fail(DEC_ECUDA, "state set-up: %s", cudaGetErrorString(e));
   }
-  cublasStatus_t bs = cublasCreate(&in->blas);
-  if (bs == CUBLAS_STATUS_SUCCESS) bs = cublasSetWorkspace(in->blas, w.pf_blas_ws, w.pf_blas_bytes);
-  if (bs != CUBLAS_STATUS_SUCCESS) {
-    dec_state_release(s);
-    return fail(DEC_ECUDA, "state set-up: cuBLAS handle (status %d)", static_cast<int>(bs));
-  }
   return DEC_OK;
 }
 
@@ -1273,7 +1246,6 @@ int dec_state_release(dec_state* s) {
   DEC_CHECK(s != nullptr, DEC_EINVAL, "state is NULL");
   auto* in = static_cast<StateInternal*>(s->internal);
   if (!in) return DEC_OK;
-  if (in->blas) cublasDestroy(in->blas);
   if (in->exec) cudaGraphExecDestroy(in->exec);
   if (in->ev_in) cudaEventDestroy(in->ev_in);
   if (in->ev_out) cudaEventDestroy(in->ev_out);
@@ -1310,9 +1282,20 @@ int dec_step_launches(const dec_model* m, const dec_state* s, int* launches) {
     return DEC_OK;
   }
   auto* in = static_cast<StateInternal*>(s->internal);
-  if (in && in->blas && 2 * s->batch <= w.pf_rows) {
-    // the GEMM path: this library's kernels around the cuBLAS GEMMs
-    *launches = (m->embed ? 1 : 0) + 8 * m->n_layers + (m->lm_head ? 3 : 1);
+  if (in && 2 * s->batch <= w.pf_rows) {
+    // the GEMM path: tensor-core GEMMs (with their split-K reductions) and
+    // the elementwise, attention and argmax kernels around them
+    const int B = s->batch, H = m->hidden, QD = m->n_heads * m->head_dim, KV = m->n_kv_heads * m->head_dim;
+    const int I = m->intermediate;
+    const size_t pb = w.gemm_part_bytes;
+    const TcSeg qkv[3] = {{nullptr, QD, nullptr}, {nullptr, KV, nullptr}, {nullptr, KV, nullptr}};
+    const TcSeg o[1] = {{nullptr, H, nullptr}};
+    const TcSeg glu[2] = {{nullptr, I, nullptr}, {nullptr, I, nullptr}};
+    const TcSeg head[1] = {{nullptr, m->vocab, nullptr}};
+    const int per_layer = 6 + tc_gemm_launches(qkv, 3, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, QD, pb, dv->sms) +
+                          tc_gemm_launches(glu, 2, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, I, pb, dv->sms);
+    *launches = (m->embed ? 1 : 0) + m->n_layers * per_layer +
+                (m->lm_head ? 3 + tc_gemm_launches(head, 1, B, H, pb, dv->sms) : 1);
     return DEC_OK;
   }
   const bool fuse = norm_fusable(s->batch, m->hidden);
@@ -1332,7 +1315,7 @@ int dec_prefill(const dec_model* m, dec_state* s, const int32_t* prompt, int P, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int B = s->batch;
   auto* in = static_cast<StateInternal*>(s->internal);
-  if (in && in->blas) return prefill_batched(m, s, dv, w, in->blas, prompt, P, st);
+  if (in) return prefill_batched(m, s, dv, w, prompt, P, st);
   DEC_CUDA(launch(set_tokens_kernel, dim3(1), dim3(32), 0, st, false, s->token, B, prompt, P, 0));
   for (int i = 0; i + 1 < P; ++i) {
     DEC_TRY(enqueue_step(m, s, dv, w, false, st));

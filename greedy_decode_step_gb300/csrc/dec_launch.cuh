@@ -69,10 +69,28 @@ cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int3
 cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st);
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
                                cudaStream_t st, int half_rows = 0);
-// Decode step at batch > 2 on the same GEMM path (halves of stacked GEMMs added).
-cudaError_t launch_rows_resid_add(const float* C, int B, int H, float* r, int sms, cudaStream_t st);
+// Decode step at batch > 2 on the same GEMM path.
 cudaError_t launch_rows_argmax(const float* C, int B, int V, unsigned long long* keys, int sms, cudaStream_t st);
 cudaError_t launch_rows_finish(const GemvIO& io, cudaStream_t st);
+
+// Tensor-core GEMM (tcgemm.cu): for each segment s,
+//   seg.C[r * ldc + n] = beta * seg.C[...] + sum_k seg.W[n][k] * (Yhi[r][k] + Ylo[r][k])
+// for r < rows, n < seg.N.  W bf16 [N][K], Yhi / Ylo bf16 [rows][K] (16-byte
+// aligned rows), C fp32.  `part` holds split-K partials (tc_gemm_part_bytes).
+// Returns 0, 1 (shape refused; *why says why) or 3 (a CUDA error).
+struct TcSeg {
+  const void* W;
+  int N;
+  float* C;
+};
+constexpr int kTcMaxSplits = 16;
+size_t tc_gemm_part_bytes(int rows, int part_cols, int max_splits);
+int tc_gemm(const TcSeg* segs, int n_seg, const uint16_t* Yhi, const uint16_t* Ylo, int rows, int K, int ldc,
+            float beta, float* part, size_t part_bytes, int sms, uint32_t* err, cudaStream_t st, const char** why);
+// Kernel launches one tc_gemm call makes (one: split-K partials are added by
+// the last split of each tile).
+int tc_gemm_launches(const TcSeg* segs, int n_seg, int rows, int K, size_t part_bytes, int sms);
+cudaError_t allow_smem_tcgemm();
 
 // Raise the dynamic shared-memory limit of every kernel of a unit (once per device).
 cudaError_t allow_smem_qkv();

@@ -1,12 +1,12 @@
 // The batched prompt pass: the prompt's positions go through the layers as
-// rows of dense GEMMs (tensor cores, through cuBLAS: bf16 operands, fp32
-// accumulation and output) instead of one decode step per token.  Every fp32
-// activation operand is split into two bf16 parts, hi = bf16(x) and lo =
-// bf16(x - hi), and each GEMM runs on both (W.hi + W.lo), which keeps about
-// 16 bits of the activations -- the decode step's fp32 activations are the
-// reference, and a single bf16 rounding of them moves attention scores far
-// enough to show in the logits.  The
-// elementwise work between the GEMMs -- the embedding gather, RMSNorm,
+// rows of dense GEMMs (this library's tcgen05 tensor-core GEMM, tcgemm.cu:
+// bf16 operands, fp32 accumulation and output) instead of one decode step
+// per token.  Every fp32 activation operand is split into two bf16 parts,
+// hi = bf16(x) and lo = bf16(x - hi), which the GEMM multiplies into the same
+// fp32 accumulator (W.hi + W.lo), keeping about 16 bits of the activations --
+// the decode step's fp32 activations are the reference, and a single bf16
+// rounding of them moves attention scores far enough to show in the logits.
+// The elementwise work between the GEMMs -- the embedding gather, RMSNorm,
 // rotate-half RoPE with the K/V store, SiLU*mul -- and the causal attention
 // (the decode attention kernel with one query row per position) are kernels
 // of this library.  Rows are laid out sequence-major: row r is position
@@ -14,8 +14,7 @@
 // positions starting at i0.
 //
 // The same kernels serve the decode step at batch > 2 (one row per sequence,
-// n = 1): there the hi and lo parts are stacked as 2B rows of ONE GEMM (the
-// weights are read once) and the kernels after it add the two halves.
+// n = 1).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -164,27 +163,18 @@ __global__ void prefill_glu_kernel(const float* gu, int I, uint16_t* h, uint16_t
   }
 }
 
-// r[b] += C[b] + C[B + b] (the two halves of a stacked GEMM).
-__global__ void rows_resid_add_kernel(const float* C, int B, int H, float* r) {
-  const size_t n = static_cast<size_t>(B) * H;
-  for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
-       k += static_cast<size_t>(gridDim.x) * blockDim.x)
-    r[k] += C[k] + C[n + k];
-}
-
-// Greedy argmax of row b of the logits C[b] + C[B + b] over a slice of the
-// vocabulary per CTA (ties to the lower index), folded into keys[b].
-__global__ void rows_argmax_kernel(const float* C, int B, int V, unsigned long long* keys) {
+// Greedy argmax of row b of the logits C[b] over a slice of the vocabulary
+// per CTA (ties to the lower index), folded into keys[b].
+__global__ void rows_argmax_kernel(const float* C, int V, unsigned long long* keys) {
   __shared__ float bv_s[8];
   __shared__ uint32_t bi_s[8];
   const int b = blockIdx.y;
   const int per = (V + gridDim.x - 1) / gridDim.x;
   const int v0 = blockIdx.x * per, v1 = min(V, v0 + per);
-  const float* lo = C + static_cast<size_t>(b) * V;
-  const float* hi = C + static_cast<size_t>(B + b) * V;
+  const float* row = C + static_cast<size_t>(b) * V;
   float bv = -INFINITY;
   uint32_t bi = 0xFFFFFFFFu;
-  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) better(bv, bi, lo[v] + hi[v], static_cast<uint32_t>(v));
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) better(bv, bi, row[v], static_cast<uint32_t>(v));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -253,14 +243,9 @@ cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_
   return cudaGetLastError();
 }
 
-cudaError_t launch_rows_resid_add(const float* C, int B, int H, float* r, int sms, cudaStream_t st) {
-  rows_resid_add_kernel<<<sms, 256, 0, st>>>(C, B, H, r);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_rows_argmax(const float* C, int B, int V, unsigned long long* keys, int sms, cudaStream_t st) {
   const dim3 grid(std::max(1, (sms * 2 + B - 1) / B), B);
-  rows_argmax_kernel<<<grid, 256, 0, st>>>(C, B, V, keys);
+  rows_argmax_kernel<<<grid, 256, 0, st>>>(C, V, keys);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,457 @@
+// Tensor-core GEMM of the batched rows (the decode step at batch > 2 and the
+// batched prompt pass), on the 5th-generation tensor cores:
+//
+//   C[r][n] = beta * C[r][n] + sum_k W[n][k] * (Yhi[r][k] + Ylo[r][k])
+//
+// W: bf16 weights [N][K] (a linear layer's layout); Yhi, Ylo: the hi and lo
+// bf16 parts of fp32 activations [rows][K] (y = hi + lo keeps about 16 bits
+// of each activation); C: fp32.  Both parts are multiplied into the SAME fp32
+// accumulator, so the split costs tensor-core time but no second pass over
+// the weights or the output.
+//
+// One CTA computes a tile of 128 weight rows x BN activation rows over a
+// range of K (split-K when there are too few tiles to fill the GPU):
+//   * warp 0, one lane: TMA copies (cp.async.bulk.tensor, 128-byte swizzle)
+//     of 64-wide K blocks of W, Yhi and Ylo into a ring of shared-memory
+//     stages, tracked by mbarriers;
+//   * warp 1: allocates the accumulator in tensor memory (TMEM) and one lane
+//     issues tcgen05.mma (M = 128, N = BN, K = 16, bf16 in, fp32 out) for
+//     every stage, releasing the stage through tcgen05.commit;
+//   * warps 2-5: wait for the last commit, read the accumulator with
+//     tcgen05.ld (warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. weight
+//     rows) and write C, or this split's partial sums.
+// With split K, the splits of a tile form one thread-block cluster: each
+// keeps its partial in shared memory and adds one slice of the tile over all
+// of them through distributed shared memory, in split order, so the result
+// does not depend on timing.
+//
+// Every wait is bounded (an error bit and an early exit instead of a hang),
+// and the accumulator is released on every path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "dec_launch.cuh"
+
+namespace dec {
+
+namespace {
+
+constexpr int kTcBM = 128;           // weight rows per tile (the MMA's M)
+constexpr int kTcBK = 64;            // K per stage: one 128-byte swizzle row of bf16
+constexpr int kTcThreads = 192;
+constexpr uint32_t kTcATile = kTcBM * kTcBK * 2;   // 16 KB
+constexpr uint32_t kTcSmemMax = 200 * 1024;
+constexpr int kTcMaxStages = 8;
+constexpr int kTcMaxSegs = 3;
+
+struct TcArgs {
+  CUtensorMap wmap[kTcMaxSegs];  // W of each segment: dims {K, N}, box {64, 128}, 128-byte swizzle
+  CUtensorMap yhi, ylo;          // dims {K, rows}, box {64, BN}, 128-byte swizzle
+  float* C[kTcMaxSegs];          // output of each segment: C[r * ldc + n]
+  int N[kTcMaxSegs];
+  int tiles_before[kTcMaxSegs + 1];  // m-tiles of the segments before this one (prefix sums)
+  int n_seg;
+  int rows, K, ldc;
+  int BN, n_tiles, splits, kb_total;
+  float beta;
+  float* part;                   // unused (split partials stay in shared memory)
+  int part_cols;                 // sum of N over the segments
+  int col_off[kTcMaxSegs];
+  int stages;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: next 8-row group
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (K-major),
+// fp32 accumulator, M = 128, N = n.
+__host__ __device__ constexpr uint32_t tc_idesc(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(kTcBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded wait on an mbarrier phase; false after kWaitLimitNs (error bit set).
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, code);
+      return false;
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned base for the swizzled tiles
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kTcMaxStages;
+  uint64_t* accum = empty + kTcMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* stop = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  unsigned char* tiles = smem + 1024;
+  const uint32_t b_tile = static_cast<uint32_t>(a.BN) * kTcBK * 2;
+  const uint32_t stage_bytes = kTcATile + 2 * b_tile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // which tile and K range
+  const int split = blockIdx.x % a.splits;
+  const int tile = blockIdx.x / a.splits;
+  const int nt = tile % a.n_tiles;
+  const int mt_all = tile / a.n_tiles;
+  int seg = 0;
+  while (seg + 1 < a.n_seg && mt_all >= a.tiles_before[seg + 1]) ++seg;
+  const int m0 = (mt_all - a.tiles_before[seg]) * kTcBM;
+  const int r0 = nt * a.BN;
+  const int kb0 = static_cast<int>((static_cast<long long>(split) * a.kb_total) / a.splits);
+  const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * a.kb_total) / a.splits);
+  const int nkb = kb1 - kb0;
+  const uint32_t ncols = a.BN <= 32 ? 32u : (a.BN <= 64 ? 64u : 128u);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *stop = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t wpol = l2_policy_evict_first();
+      const uint64_t ypol = l2_policy_evict_last();
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        if (i >= a.stages && !tc_wait(&empty[s], ((i / a.stages) - 1) & 1, a.err, kErrWaitEmpty)) {
+          *stop = 1;
+          break;
+        }
+        if (*stop) break;
+        unsigned char* st = tiles + static_cast<size_t>(s) * stage_bytes;
+        const int k = (kb0 + i) * kTcBK;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tma_load_2d(st, &a.wmap[seg], k, m0, &full[s], wpol);
+        tma_load_2d(st + kTcATile, &a.yhi, k, r0, &full[s], ypol);
+        tma_load_2d(st + kTcATile + b_tile, &a.ylo, k, r0, &full[s], ypol);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc(a.BN);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        if (!tc_wait(&full[s], (i / a.stages) & 1, a.err, kErrWaitFull)) {
+          *stop = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_addr(tiles + static_cast<size_t>(s) * stage_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(sa + kk * 32);
+          const uint64_t bh = smem_desc_sw128(sa + kTcATile + kk * 32);
+          const uint64_t bl = smem_desc_sw128(sa + kTcATile + b_tile + kk * 32);
+          tc_mma(tmem, ad, bh, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma(tmem, ad, bl, idesc, 1u);
+        }
+        tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+      }
+      tc_commit(accum);  // every MMA issued so far is complete
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue (warps 2-5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    int ok = 1;
+    if (lane == 0) ok = (tc_wait(accum, 0, a.err, kErrWaitFull) && !*stop) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);  // warp-uniform: tcgen05.ld is executed by all 32 lanes together
+    tc_fence_after();
+    const int m = m0 + 32 * q + lane;  // this thread's weight row
+    const bool row_ok = m < a.N[seg];
+    float* pbuf = reinterpret_cast<float*>(tiles);  // [BN][128] this split's partial (the ring is done)
+    if (ok && nkb > 0) {
+      for (int c0 = 0; c0 < a.BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c0), v);
+        if (a.splits > 1) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pbuf[(c0 + j) * kTcBM + 32 * q + lane] = v[j];
+          continue;
+        }
+        if (!row_ok) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = r0 + c0 + j;
+          if (r < a.rows) {
+            float* dst = a.C[seg] + static_cast<size_t>(r) * a.ldc + m;
+            *dst = a.beta != 0.f ? fmaf(a.beta, *dst, v[j]) : v[j];
+          }
+        }
+      }
+    }
+  }
+  if (a.splits > 1) {
+    // The splits of this tile are one cluster: once every CTA's partial is
+    // in its shared memory, each CTA adds one slice of the tile's outputs
+    // over all of them (distributed shared memory, in rank order: the same
+    // sum whatever the timing) and writes C.
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    const int total = a.BN * kTcBM;
+    const int per = (total + a.splits - 1) / a.splits;
+    const int o1 = min(total, (split + 1) * per);
+    const uint32_t local = smem_addr(tiles);
+    for (int o = split * per + static_cast<int>(threadIdx.x); o < o1; o += kTcThreads) {
+      const int c = o / kTcBM, ml = o - c * kTcBM;
+      float sum = 0.f;
+      for (int k = 0; k < a.splits; ++k) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local + 4u * o), "r"(k));
+        float x;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(remote) : "memory");
+        sum += x;
+      }
+      const int r = r0 + c, mm = m0 + ml;
+      if (r < a.rows && mm < a.N[seg]) {
+        float* dst = a.C[seg] + static_cast<size_t>(r) * a.ldc + mm;
+        *dst = a.beta != 0.f ? fmaf(a.beta, *dst, sum) : sum;
+      }
+    }
+    __syncwarp();
+    // no CTA leaves while others may still read its shared memory
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+  }
+}
+
+// ----------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 [outer][inner] row-major, box {64, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t allow_smem_tcgemm() {
+  return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemMax + 1024);
+}
+
+size_t tc_gemm_part_bytes(int, int, int) { return 0; }
+
+namespace {
+
+// Clusters of `size` CTAs with `smem` bytes each that the GPU holds at once
+// (cached; 0 if the query fails).
+int max_active_clusters(int size, uint32_t smem) {
+  static std::mutex mu;
+  static int cache[4][64] = {};
+  const int si = size == 1 ? 0 : size == 2 ? 1 : size == 4 ? 2 : 3;
+  const int mi = static_cast<int>(std::min<uint32_t>(63u, smem / 4096u));
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[si][mi] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(size * 64);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(size);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = -1;
+    }
+    cache[si][mi] = n;
+  }
+  return cache[si][mi];
+}
+
+// K splits (one cluster of CTAs per tile): double while the tiles alone
+// leave SMs idle, every split keeps at least 4 K blocks, and all the
+// clusters are resident at once (one wave); at most 8 (the portable
+// cluster size).
+int tc_splits(int tiles, int kb_total, int sms, uint32_t smem) {
+  int splits = 1;
+  while (splits * 2 <= 8 && tiles * splits * 2 <= sms && kb_total / (splits * 2) >= 4 &&
+         max_active_clusters(splits * 2, smem) >= tiles)
+    splits *= 2;
+  return splits;
+}
+
+}  // namespace
+
+int tc_gemm_launches(const TcSeg*, int, int, int, size_t, int) { return 1; }
+
+int tc_gemm(const TcSeg* segs, int n_seg, const uint16_t* Yhi, const uint16_t* Ylo, int rows, int K, int ldc,
+            float beta, float* part, size_t part_bytes, int sms, uint32_t* err, cudaStream_t st, const char** why) {
+  *why = nullptr;
+  if (n_seg < 1 || n_seg > kTcMaxSegs || rows < 1 || K < 8 || K % 8 != 0) {
+    *why = "shape outside the tensor-core GEMM";
+    return 1;
+  }
+  static thread_local TcArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.BN = std::min(128, (std::min(rows, 128) + 15) / 16 * 16);
+  a.n_tiles = (rows + a.BN - 1) / a.BN;
+  a.rows = rows;
+  a.K = K;
+  a.ldc = ldc;
+  a.beta = beta;
+  a.err = err;
+  a.n_seg = n_seg;
+  a.kb_total = (K + kTcBK - 1) / kTcBK;
+  int m_tiles = 0, cols = 0;
+  for (int s = 0; s < n_seg; ++s) {
+    if (segs[s].N < 1 || (reinterpret_cast<uintptr_t>(segs[s].W) & 15u)) {
+      *why = "weights must be 16-byte aligned with N >= 1";
+      return 1;
+    }
+    a.tiles_before[s] = m_tiles;
+    a.C[s] = segs[s].C;
+    a.N[s] = segs[s].N;
+    a.col_off[s] = cols;
+    cols += segs[s].N;
+    m_tiles += (segs[s].N + kTcBM - 1) / kTcBM;
+    if (!make_map(&a.wmap[s], segs[s].W, K, segs[s].N, kTcBM)) {
+      *why = "tensor map of the weights could not be made";
+      return 1;
+    }
+  }
+  a.tiles_before[n_seg] = m_tiles;
+  if (!make_map(&a.yhi, Yhi, K, rows, a.BN) || !make_map(&a.ylo, Ylo, K, rows, a.BN)) {
+    *why = "tensor map of the activations could not be made";
+    return 1;
+  }
+  const int tiles = m_tiles * a.n_tiles;
+  const uint32_t stage_bytes = kTcATile + 2u * a.BN * kTcBK * 2u;
+  a.stages = std::min<int>(kTcMaxStages, static_cast<int>((kTcSmemMax - 1024) / stage_bytes));
+  const uint32_t smem = 1024 + 1024 + static_cast<uint32_t>(a.stages) * stage_bytes;
+  const int splits = tc_splits(tiles, a.kb_total, sms, smem);
+  a.splits = splits;
+  a.part = part;
+  a.part_cols = cols;
+  (void)part_bytes;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * splits);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a);
+  if (e != cudaSuccess) {
+    *why = cudaGetErrorString(e);
+    return 3;
+  }
+  return 0;
+}
+
+}  // namespace dec

@@ -240,13 +240,13 @@ size_t dec_state_workspace_size(const dec_model* m, int B, int S_max);
 /*
  * Validates model and state, zeroes the workspace (on `stream`) and creates
  * the library-owned part of the state (pinned host word, graph cache, a
- * cuBLAS handle whose workspace lies inside the state's workspace).  Call
+ * workspace of the tensor-core GEMM's split partials).  Call
  * once before dec_step / dec_prefill / dec_decode; the workspace keeps its
  * counters at zero between calls.
  */
 int dec_state_init(const dec_model* m, dec_state* s, void* stream);
 
-/* Frees what dec_state_init created (graphs, pinned word, cuBLAS handle).  Caller memory is untouched. */
+/* Frees what dec_state_init created (graphs, pinned word, stream, events).  Caller memory is untouched. */
 int dec_state_release(dec_state* s);
 
 /*
@@ -275,9 +275,10 @@ int dec_state_set_wait(const dec_model* m, dec_state* s, unsigned long long limi
  * set by dec_decode (if any).  Without an LM head only pos advances.
  * B <= 2: one persistent kernel (fp32 activations, bf16 weights streamed by
  * TMA; bounded waits, see dec_state_set_wait).  B > 2 on an initialised
- * state: the weight GEMVs run as tensor-core GEMMs over the batch (cuBLAS; activations split into hi/lo bf16 parts,
- * fp32 accumulation) around this library's norm, RoPE, attention, SiLU and
- * argmax kernels.
+ * state: the weight GEMVs run as this library's tensor-core GEMMs over the
+ * batch (tcgen05.mma with TMEM accumulators; activations split into hi/lo
+ * bf16 parts that accumulate into one fp32 result, so each weight byte is
+ * read once) around its norm, RoPE, attention, SiLU and argmax kernels.
  */
 int dec_step(const dec_model* m, dec_state* s, void* stream);
 
@@ -285,8 +286,8 @@ int dec_step(const dec_model* m, dec_state* s, void* stream);
  * Number of this library's kernel launches one dec_step (with the LM head)
  * makes for this model and state on the current device: 1 when the whole
  * step runs as the persistent kernel (B <= 2 and the model fits its plan);
- * for B > 2 on an initialised state, the kernels around the step's cuBLAS
- * GEMMs (which are not counted); otherwise the count of single-op launches.
+ * for B > 2 on an initialised state, its GEMM and elementwise kernels;
+ * otherwise the count of single-op launches.
  * Validates like dec_step; launches nothing.
  */
 int dec_step_launches(const dec_model* m, const dec_state* s, int* launches);
@@ -298,8 +299,9 @@ int dec_step_launches(const dec_model* m, const dec_state* s, int* launches);
  * processes the last prompt token.  prompt: device int32 [B][P].  pos must
  * hold the start positions.  On an initialised state the positions run as
  * rows of dense GEMMs (chunks of up to 512 rows over all B sequences) on the
- * tensor cores through cuBLAS: bf16 weights, activations split into two bf16
- * parts (about 16 bits kept), fp32 accumulation; attention per position over
+ * tensor cores (this library's tcgen05 GEMM): bf16 weights, activations split
+ * into two bf16 parts (about 16 bits kept), fp32 accumulation; attention per
+ * position over
  * the cache (causal by construction).  Without dec_state_init it runs one
  * decode step per position instead.  Stream-ordered; asynchronous.
  */
