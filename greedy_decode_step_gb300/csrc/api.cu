@@ -331,14 +331,19 @@ size_t attn_part_bytes(int B, int Hq, int Hkv, int D, int n_split) {
   return static_cast<size_t>(B) * Hkv * n_split * (Hq / Hkv) * (D + 2) * sizeof(float);
 }
 
-uint32_t attn_smem(int D) {
-  return 512u + static_cast<uint32_t>(kAttnMaxGroup * (D + D / 8) * 4 + kAttnMaxGroup * kAttnTile * 4) +
-         static_cast<uint32_t>(kAttnSlots * 2 * kAttnTile * D * 2);
-}
-
+// Tensor maps over the K and V caches of the sequences a launch reads (rows
+// (sequence, KV head, slot), D columns), then the launch.
 int run_attn(AttnArgs& a, int B, const DeviceInfo* dv, cudaStream_t st, bool pdl) {
   a.err = dv->err;
-  cudaError_t e = launch_attn(a, B, attn_smem(a.D), st, pdl);
+  const long long n_seq = a.rows_per_seq ? (B + a.rows_per_seq - 1) / a.rows_per_seq : B;
+  const long long rows = n_seq * a.Hkv * a.S_max;
+  DEC_CHECK(rows + kAttnTile < (1ll << 31), DEC_EUNSUPPORTED, "KV cache of %lld rows: at most 2^31 - %d", rows,
+            kAttnTile);
+  AttnMaps maps;
+  DEC_CHECK(make_tmap_sw128(&maps.k, a.k_cache, a.D, rows, kAttnTile) &&
+                make_tmap_sw128(&maps.v, a.v_cache, a.D, rows, kAttnTile),
+            DEC_ECUDA, "attention: the driver refused a tensor map of the KV cache");
+  cudaError_t e = launch_attn(a, maps, B, st, pdl);
   DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "attention launch: %s", cudaGetErrorString(e));
   return DEC_OK;
 }
@@ -576,7 +581,14 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
   }
   const uint32_t x_bytes = static_cast<uint32_t>(*BT) * H * 4u;
   const uint32_t G = static_cast<uint32_t>(Hq / Hkv);
-  const uint32_t attn_bytes = 256u + G * (D + D / 8u) * 4u + G * kAttnTile * 4u + 2u * kAttnTile * D * 2u;
+  if (G > 8) return false;  // the step kernel's attention takes groups of up to 8 query heads
+  // the GEMV partial-sum area is idle during the attention phase and holds
+  // the staged query fragments there
+  part = std::max<uint32_t>(part, 4u * static_cast<uint32_t>(D == 64 ? attn_qstage_words<64, 1>()
+                                                                     : attn_qstage_words<128, 1>()));
+  const uint32_t attn_bytes =
+      kStepAttnTileOff + std::max(2u * (D == 64 ? attn_tile_bytes<64>() : attn_tile_bytes<128>()),
+                                  D == 64 ? attn_merge_bytes<64>(G) : attn_merge_bytes<128>(G));
   if (H % 8 != 0) return false;  // the norm gains travel as 16-byte bulk copies
   a->off_x = kStepHeaderBytes;
   a->off_part = align_up(a->off_x + x_bytes, 16);

@@ -2,15 +2,21 @@
 //
 // Grid (n_split, Hkv, B).  CTA (s, g, b) takes a contiguous key range of
 // sequence b and streams the K and V rows of KV head g through a shared-memory
-// ring (1-D bulk copies, one producer warp).  All Hq/Hkv query heads of the
-// group read the same K/V tile, so each KV byte leaves HBM once per step.
-// Within the range the softmax is the online form (running max, rescaled
-// sum); ranges are merged by log-sum-exp weights by the last CTA of the
-// group to finish (an atomic ticket; no CTA ever waits for another).
+// ring of 64-key tiles (2-D TMA copies with the 128-byte swizzle, one
+// producer warp).  All Hq/Hkv query heads of the group read the same K/V
+// tile, so each KV byte leaves HBM once per step.  The scores and the
+// probability-weighted sum run on the tensor cores (mma.sync, bf16 operands,
+// fp32 accumulation; query and probabilities as two bf16 parts each), each
+// of the eight consumer warps keeping its own online softmax over its 16
+// keys of every other tile; the warps' states merge at the end of the range,
+// and ranges are merged by log-sum-exp weights by the last CTA of the group
+// to finish (an atomic ticket; no CTA ever waits for another).
 //
 // Keys: the token at position p attends to cache slots 0..p, its own
 // (already stored) slot included.
 #pragma once
+
+#include <cuda.h>
 
 #include "dec_common.cuh"
 
@@ -19,7 +25,13 @@ namespace dec {
 constexpr int kAttnTile = 64;       // keys per stage
 constexpr int kAttnChunkMin = 32;   // fewest keys a split is given
 constexpr int kAttnMaxGroup = 16;   // query heads per KV head
-constexpr int kAttnSlots = 3;
+// Tiles in the ring of attn_kernel.  Even: tile t goes to slot t mod
+// kAttnSlots and to the warps of parity t mod 2, so every slot serves one
+// warp group and a group never waits on a phase the other group still owes
+// (with an odd count the parity of a slot's next phase could be met one
+// phase early).
+constexpr int kAttnSlots = 6;
+static_assert(kAttnSlots % 2 == 0 && kAttnSlots <= 8, "ring slots: even, at most 8");
 constexpr int kAttnMergeBatch = 20;  // splits folded per batch of loads in the merge
 constexpr int kAttnWarps = 8;        // consumer warps
 constexpr int kAttnConsumers = 256;
@@ -41,17 +53,13 @@ struct AttnArgs {
   int row_pos0;
 };
 
-// Queries in shared memory: head h at q_s + h * attn_qstride<D>(), element e
-// at attn_qoff(e).  Every fourth chunk of 8 floats starts 4 floats further
-// on, so the 16 chunks that the lanes of a warp read at once (chunk order
-// rotated by key) fall on each 16-byte bank group exactly twice.
-template <int D>
-__host__ __device__ constexpr int attn_qstride() {
-  return D + D / 8;
-}
-__host__ __device__ __forceinline__ int attn_qoff(int e) { return e + ((e >> 5) << 2); }
+// The K and V caches as 2-D tensors [sequences * Hkv * S_max][D] of bf16
+// (box: 64 columns x kAttnTile rows, 128-byte swizzle).
+struct AttnMaps {
+  CUtensorMap k, v;
+};
 
-// (head, dim-pair) slots per consumer thread for P.V
+// (head, dim-pair) slots per consumer thread of a merged partial
 template <int D>
 __host__ __device__ constexpr int attn_slots() {
   return (kAttnMaxGroup * (D / 2) + kAttnConsumers - 1) / kAttnConsumers;
@@ -65,98 +73,290 @@ __device__ __forceinline__ void attn_plan(int len, int n_split, int* chunk, int*
   *n_active = (len + c - 1) / c;
 }
 
-// One K/V tile of up to kAttnTile keys for the G query heads of a group:
-// scores (one (key, head) per thread per pass, chunk order rotated by key so
-// that the eight lanes of a quarter-warp hit distinct banks), the online
-// softmax update (warp h owns head h) and P.V (thread slot (head, dim pair)).
-// Run by the 256 consumer threads; ends without a barrier (the caller syncs
-// before the tile's shared memory is reused).
+// ----------------------------------------------------------------------------- tensor-core tile math
+// A K or V tile in shared memory holds kAttnTile rows (keys) of D bf16.  The
+// 16-byte chunk c of row r lies at byte attn_swz(r, c): 64-column halves
+// 8 KiB apart, rows 128 bytes apart, chunk index XOR (r mod 8) -- the layout
+// a 2-D TMA copy with a box of 64 x 64 and the 128-byte swizzle writes, so
+// that the eight rows an ldmatrix phase reads fall on distinct banks.
+__host__ __device__ __forceinline__ uint32_t attn_swz(int r, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * (kAttnTile * 128) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+}
 template <int D>
-__device__ __forceinline__ void attn_tile_math(const uint4* Ks, const uint32_t* Vs, int nk, int G, float scale,
-                                               const float* q_s, float* s_s, float* m_run, float* l_run, float* corr,
-                                               float (&acc0)[attn_slots<D>()], float (&acc1)[attn_slots<D>()]) {
-  constexpr int kChunks = D / 8;
-  constexpr int kPairsPerHead = D / 2;
-  constexpr int kMaxSlots = attn_slots<D>();
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_pairs = G * kPairsPerHead;
-    // scores: one (key, head) per thread per pass; chunk order rotated by key
-    // so that the eight lanes of a quarter-warp hit distinct banks
-    for (int idx = tid; idx < G * kAttnTile; idx += kAttnConsumers) {
-      const int h = idx / kAttnTile, j = idx - h * kAttnTile;
-      float sc = -INFINITY;
-      if (j < nk) {
-        const uint4* kr = Ks + j * kChunks;
-        const float* qh = q_s + h * attn_qstride<D>();
-        float accs = 0.f;
-#pragma unroll 4
-        for (int cc = 0; cc < kChunks; ++cc) {
-          const int c = (cc + j) & (kChunks - 1);
-          const uint4 w = kr[c];
-          const float4 q0 = reinterpret_cast<const float4*>(qh + attn_qoff(8 * c))[0];
-          const float4 q1 = reinterpret_cast<const float4*>(qh + attn_qoff(8 * c))[1];
-          accs = fmaf(bf16lo(w.x), q0.x, accs);
-          accs = fmaf(bf16hi(w.x), q0.y, accs);
-          accs = fmaf(bf16lo(w.y), q0.z, accs);
-          accs = fmaf(bf16hi(w.y), q0.w, accs);
-          accs = fmaf(bf16lo(w.z), q1.x, accs);
-          accs = fmaf(bf16hi(w.z), q1.y, accs);
-          accs = fmaf(bf16lo(w.w), q1.z, accs);
-          accs = fmaf(bf16hi(w.w), q1.w, accs);
-        }
-        sc = accs * scale;
-      }
-      s_s[h * kAttnTile + j] = sc;
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    // running max / sum per head (warp h)
-    for (int h = warp; h < G; h += kAttnWarps) {
-      float* sh = s_s + h * kAttnTile;
-      const float v0 = sh[lane], v1 = sh[lane + 32];
-      const float tmax = warp_max(fmaxf(v0, v1));
-      const float m_old = m_run[h];
-      const float m_new = fmaxf(m_old, tmax);
-      const float e0 = (lane < nk) ? expf(v0 - m_new) : 0.f;
-      const float e1 = (lane + 32 < nk) ? expf(v1 - m_new) : 0.f;
-      sh[lane] = e0;
-      sh[lane + 32] = e1;
-      const float tsum = warp_sum(e0 + e1);
-      if (lane == 0) {
-        const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
-        corr[h] = c;
-        l_run[h] = l_run[h] * c + tsum;
-        m_run[h] = m_new;
-      }
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    // P.V: thread slot (head h, dims 2dp, 2dp+1); keys in fours into two
-    // accumulator pairs (even and odd keys), then the rescaled old value
+__host__ __device__ constexpr uint32_t attn_tile_bytes() {
+  return static_cast<uint32_t>(kAttnTile) * D * 2u;
+}
+
+// Bytes of the per-warp accumulators merged at the end of a split:
+// [kAttnWarps][G][D + 4] floats.
+template <int D>
+__host__ __device__ constexpr uint32_t attn_merge_bytes(int G) {
+  return static_cast<uint32_t>(kAttnWarps) * G * (D + 4) * 4u;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// 8x8 bf16 transpose across the warp (fragment of row lane/4 -> of column lane/4)
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (x0, x1) -> bf16x2 nearest (x0 in the low half) and the bf16x2 of the remainders
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t* hi, uint32_t* lo) {
+  uint32_t h, l;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+  const float r0 = x0 - __uint_as_float(h << 16), r1 = x1 - __uint_as_float(h & 0xFFFF0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l) : "f"(r1), "f"(r0));
+  *hi = h;
+  *lo = l;
+}
+
+// The group's queries as MMA B fragments (K = dims, N = heads): for the heads
+// 8nt..8nt+7 and the dims 16ks..16ks+15, lane (g = lane/4, c = lane%4) holds
+// head 8nt+g's dims 16ks+2c, +1 (slot 0) and 16ks+8+2c, +1 (slot 1), each
+// value split into a bf16 part and the bf16 of its remainder (about 16
+// significant bits between them; the K/V operands are exact bf16).
+template <int D, int NT>
+struct AttnQFrag {
+  uint32_t hi[NT][D / 16][2], lo[NT][D / 16][2];
+  __device__ __forceinline__ void get(int nt, int ks, int j, uint32_t& h, uint32_t& l) const {
+    h = hi[nt][ks][j];
+    l = lo[nt][ks][j];
+  }
+};
+
+// The same fragments staged in shared memory (where registers are short):
+// word ((nt * D/16 + ks) * 2 + j) * 32 + lane holds the bf16 parts, the
+// remainders follow after attn_qstage_words<D, NT>() / 2 words.
+template <int D, int NT>
+__host__ __device__ constexpr int attn_qstage_words() {
+  return 2 * NT * (D / 16) * 2 * 32;
+}
+template <int D, int NT>
+struct AttnQStaged {
+  const uint32_t* w;
+  __device__ __forceinline__ void get(int nt, int ks, int j, uint32_t& h, uint32_t& l) const {
+    const int i = ((nt * (D / 16) + ks) * 2 + j) * 32 + (threadIdx.x & 31);
+    h = w[i];
+    l = w[i + attn_qstage_words<D, NT>() / 2];
+  }
+};
+
+// One warp's share of a split: the online-softmax state of its keys.  Lane
+// (g, c) holds, for the heads 8nt+2c and 8nt+2c+1, the running maxima (equal
+// across the 8 lanes of a column), partial sums of its own keys, and the
+// accumulator O^T (dims x heads) as MMA C fragments: o[nt][mt] rows
+// 16mt+g, 16mt+g+8, columns (heads) 2c, 2c+1.
+template <int D, int NT>
+struct AttnWarpState {
+  float o[NT][D / 16][4];
+  float m[NT][2];
+  float l[NT][2];
+};
+
+template <int D, int NT>
+__device__ __forceinline__ void attn_state_init(AttnWarpState<D, NT>& st) {
 #pragma unroll
-    for (int i = 0; i < kMaxSlots; ++i) {
-      const int pr = tid + i * kAttnConsumers;
-      if (pr < n_pairs) {
-        const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
-        const float c = corr[h];
-        const float* ph = s_s + h * kAttnTile;
-        float2 e = make_float2(0.f, 0.f), o = e;
-        int j = 0;
-        for (; j + 4 <= nk; j += 4) {
-          const uint32_t v0 = Vs[(j + 0) * kPairsPerHead + dp], v1 = Vs[(j + 1) * kPairsPerHead + dp];
-          const uint32_t v2 = Vs[(j + 2) * kPairsPerHead + dp], v3 = Vs[(j + 3) * kPairsPerHead + dp];
-          const float4 pj = *reinterpret_cast<const float4*>(ph + j);
-          e = __ffma2_rn(make_float2(pj.x, pj.x), make_float2(bf16lo(v0), bf16hi(v0)), e);
-          o = __ffma2_rn(make_float2(pj.y, pj.y), make_float2(bf16lo(v1), bf16hi(v1)), o);
-          e = __ffma2_rn(make_float2(pj.z, pj.z), make_float2(bf16lo(v2), bf16hi(v2)), e);
-          o = __ffma2_rn(make_float2(pj.w, pj.w), make_float2(bf16lo(v3), bf16hi(v3)), o);
-        }
-        for (; j < nk; ++j) {
-          const uint32_t v = Vs[j * kPairsPerHead + dp];
-          e = __ffma2_rn(make_float2(ph[j], ph[j]), make_float2(bf16lo(v), bf16hi(v)), e);
-        }
-        acc0[i] = fmaf(acc0[i], c, e.x + o.x);
-        acc1[i] = fmaf(acc1[i], c, e.y + o.y);
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) st.o[nt][mt][0] = st.o[nt][mt][1] = st.o[nt][mt][2] = st.o[nt][mt][3] = 0.f;
+    st.m[nt][0] = st.m[nt][1] = -INFINITY;
+    st.l[nt][0] = st.l[nt][1] = 0.f;
+  }
+}
+
+// Keys of a tile owned by warp w: rows 16 (w mod 4) .. +15 of the tiles whose
+// index within the split has parity w / 4 (two tiles are in work at once).
+__device__ __forceinline__ int attn_warp_row0(int warp) { return 16 * (warp & 3); }
+__device__ __forceinline__ int attn_warp_parity(int warp) { return warp >> 2; }
+// whether warp w owns any of a split's `len` keys (its first tile's rows)
+__device__ __forceinline__ bool attn_warp_has_keys(int warp, int len) {
+  return kAttnTile * attn_warp_parity(warp) + attn_warp_row0(warp) < len;
+}
+
+// One warp, its 16 keys (tile rows r0..r0+15, of which rows < nk are valid;
+// r0 < nk) of one K/V tile.  S^T = K Q^T on the tensor cores (keys as M, heads
+// as N, the query's two bf16 parts into separate accumulators), the online
+// softmax per head, then O^T += V^T P^T with P^T transposed in registers
+// (movmatrix) and split like the query.  V rows past nk are zeroed first (a
+// zero probability times a stale row must not make NaN); returns whether it
+// wrote to the tile.  No block-level barrier inside.
+template <int D, int NT, typename QSrc>
+__device__ __forceinline__ bool attn_warp_tile(const unsigned char* Kt, unsigned char* Vt, int r0, int nk, float scale,
+                                               const QSrc& q, AttnWarpState<D, NT>& st) {
+  constexpr int kChunks = D / 8;
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  bool wrote = false;
+  if (nk < r0 + 16) {
+    for (int i = lane; i < 16 * kChunks; i += 32) {
+      const int r = r0 + i / kChunks;
+      if (r >= nk) *reinterpret_cast<uint4*>(Vt + attn_swz(r, i % kChunks)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+    wrote = true;
+  }
+  // scores
+  float sh[NT][4], sl[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
+  const uint32_t kb = smem_addr(Kt), vb = smem_addr(Vt);
+  const int qrow = r0 + (lane & 15), qchunk = lane >> 4;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(a, kb + attn_swz(qrow, 2 * ks + qchunk));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint32_t h0, l0, h1, l1;
+      q.get(nt, ks, 0, h0, l0);
+      q.get(nt, ks, 1, h1, l1);
+      mma_bf16_16816(sh[nt], a, h0, h1);
+      mma_bf16_16816(sl[nt], a, l0, l1);
+    }
+  }
+  const bool v0 = r0 + g < nk, v1 = r0 + g + 8 < nk;
+  uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float s[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] = (sh[nt][e] + sl[nt][e]) * scale;
+    if (!v0) s[0] = s[1] = -INFINITY;
+    if (!v1) s[2] = s[3] = -INFINITY;
+    float p[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float mx = fmaxf(s[j], s[j + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(st.m[nt][j], mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float corr = expf(st.m[nt][j] - m_use);
+      p[j] = expf(s[j] - m_use);
+      p[j + 2] = expf(s[j + 2] - m_use);
+      st.l[nt][j] = fmaf(st.l[nt][j], corr, p[j] + p[j + 2]);
+      st.m[nt][j] = m_new;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        st.o[nt][mt][j] *= corr;
+        st.o[nt][mt][j + 2] *= corr;
       }
     }
+    uint32_t h0, l0, h1, l1;
+    split_bf16x2(p[0], p[1], &h0, &l0);  // keys g: heads 2c, 2c+1
+    split_bf16x2(p[2], p[3], &h1, &l1);  // keys g+8
+    bh[nt][0] = movmatrix_trans(h0);
+    bh[nt][1] = movmatrix_trans(h1);
+    bl[nt][0] = movmatrix_trans(l0);
+    bl[nt][1] = movmatrix_trans(l1);
+  }
+  // O^T += V^T P^T
+  const int vrow = r0 + (lane & 7) + ((lane >> 4) << 3), vchunk = (lane >> 3) & 1;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    uint32_t a[4];
+    ldsm_x4_trans(a, vb + attn_swz(vrow, 2 * mt + vchunk));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_bf16_16816(st.o[nt][mt], a, bh[nt][0], bh[nt][1]);
+      mma_bf16_16816(st.o[nt][mt], a, bl[nt][0], bl[nt][1]);
+    }
+  }
+  return wrote;
+}
+
+// End of a split: the eight warps' states merged into one partial in the
+// (head, dim-pair) slot layout of attn_finish (acc0 / acc1 per slot, maxima
+// and sums in m_run / l_run):  M = max_w m_w, acc = sum_w e^(m_w - M) O_w,
+// l = sum_w e^(m_w - M) l_w, summed in warp order.  `ms`, `ls` hold
+// [kAttnWarps][16] floats, `obuf` attn_merge_bytes<D>(G) bytes (it may alias
+// the tiles: the caller has synchronised the consumers after the last tile).
+// Warps that own none of the split's `len` keys hold nothing and are skipped
+// (their terms would be exact zeros).  Ends with a barrier of the 256
+// consumer threads.
+template <int D, int NT>
+__device__ __forceinline__ void attn_merge_warps(AttnWarpState<D, NT>& st, int G, int len, float* ms, float* ls,
+                                                 float* obuf,
+                                                 float (&acc0)[attn_slots<D>()], float (&acc1)[attn_slots<D>()],
+                                                 float* m_run, float* l_run) {
+  constexpr int kStride = D + 4;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  const bool mine = attn_warp_has_keys(warp, len);
+#pragma unroll
+  for (int nt = 0; nt < NT && mine; ++nt) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float l = st.l[nt][j];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      if (g == 0) {
+        ms[warp * 16 + 8 * nt + 2 * c + j] = st.m[nt][j];
+        ls[warp * 16 + 8 * nt + 2 * c + j] = l;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = 8 * nt + 2 * c + (e & 1), d = 16 * mt + g + ((e >> 1) << 3);
+        if (h < G) obuf[(warp * G + h) * kStride + d] = st.o[nt][mt][e];
+      }
+    }
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  constexpr int kPairsPerHead = D / 2;
+#pragma unroll
+  for (int i = 0; i < attn_slots<D>(); ++i) {
+    const int pr = tid + i * kAttnConsumers;
+    if (pr < G * kPairsPerHead) {
+      const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w)
+        if (attn_warp_has_keys(w, len)) M = fmaxf(M, ms[w * 16 + h]);
+      float n0 = 0.f, n1 = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        if (!attn_warp_has_keys(w, len)) continue;
+        const float mw = ms[w * 16 + h];
+        const float f = (mw == -INFINITY) ? 0.f : expf(mw - M);
+        const float2 ov = *reinterpret_cast<const float2*>(obuf + (w * G + h) * kStride + 2 * dp);
+        L = fmaf(f, ls[w * 16 + h], L);
+        n0 = fmaf(f, ov.x, n0);
+        n1 = fmaf(f, ov.y, n1);
+      }
+      acc0[i] = n0;
+      acc1[i] = n1;
+      if (dp == 0) {
+        m_run[h] = M;
+        l_run[h] = L;
+      }
+    }
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
 // One merged output o[h][d] of a (row, KV head) from its n_active split
@@ -271,21 +471,55 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
   if (tid == 0) atomicExch(ticket, 0u);
 }
 
+// The group's query fragments from the rotated fp32 queries (head h at
+// qg + h * D; heads G.. of the last n-tile are zero).
+template <int D, int NT>
+__device__ __forceinline__ void attn_q_load(AttnQFrag<D, NT>& f, const float* qg, int G) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = 8 * nt + g;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float2 x = make_float2(0.f, 0.f);
+        if (h < G) x = __ldcg(reinterpret_cast<const float2*>(qg + h * D + 16 * ks + 8 * j + 2 * c));
+        split_bf16x2(x.x, x.y, &f.hi[nt][ks][j], &f.lo[nt][ks][j]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory layout of attn_kernel (from a 1024-byte aligned base): full
+// barriers at 0, empty barriers at 64, flags at 128, m_run / l_run [16] at
+// 256, per-warp maxima / sums [8][16] at 512 / 1024, the tile ring at 2048
+// (slot = K tile then V tile).
+constexpr uint32_t kAttnRingOff = 2048;
 template <int D>
-__global__ void __launch_bounds__(288, 2) attn_kernel(const __grid_constant__ AttnArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__host__ __device__ constexpr uint32_t attn_kernel_smem() {
+  return 1024u + kAttnRingOff + kAttnSlots * 2u * attn_tile_bytes<D>();
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(288, NT == 1 ? 2 : 1)
+    attn_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ AttnMaps mp) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kAttnSlots;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 64);
-  int* is_last = reinterpret_cast<int*>(smem + 68);
-  float* m_run = reinterpret_cast<float*>(smem + 128);                 // [G]
-  float* l_run = m_run + kAttnMaxGroup;                                 // [G]
-  float* corr = l_run + kAttnMaxGroup;                                  // [G]
-  float* q_s = reinterpret_cast<float*>(smem + 512);                    // [G][attn_qstride]
-  float* s_s = q_s + kAttnMaxGroup * attn_qstride<D>();                 // [G][kAttnTile]
-  unsigned char* ring = reinterpret_cast<unsigned char*>(s_s + kAttnMaxGroup * kAttnTile);
-  constexpr uint32_t kRowBytes = D * 2;
-  constexpr uint32_t kTileBytes = kAttnTile * kRowBytes;   // one of K or V
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 128);
+  int* is_last = reinterpret_cast<int*>(smem + 132);
+  float* m_run = reinterpret_cast<float*>(smem + 256);  // [16]
+  float* l_run = m_run + kAttnMaxGroup;                 // [16]
+  float* ms = reinterpret_cast<float*>(smem + 512);     // [8][16]
+  float* ls = reinterpret_cast<float*>(smem + 1024);    // [8][16]
+  unsigned char* ring = smem + kAttnRingOff;
+  constexpr uint32_t kTileBytes = attn_tile_bytes<D>();
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv;
@@ -294,15 +528,6 @@ __global__ void __launch_bounds__(288, 2) attn_kernel(const __grid_constant__ At
   pdl_wait();
   pdl_launch_dependents();
 
-  // the group's query vectors (independent of the key plan) are fetched while
-  // the position is read
-  constexpr int kQPerThread = (kAttnMaxGroup * D + 287) / 288;
-  float qv[kQPerThread];
-#pragma unroll
-  for (int j = 0; j < kQPerThread; ++j) {
-    const int i = threadIdx.x + j * 288;
-    qv[j] = i < G * D ? a.q[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D + i] : 0.f;
-  }
   const int seq = a.rows_per_seq ? b / a.rows_per_seq : b;
   const int p = a.rows_per_seq ? a.pos[seq] + a.row_pos0 + b % a.rows_per_seq : a.pos[b];
   if (p < 0 || p >= a.S_max) {
@@ -316,55 +541,50 @@ __global__ void __launch_bounds__(288, 2) attn_kernel(const __grid_constant__ At
   const int k0 = split * chunk;
   const int k1 = min(len, k0 + chunk);
   const int n_tiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
-
-  const size_t head_off = (static_cast<size_t>(seq) * a.Hkv + g) * a.S_max;
-  const uint16_t* Kg = a.k_cache + head_off * D;
-  const uint16_t* Vg = a.v_cache + head_off * D;
+  const int row0 = (seq * a.Hkv + g) * a.S_max + k0;  // first tensor-map row of the split
 
   // the producer lane sets up the barriers and issues the first tiles at once
   int issued = 0;
   uint64_t policy = 0;
-  if (warp == 8 && lane == 0) {
+  if (warp == kAttnWarps && lane == 0) {
     for (int i = 0; i < kAttnSlots; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kAttnWarps);
+      mbar_init(&empty[i], kAttnWarps / 2);
     }
     *abort_flag = 0;
     fence_mbar_init();
-    policy = l2_policy_evict_last();
+    policy = a.rows_per_seq ? l2_policy_evict_last() : l2_policy_evict_first();
     for (int t = 0; t < min(n_tiles, kAttnSlots); ++t) {
-      const int j0 = k0 + t * kAttnTile;
-      const int nk = min(kAttnTile, k1 - j0);
       unsigned char* dst = ring + static_cast<size_t>(t) * 2 * kTileBytes;
-      mbar_arrive_expect_tx(&full[t], 2u * nk * kRowBytes);
-      bulk_copy_g2s(dst, Kg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[t], policy);
-      bulk_copy_g2s(dst + kTileBytes, Vg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[t], policy);
+      mbar_arrive_expect_tx(&full[t], 2u * kTileBytes);
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_2d(dst + h * (kAttnTile * 128), &mp.k, 64 * h, row0 + t * kAttnTile, &full[t], policy);
+        tma_load_2d(dst + kTileBytes + h * (kAttnTile * 128), &mp.v, 64 * h, row0 + t * kAttnTile, &full[t], policy);
+      }
       issued = t + 1;
     }
   }
-#pragma unroll
-  for (int j = 0; j < kQPerThread; ++j) {
-    const int i = threadIdx.x + j * 288;
-    if (i < G * D) q_s[(i / D) * attn_qstride<D>() + attn_qoff(i % D)] = qv[j];
-  }
-  if (threadIdx.x < G) {
-    m_run[threadIdx.x] = -INFINITY;
-    l_run[threadIdx.x] = 0.f;
-  }
+  // the group's query fragments (consumers) while the first tiles land
+  AttnQFrag<D, NT> qf;
+  if (warp < kAttnWarps)
+    attn_q_load<D, NT>(qf, a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D, G);
   __syncthreads();
 
-  if (warp == 8) {
+  if (warp == kAttnWarps) {
     // ----------------------------------------------------------- producer warp
     if (lane == 0) {
       for (int t = issued; t < n_tiles; ++t) {
         const int slot = t % kAttnSlots;
         if (!mbar_wait(&empty[slot], ((t / kAttnSlots) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
-        const int j0 = k0 + t * kAttnTile;
-        const int nk = min(kAttnTile, k1 - j0);
         unsigned char* dst = ring + static_cast<size_t>(slot) * 2 * kTileBytes;
-        mbar_arrive_expect_tx(&full[slot], 2u * nk * kRowBytes);
-        bulk_copy_g2s(dst, Kg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[slot], policy);
-        bulk_copy_g2s(dst + kTileBytes, Vg + static_cast<size_t>(j0) * D, nk * kRowBytes, &full[slot], policy);
+        mbar_arrive_expect_tx(&full[slot], 2u * kTileBytes);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_2d(dst + h * (kAttnTile * 128), &mp.k, 64 * h, row0 + t * kAttnTile, &full[slot], policy);
+          tma_load_2d(dst + kTileBytes + h * (kAttnTile * 128), &mp.v, 64 * h, row0 + t * kAttnTile, &full[slot],
+                      policy);
+        }
         issued = t + 1;
       }
     }
@@ -385,35 +605,30 @@ __global__ void __launch_bounds__(288, 2) attn_kernel(const __grid_constant__ At
   }
 
   // ------------------------------------------------------------- consumer warps
-  constexpr int kMaxSlots = attn_slots<D>();
-  float acc0[kMaxSlots], acc1[kMaxSlots];
-#pragma unroll
-  for (int i = 0; i < kMaxSlots; ++i) acc0[i] = acc1[i] = 0.f;
-
-  bool ok = true;
-  for (int t = 0; t < n_tiles; ++t) {
+  // warps 4 * parity .. +3 take the tiles of that parity, 16 keys each
+  AttnWarpState<D, NT> st;
+  attn_state_init<D, NT>(st);
+  const int r0 = attn_warp_row0(warp);
+  for (int t = attn_warp_parity(warp); t < n_tiles; t += 2) {
     const int slot = t % kAttnSlots;
-    const int nk = min(kAttnTile, k1 - (k0 + t * kAttnTile));
     int w_ok = 1;
     if (lane == 0) w_ok = mbar_wait(&full[slot], (t / kAttnSlots) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
     w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-    if (w_ok) (void)mbar_try_wait(&full[slot], (t / kAttnSlots) & 1);  // completed phase: acquire for every lane
-    // every consumer warp passes this barrier and gets the same verdict, so
-    // all warps leave together (none is left behind at a later barrier)
-    if (consumers_barrier_or(!w_ok)) {
-      ok = false;
-      break;
-    }
-    const uint4* Ks = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * 2 * kTileBytes);
-    const uint32_t* Vs = reinterpret_cast<const uint32_t*>(ring + static_cast<size_t>(slot) * 2 * kTileBytes +
-                                                           kTileBytes);
-    attn_tile_math<D>(Ks, Vs, nk, G, a.scale, q_s, s_s, m_run, l_run, corr, acc0, acc1);
+    if (!w_ok) break;
+    (void)mbar_try_wait(&full[slot], (t / kAttnSlots) & 1);  // completed phase: acquire for every lane
+    const int nk = min(kAttnTile, k1 - (k0 + t * kAttnTile));
+    unsigned char* Kt = ring + static_cast<size_t>(slot) * 2 * kTileBytes;
+    if (r0 < nk && attn_warp_tile<D, NT>(Kt, Kt + kTileBytes, r0, nk, a.scale, qf, st)) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
   }
+  // every wait that gave up raised the abort flag before this barrier
   asm volatile("bar.sync 2, 288;" ::: "memory");
-  if (!ok) return;
+  if (*abort_flag) return;
 
+  constexpr int kMaxSlots = attn_slots<D>();
+  float acc0[kMaxSlots], acc1[kMaxSlots];
+  attn_merge_warps<D, NT>(st, G, k1 - k0, ms, ls, reinterpret_cast<float*>(ring), acc0, acc1, m_run, l_run);
   attn_finish<D>(a, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last);
 }
 

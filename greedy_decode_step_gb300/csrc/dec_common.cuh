@@ -132,6 +132,18 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 2-D tensor copy global -> shared of the box at (x, y) of a tensor map (a
+// kernel parameter), completing its bytes on `bar`.  x * element size must
+// be a multiple of 16 bytes; y may run past the tensor (zero fill).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // ----------------------------------------------------------------------------- programmatic dependent launch
 // Block until the grids this one depends on have completed and their writes
 // are visible.  A no-op when the launch carries no programmatic dependency.

@@ -1,6 +1,7 @@
 // Launch helpers shared by the translation units of libdec.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "dec_attn.cuh"
@@ -56,7 +57,12 @@ cudaError_t launch_gemv_resid(int BT, bool xreg, const GemvArgs& a, int grid, ui
                              bool pdl);
 cudaError_t launch_gemv_head(int BT, bool xreg, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st,
                              bool pdl);
-cudaError_t launch_attn(const AttnArgs& a, int B, uint32_t smem, cudaStream_t st, bool pdl);
+// Attention (attn.cu): grid (n_split, Hkv, B); maps from make_attn_maps.
+cudaError_t launch_attn(const AttnArgs& a, const AttnMaps& maps, int B, cudaStream_t st, bool pdl);
+uint32_t attn_launch_smem(int D);
+// bf16 [outer][inner] row-major tensor map with a box of 64 x box_rows and the
+// 128-byte swizzle (false if the driver refuses it).
+bool make_tmap_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows);
 
 // Batched prompt pass (prefill.cu): rows are (sequence, position) pairs.
 cudaError_t launch_prefill_embed(const int32_t* prompt, int P, int i0, int n, int rows, int H, const uint16_t* embed,

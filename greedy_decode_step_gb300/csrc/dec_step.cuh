@@ -26,7 +26,10 @@ namespace dec {
 
 constexpr int kStepMaxLayers = 64;
 constexpr uint32_t kStepSlotBytes = 40 * 1024;
-constexpr int kAttnLoads = 9;  // 16-byte loads in flight per thread in the attention phase
+constexpr int kAttnLoads = 8;  // 16-byte loads in flight per thread in the attention phase
+// attention area: m_run / l_run at 0, per-warp maxima / sums at 256 / 768,
+// the K then V tile (and later the warp-merge buffer) from here
+constexpr uint32_t kStepAttnTileOff = 1280;
 constexpr uint32_t kStepHeaderBytes = 3328;
 
 enum StepPhase : int { kPhQKV = 0, kPhO = 1, kPhGLU = 2, kPhDown = 3, kPhHead = 4, kNumPhases = 5 };
@@ -255,24 +258,28 @@ __device__ bool consume_phase(const StepArgs& a, int ph, int l, const GemvIO& io
 }
 
 // Attention phase of layer l: work items (b, g, split) go round-robin over the
-// CTAs (one per CTA while the cache is short); each item brings its query
-// vectors and key/value tiles into shared memory with plain 16-byte loads
-// through L2 (not the TMA engine, whose queue is full of the producer's
-// weight copies), runs the same tile math as the single-op attention kernel
-// and finishes the same way (partials + last-split merge).
+// CTAs (one per CTA while the cache is short); each item brings its key/value
+// tiles into shared memory with plain 16-byte loads through L2 (not the TMA
+// engine, whose queue is full of the producer's weight copies), in the
+// swizzled tile layout of the single-op attention kernel, runs the same
+// per-warp tensor-core tile math (same keys per warp, so the same sums) and
+// finishes the same way (warp merge, partials, last-split merge).  Groups of
+// at most 8 query heads (one n-tile).
 template <int D>
-__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, const int* pos_s, const float* rope_s,
-                                const unsigned int* tick0, volatile int* abort_cta, int* is_last, uint64_t limit) {
+__device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, uint32_t* qstage, const int* pos_s,
+                                const float* rope_s, const unsigned int* tick0, volatile int* abort_cta, int* is_last,
+                                uint64_t limit) {
   constexpr int kRowChunks = D / 8;  // 16-byte chunks per cache row
   constexpr int kMaxSlots = attn_slots<D>();
   float* m_run = reinterpret_cast<float*>(area);
   float* l_run = m_run + kAttnMaxGroup;
-  float* corr = l_run + kAttnMaxGroup;
+  float* ms = reinterpret_cast<float*>(area + 256);
+  float* ls = reinterpret_cast<float*>(area + 768);
+  unsigned char* Kt = area + kStepAttnTileOff;
+  unsigned char* Vt = Kt + attn_tile_bytes<D>();
   const int G = a.Hq / a.Hkv;
-  float* q_s = reinterpret_cast<float*>(area + 256);
-  float* s_s = q_s + G * attn_qstride<D>();
-  uint4* tile = reinterpret_cast<uint4*>(s_s + G * kAttnTile);  // K rows then V rows
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int r0 = attn_warp_row0(warp);
   const StepLayer& w = a.layers[l];
   AttnArgs t{};
   t.q = a.q;
@@ -313,33 +320,25 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
     const float* Kn = a.kraw + (static_cast<size_t>(b) * a.Hkv + g) * D;
     const float* cs_b = rope_s + b * (D / 2);
     const float* sn_b = rope_s + a.B * (D / 2) + b * (D / 2);
-    if (tid < G) {
-      m_run[tid] = -INFINITY;
-      l_run[tid] = 0.f;
-    }
-    float acc0[kMaxSlots], acc1[kMaxSlots];
-#pragma unroll
-    for (int i = 0; i < kMaxSlots; ++i) acc0[i] = acc1[i] = 0.f;
+    const AttnQStaged<D, 1> qf{qstage};
+    AttnWarpState<D, 1> st;
+    attn_state_init<D, 1>(st);
     for (int tt = 0; tt < n_tiles; ++tt) {
       const int j0 = k0 + tt * kAttnTile;
       const int nk = min(kAttnTile, k1 - j0);
       const int n16 = nk * kRowChunks;
       const int newest = (j0 + nk == p + 1) ? p - j0 : -1;  // tile row of the step's own key
-      // first tile: this thread's query pairs and (for the item holding key p)
-      // the new key's pair, unrotated from L2, loaded with the tile's rows
-      constexpr int kQP = (kAttnMaxGroup * (D / 2) + kConsumerThreads - 1) / kConsumerThreads;
-      float qa[kQP], qb[kQP], ka = 0.f, kb = 0.f;
-      if (tt == 0) {
-#pragma unroll
-        for (int i = 0; i < kQP; ++i) {
-          const int pr = tid + i * kConsumerThreads;
-          qa[i] = qb[i] = 0.f;
-          if (pr < G * (D / 2)) {
-            const int h = pr / (D / 2), j = pr - h * (D / 2);
-            qa[i] = __ldcg(Qg + h * D + j);
-            qb[i] = __ldcg(Qg + h * D + j + D / 2);
-          }
-        }
+      // first tile: the unrotated query values of one staging item per thread
+      // (head qh, dims d, d+1 and d+D/2, d+D/2+1 with d = 16 qks + 8 qj + 2 qc;
+      // heads qh >= G stage zeros), loaded from L2 with the tile's rows
+      const int qc = tid & 3, qj = (tid >> 2) & 1, qh = (tid >> 3) & 7, qks = tid >> 6;
+      const int qd = 16 * qks + 8 * qj + 2 * qc;
+      const bool q_item = qks < D / 32;
+      float2 qlo = make_float2(0.f, 0.f), qhi = qlo;
+      float ka = 0.f, kb = 0.f;
+      if (tt == 0 && q_item && qh < G) {
+        qlo = __ldcg(reinterpret_cast<const float2*>(Qg + qh * D + qd));
+        qhi = __ldcg(reinterpret_cast<const float2*>(Qg + qh * D + qd + D / 2));
       }
       if (newest >= 0 && tid < D / 2) {
         ka = __ldcg(Kn + tid);
@@ -363,41 +362,43 @@ __device__ bool attention_phase(const StepArgs& a, int l, unsigned char* area, c
         for (int j = 0; j < kAttnLoads; ++j) {
           const int i = i0 + tid + j * kConsumerThreads;
           if (i < n16) {
-            if (i / kRowChunks != newest) tile[i] = v[j];
+            const int r = i / kRowChunks;
+            if (r != newest) *reinterpret_cast<uint4*>(Kt + attn_swz(r, i - r * kRowChunks)) = v[j];
           } else if (i < total) {
-            tile[kAttnTile * kRowChunks + (i - n16)] = v[j];
+            const int r = (i - n16) / kRowChunks;
+            *reinterpret_cast<uint4*>(Vt + attn_swz(r, i - n16 - r * kRowChunks)) = v[j];
           }
         }
       }
-      if (tt == 0) {
-#pragma unroll
-        for (int i = 0; i < kQP; ++i) {
-          const int pr = tid + i * kConsumerThreads;
-          if (pr < G * (D / 2)) {
-            const int h = pr / (D / 2), j = pr - h * (D / 2);
-            float l2, h2;
-            rope_rotate(qa[i], qb[i], cs_b[j], sn_b[j], &l2, &h2);
-            q_s[h * attn_qstride<D>() + attn_qoff(j)] = l2;
-            q_s[h * attn_qstride<D>() + attn_qoff(j + D / 2)] = h2;
-          }
+      if (tt == 0 && q_item) {
+        // rotate-half RoPE at p, bf16 parts, to the staged fragment order
+        float l0 = 0.f, h0 = 0.f, l1 = 0.f, h1 = 0.f;
+        if (qh < G) {
+          rope_rotate(qlo.x, qhi.x, cs_b[qd], sn_b[qd], &l0, &h0);
+          rope_rotate(qlo.y, qhi.y, cs_b[qd + 1], sn_b[qd + 1], &l1, &h1);
         }
+        constexpr int kLo = attn_qstage_words<D, 1>() / 2;
+        const int w0 = (qks * 2 + qj) * 32 + 4 * qh + qc, w1 = w0 + (D / 32) * 64;
+        split_bf16x2(l0, l1, &qstage[w0], &qstage[w0 + kLo]);
+        split_bf16x2(h0, h1, &qstage[w1], &qstage[w1 + kLo]);
       }
       if (newest >= 0 && tid < D / 2) {
         float l2, h2;
         rope_rotate(ka, kb, cs_b[tid], sn_b[tid], &l2, &h2);
         const uint16_t lo16 = f32_to_bf16(l2), hi16 = f32_to_bf16(h2);
-        uint16_t* row = reinterpret_cast<uint16_t*>(tile) + static_cast<size_t>(newest) * D;
-        row[tid] = lo16;
-        row[tid + D / 2] = hi16;
+        constexpr int kHalfChunks = D / 16;  // chunk of dim D/2 + e is e/8 + kHalfChunks
+        *reinterpret_cast<uint16_t*>(Kt + attn_swz(newest, tid >> 3) + (tid & 7) * 2) = lo16;
+        *reinterpret_cast<uint16_t*>(Kt + attn_swz(newest, (tid >> 3) + kHalfChunks) + (tid & 7) * 2) = hi16;
         uint16_t* dst = w.kc + (head_off + p) * D;
         dst[tid] = lo16;
         dst[tid + D / 2] = hi16;
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
-      attn_tile_math<D>(tile, reinterpret_cast<const uint32_t*>(tile + kAttnTile * kRowChunks), nk, G, a.attn_scale,
-                        q_s, s_s, m_run, l_run, corr, acc0, acc1);
+      if (attn_warp_parity(warp) == (tt & 1) && r0 < nk) (void)attn_warp_tile<D, 1>(Kt, Vt, r0, nk, a.attn_scale, qf, st);
       asm volatile("bar.sync 1, 256;" ::: "memory");
     }
+    float acc0[kMaxSlots], acc1[kMaxSlots];
+    attn_merge_warps<D, 1>(st, G, k1 - k0, ms, ls, reinterpret_cast<float*>(Kt), acc0, acc1, m_run, l_run);
     if (n_active == 1 || items > static_cast<int>(gridDim.x)) {
       // one split, or more items than CTAs (a CTA may hold two splits of one
       // group, so none may wait for the others): the last split merges alone
@@ -571,7 +572,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) step_kernel(const __grid_cons
                                      is_last, &GR.empty[gq & 1]) &&
          grid_sync(a, abort_cta, sense, limit);
     if (!ok) break;
-    ok = attention_phase<D>(a, l, attn_area, pos_s, rope_s, tick0, abort_cta, is_last, limit) &&
+    ok = attention_phase<D>(a, l, attn_area, reinterpret_cast<uint32_t*>(part), pos_s, rope_s, tick0, abort_cta,
+                            is_last, limit) &&
          grid_sync(a, abort_cta, sense, limit);
     if (!ok) break;
     // r += Wo o

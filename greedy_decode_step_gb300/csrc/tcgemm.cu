@@ -66,15 +66,6 @@ struct TcArgs {
   uint32_t* err;
 };
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
-      "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
@@ -316,8 +307,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // bf16 [outer][inner] row-major, box {64, box_rows}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+bool make_tmap_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -328,8 +321,6 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 cudaError_t allow_smem_tcgemm() {
   return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemMax + 1024);
@@ -415,13 +406,13 @@ int tc_gemm(const TcSeg* segs, int n_seg, const uint16_t* Yhi, const uint16_t* Y
     a.col_off[s] = cols;
     cols += segs[s].N;
     m_tiles += (segs[s].N + kTcBM - 1) / kTcBM;
-    if (!make_map(&a.wmap[s], segs[s].W, K, segs[s].N, kTcBM)) {
+    if (!make_tmap_sw128(&a.wmap[s], segs[s].W, K, segs[s].N, kTcBM)) {
       *why = "tensor map of the weights could not be made";
       return 1;
     }
   }
   a.tiles_before[n_seg] = m_tiles;
-  if (!make_map(&a.yhi, Yhi, K, rows, a.BN) || !make_map(&a.ylo, Ylo, K, rows, a.BN)) {
+  if (!make_tmap_sw128(&a.yhi, Yhi, K, rows, a.BN) || !make_tmap_sw128(&a.ylo, Ylo, K, rows, a.BN)) {
     *why = "tensor map of the activations could not be made";
     return 1;
   }
