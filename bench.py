@@ -44,7 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gemv", choices=["gemv", "reference"])
     ap.add_argument("--workload", default="dense4b",
-                    choices=["dense4b", "layer4b", "dense4b_b8", "gqa12x3_b16", "select_b16"])
+                    choices=["dense4b", "layer4b", "dense4b_b8", "gqa12x3_b16", "select_b16", "attn_gqa12x3_b16",
+                             "attn_dense4b_b8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--prompt", type=int, default=None, help="prompt length (default: the workload's 512)")
@@ -216,56 +217,105 @@ def run_layer(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize(dev)
     assert gd.device_error(clear=True) == 0
-    ms = e0.elapsed_time(e1) / args.steps
-    w_bytes, kv_bytes = bytes_per_step(m, [L0 + args.warmup], B, head=False)
-    gbs = (w_bytes + kv_bytes) / (ms / 1e3) / 1e9
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    # positions L0 + W .. L0 + W + K - 1 (the warm-up steps advanced the cache)
+    positions = list(range(L0 + args.warmup, L0 + args.warmup + args.steps))
+    w_bytes, kv_bytes = bytes_per_step(m, positions, B, head=False)
+    step_bytes = w_bytes + kv_bytes / len(positions)
+    gbs = step_bytes / (ms / 1e3) / 1e9
+    peak, src = peaks()
+    launches = gd.dec_step_launches(model, st)
+    roof = {"kernel": "step_kernel<1,128> (the whole layer step: norm, QKV+RoPE, attention, o_proj, norm, "
+                      "gate/up, down)" if launches == 1 else "per-op layer step",
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "peak_source": f"{src} copy bandwidth", "traffic": committed_traffic("step_kernel_layer4b"),
+            "algorithmic_bytes_per_launch": int(step_bytes), "avg_launch_us": round(ms * 1e3, 2),
+            "launches_timed": args.steps}
+    e2e = None
+    if not args.no_e2e:
+        # from host buffers: pinned residual in, one step, residual out
+        hr = torch.from_numpy(synth.make_residual(w.seed, B, m.hidden)).pin_memory()
+        hout = torch.empty_like(hr).pin_memory()
+        st.pos.fill_(L0)
+        torch.cuda.synchronize(dev)
+        e2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e2[0].record(stream)
+        for _ in range(args.steps):
+            st.residual.copy_(hr, non_blocking=True)
+            gd.dec_step(model, st)
+            hout.copy_(st.residual, non_blocking=True)
+        e2[1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e2[0].elapsed_time(e2[1]) / args.steps
+        e2e = {"value": round(e2e_ms * 1e3, 2), "unit": "us/step", "h2d_bytes_per_step": 4 * B * m.hidden,
+               "d2h_bytes_per_step": 4 * B * m.hidden,
+               "what": "pinned host residual -> H2D -> dec_step (one layer) -> D2H residual, per step"}
     res = {"metric": "one 4B-class layer step (b=1, 4096-token cache)", "value": round(ms * 1e3, 2),
-           "unit": "us/step", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-           "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": "layer4b: H=2560, Hq=32, Hkv=8, D=128, I=9728, b=1, eager dec_step",
-                      "step_bytes": int(w_bytes + kv_bytes), "step_hbm_gbs": round(gbs, 1),
-                      "step_hbm_frac_of_measured": round(gbs / peaks()[0], 4)},
-           "roofline": glu_roofline(gd, torch, model, m, dev, stream, reps=20),
-           "gpu_launches": gd.dec_step_launches(model, st) * args.steps, "clocks": clk.summary()}
-    return res, None
+           "unit": "us/step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 5), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic (seeded Philox weights, N(0,1) cache prefix)",
+           "config": {"workload": "layer4b: H=2560, Hq=32, Hkv=8, D=128, I=9728, b=1, 4096-token cache, dec_step",
+                      "l2": "inputs larger than L2 are not used: the layer's 202 MB of weights exceed L2 (129 MB)",
+                      "step_bytes": int(step_bytes), "step_hbm_gbs": round(gbs, 1),
+                      "step_hbm_frac_of_measured": round(gbs / peak, 4)},
+           "roofline": roof,
+           "glu_alone": glu_roofline(gd, torch, model, m, dev, stream, reps=20),
+           "gpu_launches": launches * args.steps, "clocks": clk.summary()}
+    if e2e:
+        res["e2e"] = e2e
+
+    def cpu_baseline():
+        import oracle
+        S = L0 + 64
+        kch = np.zeros((1, m.n_kv_heads, S, m.head_dim), np.uint16)
+        vch = np.zeros_like(kch)
+        synth.make_kv_prefix(w.seed, m, 0, 0, L0, "k", kch[0])
+        synth.make_kv_prefix(w.seed, m, 0, 0, L0, "v", vch[0])
+        om = oracle.Model(m, layers_h, None, None, None, [kch], [vch])
+        x = synth.make_residual(w.seed, B, m.hidden)[0].astype(np.float64)
+        done, t0 = 0, time.time()
+        while done < 60 and time.time() - t0 < 20.0:
+            om.step(0, L0 + done, x_in=x)
+            done += 1
+        el = time.time() - t0
+        return {"value": round(el / done * 1e6, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+                "sample": f"{done} one-layer steps of the fp64 oracle at positions {L0}.. over the same "
+                          f"{L0}-token cache prefix, single thread, {cpu_model()}"}
+
+    return res, cpu_baseline
 
 
 def run_batched(args, world, rank, local):
     """The batched configurations (not the headline): b=8 on the 36-layer
-    4B-class model with cache lengths U{1024..32768}, or b=16 on the 24-layer
-    H=1536 12/3-head model with 8192-token caches; decode steps through
-    dec_decode.  Weights bf16 N(0, 0.02), gains 1 + N(0, 0.02), caches bf16
-    N(0, 1), drawn on the device from a seeded torch generator (the same
-    recipe as the parity tests' Philox inputs, not the same numbers)."""
+    4B-class model with the workload's seeded cache lengths U{1024..32768}, or
+    b=16 on the 24-layer H=1536 12/3-head model with 8192-token caches; decode
+    steps through dec_decode.  Weights and gains are the seeded synthetic
+    recipe of the parity tests (bf16 N(0, 0.02), 1 + N(0, 0.02)); the caches
+    are bf16 N(0, 1) drawn on the device from a seeded torch generator (same
+    distribution, not the same numbers as the host recipe)."""
     import torch
     import greedy_decode_step_gb300 as gd
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if args.workload == "dense4b_b8":
-        L, H, Hq, Hkv, D, I, V, B = 36, 2560, 32, 8, 128, 9728, 151936, 8
-        kv = [int(x) for x in np.random.default_rng(0).integers(1024, 32769, B)]
-        steps = min(args.steps, 64)
-    else:
-        L, H, Hq, Hkv, D, I, V, B = 24, 1536, 12, 3, 128, 8960, 151936, 16
-        kv = [8192] * B
-        steps = min(args.steps, 128)
-    g = torch.Generator(device=dev)
-    g.manual_seed(0)
-    bf = torch.bfloat16
+    gd.lib()
+    name = "dense4b_b8" if args.workload == "dense4b_b8" else "gqa12x3"
+    w, m, layers_h, E_h, fn_h = host_model(name)
+    L, H, Hq, Hkv, D, I, V, B = (m.n_layers, m.hidden, m.n_heads, m.n_kv_heads, m.head_dim, m.intermediate,
+                                 m.vocab, w.batch)
+    kv = [int(x) for x in w.kv_len]
+    steps = min(args.steps, w.steps)
 
-    def w(*sh):
-        return (torch.randn(*sh, device=dev, generator=g) * 0.02).to(bf)
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    def gam(n):
-        return (1 + 0.02 * torch.randn(n, device=dev, generator=g)).to(bf)
-
-    layers = [dict(attn_norm=gam(H), wq=w(Hq * D, H), wk=w(Hkv * D, H), wv=w(Hkv * D, H), wo=w(H, Hq * D),
-                   mlp_norm=gam(H), wg=w(I, H), wu=w(I, H), wd=w(H, I)) for _ in range(L)]
-    E = w(V, H)
-    model = gd.Model(L, H, Hq, Hkv, D, I, V, 1e-6, 1e6, layers, embed=E, final_norm=gam(H), lm_head=E)
+    layers = [{k: to_dev(v) for k, v in l.items()} for l in layers_h]
+    E, fn = to_dev(E_h), to_dev(fn_h)
+    model = gd.Model(L, H, Hq, Hkv, D, I, V, m.rms_eps, m.rope_theta, layers, embed=E, final_norm=fn, lm_head=E)
     S_max = max(kv) + steps + 16 + args.warmup + 8
     st = gd.State(model, B, S_max, device=dev).init()
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
     for l in range(L):
         st.k_cache[l].normal_(generator=g)
         st.v_cache[l].normal_(generator=g)
@@ -273,17 +323,19 @@ def run_batched(args, world, rank, local):
     t0 = torch.randint(0, V, (B,), dtype=torch.int32, device=dev, generator=g)
     out = torch.empty((B, steps), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    st.pos.copy_(p0)
-    st.token.copy_(t0)
-    # the first 16-step call captures the decode graph (set-up), then W warm-up steps
-    gd.dec_decode(model, st, 16, -1, torch.empty((B, 16), dtype=torch.int32, device=dev))
-    if args.warmup > 0:
+
+    def restart():
         st.pos.copy_(p0)
         st.token.copy_(t0)
+
+    # the first 16-step call captures the decode graph (set-up), then W warm-up steps
+    restart()
+    gd.dec_decode(model, st, 16, -1, torch.empty((B, 16), dtype=torch.int32, device=dev))
+    if args.warmup > 0:
+        restart()
         gd.dec_decode(model, st, args.warmup, -1, torch.empty((B, args.warmup), dtype=torch.int32, device=dev))
     torch.cuda.synchronize(dev)
-    st.pos.copy_(p0)
-    st.token.copy_(t0)
+    restart()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         e0.record(stream)
@@ -291,22 +343,183 @@ def run_batched(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize(dev)
     assert gd.device_error(clear=True) == 0
-    ms = e0.elapsed_time(e1) / n
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
     w_bytes = L * 2 * (2 * Hq * D * H + 2 * Hkv * D * H + 3 * I * H) + 2 * V * H + L * 2 * 2 * H + 2 * H
-    kv_bytes = sum(2 * L * Hkv * D * 2 * (p + (steps - 1) / 2 + 1) for p in kv)
+    kv_bytes = sum(2 * L * Hkv * D * 2 * (p + (n - 1) / 2 + 1) for p in kv)
     gbs = (w_bytes + kv_bytes) / (ms / 1e3) / 1e9
     peak, src = peaks()
-    res = {"metric": f"greedy decode tok/s at b={B} ({args.workload}); HBM GB/s", "value": round(B / (ms / 1e3), 2),
-           "unit": "tok/s", "n_gpus": 1, "steps": n, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+    first_tok = int(out[0, 0])
+    roof = attn_roofline(gd, torch, model, st, m, dev, stream, f"attn_kernel_{args.workload}")
+    e2e = None if args.no_e2e else batched_end_to_end(gd, torch, model, st, p0, t0, steps, dev, stream, B)
+    res = {"metric": f"greedy decode tok/s at b={B} ({args.workload}); HBM GB/s", "value": round(B * world / (ms / 1e3), 2),
+           "unit": "tok/s", "n_gpus": world, "steps": n, "warmup": args.warmup, "ms_per_step": round(ms, 5),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-           "data": "synthetic (seeded torch N(0,0.02) weights, N(0,1) caches)",
-           "config": {"workload": args.workload, "batch": B, "layers": L, "kv_lens": kv,
+           "data": "synthetic (seeded Philox N(0,0.02) weights; seeded torch N(0,1) caches)",
+           "config": {"workload": f"{args.workload}: {w.description}", "batch": B, "layers": L, "kv_lens": kv,
+                      "l2": "inputs larger than L2: every step streams the weights and all caches",
                       "step_bytes": int(w_bytes + kv_bytes), "step_hbm_gbs": round(gbs, 1),
                       "step_hbm_frac_of_measured": round(gbs / peak, 4),
                       "path": "weight GEMMs on this library's tcgen05 tensor-core GEMM (hi/lo bf16 activations "
-                                   "into one fp32 accumulator), split-K attention"},
+                              "into one fp32 accumulator), split-K tensor-core attention"},
+           "roofline": roof,
            "gpu_launches": gd.dec_step_launches(model, st) * n + 2, "clocks": clk.summary()}
+    if e2e:
+        res["e2e"] = e2e
+
+    def cpu_baseline():
+        return batched_oracle_rate(torch, m, layers_h, E_h, fn_h, st, kv[0], int(t0[0]), first_tok)
+
+    return res, cpu_baseline
+
+
+def run_attn_op(args, world, rank, local):
+    """The split-K attention alone (dec_gqa_decode_attn) on one layer of a
+    batched configuration: b=16, Hq=12, Hkv=3 with 8192-token caches, or b=8,
+    Hq=32, Hkv=8 with the dense4b_b8 cache lengths.  bf16 N(0,1) caches and
+    fp32 N(0,1) queries from a seeded torch generator; inputs larger than L2
+    (201 MB / 1.1 GB of K/V per launch)."""
+    import torch
+    import greedy_decode_step_gb300 as gd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gd.lib()
+    w = synth_workload("dense4b_b8" if args.workload == "attn_dense4b_b8" else "gqa12x3")
+    m, B = w.model, w.batch
+    Hq, Hkv, D = m.n_heads, m.n_kv_heads, m.head_dim
+    kv = [int(x) for x in w.kv_len]
+    S_max = max(kv) + 8
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    K = torch.randn((B, Hkv, S_max, D), device=dev, generator=g).to(torch.bfloat16)
+    V = torch.randn((B, Hkv, S_max, D), device=dev, generator=g).to(torch.bfloat16)
+    q = torch.randn((B, Hq, D), device=dev, generator=g)
+    pos = torch.tensor(kv, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ws = gd.dec_gqa_decode_attn(q, K, V, pos, o)
+    for _ in range(max(3, args.warmup)):
+        gd.dec_gqa_decode_attn(q, K, V, pos, o, ws=ws)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(1, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(n):
+            gd.dec_gqa_decode_attn(q, K, V, pos, o, ws=ws)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    assert gd.device_error(clear=True) == 0
+    avg_s = max_over_ranks(e0.elapsed_time(e1) / n, world, dev) / 1e3
+    alg = sum(Hkv * (p + 1) * D * 2 * 2 for p in kv) + 2 * B * Hq * D * 4
+    peak, src = peaks()
+    gbs = alg / avg_s / 1e9
+    res = {"metric": f"GQA decode attention GB/s ({args.workload})", "value": round(gbs * world, 1), "unit": "GB/s",
+           "n_gpus": world, "steps": n, "warmup": max(3, args.warmup), "ms_per_step": round(avg_s * 1e3, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded torch N(0,1) caches and queries)",
+           "config": {"workload": f"{args.workload}: one layer of {w.description}", "batch": B, "Hq": Hq,
+                      "Hkv": Hkv, "head_dim": D, "kv_lens": kv,
+                      "l2": "inputs larger than L2 (K/V bytes per launch above 129 MB)"},
+           "roofline": {"kernel": f"attn_kernel<{D},1>", "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                        "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": f"{src} (burst copy)",
+                        "traffic": committed_traffic(f"attn_kernel_{args.workload[5:]}"),
+                        "algorithmic_bytes_per_launch": int(alg), "avg_launch_us": round(avg_s * 1e6, 2),
+                        "launches_timed": n,
+                        "note": "each call also carries its ticket reset (a memset node), inside the timing"},
+           "gpu_launches": n, "clocks": clk.summary()}
     return res, None
+
+
+def synth_workload(name):
+    import synth
+    return synth.workload(name)
+
+
+def attn_roofline(gd, torch, model, st, m, dev, stream, tag, reps=4):
+    """The dominant kernel of the batched step, the split-K attention, timed
+    alone through its C-ABI entry point on every layer's cache at the
+    positions the decode reached (CUDA events around reps x layers launches;
+    each call also carries its 4-byte-per-group ticket reset, a memset node,
+    so the achieved rate is a floor)."""
+    B, Hq, D = st.batch, m.n_heads, m.head_dim
+    q = torch.randn((B, Hq, D), device=dev, dtype=torch.float32)
+    o = torch.empty_like(q)
+    pos = st.pos.clone()
+    ws = gd.dec_gqa_decode_attn(q, st.k_cache[0], st.v_cache[0], pos, o)
+    for l in range(min(4, m.n_layers)):
+        gd.dec_gqa_decode_attn(q, st.k_cache[l], st.v_cache[l], pos, o, ws=ws)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    n = 0
+    for _ in range(reps):
+        for l in range(m.n_layers):
+            gd.dec_gqa_decode_attn(q, st.k_cache[l], st.v_cache[l], pos, o, ws=ws)
+            n += 1
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert gd.device_error(clear=True) == 0
+    avg_s = e0.elapsed_time(e1) / 1e3 / n
+    lens = [int(p) + 1 for p in pos.cpu().tolist()]
+    alg = sum(m.n_kv_heads * k * D * 2 * 2 for k in lens) + 2 * B * Hq * D * 4
+    peak, src = peaks()
+    achieved = alg / avg_s / 1e9
+    return {"kernel": f"attn_kernel<{D},1> (split-K GQA decode attention, tensor cores)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{src} (burst copy; kernel timed alone)", "traffic": committed_traffic(tag),
+            "algorithmic_bytes_per_launch": int(alg), "avg_launch_us": round(avg_s * 1e6, 2), "launches_timed": n,
+            "kv_lens": lens}
+
+
+def batched_end_to_end(gd, torch, model, st, p0, t0, steps, dev, stream, B):
+    """The user call from host buffers: pinned positions and tokens -> H2D,
+    dec_decode over the steps, D2H of the generated tokens."""
+    hp, ht = p0.cpu().pin_memory(), t0.cpu().pin_memory()
+    hout = torch.empty((B, steps), dtype=torch.int32).pin_memory()
+    dout = torch.empty((B, steps), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    st.pos.copy_(hp, non_blocking=True)
+    st.token.copy_(ht, non_blocking=True)
+    n = gd.dec_decode(model, st, steps, -1, dout)
+    hout.copy_(dout, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    return {"value": round(n * B / (ms / 1e3), 2), "unit": "tok/s", "h2d_bytes_per_step": round(8 * B / n, 3),
+            "d2h_bytes_per_step": 4 * B,
+            "what": "pinned host positions and tokens -> H2D -> dec_decode -> D2H tokens; tokens / wall time"}
+
+
+def batched_oracle_rate(torch, m, layers_h, E_h, fn_h, st, p, token, gpu_first, max_seconds=25.0):
+    """The fp64 oracle's decode steps of sequence 0 from the same position,
+    token and cache prefix (copied from the device), single thread, for up to
+    max_seconds; its first token is compared with the GPU's."""
+    import oracle
+    S = p + 16  # the oracle's steps stay below this slot
+
+    def host(t):
+        return t[:1, :, :S].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    kc = [host(st.k_cache[l]) for l in range(m.n_layers)]
+    vc = [host(st.v_cache[l]) for l in range(m.n_layers)]
+    om = oracle.Model(m, layers_h, E_h, fn_h, E_h, kc, vc)
+    done, t0 = 0, time.time()
+    first = None
+    while True:
+        token, logits, _ = om.step(0, p + done, token=token)
+        if first is None:
+            first = (token, float(np.sort(logits)[-1] - np.sort(logits)[-2]))
+        done += 1
+        if time.time() - t0 > max_seconds or done >= 8:
+            break
+    el = time.time() - t0
+    return {"value": round(done / el, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} decode steps of sequence 0 (all {m.n_layers} layers + LM head, cache of {p} "
+                      f"tokens copied from the device) by the fp64 oracle, single thread, {cpu_model()}",
+            "first_token_oracle": first[0], "first_token_gpu": gpu_first, "oracle_top2_margin": round(first[1], 5)}
 
 
 def run_select(args, world, rank, local):
@@ -551,7 +764,14 @@ def run_gpu(args, world, rank, local):
     }
     if e2e:
         res["e2e"] = e2e
-    return res, (m, layers_h, E_h, fn_h, prompt_h)
+
+    def cpu_baseline():
+        done, el = oracle_rate(m, layers_h, E_h, fn_h, 3, max_seconds=25.0)
+        return {"value": round(done / el, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                "sample": f"{done} full decode steps (36 layers + LM head) of the fp64 oracle at positions 511.. "
+                          f"over a 511-token N(0,1) cache, single thread, {cpu_model()}"}
+
+    return res, cpu_baseline
 
 
 def glu_roofline(gd, torch, model, m, dev, stream, reps=3):
@@ -680,15 +900,12 @@ def main():
         res, host = run_batched(args, world, rank, local)
     elif args.workload == "select_b16":
         res, host = run_select(args, world, rank, local)
+    elif args.workload.startswith("attn_"):
+        res, host = run_attn_op(args, world, rank, local)
     else:
         res, host = run_gpu(args, world, rank, local)
     if rank == 0 and host is not None and not args.no_cpu_baseline:
-        m, layers_h, E_h, fn_h, _ = host
-        done, el = oracle_rate(m, layers_h, E_h, fn_h, 3, max_seconds=25.0)
-        res["cpu_baseline"] = {"value": round(done / el, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
-                               "sample": f"{done} full decode steps (36 layers + LM head) of the fp64 oracle at "
-                                         f"positions 511.. over a 511-token N(0,1) cache, single thread, "
-                                         f"{cpu_model()}"}
+        res["cpu_baseline"] = host()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
