@@ -872,7 +872,7 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
       t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
       t.rows_per_seq = n;
       t.row_pos0 = i0;
-      DEC_TRY(run_attn(t, R, dv, st, false));
+      DEC_TRY(run_attn(t, R, dv, st, true));
       DEC_CUDA(launch_prefill_cast(w.pf_o, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R) * QD, dv->sms, st));
       DEC_TRY(gemm_rows(dv, w, {{lw.wo, H, w.pf_r}}, QD, w.pf_bf, w.pf_bf_lo, R, H, 1.f, st));
       DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, w.pf_bf,
@@ -927,7 +927,7 @@ int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, cons
     t.S_max = s->max_seq;
     t.n_split = w.n_split;
     t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
-    DEC_TRY(run_attn(t, B, dv, st, false));
+    DEC_TRY(run_attn(t, B, dv, st, true));
     DEC_CUDA(launch_prefill_cast(w.o, xs, xs + static_cast<size_t>(B) * QD, static_cast<size_t>(B) * QD, dv->sms,
                                  st));
     DEC_TRY(gemm_rows(dv, w, {{lw.wo, H, r}}, QD, xs, xs + static_cast<size_t>(B) * QD, B, H, 1.f, st));

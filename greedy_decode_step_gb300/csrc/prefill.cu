@@ -14,7 +14,9 @@
 // positions starting at i0.
 //
 // The same kernels serve the decode step at batch > 2 (one row per sequence,
-// n = 1).
+// n = 1).  Every kernel here is launched with programmatic dependent launch
+// and waits for its predecessor (griddepcontrol.wait) before touching any
+// activation, so a launch's set-up overlaps the previous kernel's tail.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -29,6 +31,8 @@ namespace {
 // r[row] = embedding row of the row's prompt token (fp32).
 __global__ void prefill_embed_kernel(const int32_t* prompt, int P, int i0, int n, int H, const uint16_t* embed,
                                      int vocab, float* r, uint32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x;
   const int b = row / n, i = row - b * n;
   const int tok = prompt[static_cast<size_t>(b) * P + i0 + i];
@@ -50,6 +54,8 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t* hi, uint16_t* lo) 
 // y = r / sqrt(mean(r^2) + eps) * gamma as hi/lo bf16 parts; one CTA of 256 per row.
 __global__ void prefill_norm_kernel(const float* r, const uint16_t* gamma, float eps, int H, uint16_t* y,
                                     uint16_t* y_lo) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[8];
   constexpr int kKeep = 16;  // values per thread kept in registers between the two passes
   const float* x = r + static_cast<size_t>(blockIdx.x) * H;
@@ -97,6 +103,8 @@ struct RopeArgs {
 // Rotate-half RoPE of q (to q_out) and k at the row's position, k and v to
 // the cache.  One CTA per row; thread t takes pair t of each head.
 __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x;
   const int b = row / a.n, i = row - b * a.n;
   const int p = a.pos[b] + a.i0 + i;
@@ -140,6 +148,8 @@ __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
 
 // hi/lo bf16 parts of an fp32 array.
 __global__ void prefill_cast_kernel(const float* x, uint16_t* y, uint16_t* y_lo, size_t n) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
        k += static_cast<size_t>(gridDim.x) * blockDim.x)
     split_bf16(x[k], &y[k], &y_lo[k]);
@@ -148,6 +158,8 @@ __global__ void prefill_cast_kernel(const float* x, uint16_t* y, uint16_t* y_lo,
 // h = silu(g) * u as hi/lo bf16 parts, from gu = [rows][2 I] (gate columns,
 // then up; with half_rows > 0 rows r and r + half_rows added).
 __global__ void prefill_glu_kernel(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int half_rows) {
+  pdl_wait();
+  pdl_launch_dependents();
   const size_t n = rows * I;
   for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
        k += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -166,6 +178,8 @@ __global__ void prefill_glu_kernel(const float* gu, int I, uint16_t* h, uint16_t
 // Greedy argmax of row b of the logits C[b] over a slice of the vocabulary
 // per CTA (ties to the lower index), folded into keys[b].
 __global__ void rows_argmax_kernel(const float* C, int V, unsigned long long* keys) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float bv_s[8];
   __shared__ uint32_t bi_s[8];
   const int b = blockIdx.y;
@@ -193,20 +207,22 @@ __global__ void rows_argmax_kernel(const float* C, int V, unsigned long long* ke
 }
 
 // The step's bookkeeping (one warp) once every row's key is in.
-__global__ void rows_finish_kernel(const GemvIO io) { finish_rows(io, io.B); }
+__global__ void rows_finish_kernel(const GemvIO io) {
+  pdl_wait();
+  pdl_launch_dependents();
+  finish_rows(io, io.B);
+}
 
 }  // namespace
 
 cudaError_t launch_prefill_embed(const int32_t* prompt, int P, int i0, int n, int rows, int H, const uint16_t* embed,
                                  int vocab, float* r, uint32_t* err, cudaStream_t st) {
-  prefill_embed_kernel<<<rows, 256, 0, st>>>(prompt, P, i0, n, H, embed, vocab, r, err);
-  return cudaGetLastError();
+  return launch(prefill_embed_kernel, dim3(rows), dim3(256), 0, st, true, prompt, P, i0, n, H, embed, vocab, r, err);
 }
 
 cudaError_t launch_prefill_norm(const float* r, const uint16_t* gamma, float eps, int H, uint16_t* y, uint16_t* y_lo,
                                 int rows, cudaStream_t st) {
-  prefill_norm_kernel<<<rows, 256, 0, st>>>(r, gamma, eps, H, y, y_lo);
-  return cudaGetLastError();
+  return launch(prefill_norm_kernel, dim3(rows), dim3(256), 0, st, true, r, gamma, eps, H, y, y_lo);
 }
 
 cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int32_t* pos, uint16_t* k_cache,
@@ -228,30 +244,25 @@ cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int3
   a.err = err;
   for (int j = 0; j < D / 2; ++j)
     a.inv_freq[j] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(D));
-  prefill_rope_store_kernel<<<rows, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch(prefill_rope_store_kernel, dim3(rows), dim3(256), 0, st, true, a);
 }
 
 cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st) {
-  prefill_cast_kernel<<<sms * 4, 256, 0, st>>>(x, y, y_lo, n);
-  return cudaGetLastError();
+  return launch(prefill_cast_kernel, dim3(sms * 4), dim3(256), 0, st, true, x, y, y_lo, n);
 }
 
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
                                cudaStream_t st, int half_rows) {
-  prefill_glu_kernel<<<sms * 4, 256, 0, st>>>(gu, I, h, h_lo, rows, half_rows);
-  return cudaGetLastError();
+  return launch(prefill_glu_kernel, dim3(sms * 4), dim3(256), 0, st, true, gu, I, h, h_lo, rows, half_rows);
 }
 
 cudaError_t launch_rows_argmax(const float* C, int B, int V, unsigned long long* keys, int sms, cudaStream_t st) {
   const dim3 grid(std::max(1, (sms * 2 + B - 1) / B), B);
-  rows_argmax_kernel<<<grid, 256, 0, st>>>(C, V, keys);
-  return cudaGetLastError();
+  return launch(rows_argmax_kernel, grid, dim3(256), 0, st, true, C, V, keys);
 }
 
 cudaError_t launch_rows_finish(const GemvIO& io, cudaStream_t st) {
-  rows_finish_kernel<<<1, 32, 0, st>>>(io);
-  return cudaGetLastError();
+  return launch(rows_finish_kernel, dim3(1), dim3(32), 0, st, true, io);
 }
 
 }  // namespace dec

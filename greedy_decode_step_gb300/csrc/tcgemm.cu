@@ -48,6 +48,7 @@ constexpr uint32_t kTcATile = kTcBM * kTcBK * 2;   // 16 KB
 constexpr uint32_t kTcSmemMax = 200 * 1024;
 constexpr int kTcMaxStages = 8;
 constexpr int kTcMaxSegs = 3;
+constexpr int kTcMaxClusterSplits = 8;  // K splits of a tile: one portable cluster
 
 struct TcArgs {
   CUtensorMap wmap[kTcMaxSegs];  // W of each segment: dims {K, N}, box {64, 128}, 128-byte swizzle
@@ -155,7 +156,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   const int kb0 = static_cast<int>((static_cast<long long>(split) * a.kb_total) / a.splits);
   const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * a.kb_total) / a.splits);
   const int nkb = kb1 - kb0;
-  const uint32_t ncols = a.BN <= 32 ? 32u : (a.BN <= 64 ? 64u : 128u);
+  // accumulator columns: [0, BN) the products with the hi parts, [BN, 2 BN)
+  // with the lo parts (one MMA of N = 2 BN per K step)
+  const uint32_t ncols = 2 * a.BN <= 32 ? 32u : (2 * a.BN <= 64 ? 64u : (2 * a.BN <= 128 ? 128u : 256u));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -182,7 +185,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     if (lane == 0) {
       const uint64_t wpol = l2_policy_evict_first();
       const uint64_t ypol = l2_policy_evict_last();
-      for (int i = 0; i < nkb; ++i) {
+      // the weights (never written by a kernel) of the first stages go out
+      // before the wait for the kernel that writes the activations
+      const int pre = min(nkb, a.stages);
+      for (int i = 0; i < pre; ++i) {
+        unsigned char* st = tiles + static_cast<size_t>(i) * stage_bytes;
+        mbar_arrive_expect_tx(&full[i], stage_bytes);
+        tma_load_2d(st, &a.wmap[seg], (kb0 + i) * kTcBK, m0, &full[i], wpol);
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      for (int i = 0; i < pre; ++i) {
+        unsigned char* st = tiles + static_cast<size_t>(i) * stage_bytes;
+        tma_load_2d(st + kTcATile, &a.yhi, (kb0 + i) * kTcBK, r0, &full[i], ypol);
+        tma_load_2d(st + kTcATile + b_tile, &a.ylo, (kb0 + i) * kTcBK, r0, &full[i], ypol);
+      }
+      for (int i = pre; i < nkb; ++i) {
         const int s = i % a.stages;
         if (i >= a.stages && !tc_wait(&empty[s], ((i / a.stages) - 1) & 1, a.err, kErrWaitEmpty)) {
           *stop = 1;
@@ -198,9 +216,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------------- MMA issuer (shared memory and TMEM only)
     if (lane == 0) {
-      const uint32_t idesc = tc_idesc(a.BN);
+      const uint32_t idesc = tc_idesc(2 * a.BN);
       for (int i = 0; i < nkb; ++i) {
         const int s = i % a.stages;
         if (!tc_wait(&full[s], (i / a.stages) & 1, a.err, kErrWaitFull)) {
@@ -211,11 +229,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         const uint32_t sa = smem_addr(tiles + static_cast<size_t>(s) * stage_bytes);
 #pragma unroll
         for (int kk = 0; kk < kTcBK / 16; ++kk) {
+          // B: the BN hi rows then the BN lo rows, one 2 BN-row operand
           const uint64_t ad = smem_desc_sw128(sa + kk * 32);
-          const uint64_t bh = smem_desc_sw128(sa + kTcATile + kk * 32);
-          const uint64_t bl = smem_desc_sw128(sa + kTcATile + b_tile + kk * 32);
-          tc_mma(tmem, ad, bh, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-          tc_mma(tmem, ad, bl, idesc, 1u);
+          const uint64_t bd = smem_desc_sw128(sa + kTcATile + kk * 32);
+          tc_mma(tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
       }
@@ -223,6 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------- epilogue (warps 2-5)
+    pdl_wait();  // C may be the output of an earlier kernel
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     int ok = 1;
     if (lane == 0) ok = (tc_wait(accum, 0, a.err, kErrWaitFull) && !*stop) ? 1 : 0;
@@ -233,8 +251,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     float* pbuf = reinterpret_cast<float*>(tiles);  // [BN][128] this split's partial (the ring is done)
     if (ok && nkb > 0) {
       for (int c0 = 0; c0 < a.BN; c0 += 16) {
-        float v[16];
+        float v[16], vl[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c0), v);
+        tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(a.BN + c0), vl);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] += vl[j];
         if (a.splits > 1) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) pbuf[(c0 + j) * kTcBM + 32 * q + lane] = v[j];
@@ -257,6 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     // in its shared memory, each CTA adds one slice of the tile's outputs
     // over all of them (distributed shared memory, in rank order: the same
     // sum whatever the timing) and writes C.
+    pdl_wait();  // every thread writes C here
     __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     const int total = a.BN * kTcBM;
@@ -265,14 +287,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     const uint32_t local = smem_addr(tiles);
     for (int o = split * per + static_cast<int>(threadIdx.x); o < o1; o += kTcThreads) {
       const int c = o / kTcBM, ml = o - c * kTcBM;
-      float sum = 0.f;
-      for (int k = 0; k < a.splits; ++k) {
-        uint32_t remote;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local + 4u * o), "r"(k));
-        float x;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(remote) : "memory");
-        sum += x;
+      // every rank's value in flight at once, then the sum in rank order
+      float x[kTcMaxClusterSplits];
+#pragma unroll
+      for (int k = 0; k < kTcMaxClusterSplits; ++k) {
+        x[k] = 0.f;
+        if (k < a.splits) {
+          uint32_t remote;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local + 4u * o), "r"(k));
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x[k]) : "r"(remote));
+        }
       }
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < kTcMaxClusterSplits; ++k)
+        if (k < a.splits) sum += x[k];
       const int r = r0 + c, mm = m0 + ml;
       if (r < a.rows && mm < a.N[seg]) {
         float* dst = a.C[seg] + static_cast<size_t>(r) * a.ldc + mm;
@@ -366,7 +395,7 @@ int max_active_clusters(int size, uint32_t smem) {
 // cluster size).
 int tc_splits(int tiles, int kb_total, int sms, uint32_t smem) {
   int splits = 1;
-  while (splits * 2 <= 8 && tiles * splits * 2 <= sms && kb_total / (splits * 2) >= 4 &&
+  while (splits * 2 <= kTcMaxClusterSplits && tiles * splits * 2 <= sms && kb_total / (splits * 2) >= 4 &&
          max_active_clusters(splits * 2, smem) >= tiles)
     splits *= 2;
   return splits;
@@ -430,13 +459,15 @@ int tc_gemm(const TcSeg* segs, int n_seg, const uint16_t* Yhi, const uint16_t* Y
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a);
   if (e != cudaSuccess) {
     *why = cudaGetErrorString(e);
