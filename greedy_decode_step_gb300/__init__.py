@@ -33,7 +33,9 @@ class DecError(RuntimeError):
 
 class DecLayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")]
+                ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")] + \
+               [("rot_dim", ctypes.c_int), ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
+                ("w_gate", ctypes.c_void_p)]
 
 
 class DecModel(ctypes.Structure):
@@ -229,7 +231,9 @@ LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")
 class Model:
     """Device weights of a dense GQA decoder wrapped in a ``dec_model``.
 
-    layers: list of dicts with LAYER_KEYS -> bf16 CUDA tensors.
+    layers: list of dicts with LAYER_KEYS -> bf16 CUDA tensors; a gated-attention
+    layer adds any of "rot_dim" (int), "q_norm", "k_norm" ([D] gains) and
+    "w_gate" (or "wgate", [Hq*D, H]).
     embed / final_norm / lm_head: bf16 CUDA tensors (lm_head may be embed; any may be None).
     """
 
@@ -241,6 +245,10 @@ class Model:
         for i, l in enumerate(layers):
             for k in LAYER_KEYS:
                 setattr(self._lw[i], k, _ptr(l[k], _bf16, k))
+            self._lw[i].rot_dim = int(l.get("rot_dim", 0) or 0)
+            for k in ("q_norm", "k_norm", "w_gate"):
+                t = l.get(k) if l.get(k) is not None else l.get(k.replace("_", ""))  # "wgate" as well
+                setattr(self._lw[i], k, _ptr(t, _bf16, k))
         self.c = DecModel(n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, rms_eps, rope_theta,
                           _ptr(embed, _bf16, "embed"), _ptr(final_norm, _bf16, "final_norm"),
                           _ptr(lm_head, _bf16, "lm_head"), self._lw)

@@ -204,6 +204,26 @@ int bt_bucket(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 
 
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+// A layer of the gated-attention variant: q/k head norms, a partial rotary
+// or an output gate.
+bool layer_gated(const dec_layer_weights& w, int D) {
+  return (w.rot_dim != 0 && w.rot_dim != D) || w.q_norm || w.k_norm || w.w_gate;
+}
+bool model_gated(const dec_model* m) {
+  for (int l = 0; l < m->n_layers; ++l)
+    if (layer_gated(m->layers[l], m->head_dim)) return true;
+  return false;
+}
+// Columns of the batched path's QKV GEMM output row: q | k | v, then the
+// output gate when the model has one.
+size_t qkv_width(const dec_model* m) {
+  const size_t QD = static_cast<size_t>(m->n_heads) * m->head_dim;
+  bool gate = false;
+  for (int l = 0; l < m->n_layers; ++l) gate = gate || m->layers[l].w_gate != nullptr;
+  return QD + 2ull * m->n_kv_heads * m->head_dim + (gate ? QD : 0);
+}
+
+
 // ------------------------------------------------------------------------------- GEMV planning
 
 constexpr uint32_t kPartTarget = 24 * 1024;    // shared-memory path: bytes of the rows worked on side by side
@@ -378,7 +398,7 @@ struct StateWs {
   // batched prompt pass: rows of up to pf_rows positions (all sequences)
   int pf_rows;
   float* pf_r;          // [rows][H] residual
-  float* pf_big;        // [rows][max((Hq + 2 Hkv) D, 2 I)] GEMM outputs (q|k|v, then gate|up)
+  float* pf_big;        // [rows][max(qkv_width, 2 I)] GEMM outputs (q|k|v[|output gate], then gate|up)
   float* pf_q;          // [rows][Hq D] rotated queries
   float* pf_o;          // [rows][Hq D] attention output
   uint16_t* pf_bf;      // [rows][max(H, Hq D, I)] bf16 GEMM operand (hi part)
@@ -417,9 +437,9 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   w.pf_rows = B * pf_pos;
   const size_t R = static_cast<size_t>(w.pf_rows);
   const size_t H = m->hidden, QD = static_cast<size_t>(m->n_heads) * m->head_dim;
-  const size_t QKV = static_cast<size_t>(m->n_heads + 2 * m->n_kv_heads) * m->head_dim, I = m->intermediate;
+  const size_t I = m->intermediate;
   const size_t o_pf_r = c.take(sizeof(float) * R * H);
-  const size_t o_pf_big = c.take(sizeof(float) * R * std::max(QKV, 2 * I));
+  const size_t o_pf_big = c.take(sizeof(float) * R * std::max(qkv_width(m), 2 * I));
   const size_t o_pf_q = c.take(sizeof(float) * R * QD);
   const size_t o_pf_o = c.take(sizeof(float) * R * QD);
   const size_t o_pf_bf = c.take(sizeof(uint16_t) * R * std::max(H, std::max(QD, I)));
@@ -510,6 +530,12 @@ int check_model(const dec_model* m) {
     const void* p[] = {w.attn_norm, w.wq, w.wk, w.wv, w.wo, w.mlp_norm, w.wg, w.wu, w.wd};
     for (const void* q : p)
       DEC_CHECK(q != nullptr && aligned16(q), DEC_EINVAL, "layer %d: weights must be non-null and 16-byte aligned", l);
+    DEC_CHECK(w.rot_dim == 0 || (w.rot_dim >= 2 && w.rot_dim <= m->head_dim && w.rot_dim % 2 == 0), DEC_EINVAL,
+              "layer %d: rot_dim %d must be 0 or even in 2..head_dim", l, w.rot_dim);
+    const void* g[] = {w.q_norm, w.k_norm, w.w_gate};
+    for (const void* q : g)
+      DEC_CHECK(q == nullptr || aligned16(q), DEC_EINVAL, "layer %d: q_norm, k_norm and w_gate must be 16-byte aligned",
+                l);
   }
   return DEC_OK;
 }
@@ -563,7 +589,7 @@ bool plan_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, con
                StepArgs* a, uint32_t* smem, int* BT) {
   const bool with_head = head && m->lm_head != nullptr;
   const int B = s->batch;
-  if (B > 2 || m->n_layers > kStepMaxLayers) return false;
+  if (B > 2 || m->n_layers > kStepMaxLayers || model_gated(m)) return false;
   *BT = bt_bucket(B);
   const int H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
   uint32_t part = 0, pb = 0;
@@ -673,11 +699,12 @@ int enqueue_step(const dec_model* m, const dec_state* s, const DeviceInfo* dv, c
     // batch > 2: the weight GEMVs as tensor-core GEMMs with the batch as rows
     auto* in = static_cast<StateInternal*>(s->internal);
     const size_t need = 2ull * s->batch * std::max<size_t>(static_cast<size_t>(m->vocab), 1);
-    const size_t have = static_cast<size_t>(w.pf_rows) *
-                        std::max<size_t>(static_cast<size_t>(m->n_heads + 2 * m->n_kv_heads) * m->head_dim,
-                                         2ull * m->intermediate);
+    const size_t have = static_cast<size_t>(w.pf_rows) * std::max<size_t>(qkv_width(m), 2ull * m->intermediate);
     if (in && 2 * s->batch <= w.pf_rows && (!m->lm_head || need <= have))
       return step_gemm(m, s, dv, w, head, st);
+    DEC_CHECK(!model_gated(m), DEC_EUNSUPPORTED,
+              "gated-attention layers run on the batched-row path, which needs an initialised state "
+              "(dec_state_init) whose workspace holds the step's logits");
   }
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, I = m->intermediate;
   const bool fuse = norm_fusable(B, H);
@@ -824,6 +851,40 @@ int gemm_rows(const DeviceInfo* dv, const StateWs& w, std::initializer_list<TcSe
   return DEC_OK;
 }
 
+// The attention block's front half on the batched-row path: one GEMM for
+// [Wq; Wk; Wv] (and the output gate of a gated layer, as a fourth segment)
+// into rows of `ld` floats of c2, then the per-head norms / RoPE / K,V store.
+// Returns the gate's columns (null for a plain layer).
+int qkv_block(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, int l, const uint16_t* x,
+              const uint16_t* x_lo, int rows, int n, int i0, float* c2, float* q_out, cudaStream_t st,
+              const float** gate) {
+  const dec_layer_weights& lw = m->layers[l];
+  const int H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim, QD = Hq * D;
+  const int QKV = (Hq + 2 * Hkv) * D;
+  const int ld = static_cast<int>(qkv_width(m));
+  const TcSeg segs[4] = {{lw.wq, QD, c2}, {lw.wk, Hkv * D, c2 + QD}, {lw.wv, Hkv * D, c2 + QD + Hkv * D},
+                         {lw.w_gate, QD, c2 + QKV}};
+  const char* why = nullptr;
+  const int rc = tc_gemm(segs, lw.w_gate ? 4 : 3, x, x_lo, rows, H, ld, 0.f, w.gemm_part, w.gemm_part_bytes, dv->sms,
+                         dv->err, st, &why);
+  DEC_CHECK(rc == 0, rc == 1 ? DEC_EUNSUPPORTED : DEC_ECUDA, "tensor-core GEMM (%d rows, K %d): %s", rows, H,
+            why ? why : "failed");
+  RopeIO io{};
+  io.qkv = c2;
+  io.ld = ld;
+  io.q_out = q_out;
+  io.pos = s->pos;
+  io.k_cache = static_cast<uint16_t*>(s->k_cache[l]);
+  io.v_cache = static_cast<uint16_t*>(s->v_cache[l]);
+  io.q_norm = static_cast<const uint16_t*>(lw.q_norm);
+  io.k_norm = static_cast<const uint16_t*>(lw.k_norm);
+  io.rot_dim = lw.rot_dim;
+  io.eps = m->rms_eps;
+  DEC_CUDA(launch_prefill_rope_store(io, n, i0, rows, Hq, Hkv, D, s->max_seq, m->rope_theta, dv->err, st));
+  *gate = lw.w_gate ? c2 + QKV : nullptr;
+  return DEC_OK;
+}
+
 __global__ void prefill_finish_kernel(int32_t* token, int32_t* pos, int B, const int32_t* prompt, int P) {
   const int b = threadIdx.x;
   if (b < B) {
@@ -839,7 +900,7 @@ __global__ void prefill_finish_kernel(int32_t* token, int32_t* pos, int B, const
 int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, const StateWs& w, const int32_t* prompt,
                     int P, cudaStream_t st) {
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
-  const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D, WB = std::max(QKV, 2 * I);
+  const int I = m->intermediate, QD = Hq * D;
   const int per = w.pf_rows / B;
   for (int i0 = 0; i0 < P - 1; i0 += per) {
     const int n = std::min(per, P - 1 - i0);
@@ -852,11 +913,11 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
       uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
       DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, w.pf_bf,
                                    w.pf_bf_lo, R, st));
-      DEC_TRY(gemm_rows(dv, w, {{lw.wq, QD, w.pf_big}, {lw.wk, Hkv * D, w.pf_big + QD}, {lw.wv, Hkv * D,
-                        w.pf_big + QD + Hkv * D}}, H, w.pf_bf, w.pf_bf_lo, R, QKV, 0.f, st));
-      DEC_CUDA(launch_prefill_rope_store(w.pf_big, w.pf_q, s->pos, kc, vc, n, i0, R, Hq, Hkv, D, s->max_seq,
-                                         m->rope_theta, dv->err, st));
+      const float* gate = nullptr;
+      DEC_TRY(qkv_block(m, s, dv, w, l, w.pf_bf, w.pf_bf_lo, R, n, i0, w.pf_big, w.pf_q, st, &gate));
       AttnArgs t{};
+      t.gate = gate;
+      t.gate_ld = static_cast<int>(qkv_width(m));
       t.q = w.pf_q;
       t.k_cache = kc;
       t.v_cache = vc;
@@ -883,7 +944,6 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
       DEC_TRY(gemm_rows(dv, w, {{lw.wd, H, w.pf_r}}, I, w.pf_bf, w.pf_bf_lo, R, H, 1.f, st));
     }
   }
-  (void)WB;
   DEC_CUDA(launch(prefill_finish_kernel, dim3(1), dim3(32), 0, st, false, s->token, s->pos, B, prompt, P));
   return DEC_OK;
 }
@@ -897,7 +957,7 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
 int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, const StateWs& w, bool head,
               cudaStream_t st) {
   const int B = s->batch, H = m->hidden, Hq = m->n_heads, Hkv = m->n_kv_heads, D = m->head_dim;
-  const int I = m->intermediate, QD = Hq * D, QKV = (Hq + 2 * Hkv) * D;
+  const int I = m->intermediate, QD = Hq * D;
   float* r = s->residual;
   uint16_t* xs = w.pf_bf;   // [B][K] hi parts, then [B][K] lo parts
   float* c2 = w.pf_big;     // [B][N] GEMM output
@@ -909,11 +969,11 @@ int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, cons
     uint16_t* vc = static_cast<uint16_t*>(s->v_cache[l]);
     DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(lw.attn_norm), m->rms_eps, H, xs,
                                  xs + static_cast<size_t>(B) * H, B, st));
-    DEC_TRY(gemm_rows(dv, w, {{lw.wq, QD, c2}, {lw.wk, Hkv * D, c2 + QD}, {lw.wv, Hkv * D, c2 + QD + Hkv * D}}, H, xs,
-                      xs + static_cast<size_t>(B) * H, B, QKV, 0.f, st));
-    DEC_CUDA(launch_prefill_rope_store(c2, w.q, s->pos, kc, vc, 1, 0, B, Hq, Hkv, D, s->max_seq, m->rope_theta,
-                                       dv->err, st));
+    const float* gate = nullptr;
+    DEC_TRY(qkv_block(m, s, dv, w, l, xs, xs + static_cast<size_t>(B) * H, B, 1, 0, c2, w.q, st, &gate));
     AttnArgs t{};
+    t.gate = gate;
+    t.gate_ld = static_cast<int>(qkv_width(m));
     t.q = w.q;
     t.k_cache = kc;
     t.v_cache = vc;

@@ -51,7 +51,17 @@ struct AttnArgs {
   // r % rows_per_seq of sequence r / rows_per_seq (0: row r is sequence r at pos[r])
   int rows_per_seq;
   int row_pos0;
+  // optional output gate: o[b][h][d] *= sigmoid(gate[b * gate_ld + h * D + d])
+  const float* gate;
+  int gate_ld;
 };
+
+// The output gate's factor for element e = h * D + d of row b (1 without a gate).
+__device__ __forceinline__ float attn_gate(const AttnArgs& a, int b, int e) {
+  if (!a.gate) return 1.f;
+  const float z = __ldcg(a.gate + static_cast<size_t>(b) * a.gate_ld + e);
+  return 1.0f / (1.0f + expf(-z));
+}
 
 // The K and V caches as 2-D tensors [sequences * Hkv * S_max][D] of bf16
 // (box: 64 columns x kAttnTile rows, 128-byte swizzle).
@@ -443,9 +453,10 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
       if (pr < n_pairs) {
         const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
         const float inv = 1.0f / l_run[h];
-        float* dst = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + 2 * dp;
-        dst[0] = acc0[i] * inv;
-        dst[1] = acc1[i] * inv;
+        const int e = (g * G + h) * D + 2 * dp;
+        float* dst = a.o + static_cast<size_t>(b) * a.Hq * D + e;
+        dst[0] = acc0[i] * inv * attn_gate(a, b, e);
+        dst[1] = acc1[i] * inv * attn_gate(a, b, e + 1);
       }
     }
     return;
@@ -466,7 +477,7 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
   for (int e = tid; e < G * D; e += kAttnConsumers) {
     const int h = e / D, d = e - h * D;
     a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] =
-        attn_merge_one<D>(base, stride, n_active, G, h, d);
+        attn_merge_one<D>(base, stride, n_active, G, h, d) * attn_gate(a, b, g * G * D + e);
   }
   if (tid == 0) atomicExch(ticket, 0u);
 }

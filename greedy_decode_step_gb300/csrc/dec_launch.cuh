@@ -69,8 +69,21 @@ cudaError_t launch_prefill_embed(const int32_t* prompt, int P, int i0, int n, in
                                  int vocab, float* r, uint32_t* err, cudaStream_t st);
 cudaError_t launch_prefill_norm(const float* r, const uint16_t* gamma, float eps, int H, uint16_t* y, uint16_t* y_lo,
                                 int rows, cudaStream_t st);
-cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int32_t* pos, uint16_t* k_cache,
-                                      uint16_t* v_cache, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
+// Buffers of the RoPE + K/V store: qkv rows of ld floats (q | k | v ...);
+// optional per-head q / k RMSNorm gains (bf16 [D]) with eps; rot_dim 0 = D.
+struct RopeIO {
+  const float* qkv;
+  int ld;
+  float* q_out;
+  const int32_t* pos;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  const uint16_t* q_norm;
+  const uint16_t* k_norm;
+  int rot_dim;
+  float eps;
+};
+cudaError_t launch_prefill_rope_store(const RopeIO& io, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
                                       float theta, uint32_t* err, cudaStream_t st, int half_rows = 0);
 cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st);
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,

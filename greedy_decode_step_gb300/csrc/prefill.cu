@@ -89,19 +89,25 @@ __global__ void prefill_norm_kernel(const float* r, const uint16_t* gamma, float
 }
 
 struct RopeArgs {
-  const float* qkv;     // [rows][(Hq + 2 Hkv) * D]
+  const float* qkv;     // [rows][ld]: q [Hq*D] | k [Hkv*D] | v [Hkv*D] (| more columns)
   float* q_out;         // [rows][Hq * D] rotated queries
   const int32_t* pos;   // [B]
   uint16_t* k_cache;    // [B][Hkv][S_max][D]
   uint16_t* v_cache;
+  const uint16_t* q_norm;  // per-head RMSNorm gain [D] of the queries, or null
+  const uint16_t* k_norm;  // ... of the keys, or null
   int n, i0, Hq, Hkv, D, S_max;
+  int ld;               // row stride of qkv (floats)
+  int rot;              // rotary dims per head: pairs (j, j + rot/2), j < rot/2
+  float eps;
   int half_rows;        // > 0: row r of the GEMM output is rows r and r + half_rows added
   uint32_t* err;
-  double inv_freq[64];
+  double inv_freq[64];  // theta^(-2j/rot)
 };
 
-// Rotate-half RoPE of q (to q_out) and k at the row's position, k and v to
-// the cache.  One CTA per row; thread t takes pair t of each head.
+// Per q / k head (one warp each): the optional per-head RMSNorm, rotate-half
+// RoPE of the first `rot` dims at the row's position (the rest unrotated),
+// then q to q_out and k to the cache; v to the cache.  One CTA per row.
 __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
   pdl_wait();
   pdl_launch_dependents();
@@ -112,31 +118,50 @@ __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
     if (threadIdx.x == 0) atomicOr(a.err, kErrPosRange);
     return;
   }
-  const int half = a.D / 2;
-  const int width = (a.Hq + 2 * a.Hkv) * a.D;
-  const float* x = a.qkv + static_cast<size_t>(row) * width;
-  const float* x2 = a.half_rows ? x + static_cast<size_t>(a.half_rows) * width : nullptr;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rh = a.rot / 2;
+  const float* x = a.qkv + static_cast<size_t>(row) * a.ld;
+  const float* x2 = a.half_rows ? x + static_cast<size_t>(a.half_rows) * a.ld : nullptr;
   // the row's angles once (double-precision reduction), then every head
   __shared__ float cs_s[64], sn_s[64];
-  for (int j = threadIdx.x; j < half; j += blockDim.x) rope_cos_sin(p, a.inv_freq[j], &cs_s[j], &sn_s[j]);
+  __shared__ float hv_s[8][128];
+  for (int j = threadIdx.x; j < rh; j += blockDim.x) rope_cos_sin(p, a.inv_freq[j], &cs_s[j], &sn_s[j]);
   __syncthreads();
-  for (int t = threadIdx.x; t < (a.Hq + a.Hkv) * half; t += blockDim.x) {
-    const int hh = t / half, j = t - hh * half;
-    const float cs = cs_s[j], sn = sn_s[j];
-    float l2, h2;
-    const int e = hh * a.D + j;
-    const float lo = x2 ? x[e] + x2[e] : x[e];
-    const float hi = x2 ? x[e + half] + x2[e + half] : x[e + half];
-    rope_rotate(lo, hi, cs, sn, &l2, &h2);
-    if (hh < a.Hq) {
-      float* q = a.q_out + static_cast<size_t>(row) * a.Hq * a.D + hh * a.D;
-      q[j] = l2;
-      q[j + half] = h2;
-    } else {
-      uint16_t* dst = a.k_cache + ((static_cast<size_t>(b) * a.Hkv + (hh - a.Hq)) * a.S_max + p) * a.D;
-      dst[j] = f32_to_bf16(l2);
-      dst[j + half] = f32_to_bf16(h2);
+  float* hv = hv_s[warp];
+  for (int hh = warp; hh < a.Hq + a.Hkv; hh += 8) {
+    const float* xh = x + hh * a.D;
+    float ss = 0.f;
+    for (int e = lane; e < a.D; e += 32) {
+      const float v = x2 ? xh[e] + x2[hh * a.D + e] : xh[e];
+      hv[e] = v;
+      ss = fmaf(v, v, ss);
     }
+    const uint16_t* gain = hh < a.Hq ? a.q_norm : a.k_norm;
+    if (gain) {
+      const float inv = 1.0f / sqrtf(warp_sum(ss) / static_cast<float>(a.D) + a.eps);
+      for (int e = lane; e < a.D; e += 32)
+        hv[e] = (hv[e] * inv) * __uint_as_float(static_cast<uint32_t>(gain[e]) << 16);
+    }
+    __syncwarp();
+    float* q = hh < a.Hq ? a.q_out + static_cast<size_t>(row) * a.Hq * a.D + hh * a.D : nullptr;
+    uint16_t* dst =
+        hh < a.Hq ? nullptr : a.k_cache + ((static_cast<size_t>(b) * a.Hkv + (hh - a.Hq)) * a.S_max + p) * a.D;
+    for (int j = lane; j < rh; j += 32) {
+      float l2, h2;
+      rope_rotate(hv[j], hv[j + rh], cs_s[j], sn_s[j], &l2, &h2);
+      if (q) {
+        q[j] = l2;
+        q[j + rh] = h2;
+      } else {
+        dst[j] = f32_to_bf16(l2);
+        dst[j + rh] = f32_to_bf16(h2);
+      }
+    }
+    for (int e = a.rot + lane; e < a.D; e += 32) {
+      if (q) q[e] = hv[e];
+      else dst[e] = f32_to_bf16(hv[e]);
+    }
+    __syncwarp();
   }
   const int vo = (a.Hq + a.Hkv) * a.D;
   for (int t = threadIdx.x; t < a.Hkv * a.D; t += blockDim.x) {
@@ -225,16 +250,20 @@ cudaError_t launch_prefill_norm(const float* r, const uint16_t* gamma, float eps
   return launch(prefill_norm_kernel, dim3(rows), dim3(256), 0, st, true, r, gamma, eps, H, y, y_lo);
 }
 
-cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int32_t* pos, uint16_t* k_cache,
-                                      uint16_t* v_cache, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
+cudaError_t launch_prefill_rope_store(const RopeIO& io, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
                                       float theta, uint32_t* err, cudaStream_t st, int half_rows) {
   RopeArgs a{};
   a.half_rows = half_rows;
-  a.qkv = qkv;
-  a.q_out = q_out;
-  a.pos = pos;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
+  a.qkv = io.qkv;
+  a.q_out = io.q_out;
+  a.pos = io.pos;
+  a.k_cache = io.k_cache;
+  a.v_cache = io.v_cache;
+  a.q_norm = io.q_norm;
+  a.k_norm = io.k_norm;
+  a.ld = io.ld;
+  a.rot = io.rot_dim > 0 ? io.rot_dim : D;
+  a.eps = io.eps;
   a.n = n;
   a.i0 = i0;
   a.Hq = Hq;
@@ -242,8 +271,8 @@ cudaError_t launch_prefill_rope_store(const float* qkv, float* q_out, const int3
   a.D = D;
   a.S_max = S_max;
   a.err = err;
-  for (int j = 0; j < D / 2; ++j)
-    a.inv_freq[j] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(D));
+  for (int j = 0; j < a.rot / 2; ++j)
+    a.inv_freq[j] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(a.rot));
   return launch(prefill_rope_store_kernel, dim3(rows), dim3(256), 0, st, true, a);
 }
 

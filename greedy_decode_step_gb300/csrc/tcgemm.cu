@@ -47,7 +47,7 @@ constexpr int kTcThreads = 192;
 constexpr uint32_t kTcATile = kTcBM * kTcBK * 2;   // 16 KB
 constexpr uint32_t kTcSmemMax = 200 * 1024;
 constexpr int kTcMaxStages = 8;
-constexpr int kTcMaxSegs = 3;
+constexpr int kTcMaxSegs = 4;
 constexpr int kTcMaxClusterSplits = 8;  // K splits of a tile: one portable cluster
 
 struct TcArgs {

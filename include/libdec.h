@@ -210,6 +210,18 @@ typedef struct dec_layer_weights {
   const void* wg;        /* bf16 [I][H] */
   const void* wu;        /* bf16 [I][H] */
   const void* wd;        /* bf16 [H][I] */
+  /* Gated-attention variant (PR 8602, review "Two more decode-path
+   * suggestions", item 1): per-head RMSNorm of q and k with an effective
+   * gain, partial rotate-half RoPE over the first rot_dim dims of each head
+   * (angles p * theta^(-2i/rot_dim), pairs (i, i + rot_dim/2)), and the
+   * attention output multiplied elementwise by sigmoid(w_gate y) before
+   * o_proj, y the layer's normed input.  All zero / NULL: the plain layer.
+   * A model with any gated layer runs every step on the batched-row path
+   * (tensor-core GEMMs), whatever the batch. */
+  int rot_dim;           /* rotary dims per head: 0 (all D) or even, 2..D */
+  const void* q_norm;    /* bf16 [D] gain of the per-head query RMSNorm, or NULL */
+  const void* k_norm;    /* bf16 [D] gain of the per-head key RMSNorm, or NULL */
+  const void* w_gate;    /* bf16 [Hq*D][H] output-gate projection, or NULL */
 } dec_layer_weights;
 
 typedef struct dec_model {
