@@ -209,8 +209,9 @@ def test_teacher_forced_tokens_match_oracle(case):
         gd.dec_step(p.model, p.state)
         got = p.state.token.cpu().numpy()
         for b in range(B):
-            # the prompt pass runs its GEMMs on bf16-rounded activations, so
-            # the cache it leaves differs from the oracle's by bf16 roundings
+            # the prompt pass runs its GEMMs on hi/lo bf16 parts of the fp32
+            # activations and stores K/V as bf16, so its cache differs from
+            # the oracle's by roundings of that order
             assert_close(p.state.residual[b].cpu().numpy(), resid[b][s], TOL, f"residual step {s} row {b}")
             if margins[b, s] > MARGIN:
                 assert got[b] == toks[b, s], f"step {s} row {b}: gpu {got[b]} oracle {toks[b, s]}"
