@@ -347,8 +347,14 @@ int attn_splits(int B, int Hkv, int S_max, int sms, int requested, int waves = 1
   return std::max(1, std::min(std::max(one_wave, by_len), cap));
 }
 
-size_t attn_part_bytes(int B, int Hq, int Hkv, int D, int n_split) {
-  return static_cast<size_t>(B) * Hkv * n_split * (Hq / Hkv) * (D + 2) * sizeof(float);
+// Many rows and no prompt pass: the balanced schedule (one CTA per SM).
+bool attn_lean(int B, int Hkv, int rows_per_seq) { return rows_per_seq == 0 && B > 2 && B * Hkv <= kLeanMaxItems; }
+
+// Partial slots: n_split per (row, KV head), or two per CTA of the balanced schedule.
+size_t attn_part_bytes(int B, int Hq, int Hkv, int D, int n_split, int sms) {
+  const size_t slots = std::max<size_t>(static_cast<size_t>(B) * Hkv * n_split,
+                                        attn_lean(B, Hkv, 0) ? 2ull * sms : 0ull);
+  return slots * (Hq / Hkv) * (D + 2) * sizeof(float);
 }
 
 // Tensor maps over the K and V caches of the sequences a launch reads (rows
@@ -363,7 +369,10 @@ int run_attn(AttnArgs& a, int B, const DeviceInfo* dv, cudaStream_t st, bool pdl
   DEC_CHECK(make_tmap_sw128(&maps.k, a.k_cache, a.D, rows, kAttnTile) &&
                 make_tmap_sw128(&maps.v, a.v_cache, a.D, rows, kAttnTile),
             DEC_ECUDA, "attention: the driver refused a tensor map of the KV cache");
-  cudaError_t e = launch_attn(a, maps, B, st, pdl);
+  // the balanced schedule where the split grid would take more than one wave
+  const bool lean = attn_lean(B, a.Hkv, a.rows_per_seq) && static_cast<long long>(B) * a.Hkv * a.n_split > dv->sms;
+  a.B = B;
+  cudaError_t e = launch_attn(a, maps, B, lean ? dv->sms : 0, st, pdl);
   DEC_CHECK(e == cudaSuccess, DEC_ECUDA, "attention launch: %s", cudaGetErrorString(e));
   return DEC_OK;
 }
@@ -428,7 +437,7 @@ StateWs carve_state(const dec_model* m, int B, int S_max, int sms, unsigned char
   // the persistent step kernel (b <= 2) wants one item per CTA; the
   // single-op attention kernel holds two CTAs per SM
   w.n_split = attn_splits(B, m->n_kv_heads, S_max, sms, 0, B > 2 ? 2 : 1);
-  const size_t o_part = c.take(attn_part_bytes(B, m->n_heads, m->n_kv_heads, m->head_dim, w.n_split));
+  const size_t o_part = c.take(attn_part_bytes(B, m->n_heads, m->n_kv_heads, m->head_dim, w.n_split, sms));
   const size_t o_gbar = c.take(sizeof(unsigned int));
   const size_t o_abort = c.take(sizeof(int));
   const size_t o_exit = c.take(sizeof(unsigned int));
@@ -1097,9 +1106,9 @@ size_t dec_attn_workspace_size(int B, int Hq, int Hkv, int D, int S_max, int num
   if (B < 1 || Hkv < 1 || Hq < Hkv || S_max < 1 || D < 1) return 0;
   int sms = 152;
   DeviceInfo* dv;
-  if (num_splits <= 0 && device_info(&dv) == DEC_OK) sms = dv->sms;
+  if (device_info(&dv) == DEC_OK) sms = dv->sms;
   const int n = attn_splits(B, Hkv, S_max, sms, num_splits);
-  return 256 + (attn_part_bytes(B, Hq, Hkv, D, n) + 255) / 256 * 256 +
+  return 256 + (attn_part_bytes(B, Hq, Hkv, D, n, sms) + 255) / 256 * 256 +
          (sizeof(unsigned int) * B * Hkv + 255) / 256 * 256;
 }
 
@@ -1120,7 +1129,7 @@ int dec_gqa_decode_attn(const float* q, const void* k_cache, const void* v_cache
   DeviceInfo* dv;
   DEC_TRY(device_info(&dv));
   const int n = attn_splits(B, Hkv, S_max, dv->sms, num_splits);
-  const size_t part = (attn_part_bytes(B, Hq, Hkv, D, n) + 255) / 256 * 256;
+  const size_t part = (attn_part_bytes(B, Hq, Hkv, D, n, dv->sms) + 255) / 256 * 256;
   const size_t need = 256 + part + (sizeof(unsigned int) * B * Hkv + 255) / 256 * 256;
   DEC_CHECK(ws_bytes >= need, DEC_EINVAL, "attention workspace has %zu bytes, needs %zu", ws_bytes, need);
   unsigned char* base = static_cast<unsigned char*>(ws);
@@ -1536,7 +1545,7 @@ extern "C" int dec_gqa_decode_attn_noalloc(const float* q, const void* k_cache, 
   DeviceInfo* dv;
   DEC_TRY(device_info(&dv));
   const int n = attn_splits(B, Hkv, S_max, dv->sms, num_splits);
-  const size_t part = (attn_part_bytes(B, Hq, Hkv, D, n) + 255) / 256 * 256;
+  const size_t part = (attn_part_bytes(B, Hq, Hkv, D, n, dv->sms) + 255) / 256 * 256;
   const size_t tick = (sizeof(unsigned int) * B * Hkv + 255) / 256 * 256;
   const size_t need = 256 + part + tick;
   DEC_CHECK(need <= kNoAllocScratchBytes, DEC_ECAPACITY,

@@ -54,6 +54,8 @@ struct AttnArgs {
   // optional output gate: o[b][h][d] *= sigmoid(gate[b * gate_ld + h * D + d])
   const float* gate;
   int gate_ld;
+  // balanced schedule (attn_lean_kernel): the number of query rows
+  int B;
 };
 
 // The output gate's factor for element e = h * D + d of row b (1 without a gate).
@@ -303,17 +305,17 @@ __device__ __forceinline__ bool attn_warp_tile(const unsigned char* Kt, unsigned
 // l = sum_w e^(m_w - M) l_w, summed in warp order.  `ms`, `ls` hold
 // [kAttnWarps][16] floats, `obuf` attn_merge_bytes<D>(G) bytes (it may alias
 // the tiles: the caller has synchronised the consumers after the last tile).
-// Warps that own none of the split's `len` keys hold nothing and are skipped
-// (their terms would be exact zeros).  Ends with a barrier of the 256
+// Warps outside the mask `keys` own none of the split's keys, hold nothing
+// and are skipped (their terms would be exact zeros).  Ends with a barrier of the 256
 // consumer threads.
 template <int D, int NT>
-__device__ __forceinline__ void attn_merge_warps(AttnWarpState<D, NT>& st, int G, int len, float* ms, float* ls,
-                                                 float* obuf,
+__device__ __forceinline__ void attn_merge_warps_mask(AttnWarpState<D, NT>& st, int G, uint32_t keys, float* ms,
+                                                      float* ls, float* obuf,
                                                  float (&acc0)[attn_slots<D>()], float (&acc1)[attn_slots<D>()],
                                                  float* m_run, float* l_run) {
   constexpr int kStride = D + 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
-  const bool mine = attn_warp_has_keys(warp, len);
+  const bool mine = (keys >> warp) & 1u;
 #pragma unroll
   for (int nt = 0; nt < NT && mine; ++nt) {
 #pragma unroll
@@ -346,11 +348,11 @@ __device__ __forceinline__ void attn_merge_warps(AttnWarpState<D, NT>& st, int G
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kAttnWarps; ++w)
-        if (attn_warp_has_keys(w, len)) M = fmaxf(M, ms[w * 16 + h]);
+        if ((keys >> w) & 1u) M = fmaxf(M, ms[w * 16 + h]);
       float n0 = 0.f, n1 = 0.f, L = 0.f;
 #pragma unroll
       for (int w = 0; w < kAttnWarps; ++w) {
-        if (!attn_warp_has_keys(w, len)) continue;
+        if (!((keys >> w) & 1u)) continue;
         const float mw = ms[w * 16 + h];
         const float f = (mw == -INFINITY) ? 0.f : expf(mw - M);
         const float2 ov = *reinterpret_cast<const float2*>(obuf + (w * G + h) * kStride + 2 * dp);
@@ -367,6 +369,20 @@ __device__ __forceinline__ void attn_merge_warps(AttnWarpState<D, NT>& st, int G
     }
   }
   asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// Warps that hold keys of a split whose `len` keys start at its first tile.
+__device__ __forceinline__ uint32_t attn_keys_mask(int len) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int w = 0; w < kAttnWarps; ++w) m |= attn_warp_has_keys(w, len) ? (1u << w) : 0u;
+  return m;
+}
+template <int D, int NT>
+__device__ __forceinline__ void attn_merge_warps(AttnWarpState<D, NT>& st, int G, int len, float* ms, float* ls,
+                                                 float* obuf, float (&acc0)[attn_slots<D>()],
+                                                 float (&acc1)[attn_slots<D>()], float* m_run, float* l_run) {
+  attn_merge_warps_mask<D, NT>(st, G, attn_keys_mask(len), ms, ls, obuf, acc0, acc1, m_run, l_run);
 }
 
 // One merged output o[h][d] of a (row, KV head) from its n_active split
@@ -641,6 +657,237 @@ __global__ void __launch_bounds__(288, NT == 1 ? 2 : 1)
   float acc0[kMaxSlots], acc1[kMaxSlots];
   attn_merge_warps<D, NT>(st, G, k1 - k0, ms, ls, reinterpret_cast<float*>(ring), acc0, acc1, m_run, l_run);
   attn_finish<D>(a, b, g, split, n_active, G, acc0, acc1, m_run, l_run, is_last);
+}
+
+// ----------------------------------------------------------------------------- balanced schedule
+// For many rows (the batched decode step): the (row, KV head) items of
+// ceil(len / 64) tiles each are laid end to end, T tiles in all, and CTA c of
+// n = min(CTAs launched (one per SM), T) takes tiles [T c / n, T (c + 1) / n)
+// -- equal shares whatever the rows' cache lengths, one wave, and one TMA
+// ring that runs across item boundaries.  An item inside one CTA's range is finished
+// there; an item cut between CTAs leaves one partial per CTA (slot 2c for
+// the CTA's first item, 2c + 1 for its last), and the last of them to finish
+// (an atomic ticket) merges them in CTA order.
+constexpr int kLeanMaxItems = 255;
+constexpr uint32_t kLeanPrefOff = 2048;   // int [kLeanMaxItems + 1]: tile prefix of the items
+constexpr uint32_t kLeanSlotOff = 3072;   // int [256]: partial slots of the item being merged
+constexpr uint32_t kLeanRingOff = 4096;
+
+template <int D>
+__host__ __device__ constexpr int attn_lean_slots(int G) {
+  return (G <= 4 || D == 64) ? 6 : 4;
+}
+template <int D>
+__host__ __device__ constexpr uint32_t attn_lean_smem(int G) {
+  return 1024u + kLeanRingOff + static_cast<uint32_t>(attn_lean_slots<D>(G)) * 2u * attn_tile_bytes<D>() +
+         attn_merge_bytes<D>(G);
+}
+
+// The item holding tile t (Tpre ascending; items without tiles are skipped).
+__device__ __forceinline__ int lean_item(const int* Tpre, int items, int t) {
+  int lo = 0, hi = items - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (Tpre[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+// The CTA whose range holds tile x, and the first tile of CTA c.
+__device__ __forceinline__ int lean_cta(int x, int n, int T) {
+  return static_cast<int>(((static_cast<long long>(x) + 1) * n - 1) / T);
+}
+__device__ __forceinline__ int lean_t0(int c, int n, int T) {
+  return static_cast<int>(static_cast<long long>(T) * c / n);
+}
+
+template <int D, int NT, int SLOTS>
+__global__ void __launch_bounds__(288, 1)
+    attn_lean_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ AttnMaps mp) {
+  static_assert(SLOTS % 2 == 0, "ring slots: even");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 128);
+  int* is_last = reinterpret_cast<int*>(smem + 132);
+  float* m_run = reinterpret_cast<float*>(smem + 256);
+  float* l_run = m_run + kAttnMaxGroup;
+  float* ms = reinterpret_cast<float*>(smem + 512);
+  float* ls = reinterpret_cast<float*>(smem + 1024);
+  int* Tpre = reinterpret_cast<int*>(smem + kLeanPrefOff);
+  int* slots_s = reinterpret_cast<int*>(smem + kLeanSlotOff);
+  unsigned char* ring = smem + kLeanRingOff;
+  constexpr uint32_t kTileBytes = attn_tile_bytes<D>();
+  float* obuf = reinterpret_cast<float*>(ring + SLOTS * 2 * kTileBytes);
+  const int G = a.Hq / a.Hkv;
+  const int items = a.B * a.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // tiles per item and their prefix (warp 0, 32 items per round)
+  if (warp == 0) {
+    int carry = 0;
+    if (lane == 0) Tpre[0] = 0;
+    for (int base = 0; base < items; base += 32) {
+      const int i = base + lane;
+      int nt = 0;
+      if (i < items) {
+        const int p = a.pos[i / a.Hkv];
+        if (p < 0 || p >= a.S_max) {
+          if (i % a.Hkv == 0 && blockIdx.x == 0) atomicOr(a.err, kErrPosRange);
+        } else {
+          nt = (p + kAttnTile) / kAttnTile;  // ceil((p + 1) / 64)
+        }
+      }
+      int v = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (i < items) Tpre[i + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  if (warp == kAttnWarps && lane == 0) {
+    for (int i = 0; i < SLOTS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kAttnWarps / 2);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // with fewer tiles than CTAs only the first T CTAs work, so that every CTA
+  // in use holds at least one tile and the CTAs holding an item are consecutive
+  const int T = Tpre[items];
+  const int n = min(static_cast<int>(gridDim.x), T), c = blockIdx.x;
+  if (c >= n) return;  // the same verdict in every thread
+  const int t0 = lean_t0(c, n, T), t1 = lean_t0(c + 1, n, T);
+
+  if (warp == kAttnWarps) {
+    // ----------------------------------------------------------- producer warp
+    int issued = 0;
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int i = lean_item(Tpre, items, t0);
+      for (int t = t0; t < t1; ++t) {
+        while (t >= Tpre[i + 1]) ++i;
+        const int k = t - t0, slot = k % SLOTS;
+        if (k >= SLOTS && !mbar_wait(&empty[slot], ((k / SLOTS) - 1) & 1, abort_flag, a.err, kErrWaitEmpty)) break;
+        const int b = i / a.Hkv, g = i - b * a.Hkv;
+        const int y = (b * a.Hkv + g) * a.S_max + (t - Tpre[i]) * kAttnTile;
+        unsigned char* dst = ring + static_cast<size_t>(slot) * 2 * kTileBytes;
+        mbar_arrive_expect_tx(&full[slot], 2u * kTileBytes);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_2d(dst + h * (kAttnTile * 128), &mp.k, 64 * h, y, &full[slot], policy);
+          tma_load_2d(dst + kTileBytes + h * (kAttnTile * 128), &mp.v, 64 * h, y, &full[slot], policy);
+        }
+        issued = k + 1;
+      }
+    }
+    __syncwarp();
+    asm volatile("bar.sync 2, 288;" ::: "memory");
+    if (lane == 0) {
+      for (int k = max(0, issued - SLOTS); k < issued; ++k) {
+        const uint64_t ts = globaltimer_ns();
+        while (!mbar_try_wait(&full[k % SLOTS], (k / SLOTS) & 1)) {
+          if (globaltimer_ns() - ts > kWaitLimitNs) {
+            atomicOr(a.err, kErrDrain);
+            break;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- consumer warps
+  const int r0 = attn_warp_row0(warp), par = attn_warp_parity(warp);
+  const int first_item = lean_item(Tpre, items, t0);
+  const size_t stride = static_cast<size_t>(G) * (D + 2);
+  constexpr int kMaxSlots = attn_slots<D>();
+  int i = first_item;
+  for (int t = t0; t < t1;) {  // one item (its part in this range) per round; CTA-uniform
+    while (t >= Tpre[i + 1]) ++i;
+    const int seg_a = t, seg_end = min(t1, Tpre[i + 1]);
+    const int b = i / a.Hkv, g = i - b * a.Hkv;
+    const int len = a.pos[b] + 1;
+    AttnQFrag<D, NT> qf;
+    attn_q_load<D, NT>(qf, a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D, G);
+    AttnWarpState<D, NT> st;
+    attn_state_init<D, NT>(st);
+    bool ok = true;
+    for (int tt = seg_a + ((par - (seg_a - t0)) & 1); tt < seg_end; tt += 2) {
+      const int k = tt - t0, slot = k % SLOTS;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&full[slot], (k / SLOTS) & 1, abort_flag, a.err, kErrWaitFull) ? 1 : 0;
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      if (!w_ok) {
+        ok = false;
+        break;
+      }
+      (void)mbar_try_wait(&full[slot], (k / SLOTS) & 1);  // completed phase: acquire for every lane
+      const int nk = min(kAttnTile, len - (tt - Tpre[i]) * kAttnTile);
+      unsigned char* Kt = ring + static_cast<size_t>(slot) * 2 * kTileBytes;
+      if (r0 < nk && attn_warp_tile<D, NT>(Kt, Kt + kTileBytes, r0, nk, a.scale, qf, st)) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (consumers_barrier_or(!ok)) break;
+    // the warps holding keys: those whose first tile of the segment reaches their rows
+    uint32_t keys = 0;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const int first = seg_a + ((attn_warp_parity(w) - (seg_a - t0)) & 1);
+      if (first < seg_end && attn_warp_row0(w) < len - (first - Tpre[i]) * kAttnTile) keys |= 1u << w;
+    }
+    float acc0[kMaxSlots], acc1[kMaxSlots];
+    attn_merge_warps_mask<D, NT>(st, G, keys, ms, ls, obuf, acc0, acc1, m_run, l_run);
+    const int c_first = lean_cta(Tpre[i], n, T), c_last = lean_cta(Tpre[i + 1] - 1, n, T);
+    if (c_first == c_last) {
+      attn_finish<D>(a, b, g, 0, 1, G, acc0, acc1, m_run, l_run, is_last);  // the whole item: final output
+    } else {
+      float* mine = a.part + static_cast<size_t>(2 * c + (i == first_item ? 0 : 1)) * stride;
+      attn_store_partial<D>(mine, G, acc0, acc1, m_run, l_run);
+      __threadfence();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      unsigned int* ticket = a.tickets + i;
+      if (tid == 0) *is_last = (atomicAdd(ticket, 1u) == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (*is_last) {
+        __threadfence();
+        const int nseg = c_last - c_first + 1;
+        for (int j = tid; j < nseg; j += kAttnConsumers) {
+          const int cc = c_first + j;
+          slots_s[j] = 2 * cc + (lean_item(Tpre, items, lean_t0(cc, n, T)) == i ? 0 : 1);
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        for (int e = tid; e < G * D; e += kAttnConsumers) {
+          const int h = e / D, d = e - h * D;
+          float M = -INFINITY;
+          for (int j = 0; j < nseg; ++j) M = fmaxf(M, __ldcg(a.part + slots_s[j] * stride + G * D + h));
+          float L = 0.f, num = 0.f;
+          for (int j = 0; j < nseg; ++j) {
+            const float* ps = a.part + slots_s[j] * stride;
+            const float w = expf(__ldcg(ps + G * D + h) - M);
+            L = fmaf(w, __ldcg(ps + G * D + G + h), L);
+            num = fmaf(w, __ldcg(ps + h * D + d), num);
+          }
+          a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] =
+              num / L * attn_gate(a, b, g * G * D + e);
+        }
+        if (tid == 0) atomicExch(ticket, 0u);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
+    t = seg_end;
+  }
+  asm volatile("bar.sync 2, 288;" ::: "memory");
 }
 
 }  // namespace dec

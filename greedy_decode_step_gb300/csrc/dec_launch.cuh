@@ -57,8 +57,9 @@ cudaError_t launch_gemv_resid(int BT, bool xreg, const GemvArgs& a, int grid, ui
                              bool pdl);
 cudaError_t launch_gemv_head(int BT, bool xreg, const GemvArgs& a, int grid, uint32_t smem, cudaStream_t st,
                              bool pdl);
-// Attention (attn.cu): grid (n_split, Hkv, B); maps from make_attn_maps.
-cudaError_t launch_attn(const AttnArgs& a, const AttnMaps& maps, int B, cudaStream_t st, bool pdl);
+// Attention (attn.cu): grid (n_split, Hkv, B), or with lean_ctas > 0 the
+// balanced schedule over a.B rows on lean_ctas CTAs.
+cudaError_t launch_attn(const AttnArgs& a, const AttnMaps& maps, int B, int lean_ctas, cudaStream_t st, bool pdl);
 uint32_t attn_launch_smem(int D);
 // bf16 [outer][inner] row-major tensor map with a box of 64 x box_rows and the
 // 128-byte swizzle (false if the driver refuses it).

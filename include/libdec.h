@@ -109,8 +109,14 @@ size_t dec_attn_workspace_size(int B, int Hq, int Hkv, int D, int S_max, int num
  *   o[b][h] = sum_j softmax_j(q[b][h] . K[b][g][j] / sqrt(D)) V[b][g][j]
  * q, o: fp32 [B][Hq][D]; caches bf16 [B][Hkv][S_max][D].  Keys are split into
  * up to num_splits ranges (0 = a choice from B, Hkv and S_max), merged by
- * log-sum-exp.  ws: device workspace of dec_attn_workspace_size() bytes; its
- * counters are reset by this call.
+ * log-sum-exp.  With B > 2 rows and more (row, KV head, split) work items than
+ * the GPU has SMs, the balanced schedule runs instead: one CTA per SM, each
+ * taking an equal run of the rows' 64-key tiles laid end to end, rows cut
+ * between CTAs merged the same way.  The caches are read through 2-D TMA
+ * tensor maps made on the host for each call (16-byte aligned caches,
+ * B * Hkv * S_max below 2^31 rows, else DEC_EUNSUPPORTED).  ws: device
+ * workspace of dec_attn_workspace_size() bytes; its counters are reset by this
+ * call.
  */
 int dec_gqa_decode_attn(const float* q, const void* k_cache, const void* v_cache, const int32_t* pos, float* o,
                         void* ws, size_t ws_bytes, int B, int Hq, int Hkv, int D, int S_max, int num_splits,

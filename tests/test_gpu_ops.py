@@ -241,3 +241,25 @@ def test_lmhead_ties_pick_lowest_index():
         W2[V - 1 if first != V - 1 else 0] = W[w]
         gd.dec_lmhead_argmax(dev_f32(r), dev_bf16(g), 1e-6, dev_bf16(W2), tok)
         assert int(tok.item()) == min(first, w, V - 1 if first != V - 1 else 0)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,pos", [
+    (3, 4, 2, 64, [40, 17, 64]),          # fewer tiles than SMs: one tile per CTA, the 2-tile item split
+    (5, 12, 3, 128, [8191, 0, 76, 2999, 4095]),
+    (16, 12, 3, 128, [511] * 16),
+    (4, 32, 2, 128, [300, 1, 5000, 64]),  # 16-head groups
+])
+def test_attention_balanced_schedule_rows(B, Hq, Hkv, D, pos):
+    """b > 2 with more split work items than one wave (64 splits requested)
+    takes the balanced schedule (one CTA per SM over the rows' tiles laid end
+    to end; items cut between CTAs merge their partials): every row against
+    the oracle, and twice the same bits."""
+    S_max = max(pos) + 8
+    Kb, Vb, q, o = _attn_case(B, Hq, Hkv, D, S_max, pos, seed=11)
+    Kd, Vd, qd, pd = dev_bf16(Kb), dev_bf16(Vb), dev_f32(q), dev_i32(pos)
+    ws = gd.dec_gqa_decode_attn(qd, Kd, Vd, pd, o, num_splits=64)
+    o2 = torch.empty_like(o)
+    gd.dec_gqa_decode_attn(qd, Kd, Vd, pd, o2, ws=ws, num_splits=64)
+    assert torch.equal(o, o2)
+    for b in range(B):
+        assert rel_err(o[b].cpu().numpy(), oracle.attention(q[b], Kb[b], Vb[b], pos[b] + 1)) < 1e-4, b
