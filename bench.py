@@ -421,7 +421,8 @@ def run_attn_op(args, world, rank, local):
            "config": {"workload": f"{args.workload}: one layer of {w.description}", "batch": B, "Hq": Hq,
                       "Hkv": Hkv, "head_dim": D, "kv_lens": kv,
                       "l2": "inputs larger than L2 (K/V bytes per launch above 129 MB)"},
-           "roofline": {"kernel": f"attn_kernel<{D},1>", "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+           "roofline": {"kernel": "attn_kernel / attn_lean_kernel (balanced schedule beyond one wave)", "bound": "hbm",
+                        "achieved": round(gbs, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": f"{src} (burst copy)",
                         "traffic": committed_traffic(f"attn_kernel_{args.workload[5:]}"),
                         "algorithmic_bytes_per_launch": int(alg), "avg_launch_us": round(avg_s * 1e6, 2),
@@ -465,7 +466,8 @@ def attn_roofline(gd, torch, model, st, m, dev, stream, tag, reps=4):
     alg = sum(m.n_kv_heads * k * D * 2 * 2 for k in lens) + 2 * B * Hq * D * 4
     peak, src = peaks()
     achieved = alg / avg_s / 1e9
-    return {"kernel": f"attn_kernel<{D},1> (split-K GQA decode attention, tensor cores)", "bound": "hbm",
+    return {"kernel": "split-K GQA decode attention on the tensor cores (attn_kernel; attn_lean_kernel, the "
+                      "balanced schedule, when the split grid exceeds one wave)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "peak_source": f"{src} (burst copy; kernel timed alone)", "traffic": committed_traffic(tag),
             "algorithmic_bytes_per_launch": int(alg), "avg_launch_us": round(avg_s * 1e6, 2), "launches_timed": n,

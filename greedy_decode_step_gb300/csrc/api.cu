@@ -932,6 +932,8 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
       t.v_cache = vc;
       t.pos = s->pos;
       t.o = w.pf_o;
+      t.o_hi = w.pf_bf;  // the o_proj GEMM's operand parts, written by the attention kernel
+      t.o_lo = w.pf_bf_lo;
       t.part = w.attn_part;
       t.tickets = w.attn_tickets;
       t.Hq = Hq;
@@ -943,7 +945,7 @@ int prefill_batched(const dec_model* m, dec_state* s, const DeviceInfo* dv, cons
       t.rows_per_seq = n;
       t.row_pos0 = i0;
       DEC_TRY(run_attn(t, R, dv, st, true));
-      DEC_CUDA(launch_prefill_cast(w.pf_o, w.pf_bf, w.pf_bf_lo, static_cast<size_t>(R) * QD, dv->sms, st));
+
       DEC_TRY(gemm_rows(dv, w, {{lw.wo, H, w.pf_r}}, QD, w.pf_bf, w.pf_bf_lo, R, H, 1.f, st));
       DEC_CUDA(launch_prefill_norm(w.pf_r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, w.pf_bf,
                                    w.pf_bf_lo, R, st));
@@ -988,6 +990,8 @@ int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, cons
     t.v_cache = vc;
     t.pos = s->pos;
     t.o = w.o;
+    t.o_hi = xs;  // the o_proj GEMM's operand parts, written by the attention kernel
+    t.o_lo = xs + static_cast<size_t>(B) * QD;
     t.part = w.attn_part;
     t.tickets = w.attn_tickets;
     t.Hq = Hq;
@@ -997,8 +1001,7 @@ int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, cons
     t.n_split = w.n_split;
     t.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
     DEC_TRY(run_attn(t, B, dv, st, true));
-    DEC_CUDA(launch_prefill_cast(w.o, xs, xs + static_cast<size_t>(B) * QD, static_cast<size_t>(B) * QD, dv->sms,
-                                 st));
+
     DEC_TRY(gemm_rows(dv, w, {{lw.wo, H, r}}, QD, xs, xs + static_cast<size_t>(B) * QD, B, H, 1.f, st));
     DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, xs,
                                  xs + static_cast<size_t>(B) * H, B, st));
@@ -1373,7 +1376,7 @@ int dec_step_launches(const dec_model* m, const dec_state* s, int* launches) {
     const TcSeg o[1] = {{nullptr, H, nullptr}};
     const TcSeg glu[2] = {{nullptr, I, nullptr}, {nullptr, I, nullptr}};
     const TcSeg head[1] = {{nullptr, m->vocab, nullptr}};
-    const int per_layer = 6 + tc_gemm_launches(qkv, 3, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, QD, pb, dv->sms) +
+    const int per_layer = 5 + tc_gemm_launches(qkv, 3, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, QD, pb, dv->sms) +
                           tc_gemm_launches(glu, 2, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, I, pb, dv->sms);
     *launches = (m->embed ? 1 : 0) + m->n_layers * per_layer +
                 (m->lm_head ? 3 + tc_gemm_launches(head, 1, B, H, pb, dv->sms) : 1);

@@ -56,7 +56,21 @@ struct AttnArgs {
   int gate_ld;
   // balanced schedule (attn_lean_kernel): the number of query rows
   int B;
+  // optional: the output also as bf16 parts for a GEMM, hi = bf16(o) and
+  // lo = bf16(o - hi), each [B][Hq * D] (o_hi null: fp32 o only)
+  uint16_t* o_hi;
+  uint16_t* o_lo;
 };
+
+// Writes output element e = ((b * Hq) + head) * D + d (fp32, and its bf16 parts when asked).
+__device__ __forceinline__ void attn_out(const AttnArgs& a, size_t e, float v) {
+  a.o[e] = v;
+  if (a.o_hi) {
+    const uint16_t h = f32_to_bf16(v);
+    a.o_hi[e] = h;
+    a.o_lo[e] = f32_to_bf16(v - __uint_as_float(static_cast<uint32_t>(h) << 16));
+  }
+}
 
 // The output gate's factor for element e = h * D + d of row b (1 without a gate).
 __device__ __forceinline__ float attn_gate(const AttnArgs& a, int b, int e) {
@@ -470,9 +484,9 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
         const int h = pr / kPairsPerHead, dp = pr - h * kPairsPerHead;
         const float inv = 1.0f / l_run[h];
         const int e = (g * G + h) * D + 2 * dp;
-        float* dst = a.o + static_cast<size_t>(b) * a.Hq * D + e;
-        dst[0] = acc0[i] * inv * attn_gate(a, b, e);
-        dst[1] = acc1[i] * inv * attn_gate(a, b, e + 1);
+        const size_t at = static_cast<size_t>(b) * a.Hq * D + e;
+        attn_out(a, at, acc0[i] * inv * attn_gate(a, b, e));
+        attn_out(a, at + 1, acc1[i] * inv * attn_gate(a, b, e + 1));
       }
     }
     return;
@@ -492,8 +506,8 @@ __device__ __forceinline__ void attn_finish(const AttnArgs& a, int b, int g, int
   const float* base = a.part + (static_cast<size_t>(b) * a.Hkv + g) * a.n_split * stride;
   for (int e = tid; e < G * D; e += kAttnConsumers) {
     const int h = e / D, d = e - h * D;
-    a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] =
-        attn_merge_one<D>(base, stride, n_active, G, h, d) * attn_gate(a, b, g * G * D + e);
+    attn_out(a, (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d,
+             attn_merge_one<D>(base, stride, n_active, G, h, d) * attn_gate(a, b, g * G * D + e));
   }
   if (tid == 0) atomicExch(ticket, 0u);
 }
@@ -878,8 +892,8 @@ __global__ void __launch_bounds__(288, 1)
             L = fmaf(w, __ldcg(ps + G * D + G + h), L);
             num = fmaf(w, __ldcg(ps + h * D + d), num);
           }
-          a.o[(static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d] =
-              num / L * attn_gate(a, b, g * G * D + e);
+          attn_out(a, (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G + h) * D + d,
+                   num / L * attn_gate(a, b, g * G * D + e));
         }
         if (tid == 0) atomicExch(ticket, 0u);
       }

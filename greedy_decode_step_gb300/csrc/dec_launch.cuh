@@ -86,7 +86,6 @@ struct RopeIO {
 };
 cudaError_t launch_prefill_rope_store(const RopeIO& io, int n, int i0, int rows, int Hq, int Hkv, int D, int S_max,
                                       float theta, uint32_t* err, cudaStream_t st, int half_rows = 0);
-cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st);
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
                                cudaStream_t st, int half_rows = 0);
 // Decode step at batch > 2 on the same GEMM path.

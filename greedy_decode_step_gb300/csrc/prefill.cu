@@ -8,8 +8,9 @@
 // rounding of them moves attention scores far enough to show in the logits.
 // The elementwise work between the GEMMs -- the embedding gather, RMSNorm,
 // rotate-half RoPE with the K/V store, SiLU*mul -- and the causal attention
-// (the decode attention kernel with one query row per position) are kernels
-// of this library.  Rows are laid out sequence-major: row r is position
+// (the decode attention kernel with one query row per position, which also
+// writes its output as the o_proj GEMM's bf16 parts) are kernels of this
+// library.  Rows are laid out sequence-major: row r is position
 // pos[b] + i0 + i of sequence b = r / n, i = r % n, for a chunk of n
 // positions starting at i0.
 //
@@ -171,15 +172,6 @@ __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
   }
 }
 
-// hi/lo bf16 parts of an fp32 array.
-__global__ void prefill_cast_kernel(const float* x, uint16_t* y, uint16_t* y_lo, size_t n) {
-  pdl_wait();
-  pdl_launch_dependents();
-  for (size_t k = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; k < n;
-       k += static_cast<size_t>(gridDim.x) * blockDim.x)
-    split_bf16(x[k], &y[k], &y_lo[k]);
-}
-
 // h = silu(g) * u as hi/lo bf16 parts, from gu = [rows][2 I] (gate columns,
 // then up; with half_rows > 0 rows r and r + half_rows added).
 __global__ void prefill_glu_kernel(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int half_rows) {
@@ -274,10 +266,6 @@ cudaError_t launch_prefill_rope_store(const RopeIO& io, int n, int i0, int rows,
   for (int j = 0; j < a.rot / 2; ++j)
     a.inv_freq[j] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(a.rot));
   return launch(prefill_rope_store_kernel, dim3(rows), dim3(256), 0, st, true, a);
-}
-
-cudaError_t launch_prefill_cast(const float* x, uint16_t* y, uint16_t* y_lo, size_t n, int sms, cudaStream_t st) {
-  return launch(prefill_cast_kernel, dim3(sms * 4), dim3(256), 0, st, true, x, y, y_lo, n);
 }
 
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,

@@ -295,7 +295,7 @@ def test_step_launch_count():
     the GEMM); then the final norm, the LM-head GEMM, the row argmax and the
     bookkeeping."""
     m = synth.workload("tiny", n_layers=2).model
-    for B, want in ((1, {1}), (2, {1}), (3, {1 + 2 * (6 + 4) + 4})):
+    for B, want in ((1, {1}), (2, {1}), (3, {1 + 2 * (5 + 4) + 4})):
         p = _fresh(m, B, 64)
         assert gd.dec_step_launches(p.model, p.state) in want
 
