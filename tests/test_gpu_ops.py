@@ -248,6 +248,7 @@ def test_lmhead_ties_pick_lowest_index():
     (5, 12, 3, 128, [8191, 0, 76, 2999, 4095]),
     (16, 12, 3, 128, [511] * 16),
     (4, 32, 2, 128, [300, 1, 5000, 64]),  # 16-head groups
+    (3, 8, 1, 128, [20000, 5, 5]),        # one row cut across ~150 CTAs (their partials merged), 8-head groups
 ])
 def test_attention_balanced_schedule_rows(B, Hq, Hkv, D, pos):
     """b > 2 with more split work items than one wave (64 splits requested)
@@ -262,4 +263,18 @@ def test_attention_balanced_schedule_rows(B, Hq, Hkv, D, pos):
     gd.dec_gqa_decode_attn(qd, Kd, Vd, pd, o2, ws=ws, num_splits=64)
     assert torch.equal(o, o2)
     for b in range(B):
+        assert rel_err(o[b].cpu().numpy(), oracle.attention(q[b], Kb[b], Vb[b], pos[b] + 1)) < 1e-4, b
+
+
+def test_attention_balanced_schedule_position_outside_cache():
+    """A row whose position lies outside the cache contributes no tiles to the
+    balanced schedule: the error bit is set, nothing is read for it, and the
+    other rows are still right."""
+    B, Hq, Hkv, D, S_max = 4, 16, 4, 128, 2048
+    pos = [2047, S_max, 900, 0]
+    Kb, Vb, q, o = _attn_case(B, Hq, Hkv, D, S_max, [2047, 0, 900, 0], seed=12)
+    o.zero_()
+    gd.dec_gqa_decode_attn(dev_f32(q), dev_bf16(Kb), dev_bf16(Vb), dev_i32(pos), o, num_splits=64)
+    assert gd.device_error(clear=True) & 4
+    for b in (0, 2, 3):
         assert rel_err(o[b].cpu().numpy(), oracle.attention(q[b], Kb[b], Vb[b], pos[b] + 1)) < 1e-4, b
