@@ -121,6 +121,8 @@ CASES = [
     (VOCAB, 8.0, True, 0.6, 0, 0.95, 1.3, 0.5),
     (4104, 2.0, True, 1.0, 5000, 0.3, 1.0, 0.5),   # top_k >= V: no cut
     (256000, 4.0, True, 0.8, 64, 0.9, 1.0, 0.5),   # 32,000 logits per CTA
+    (VOCAB, 2.0, True, 1.0, 1000, 0.9, 1.0, 0.5),  # more top-k candidates than one CTA finishes: cluster path
+    (VOCAB, 4.0, True, 0.7, 512, 0.9, 1.0, 0.5),   # exactly the candidates one CTA takes
 ]
 
 
@@ -206,3 +208,18 @@ def test_greedy_selection_of_lmhead_logits_equals_its_argmax(gd):
     gd.dec_select_tokens(logits, out)
     torch.cuda.synchronize()
     assert torch.equal(out, tok)
+
+
+def test_top_k_cut_inside_a_large_tie_group(gd):
+    """Top-k keeps every token tied at the cut: with 3 large logits and the
+    rest equal, top_k = 5 keeps the whole tie group (more candidates than one
+    CTA finishes, so the cluster path decides), and top_k = 3 keeps the three."""
+    V, B = VOCAB, 4
+    z = np.zeros((B, V), np.float32)
+    z[:, [10, 70_000, 151_000]] = [3.0, 2.5, 2.0]
+    u = np.array([0.1, 0.5, 0.9, 0.999], dtype=np.float32)
+    for K in (5, 3):
+        got = run(gd, z, u=u, temperature=1.0, top_k=K)
+        # the tie group spreads the draw over ~150,000 near-equal weights: every
+        # row lies near a boundary there and is checked against its neighbours
+        check_rows(got, z, u, None, 1.0, 1.0, K, 1.0, min_exact=1.0 if K == 3 else 0.0)
