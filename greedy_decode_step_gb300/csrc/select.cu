@@ -31,6 +31,15 @@
 // every sum is exact and independent of order: the cuts, the kept weight and
 // the draw are reproducible, and the draw lands in exactly one token.  No
 // step uses double precision.
+//
+// With a top-k cut of at most 256 the searches are usually skipped: every
+// survivor of the row is among each CTA's keys at or above the top_k-th
+// largest of its 512 thread maxima (top_k keys reach that bound, so it lies
+// at or below the CTA's own top_k-th largest key).  When those candidates
+// are few, each CTA orders its own and writes them into CTA 0, which ranks
+// them by binary search, applies top-p and draws, with the same integer
+// weights and rules; three cluster barriers in all.  Otherwise (large top_k,
+// wide ties at the cut, no top-k) the searches run as above.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -48,6 +57,7 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelPhases = 40;  // 1 (max) + 16 (top-k) + 16 (top-p) + 1 (draw), rounded up
 constexpr int kSelVals = 4;     // values one CTA publishes per phase
+constexpr int kSelCandMax = 256;  // top-k candidates a CTA may pass to the ranking in CTA 0
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 using u64 = unsigned long long;
@@ -60,6 +70,20 @@ struct SelShared {
   u64 warp_max[kSelWarps];
   u64 max_slot;
   u64 max_bcast;
+  // the top-k candidate path
+  uint32_t tsorted[kSelThreads];   // each warp's thread maxima, descending
+  uint32_t tcut;
+  uint32_t ckey[kSelCandMax];      // this CTA's candidates: keys and slice indices
+  uint16_t cand[kSelCandMax];
+  int cand_n, surv_n, token;
+  int cnt_slot;                    // read by the other CTAs of the cluster
+  int cnt_all[kSelCluster];
+};
+
+// A survivor of the top-k cut, ranked in CTA 0.
+struct SelSurvivor {
+  uint32_t key, idx;
+  u64 w;
 };
 
 // Monotone map of a float to an unsigned key (larger float, larger key); -0
@@ -235,6 +259,159 @@ __device__ uint32_t key_search(SelShared& sh, cg::cluster_group& cl, int& phase,
   return k;
 }
 
+// The 32 lanes' values in descending order (lane 0 the largest): a bitonic
+// network of compare-exchanges between lanes.
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(kFull, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? max(v, o) : min(v, o);
+    }
+  }
+  return v;
+}
+
+// A lower bound of this CTA's local goal-th largest key (goal <= 512): the
+// goal-th largest of the 512 threads' largest keys (`tmax`, 0 for a thread
+// without keys).  goal distinct keys reach it, so every key at or above the
+// CTA's goal-th largest does too.  Each warp sorts its 32 values; a value's
+// rank is the number of values above it, a binary search in each warp's
+// list; the bound is the smallest value with fewer than goal values above.
+__device__ uint32_t cta_kth_thread_max(SelShared& sh, uint32_t tmax, int goal) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t v = warp_sort_desc(tmax);
+  sh.tsorted[warp * 32 + lane] = v;
+  if (tid == 0) sh.tcut = 0xFFFFFFFFu;
+  __syncthreads();
+  int above = 0;
+#pragma unroll 4
+  for (int w = 0; w < kSelWarps; ++w) {
+    const uint32_t* L = sh.tsorted + w * 32;
+    int l = 0, h = 32;
+    while (l < h) {
+      const int mid = (l + h) >> 1;
+      if (L[mid] > v)
+        l = mid + 1;
+      else
+        h = mid;
+    }
+    above += l;
+  }
+  if (above < goal) atomicMin(&sh.tcut, v);
+  __syncthreads();
+  return sh.tcut;
+}
+
+// Sum over the CTA of one value per thread (slot: a column of warp_part not
+// used since the last barrier); every thread returns the total.
+__device__ u64 cta_sum(SelShared& sh, u64 v, int slot) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) sh.warp_part[threadIdx.x >> 5][slot] = v;
+  __syncthreads();
+  u64 t = 0ull;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) t += sh.warp_part[w][slot];
+  return t;
+}
+
+// CTA 0 of the top-k candidate path: each CTA's candidates sit in `buf`
+// (cap entries per CTA, key descending then index ascending, cnt[c] of
+// them).  A candidate's rank is the number of candidates with a strictly
+// larger key (a binary search per CTA list).  That is its rank in the whole row
+// whenever it is below top_k: a CTA whose local cut lies above the key
+// contributes at least top_k larger keys by itself.  The survivors (rank <
+// top_k) then take the top-p cut and the draw with the same integer weights
+// and rules as the search path.
+__device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* buf, int cap, int m_all,
+                              SelSurvivor* surv, float zmax, float T, int32_t greedy, int row) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sh.surv_n = 0;
+    sh.token = -1;
+  }
+  __syncthreads();
+  for (int e = tid; e < m_all; e += kSelThreads) {
+    int c = 0, j = e;
+    while (j >= sh.cnt_all[c]) {
+      j -= sh.cnt_all[c];
+      ++c;
+    }
+    const uint2 me = buf[c * cap + j];
+    int gt = 0;
+    for (int c2 = 0; c2 < kSelCluster; ++c2) {
+      const uint2* sg = buf + c2 * cap;
+      int l = 0, h = sh.cnt_all[c2];
+      while (l < h) {
+        const int mid = (l + h) >> 1;
+        if (sg[mid].x > me.x)
+          l = mid + 1;
+        else
+          h = mid;
+      }
+      gt += l;
+    }
+    if (gt < a.top_k) {
+      const int p = atomicAdd(&sh.surv_n, 1);
+      surv[p] = SelSurvivor{me.x, me.y, weight_fixed(me.x, zmax, T)};
+    }
+  }
+  __syncthreads();
+  const int s = sh.surv_n;  // at most 4 per thread (m_all <= 2048)
+
+  // top-p: a survivor stays iff the survivors with a larger key weigh less than ceil(p * Z)
+  if (a.top_p < 1.0f) {
+    u64 z = 0ull;
+    for (int j = tid; j < s; j += kSelThreads) z += surv[j].w;
+    const u64 Z = cta_sum(sh, z, 0);
+    u64 target = scale_fixed(a.top_p, Z, true);
+    target = target > 0ull ? target : 1ull;
+    bool keep[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = tid + q * kSelThreads;
+      keep[q] = true;
+      if (j < s) {
+        const uint32_t kj = surv[j].key;
+        u64 wgt = 0ull;
+        for (int u = 0; u < s; ++u) wgt += surv[u].key > kj ? surv[u].w : 0ull;
+        keep[q] = wgt < target;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = tid + q * kSelThreads;
+      if (j < s && !keep[q]) surv[j].w = 0ull;
+    }
+    __syncthreads();
+  }
+
+  // the draw: the kept token whose interval of the running kept weight (index order) holds t
+  u64 mm = 0ull;
+  for (int j = tid; j < s; j += kSelThreads) mm += surv[j].w;
+  const u64 M = cta_sum(sh, mm, 1);
+  float uu = a.u[row];
+  uu = uu >= 0.f ? uu : 0.f;  // also maps NaN to 0
+  uu = uu < 1.f ? uu : 0x1.fffffep-1f;
+  const u64 t = scale_fixed(uu, M, false);
+  if (M > 0ull) {
+    for (int j = tid; j < s; j += kSelThreads) {
+      const u64 wj = surv[j].w;
+      if (wj == 0ull) continue;
+      const uint32_t ij = surv[j].idx;
+      u64 P = 0ull;
+      for (int u = 0; u < s; ++u) P += surv[u].idx < ij ? surv[u].w : 0ull;
+      if (P <= t && t - P < wj) sh.token = static_cast<int>(ij);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) a.token_out[row] = (M > 0ull && sh.token >= 0) ? sh.token : greedy;
+}
+
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
     select_kernel(const __grid_constant__ SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -247,8 +424,8 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   const int n = max(0, min(a.chunk, a.V - lo));
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
   uint32_t* seen = reinterpret_cast<uint32_t*>(smem + static_cast<size_t>(a.chunk) * 4);
-  uint16_t* list =
-      reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(a.chunk) * 4 + a.chunk / 8) + tid * a.list_cap;
+  uint16_t* list_base = reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(a.chunk) * 4 + a.chunk / 8);
+  uint16_t* list = list_base + tid * a.list_cap;
   const int seen_words = a.chunk / 32;
   int phase = 0;
 
@@ -267,23 +444,37 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 
   // ---- phase 0: keys of the penalised logits and the row maximum (smallest index on ties)
   u64 best = 0ull;
+  uint32_t tmax = 0u;  // this thread's largest key
   {
+    // thread t holds the keys of float4 blocks t, t + 512, ...; four blocks' loads in flight at once
     const float4* src = reinterpret_cast<const float4*>(a.logits + static_cast<size_t>(row) * a.V + lo);
-    for (int i4 = tid; i4 < n / 4; i4 += kSelThreads) {
-      const float4 v4 = src[i4];
-      const float zs[4] = {v4.x, v4.y, v4.z, v4.w};
+    const int n4 = n / 4;
+    for (int b0 = tid; b0 < n4; b0 += 4 * kSelThreads) {
+      float4 v4[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = i4 * 4 + e;
-        float z = zs[e];
-        if (penalise && ((seen[i >> 5] >> (i & 31)) & 1u))
-          z = z < 0.f ? __fmul_rn(z, a.penalty) : __fdiv_rn(z, a.penalty);
-        const uint32_t k = order_key(z);
-        keys[i] = k;
-        const u64 packed = (static_cast<u64>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(lo + i));
-        best = packed > best ? packed : best;
+      for (int q = 0; q < 4; ++q) {
+        const int i4 = b0 + q * kSelThreads;
+        v4[q] = i4 < n4 ? src[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i4 = b0 + q * kSelThreads;
+        if (i4 >= n4) break;
+        const float zs[4] = {v4[q].x, v4[q].y, v4[q].z, v4[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i4 * 4 + e;
+          float z = zs[e];
+          if (penalise && ((seen[i >> 5] >> (i & 31)) & 1u))
+            z = z < 0.f ? __fmul_rn(z, a.penalty) : __fdiv_rn(z, a.penalty);
+          const uint32_t k = order_key(z);
+          keys[i] = k;
+          const u64 packed = (static_cast<u64>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(lo + i));
+          best = packed > best ? packed : best;
+        }
       }
     }
+    tmax = static_cast<uint32_t>(best >> 32);
     best = warp_max(best);
     if (lane == 0) sh.warp_max[warp] = best;
     __syncthreads();
@@ -309,6 +500,63 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   }
   const float zmax = key_value(static_cast<uint32_t>(best >> 32));
   const float T = a.temperature;
+
+  // ---- top-k by candidates: each CTA's keys at or above its local top_k-th
+  // largest (ties included) hold every survivor of the row.  When they are
+  // few, each CTA orders its own and hands them to CTA 0, which ranks them
+  // and finishes the row alone (select_ranked); otherwise the cluster-wide
+  // searches below decide.
+  const int cap = min(kSelCandMax, a.list_cap * 16);  // CTA 0's buffer: 8 * cap * 8 bytes in the list area
+  if (a.top_k > 0 && a.top_k < a.V && a.top_k <= cap) {
+    if (tid == 0) sh.cand_n = 0;
+    const uint32_t lc = cta_kth_thread_max(sh, tmax, a.top_k);
+    if (tmax >= lc) {  // only a thread whose largest key reaches the bound holds candidates
+      for (int i4 = tid; i4 < n / 4; i4 += kSelThreads) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i4 * 4 + e;
+          const uint32_t key = keys[i];
+          if (key >= lc) {
+            const int p = atomicAdd(&sh.cand_n, 1);
+            if (p < kSelCandMax) {
+              sh.cand[p] = static_cast<uint16_t>(i);
+              sh.ckey[p] = key;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const int cnt = sh.cand_n;
+    if (tid == 0) sh.cnt_slot = cnt;
+    cl.sync();
+    if (tid < kSelCluster) sh.cnt_all[tid] = *cl.map_shared_rank(&sh.cnt_slot, tid);
+    __syncthreads();
+    int m_all = 0, most = 0;
+    for (int r = 0; r < kSelCluster; ++r) {
+      m_all += sh.cnt_all[r];
+      most = max(most, sh.cnt_all[r]);
+    }
+    // the same decision in every CTA; CTA 0's survivors (16 bytes each) fit its key area
+    if (most <= cap && m_all <= a.chunk / 4) {
+      uint2* dst = cl.map_shared_rank(reinterpret_cast<uint2*>(list_base), 0) + rank * cap;
+      for (int j = tid; j < cnt; j += kSelThreads) {
+        const uint32_t kj = sh.ckey[j];
+        const int ij = sh.cand[j];
+        int pos = 0;
+        for (int u = 0; u < cnt; ++u) {
+          const uint32_t ku = sh.ckey[u];
+          pos += (ku > kj || (ku == kj && sh.cand[u] < ij)) ? 1 : 0;
+        }
+        dst[pos] = make_uint2(kj, static_cast<uint32_t>(lo + ij));
+      }
+      cl.sync();  // the lists are in CTA 0; no shared memory of another CTA is read after this
+      if (rank == 0)
+        select_ranked(a, sh, reinterpret_cast<const uint2*>(list_base), cap, m_all,
+                      reinterpret_cast<SelSurvivor*>(smem), zmax, T, greedy, row);
+      return;
+    }
+  }
 
   // ---- top-k: largest key k with count(key >= k) >= top_k
   uint32_t kcut = 0u;
