@@ -288,20 +288,17 @@ __device__ uint32_t cta_kth_thread_max(SelShared& sh, uint32_t tmax, int goal) {
   if (tid == 0) sh.tcut = 0xFFFFFFFFu;
   __syncthreads();
   int above = 0;
-#pragma unroll 4
-  for (int w = 0; w < kSelWarps; ++w) {
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {  // 16 independent fixed-step searches
     const uint32_t* L = sh.tsorted + w * 32;
-    int l = 0, h = 32;
-    while (l < h) {
-      const int mid = (l + h) >> 1;
-      if (L[mid] > v)
-        l = mid + 1;
-      else
-        h = mid;
-    }
-    above += l;
+    int pos = 0;
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1) pos += L[pos + step - 1] > v ? step : 0;
+    pos += L[pos] > v ? 1 : 0;  // pos <= 31 here; 32 when all are above
+    above += pos;
   }
-  if (above < goal) atomicMin(&sh.tcut, v);
+  const uint32_t m = __reduce_min_sync(kFull, above < goal ? v : 0xFFFFFFFFu);
+  if (lane == 0 && m != 0xFFFFFFFFu) atomicMin(&sh.tcut, m);
   __syncthreads();
   return sh.tcut;
 }
@@ -327,8 +324,20 @@ __device__ u64 cta_sum(SelShared& sh, u64 v, int slot) {
 // top_k) then take the top-p cut and the draw with the same integer weights
 // and rules as the search path.
 __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* buf, int cap, int m_all,
-                              SelSurvivor* surv, float zmax, float T, int32_t greedy, int row) {
+                              SelSurvivor* surv, float T, int row) {
   const int tid = threadIdx.x;
+  // the row maximum (smallest index on ties): the best first entry of the lists
+  u64 top = 0ull;
+#pragma unroll
+  for (int c = 0; c < kSelCluster; ++c) {
+    if (sh.cnt_all[c] > 0) {
+      const uint2 h = buf[c * cap];
+      const u64 packed = (static_cast<u64>(h.x) << 32) | (0xFFFFFFFFu - h.y);
+      top = packed > top ? packed : top;
+    }
+  }
+  const float zmax = key_value(static_cast<uint32_t>(top >> 32));
+  const int32_t greedy = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(top & 0xFFFFFFFFull));
   if (tid == 0) {
     sh.surv_n = 0;
     sh.token = -1;
@@ -342,17 +351,16 @@ __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* b
     }
     const uint2 me = buf[c * cap + j];
     int gt = 0;
-    for (int c2 = 0; c2 < kSelCluster; ++c2) {
+#pragma unroll
+    for (int c2 = 0; c2 < kSelCluster; ++c2) {  // 8 independent fixed-step searches (cap <= 256)
       const uint2* sg = buf + c2 * cap;
-      int l = 0, h = sh.cnt_all[c2];
-      while (l < h) {
-        const int mid = (l + h) >> 1;
-        if (sg[mid].x > me.x)
-          l = mid + 1;
-        else
-          h = mid;
-      }
-      gt += l;
+      const int cn = sh.cnt_all[c2];
+      int pos = 0;
+#pragma unroll
+      for (int step = kSelCandMax / 2; step >= 1; step >>= 1)
+        pos += (pos + step <= cn && sg[pos + step - 1].x > me.x) ? step : 0;
+      pos += (pos < cn && sg[pos].x > me.x) ? 1 : 0;
+      gt += pos;
     }
     if (gt < a.top_k) {
       const int p = atomicAdd(&sh.surv_n, 1);
@@ -377,6 +385,7 @@ __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* b
       if (j < s) {
         const uint32_t kj = surv[j].key;
         u64 wgt = 0ull;
+#pragma unroll 4
         for (int u = 0; u < s; ++u) wgt += surv[u].key > kj ? surv[u].w : 0ull;
         keep[q] = wgt < target;
       }
@@ -404,6 +413,7 @@ __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* b
       if (wj == 0ull) continue;
       const uint32_t ij = surv[j].idx;
       u64 P = 0ull;
+#pragma unroll 4
       for (int u = 0; u < s; ++u) P += surv[u].idx < ij ? surv[u].w : 0ull;
       if (P <= t && t - P < wj) sh.token = static_cast<int>(ij);
     }
@@ -442,9 +452,13 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     __syncthreads();
   }
 
-  // ---- phase 0: keys of the penalised logits and the row maximum (smallest index on ties)
+  // the wait before the first access to another CTA's shared memory: every CTA has started
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  // ---- phase 0: keys of the penalised logits; each thread's largest keys
   u64 best = 0ull;
-  uint32_t tmax = 0u;  // this thread's largest key
+  uint32_t tmax = 0u, tsec = 0u;  // this thread's largest and second-largest keys (0: none)
+  u64 tbest = 0ull;               // this thread's largest key and its index, packed like best
   {
     // thread t holds the keys of float4 blocks t, t + 512, ...; four blocks' loads in flight at once
     const float4* src = reinterpret_cast<const float4*>(a.logits + static_cast<size_t>(row) * a.V + lo);
@@ -471,10 +485,87 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
           keys[i] = k;
           const u64 packed = (static_cast<u64>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(lo + i));
           best = packed > best ? packed : best;
+          tsec = max(tsec, min(tmax, k));
+          tmax = max(tmax, k);
         }
       }
     }
-    tmax = static_cast<uint32_t>(best >> 32);
+    tbest = best;
+  }
+  const float T = a.temperature;
+
+  // ---- top-k by candidates: every survivor of the row is among each CTA's
+  // keys at or above the bound of its thread maxima (ties included).  When
+  // they are few, each CTA orders its own and writes them into CTA 0, which
+  // ranks them and finishes the row alone (select_ranked): one cluster
+  // barrier, no exchange of the row maximum (it is the first entry of one of
+  // the lists).  Otherwise the cluster-wide searches below decide.
+  const int cap = min(kSelCandMax, a.list_cap * 16);  // CTA 0's buffer: 8 * cap * 8 bytes in the list area
+  const bool by_candidates = T > 0.f && a.top_k > 0 && a.top_k < a.V && a.top_k <= cap;  // the same in every CTA
+  if (by_candidates) {
+    if (tid == 0) sh.cand_n = 0;
+    const uint32_t lc = cta_kth_thread_max(sh, tmax, a.top_k);
+    if (tmax >= lc && tsec < lc && tid < n / 4) {
+      // the thread's one candidate is its largest key
+      const int p = atomicAdd(&sh.cand_n, 1);
+      if (p < kSelCandMax) {
+        sh.cand[p] = static_cast<uint16_t>(0xFFFFFFFFu - static_cast<uint32_t>(tbest & 0xFFFFFFFFull) - lo);
+        sh.ckey[p] = tmax;
+      }
+    } else if (tmax >= lc && tid < n / 4) {  // two or more of its keys reach the bound: look at them all
+      for (int i4 = tid; i4 < n / 4; i4 += kSelThreads) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i4 * 4 + e;
+          const uint32_t key = keys[i];
+          if (key >= lc) {
+            const int p = atomicAdd(&sh.cand_n, 1);
+            if (p < kSelCandMax) {
+              sh.cand[p] = static_cast<uint16_t>(i);
+              sh.ckey[p] = key;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const int cnt = sh.cand_n;
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
+    if (cnt <= cap) {
+      // this CTA's candidates, key descending then index ascending, into CTA 0's list area
+      uint2* dst = cl.map_shared_rank(reinterpret_cast<uint2*>(list_base), 0) + rank * cap;
+      for (int j = tid; j < cnt; j += kSelThreads) {
+        const uint32_t kj = sh.ckey[j];
+        const int ij = sh.cand[j];
+        int pos = 0;
+#pragma unroll 4
+        for (int u = 0; u < cnt; ++u) {
+          const uint32_t ku = sh.ckey[u];
+          pos += (ku > kj || (ku == kj && sh.cand[u] < ij)) ? 1 : 0;
+        }
+        dst[pos] = make_uint2(kj, static_cast<uint32_t>(lo + ij));
+      }
+    }
+    if (tid < kSelCluster) *cl.map_shared_rank(&sh.cnt_all[rank], tid) = cnt;  // every CTA learns every count
+    cl.sync();  // lists and counts delivered; no shared memory of another CTA is read after this
+    int m_all = 0, most = 0;
+    for (int r = 0; r < kSelCluster; ++r) {
+      m_all += sh.cnt_all[r];
+      most = max(most, sh.cnt_all[r]);
+    }
+    // the same decision in every CTA; CTA 0's survivors (16 bytes each) fit its key area
+    if (most <= cap && m_all <= a.chunk / 4) {
+      if (rank == 0)
+        select_ranked(a, sh, reinterpret_cast<const uint2*>(list_base), cap, m_all,
+                      reinterpret_cast<SelSurvivor*>(smem), T, row);
+      return;
+    }
+  } else {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
+  }
+
+  // ---- the row maximum (smallest index on ties): one exchange
+  {
     best = warp_max(best);
     if (lane == 0) sh.warp_max[warp] = best;
     __syncthreads();
@@ -493,70 +584,12 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   }
   const int32_t greedy = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
 
-  if (!(a.temperature > 0.f)) {
+  if (!(T > 0.f)) {
     if (rank == 0 && tid == 0) a.token_out[row] = greedy;
     cl.sync();  // no CTA leaves while a peer may still read its shared memory
     return;
   }
   const float zmax = key_value(static_cast<uint32_t>(best >> 32));
-  const float T = a.temperature;
-
-  // ---- top-k by candidates: each CTA's keys at or above its local top_k-th
-  // largest (ties included) hold every survivor of the row.  When they are
-  // few, each CTA orders its own and hands them to CTA 0, which ranks them
-  // and finishes the row alone (select_ranked); otherwise the cluster-wide
-  // searches below decide.
-  const int cap = min(kSelCandMax, a.list_cap * 16);  // CTA 0's buffer: 8 * cap * 8 bytes in the list area
-  if (a.top_k > 0 && a.top_k < a.V && a.top_k <= cap) {
-    if (tid == 0) sh.cand_n = 0;
-    const uint32_t lc = cta_kth_thread_max(sh, tmax, a.top_k);
-    if (tmax >= lc) {  // only a thread whose largest key reaches the bound holds candidates
-      for (int i4 = tid; i4 < n / 4; i4 += kSelThreads) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = i4 * 4 + e;
-          const uint32_t key = keys[i];
-          if (key >= lc) {
-            const int p = atomicAdd(&sh.cand_n, 1);
-            if (p < kSelCandMax) {
-              sh.cand[p] = static_cast<uint16_t>(i);
-              sh.ckey[p] = key;
-            }
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int cnt = sh.cand_n;
-    if (tid == 0) sh.cnt_slot = cnt;
-    cl.sync();
-    if (tid < kSelCluster) sh.cnt_all[tid] = *cl.map_shared_rank(&sh.cnt_slot, tid);
-    __syncthreads();
-    int m_all = 0, most = 0;
-    for (int r = 0; r < kSelCluster; ++r) {
-      m_all += sh.cnt_all[r];
-      most = max(most, sh.cnt_all[r]);
-    }
-    // the same decision in every CTA; CTA 0's survivors (16 bytes each) fit its key area
-    if (most <= cap && m_all <= a.chunk / 4) {
-      uint2* dst = cl.map_shared_rank(reinterpret_cast<uint2*>(list_base), 0) + rank * cap;
-      for (int j = tid; j < cnt; j += kSelThreads) {
-        const uint32_t kj = sh.ckey[j];
-        const int ij = sh.cand[j];
-        int pos = 0;
-        for (int u = 0; u < cnt; ++u) {
-          const uint32_t ku = sh.ckey[u];
-          pos += (ku > kj || (ku == kj && sh.cand[u] < ij)) ? 1 : 0;
-        }
-        dst[pos] = make_uint2(kj, static_cast<uint32_t>(lo + ij));
-      }
-      cl.sync();  // the lists are in CTA 0; no shared memory of another CTA is read after this
-      if (rank == 0)
-        select_ranked(a, sh, reinterpret_cast<const uint2*>(list_base), cap, m_all,
-                      reinterpret_cast<SelSurvivor*>(smem), zmax, T, greedy, row);
-      return;
-    }
-  }
 
   // ---- top-k: largest key k with count(key >= k) >= top_k
   uint32_t kcut = 0u;
