@@ -600,9 +600,10 @@ def run_select(args, world, rank, local):
                                   "top_k=50, top_p=0.9; L2 flushed before each call",
                       "tokens_equal_to_oracle": f"{agree}/{B}", "one_row_us": round(ms1 * 1e3, 2)},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                        "frac": round(gbs / peak, 4), "traffic": None, "peak_source": src,
-                        "note": "one cluster of 8 CTAs per row; top-k 50 takes the candidate path (three "
-                                "cluster barriers); latency of the dependent steps, not DRAM, bounds the call"},
+                        "frac": round(gbs / peak, 4), "traffic": committed_traffic("select_kernel_b16"),
+                        "peak_source": src,
+                        "note": "one cluster of 8 CTAs per row; top-k 50 takes the candidate path (one "
+                                "cluster barrier); latency of the dependent steps, not DRAM, bounds the call"},
            "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "us/call", "h2d_bytes_per_step": int(algo - B * 4),
                    "d2h_bytes_per_step": B * 4},
            "cpu_baseline": {"value": round(cpu_ms * 1e3, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
