@@ -108,7 +108,9 @@ struct RopeArgs {
 
 // Per q / k head (one warp each): the optional per-head RMSNorm, rotate-half
 // RoPE of the first `rot` dims at the row's position (the rest unrotated),
-// then q to q_out and k to the cache; v to the cache.  One CTA per row.
+// then q to q_out and k to the cache; v to the cache.  A row's heads are
+// spread over ceil((Hq + Hkv) / 8) CTAs of 8 warps, one head per warp, and
+// the V entries over the same CTAs.
 __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
   pdl_wait();
   pdl_launch_dependents();
@@ -116,59 +118,87 @@ __global__ void prefill_rope_store_kernel(const __grid_constant__ RopeArgs a) {
   const int b = row / a.n, i = row - b * a.n;
   const int p = a.pos[b] + a.i0 + i;
   if (p < 0 || p >= a.S_max) {
-    if (threadIdx.x == 0) atomicOr(a.err, kErrPosRange);
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, kErrPosRange);
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rh = a.rot / 2;
+  const int hh = blockIdx.y * 8 + warp;  // this warp's head: q heads, then k heads
+  const bool has_head = hh < a.Hq + a.Hkv;
   const float* x = a.qkv + static_cast<size_t>(row) * a.ld;
   const float* x2 = a.half_rows ? x + static_cast<size_t>(a.half_rows) * a.ld : nullptr;
-  // the row's angles once (double-precision reduction), then every head
+  // the head's values and this thread's V entries are loaded first, so the
+  // loads are in flight while the row's angles are computed
+  float hvr[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = lane + 32 * q;
+    hvr[q] = 0.f;
+    if (has_head && e < a.D) hvr[q] = x2 ? x[hh * a.D + e] + x2[hh * a.D + e] : x[hh * a.D + e];
+  }
+  const int vo = (a.Hq + a.Hkv) * a.D;
+  const int t_v = blockIdx.y * blockDim.x + threadIdx.x;  // V entries t_v, t_v + V stride, ...
+  const int v_stride = gridDim.y * blockDim.x;
+  float vv[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int t = t_v + q * v_stride;
+    vv[q] = 0.f;
+    if (t < a.Hkv * a.D) vv[q] = x2 ? x[vo + t] + x2[vo + t] : x[vo + t];
+  }
+  // the row's angles (double-precision reduction)
   __shared__ float cs_s[64], sn_s[64];
   __shared__ float hv_s[8][128];
   for (int j = threadIdx.x; j < rh; j += blockDim.x) rope_cos_sin(p, a.inv_freq[j], &cs_s[j], &sn_s[j]);
-  __syncthreads();
-  float* hv = hv_s[warp];
-  for (int hh = warp; hh < a.Hq + a.Hkv; hh += 8) {
-    const float* xh = x + hh * a.D;
-    float ss = 0.f;
-    for (int e = lane; e < a.D; e += 32) {
-      const float v = x2 ? xh[e] + x2[hh * a.D + e] : xh[e];
-      hv[e] = v;
-      ss = fmaf(v, v, ss);
-    }
-    const uint16_t* gain = hh < a.Hq ? a.q_norm : a.k_norm;
-    if (gain) {
-      const float inv = 1.0f / sqrtf(warp_sum(ss) / static_cast<float>(a.D) + a.eps);
-      for (int e = lane; e < a.D; e += 32)
-        hv[e] = (hv[e] * inv) * __uint_as_float(static_cast<uint32_t>(gain[e]) << 16);
-    }
-    __syncwarp();
-    float* q = hh < a.Hq ? a.q_out + static_cast<size_t>(row) * a.Hq * a.D + hh * a.D : nullptr;
-    uint16_t* dst =
-        hh < a.Hq ? nullptr : a.k_cache + ((static_cast<size_t>(b) * a.Hkv + (hh - a.Hq)) * a.S_max + p) * a.D;
-    for (int j = lane; j < rh; j += 32) {
-      float l2, h2;
-      rope_rotate(hv[j], hv[j + rh], cs_s[j], sn_s[j], &l2, &h2);
-      if (q) {
-        q[j] = l2;
-        q[j + rh] = h2;
-      } else {
-        dst[j] = f32_to_bf16(l2);
-        dst[j + rh] = f32_to_bf16(h2);
-      }
-    }
-    for (int e = a.rot + lane; e < a.D; e += 32) {
-      if (q) q[e] = hv[e];
-      else dst[e] = f32_to_bf16(hv[e]);
-    }
-    __syncwarp();
-  }
-  const int vo = (a.Hq + a.Hkv) * a.D;
-  for (int t = threadIdx.x; t < a.Hkv * a.D; t += blockDim.x) {
+  for (int t = t_v + 2 * v_stride; t < a.Hkv * a.D; t += v_stride) {  // V past two entries a thread
     const int g = t / a.D, d = t - g * a.D;
     const float v = x2 ? x[vo + t] + x2[vo + t] : x[vo + t];
     a.v_cache[((static_cast<size_t>(b) * a.Hkv + g) * a.S_max + p) * a.D + d] = f32_to_bf16(v);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int t = t_v + q * v_stride;
+    if (t < a.Hkv * a.D) {
+      const int g = t / a.D, d = t - g * a.D;
+      a.v_cache[((static_cast<size_t>(b) * a.Hkv + g) * a.S_max + p) * a.D + d] = f32_to_bf16(vv[q]);
+    }
+  }
+  __syncthreads();
+  if (!has_head) return;
+  float* hv = hv_s[warp];
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = lane + 32 * q;
+    if (e < a.D) {
+      hv[e] = hvr[q];
+      ss = fmaf(hvr[q], hvr[q], ss);
+    }
+  }
+  const uint16_t* gain = hh < a.Hq ? a.q_norm : a.k_norm;
+  if (gain) {
+    const float inv = 1.0f / sqrtf(warp_sum(ss) / static_cast<float>(a.D) + a.eps);
+    for (int e = lane; e < a.D; e += 32)
+      hv[e] = (hv[e] * inv) * __uint_as_float(static_cast<uint32_t>(gain[e]) << 16);
+  }
+  __syncwarp();
+  float* q = hh < a.Hq ? a.q_out + static_cast<size_t>(row) * a.Hq * a.D + hh * a.D : nullptr;
+  uint16_t* dst =
+      hh < a.Hq ? nullptr : a.k_cache + ((static_cast<size_t>(b) * a.Hkv + (hh - a.Hq)) * a.S_max + p) * a.D;
+  for (int j = lane; j < rh; j += 32) {
+    float l2, h2;
+    rope_rotate(hv[j], hv[j + rh], cs_s[j], sn_s[j], &l2, &h2);
+    if (q) {
+      q[j] = l2;
+      q[j + rh] = h2;
+    } else {
+      dst[j] = f32_to_bf16(l2);
+      dst[j + rh] = f32_to_bf16(h2);
+    }
+  }
+  for (int e = a.rot + lane; e < a.D; e += 32) {
+    if (q) q[e] = hv[e];
+    else dst[e] = f32_to_bf16(hv[e]);
   }
 }
 
@@ -265,7 +295,8 @@ cudaError_t launch_prefill_rope_store(const RopeIO& io, int n, int i0, int rows,
   a.err = err;
   for (int j = 0; j < a.rot / 2; ++j)
     a.inv_freq[j] = std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(a.rot));
-  return launch(prefill_rope_store_kernel, dim3(rows), dim3(256), 0, st, true, a);
+  // one warp per head: a row's heads over ceil((Hq + Hkv) / 8) CTAs of 8 warps
+  return launch(prefill_rope_store_kernel, dim3(rows, (Hq + Hkv + 7) / 8), dim3(256), 0, st, true, a);
 }
 
 cudaError_t launch_prefill_glu(const float* gu, int I, uint16_t* h, uint16_t* h_lo, size_t rows, int sms,
