@@ -223,3 +223,46 @@ def test_top_k_cut_inside_a_large_tie_group(gd):
         # the tie group spreads the draw over ~150,000 near-equal weights: every
         # row lies near a boundary there and is checked against its neighbours
         check_rows(got, z, u, None, 1.0, 1.0, K, 1.0, min_exact=1.0 if K == 3 else 0.0)
+
+
+@pytest.mark.parametrize("K", [256, 257])
+def test_top_k_at_the_candidate_limit(gd, K):
+    """top_k = 256 is the largest cut that the candidate path takes (each CTA
+    hands at most 256 candidates to CTA 0); 257 goes to the cluster searches.
+    Both agree with the oracle on the same rows."""
+    V, B = VOCAB, 6
+    z = synth.make_logits(18, "sel.cap", B, V, 3.0, True)
+    u = synth.make_uniforms(18, "sel.cap.u", B)
+    got = run(gd, z, u=u, temperature=0.9, top_k=K, top_p=0.95)
+    check_rows(got, z, u, None, 1.0, 0.9, K, float(np.float32(0.95)))
+
+
+def test_candidates_of_a_cta_below_another_ctas_cut(gd):
+    """All large logits in the first CTA's slice: every other CTA's local
+    candidates rank below the row's top_k and must drop out when CTA 0 ranks
+    them.  With top-p 1 and the draw spread over the survivors, the token must
+    be one of the 50 largest."""
+    V, B, K = VOCAB, 4, 50
+    rng_z = synth.make_logits(19, "sel.skew", B, V, 1.0, True)
+    idx = synth.uniform_int(19, "sel.skew.idx", (B, 200), 0, V // 8 - 1)
+    z = rng_z.copy()
+    for b in range(B):
+        z[b, idx[b]] += 8.0
+    u = synth.make_uniforms(19, "sel.skew.u", B)
+    got = run(gd, z, u=u, temperature=1.0, top_k=K)
+    check_rows(got, z, u, None, 1.0, 1.0, K, 1.0)
+    for b in range(B):
+        top = np.argsort(-z[b], kind="stable")[:K]
+        assert got[b] in set(top.tolist()) and got[b] < V // 8
+
+
+def test_candidate_path_with_masked_logits(gd):
+    """Half of the vocabulary at -inf with a small top-k: masked keys never
+    become candidates above a finite cut, and the drawn token is finite."""
+    V, B = VOCAB, 4
+    z = synth.make_logits(20, "sel.mask", B, V, 2.0, True)
+    z[:, 1::2] = -np.inf
+    u = synth.make_uniforms(20, "sel.mask.u", B)
+    got = run(gd, z, u=u, temperature=0.8, top_k=5, top_p=0.9)
+    check_rows(got, z, u, None, 1.0, 0.8, 5, float(np.float32(0.9)))
+    assert all(int(t) % 2 == 0 for t in got)
