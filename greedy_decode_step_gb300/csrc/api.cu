@@ -851,10 +851,10 @@ int state_views(const dec_model* m, dec_state* s, const DeviceInfo* dv, StateWs*
 // = beta * C + (Y[r] + Y_lo[r]) . W[n] with bf16 operands, fp32 accumulation
 // and output.
 int gemm_rows(const DeviceInfo* dv, const StateWs& w, std::initializer_list<TcSeg> segs, int K, const uint16_t* Y,
-              const uint16_t* Y_lo, int rows, int ldc, float beta, cudaStream_t st) {
+              const uint16_t* Y_lo, int rows, int ldc, float beta, cudaStream_t st, const TcGluOut* glu = nullptr) {
   const char* why = nullptr;
   const int rc = tc_gemm(segs.begin(), static_cast<int>(segs.size()), Y, Y_lo, rows, K, ldc, beta, w.gemm_part,
-                         w.gemm_part_bytes, dv->sms, dv->err, st, &why);
+                         w.gemm_part_bytes, dv->sms, dv->err, st, &why, glu);
   DEC_CHECK(rc == 0, rc == 1 ? DEC_EUNSUPPORTED : DEC_ECUDA, "tensor-core GEMM (%d rows, K %d): %s", rows, K,
             why ? why : "failed");
   return DEC_OK;
@@ -1005,10 +1005,13 @@ int step_gemm(const dec_model* m, const dec_state* s, const DeviceInfo* dv, cons
     DEC_TRY(gemm_rows(dv, w, {{lw.wo, H, r}}, QD, xs, xs + static_cast<size_t>(B) * QD, B, H, 1.f, st));
     DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(lw.mlp_norm), m->rms_eps, H, xs,
                                  xs + static_cast<size_t>(B) * H, B, st));
-    DEC_TRY(gemm_rows(dv, w, {{lw.wg, I, c2}, {lw.wu, I, c2 + I}}, H, xs, xs + static_cast<size_t>(B) * H, B, 2 * I,
-                      0.f, st));
-    DEC_CUDA(launch_prefill_glu(c2, I, xs, xs + static_cast<size_t>(B) * I, static_cast<size_t>(B), dv->sms, st));
-    DEC_TRY(gemm_rows(dv, w, {{lw.wd, H, r}}, I, xs, xs + static_cast<size_t>(B) * I, B, H, 1.f, st));
+    // gate/up with SiLU * up in the GEMM's epilogue: h as hi / lo bf16 parts
+    // in c2's space (xs is still being read), the down GEMM's operand
+    uint16_t* h = reinterpret_cast<uint16_t*>(c2);
+    const TcGluOut hout{h, h + static_cast<size_t>(B) * I};
+    DEC_TRY(gemm_rows(dv, w, {{lw.wg, I, nullptr}, {lw.wu, I, nullptr}}, H, xs, xs + static_cast<size_t>(B) * H, B,
+                      2 * I, 0.f, st, &hout));
+    DEC_TRY(gemm_rows(dv, w, {{lw.wd, H, r}}, I, hout.hi, hout.lo, B, H, 1.f, st));
   }
   if (head && m->lm_head) {
     DEC_CUDA(launch_prefill_norm(r, static_cast<const uint16_t*>(m->final_norm), m->rms_eps, H, xs,
@@ -1376,7 +1379,7 @@ int dec_step_launches(const dec_model* m, const dec_state* s, int* launches) {
     const TcSeg o[1] = {{nullptr, H, nullptr}};
     const TcSeg glu[2] = {{nullptr, I, nullptr}, {nullptr, I, nullptr}};
     const TcSeg head[1] = {{nullptr, m->vocab, nullptr}};
-    const int per_layer = 5 + tc_gemm_launches(qkv, 3, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, QD, pb, dv->sms) +
+    const int per_layer = 4 + tc_gemm_launches(qkv, 3, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, QD, pb, dv->sms) +
                           tc_gemm_launches(glu, 2, B, H, pb, dv->sms) + tc_gemm_launches(o, 1, B, I, pb, dv->sms);
     *launches = (m->embed ? 1 : 0) + m->n_layers * per_layer +
                 (m->lm_head ? 3 + tc_gemm_launches(head, 1, B, H, pb, dv->sms) : 1);

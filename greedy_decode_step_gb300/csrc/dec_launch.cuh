@@ -102,10 +102,18 @@ struct TcSeg {
   int N;
   float* C;
 };
+// Gate/up mode: segs = {gate W, up W} of equal N, beta 0; the output is
+// h[r][n] = silu(gate . y) * (up . y) as hi / lo bf16 parts [rows][N]
+// (16-byte aligned), written instead of C.
+struct TcGluOut {
+  uint16_t* hi;
+  uint16_t* lo;
+};
 constexpr int kTcMaxSplits = 16;
 size_t tc_gemm_part_bytes(int rows, int part_cols, int max_splits);
 int tc_gemm(const TcSeg* segs, int n_seg, const uint16_t* Yhi, const uint16_t* Ylo, int rows, int K, int ldc,
-            float beta, float* part, size_t part_bytes, int sms, uint32_t* err, cudaStream_t st, const char** why);
+            float beta, float* part, size_t part_bytes, int sms, uint32_t* err, cudaStream_t st, const char** why,
+            const TcGluOut* glu = nullptr);
 // Kernel launches one tc_gemm call makes (one: split-K partials are added by
 // the last split of each tile).
 int tc_gemm_launches(const TcSeg* segs, int n_seg, int rows, int K, size_t part_bytes, int sms);

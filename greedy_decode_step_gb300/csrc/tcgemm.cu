@@ -20,6 +20,9 @@
 //   * warps 2-5: wait for the last commit, read the accumulator with
 //     tcgen05.ld (warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. weight
 //     rows) and write C, or this split's partial sums.
+// In gate/up mode a tile is 64 rows of the gate weights and the same 64 rows
+// of the up weights (two TMA boxes), and the epilogue writes h = silu(g) * u
+// as the hi / lo bf16 parts the next GEMM takes, instead of C.
 // With split K, the splits of a tile form one thread-block cluster: each
 // keeps its partial in shared memory and adds one slice of the tile over all
 // of them through distributed shared memory, in split order, so the result
@@ -65,6 +68,11 @@ struct TcArgs {
   int col_off[kTcMaxSegs];
   int stages;
   uint32_t* err;
+  // gate/up mode (glu_hi non-null): segment 0 holds the gate rows, segment 1
+  // the up rows; a tile is 64 rows of each (units m0 .. m0 + 63), and the
+  // output is h = silu(gate) * up as hi / lo bf16 parts [rows][N[0]]
+  uint16_t* glu_hi;
+  uint16_t* glu_lo;
 };
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
@@ -130,6 +138,18 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, uint32_t
   return true;
 }
 
+__device__ __forceinline__ float tc_silu(float z) { return z / (1.0f + expf(-z)); }
+
+// h = silu(g) * u of unit `unit` in activation row r, stored as hi = bf16(h)
+// and lo = bf16(h - hi).
+__device__ __forceinline__ void tc_glu_store(const TcArgs& a, int r, int unit, float g, float u) {
+  const float h = tc_silu(g) * u;
+  const uint16_t hi = f32_to_bf16(h);
+  const size_t at = static_cast<size_t>(r) * a.N[0] + unit;
+  a.glu_hi[at] = hi;
+  a.glu_lo[at] = f32_to_bf16(h - __uint_as_float(static_cast<uint32_t>(hi) << 16));
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned base for the swizzled tiles
@@ -149,9 +169,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   const int tile = blockIdx.x / a.splits;
   const int nt = tile % a.n_tiles;
   const int mt_all = tile / a.n_tiles;
+  const bool glu = a.glu_hi != nullptr;
   int seg = 0;
-  while (seg + 1 < a.n_seg && mt_all >= a.tiles_before[seg + 1]) ++seg;
-  const int m0 = (mt_all - a.tiles_before[seg]) * kTcBM;
+  while (!glu && seg + 1 < a.n_seg && mt_all >= a.tiles_before[seg + 1]) ++seg;
+  // gate/up mode: units m0 .. m0 + 63 of both segments; otherwise 128 rows of one
+  const int m0 = glu ? mt_all * (kTcBM / 2) : (mt_all - a.tiles_before[seg]) * kTcBM;
   const int r0 = nt * a.BN;
   const int kb0 = static_cast<int>((static_cast<long long>(split) * a.kb_total) / a.splits);
   const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * a.kb_total) / a.splits);
@@ -191,7 +213,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       for (int i = 0; i < pre; ++i) {
         unsigned char* st = tiles + static_cast<size_t>(i) * stage_bytes;
         mbar_arrive_expect_tx(&full[i], stage_bytes);
-        tma_load_2d(st, &a.wmap[seg], (kb0 + i) * kTcBK, m0, &full[i], wpol);
+        if (glu) {
+          tma_load_2d(st, &a.wmap[0], (kb0 + i) * kTcBK, m0, &full[i], wpol);
+          tma_load_2d(st + kTcATile / 2, &a.wmap[1], (kb0 + i) * kTcBK, m0, &full[i], wpol);
+        } else {
+          tma_load_2d(st, &a.wmap[seg], (kb0 + i) * kTcBK, m0, &full[i], wpol);
+        }
       }
       pdl_wait();
       pdl_launch_dependents();
@@ -210,7 +237,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         unsigned char* st = tiles + static_cast<size_t>(s) * stage_bytes;
         const int k = (kb0 + i) * kTcBK;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
-        tma_load_2d(st, &a.wmap[seg], k, m0, &full[s], wpol);
+        if (glu) {
+          tma_load_2d(st, &a.wmap[0], k, m0, &full[s], wpol);
+          tma_load_2d(st + kTcATile / 2, &a.wmap[1], k, m0, &full[s], wpol);
+        } else {
+          tma_load_2d(st, &a.wmap[seg], k, m0, &full[s], wpol);
+        }
         tma_load_2d(st + kTcATile, &a.yhi, k, r0, &full[s], ypol);
         tma_load_2d(st + kTcATile + b_tile, &a.ylo, k, r0, &full[s], ypol);
       }
@@ -256,7 +288,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(a.BN + c0), vl);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] += vl[j];
-        if (a.splits > 1) {
+        if (a.splits > 1 || glu) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) pbuf[(c0 + j) * kTcBM + 32 * q + lane] = v[j];
           continue;
@@ -272,6 +304,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         }
       }
     }
+    if (glu && a.splits == 1) {
+      // gate row mm and up row mm + 64 of the tile meet in shared memory
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      for (int e = threadIdx.x - 64; e < a.BN * (kTcBM / 2); e += 128) {
+        const int c = e / (kTcBM / 2), mm = e - c * (kTcBM / 2);
+        const int r = r0 + c, unit = m0 + mm;
+        if (r < a.rows && unit < a.N[0]) tc_glu_store(a, r, unit, pbuf[c * kTcBM + mm], pbuf[c * kTcBM + mm + 64]);
+      }
+    }
   }
   if (a.splits > 1) {
     // The splits of this tile are one cluster: once every CTA's partial is
@@ -281,10 +322,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     pdl_wait();  // every thread writes C here
     __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    const int total = a.BN * kTcBM;
+    const uint32_t local = smem_addr(tiles);
+    if (glu) {
+      // pairs (gate row mm, up row mm + 64): a slice of BN * 64 pairs per rank
+      const int pairs = a.BN * (kTcBM / 2);
+      const int per2 = (pairs + a.splits - 1) / a.splits;
+      const int e1 = min(pairs, (split + 1) * per2);
+      for (int e = split * per2 + static_cast<int>(threadIdx.x); e < e1; e += kTcThreads) {
+        const int c = e / (kTcBM / 2), mm = e - c * (kTcBM / 2);
+        const uint32_t og = 4u * static_cast<uint32_t>(c * kTcBM + mm), ou = og + 4u * (kTcBM / 2);
+        float xg[kTcMaxClusterSplits], xu[kTcMaxClusterSplits];
+#pragma unroll
+        for (int k = 0; k < kTcMaxClusterSplits; ++k) {
+          xg[k] = 0.f;
+          xu[k] = 0.f;
+          if (k < a.splits) {
+            uint32_t rg, ru;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rg) : "r"(local + og), "r"(k));
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ru) : "r"(local + ou), "r"(k));
+            asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(xg[k]) : "r"(rg));
+            asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(xu[k]) : "r"(ru));
+          }
+        }
+        float g = 0.f, u = 0.f;
+#pragma unroll
+        for (int k = 0; k < kTcMaxClusterSplits; ++k)
+          if (k < a.splits) {
+            g += xg[k];
+            u += xu[k];
+          }
+        const int r = r0 + c, unit = m0 + mm;
+        if (r < a.rows && unit < a.N[0]) tc_glu_store(a, r, unit, g, u);
+      }
+    }
+    const int total = glu ? 0 : a.BN * kTcBM;
     const int per = (total + a.splits - 1) / a.splits;
     const int o1 = min(total, (split + 1) * per);
-    const uint32_t local = smem_addr(tiles);
     for (int o = split * per + static_cast<int>(threadIdx.x); o < o1; o += kTcThreads) {
       const int c = o / kTcBM, ml = o - c * kTcBM;
       // every rank's value in flight at once, then the sum in rank order
@@ -406,10 +479,15 @@ int tc_splits(int tiles, int kb_total, int sms, uint32_t smem) {
 int tc_gemm_launches(const TcSeg*, int, int, int, size_t, int) { return 1; }
 
 int tc_gemm(const TcSeg* segs, int n_seg, const uint16_t* Yhi, const uint16_t* Ylo, int rows, int K, int ldc,
-            float beta, float* part, size_t part_bytes, int sms, uint32_t* err, cudaStream_t st, const char** why) {
+            float beta, float* part, size_t part_bytes, int sms, uint32_t* err, cudaStream_t st, const char** why,
+            const TcGluOut* glu) {
   *why = nullptr;
   if (n_seg < 1 || n_seg > kTcMaxSegs || rows < 1 || K < 8 || K % 8 != 0) {
     *why = "shape outside the tensor-core GEMM";
+    return 1;
+  }
+  if (glu && (n_seg != 2 || segs[0].N != segs[1].N || !glu->hi || !glu->lo || beta != 0.f)) {
+    *why = "gate/up mode takes two segments of equal N and beta 0";
     return 1;
   }
   static thread_local TcArgs a;
@@ -435,10 +513,16 @@ int tc_gemm(const TcSeg* segs, int n_seg, const uint16_t* Yhi, const uint16_t* Y
     a.col_off[s] = cols;
     cols += segs[s].N;
     m_tiles += (segs[s].N + kTcBM - 1) / kTcBM;
-    if (!make_tmap_sw128(&a.wmap[s], segs[s].W, K, segs[s].N, kTcBM)) {
+    // gate/up mode: 64-row boxes of each segment fill the two halves of a tile
+    if (!make_tmap_sw128(&a.wmap[s], segs[s].W, K, segs[s].N, glu ? kTcBM / 2 : kTcBM)) {
       *why = "tensor map of the weights could not be made";
       return 1;
     }
+  }
+  if (glu) {
+    m_tiles = (segs[0].N + kTcBM / 2 - 1) / (kTcBM / 2);
+    a.glu_hi = glu->hi;
+    a.glu_lo = glu->lo;
   }
   a.tiles_before[n_seg] = m_tiles;
   if (!make_tmap_sw128(&a.yhi, Yhi, K, rows, a.BN) || !make_tmap_sw128(&a.ylo, Ylo, K, rows, a.BN)) {

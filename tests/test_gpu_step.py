@@ -289,13 +289,13 @@ def test_decode_rejects_bad_arguments():
 
 def test_step_launch_count():
     """One launch per step while the persistent kernel applies (b <= 2); above
-    that the step's own kernels: 1 embedding gather; per layer 6 (two norms,
-    RoPE + cache store, attention, the attention output's hi/lo split,
-    SiLU * up) around 4 tensor-core GEMMs (split-K partials are added inside
-    the GEMM); then the final norm, the LM-head GEMM, the row argmax and the
-    bookkeeping."""
+    that the step's own kernels: 1 embedding gather; per layer 4 (two norms,
+    RoPE + cache store, attention) around 4 tensor-core GEMMs (split-K
+    partials are added inside the GEMM, the attention writes the o_proj
+    operand, the gate/up GEMM applies SiLU * up in its epilogue); then the
+    final norm, the LM-head GEMM, the row argmax and the bookkeeping."""
     m = synth.workload("tiny", n_layers=2).model
-    for B, want in ((1, {1}), (2, {1}), (3, {1 + 2 * (5 + 4) + 4})):
+    for B, want in ((1, {1}), (2, {1}), (3, {1 + 2 * (4 + 4) + 4})):
         p = _fresh(m, B, 64)
         assert gd.dec_step_launches(p.model, p.state) in want
 
