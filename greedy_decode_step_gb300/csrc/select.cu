@@ -38,8 +38,9 @@
 // at or below the CTA's own top_k-th largest key).  When those candidates
 // are few, each CTA orders its own and writes them into CTA 0, which ranks
 // them by binary search, applies top-p and draws, with the same integer
-// weights and rules; three cluster barriers in all.  Otherwise (large top_k,
-// wide ties at the cut, no top-k) the searches run as above.
+// weights and rules; one cluster barrier in all (the row maximum is the best
+// head of the CTA lists).  Otherwise (large top_k, wide ties at the cut, no
+// top-k) the row maximum is exchanged and the searches run as above.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
