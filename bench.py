@@ -570,6 +570,15 @@ def run_select(args, world, rank, local):
         e1.record(stream)
     torch.cuda.synchronize(dev)
     ms1 = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev1)
+    # the same row with top-p alone (no top-k cut): the sampling of the pages' rollout
+    kw_p = dict(kw, top_k=0)
+    for e0, e1 in ev1:
+        flush.zero_()
+        e0.record(stream)
+        gd.dec_select_tokens(zd[:1], out1, u=ud[:1], prev_tokens=pd[:1], **kw_p)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms1p = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev1)
     # end to end from pinned host buffers: logits, draws and ids in, tokens out
     zh, uh, ph = (torch.from_numpy(x).pin_memory() for x in (z, u, prev))
     oh = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -598,7 +607,8 @@ def run_select(args, world, rank, local):
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (synth logits, std 4)",
            "config": {"workload": "select_b16: 16 rows x 151936 fp32 logits, 512 penalised ids per row, T=0.7, "
                                   "top_k=50, top_p=0.9; L2 flushed before each call",
-                      "tokens_equal_to_oracle": f"{agree}/{B}", "one_row_us": round(ms1 * 1e3, 2)},
+                      "tokens_equal_to_oracle": f"{agree}/{B}", "one_row_us": round(ms1 * 1e3, 2),
+                      "one_row_top_p_only_us": round(ms1p * 1e3, 2)},
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(gbs / peak, 4), "traffic": committed_traffic("select_kernel_b16"),
                         "peak_source": src,

@@ -79,6 +79,8 @@ struct SelShared {
   int cand_n, surv_n, token;
   int cnt_slot;                    // read by the other CTAs of the cluster
   int cnt_all[kSelCluster];
+  u64 z_all[kSelCluster];          // speculative top-p: each CTA's total weight
+  int verdict;                     // speculative top-p: CTA 0's answer (the nucleus is among the survivors)
 };
 
 // A survivor of the top-k cut, ranked in CTA 0.
@@ -316,7 +318,9 @@ __device__ u64 cta_sum(SelShared& sh, u64 v, int slot) {
   return t;
 }
 
-// CTA 0 of the top-k candidate path: each CTA's candidates sit in `buf`
+// CTA 0 of the candidate path (kc: the top-k cut; z_row: the row's total
+// weight for the top-p target when the cut is a speculative one, else 0 and
+// the survivors' total is used): each CTA's candidates sit in `buf`
 // (cap entries per CTA, key descending then index ascending, cnt[c] of
 // them).  A candidate's rank is the number of candidates with a strictly
 // larger key (a binary search per CTA list).  That is its rank in the whole row
@@ -325,7 +329,7 @@ __device__ u64 cta_sum(SelShared& sh, u64 v, int slot) {
 // top_k) then take the top-p cut and the draw with the same integer weights
 // and rules as the search path.
 __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* buf, int cap, int m_all,
-                              SelSurvivor* surv, float T, int row) {
+                              SelSurvivor* surv, float T, int row, int kc, u64 z_row) {
   const int tid = threadIdx.x;
   // the row maximum (smallest index on ties): the best first entry of the lists
   u64 top = 0ull;
@@ -363,7 +367,7 @@ __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* b
       pos += (pos < cn && sg[pos].x > me.x) ? 1 : 0;
       gt += pos;
     }
-    if (gt < a.top_k) {
+    if (gt < kc) {
       const int p = atomicAdd(&sh.surv_n, 1);
       surv[p] = SelSurvivor{me.x, me.y, weight_fixed(me.x, zmax, T)};
     }
@@ -375,7 +379,8 @@ __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* b
   if (a.top_p < 1.0f) {
     u64 z = 0ull;
     for (int j = tid; j < s; j += kSelThreads) z += surv[j].w;
-    const u64 Z = cta_sum(sh, z, 0);
+    u64 Z = cta_sum(sh, z, 0);
+    if (z_row != 0ull) Z = z_row;  // speculative top-p: the whole row's weight
     u64 target = scale_fixed(a.top_p, Z, true);
     target = target > 0ull ? target : 1ull;
     bool keep[4];
@@ -421,6 +426,43 @@ __device__ void select_ranked(const SelectArgs& a, SelShared& sh, const uint2* b
   }
   __syncthreads();
   if (tid == 0) a.token_out[row] = (M > 0ull && sh.token >= 0) ? sh.token : greedy;
+}
+
+// Speculative top-p, CTA 0: do the survivors of the top-kc cut weigh at
+// least ceil(p * Z), Z the row's weight?  They are every token at or above
+// the kc-th largest key, so the nucleus (the tokens at or above the largest
+// key whose upper weight reaches the target) then lies among them.
+__device__ bool spec_nucleus_inside(const SelectArgs& a, SelShared& sh, const uint2* buf, int cap, int m_all, int kc,
+                                    float zmax, float T) {
+  u64 ws = 0ull;
+  for (int e = threadIdx.x; e < m_all; e += kSelThreads) {
+    int c = 0, j = e;
+    while (j >= sh.cnt_all[c]) {
+      j -= sh.cnt_all[c];
+      ++c;
+    }
+    const uint2 me = buf[c * cap + j];
+    int gt = 0;
+#pragma unroll
+    for (int c2 = 0; c2 < kSelCluster; ++c2) {
+      const uint2* sg = buf + c2 * cap;
+      const int cn = sh.cnt_all[c2];
+      int pos = 0;
+#pragma unroll
+      for (int step = kSelCandMax / 2; step >= 1; step >>= 1)
+        pos += (pos + step <= cn && sg[pos + step - 1].x > me.x) ? step : 0;
+      pos += (pos < cn && sg[pos].x > me.x) ? 1 : 0;
+      gt += pos;
+    }
+    if (gt < kc) ws += weight_fixed(me.x, zmax, T);
+  }
+  const u64 W = cta_sum(sh, ws, 3);
+  u64 Z = 0ull;
+#pragma unroll
+  for (int c = 0; c < kSelCluster; ++c) Z += sh.z_all[c];
+  u64 target = scale_fixed(a.top_p, Z, true);
+  target = target > 0ull ? target : 1ull;
+  return W >= target;
 }
 
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
@@ -495,17 +537,58 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   }
   const float T = a.temperature;
 
-  // ---- top-k by candidates: every survivor of the row is among each CTA's
-  // keys at or above the bound of its thread maxima (ties included).  When
-  // they are few, each CTA orders its own and writes them into CTA 0, which
-  // ranks them and finishes the row alone (select_ranked): one cluster
-  // barrier, no exchange of the row maximum (it is the first entry of one of
-  // the lists).  Otherwise the cluster-wide searches below decide.
+  // ---- the row maximum (smallest index on ties): one exchange, made when
+  // the step after it needs the maximum in every CTA
+  bool have_max = false;
+  auto exchange_max = [&]() {
+    best = warp_max(best);
+    if (lane == 0) sh.warp_max[warp] = best;
+    __syncthreads();
+    if (tid < 32) {
+      const u64 v = warp_max(tid < kSelWarps ? sh.warp_max[tid] : 0ull);
+      if (tid == 0) sh.max_slot = v;
+    }
+    cl.sync();
+    if (tid < 32) {
+      const u64 v = warp_max(tid < kSelCluster ? *cl.map_shared_rank(&sh.max_slot, tid) : 0ull);
+      if (tid == 0) sh.max_bcast = v;
+    }
+    __syncthreads();
+    best = sh.max_bcast;
+    ++phase;
+    have_max = true;
+  };
+
+  // ---- the candidate path: every survivor of a top-k cut of at most `cap`
+  // is among each CTA's keys at or above the bound of its thread maxima
+  // (ties included).  When they are few, each CTA orders its own and writes
+  // them into CTA 0, which ranks them and finishes the row alone
+  // (select_ranked): one cluster barrier, no exchange of the row maximum (it
+  // is the first entry of one of the lists).  Top-p without a top-k cut runs
+  // it as a speculative top-(cap/2) cut: the row maximum is exchanged first,
+  // every CTA passes on its total weight, and CTA 0 tells the others whether
+  // the survivors hold the nucleus (one more barrier).  Otherwise the
+  // cluster-wide searches below decide.
   const int cap = min(kSelCandMax, a.list_cap * 16);  // CTA 0's buffer: 8 * cap * 8 bytes in the list area
-  const bool by_candidates = T > 0.f && a.top_k > 0 && a.top_k < a.V && a.top_k <= cap;  // the same in every CTA
-  if (by_candidates) {
+  const bool topk_cut = T > 0.f && a.top_k > 0 && a.top_k < a.V && a.top_k <= cap;  // the same in every CTA
+  const int kspec = cap / 2;
+  const bool topp_spec = T > 0.f && a.top_p < 1.0f && (a.top_k <= 0 || a.top_k >= a.V) && kspec >= 1 && kspec < a.V;
+  const int kc = topk_cut ? a.top_k : kspec;
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
+  u64 z_cta = 0ull;
+  if (topp_spec) {
+    exchange_max();
+    const float zm = key_value(static_cast<uint32_t>(best >> 32));
+    u64 zt = 0ull;
+    for (int i4 = tid; i4 < n / 4; i4 += kSelThreads) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) zt += weight_fixed(keys[i4 * 4 + e], zm, T);
+    }
+    z_cta = cta_sum(sh, zt, 2);
+  }
+  if (topk_cut || topp_spec) {
     if (tid == 0) sh.cand_n = 0;
-    const uint32_t lc = cta_kth_thread_max(sh, tmax, a.top_k);
+    const uint32_t lc = cta_kth_thread_max(sh, tmax, kc);
     if (tmax >= lc && tsec < lc && tid < n / 4) {
       // the thread's one candidate is its largest key
       const int p = atomicAdd(&sh.cand_n, 1);
@@ -531,7 +614,6 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     }
     __syncthreads();
     const int cnt = sh.cand_n;
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
     if (cnt <= cap) {
       // this CTA's candidates, key descending then index ascending, into CTA 0's list area
       uint2* dst = cl.map_shared_rank(reinterpret_cast<uint2*>(list_base), 0) + rank * cap;
@@ -547,7 +629,10 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
         dst[pos] = make_uint2(kj, static_cast<uint32_t>(lo + ij));
       }
     }
-    if (tid < kSelCluster) *cl.map_shared_rank(&sh.cnt_all[rank], tid) = cnt;  // every CTA learns every count
+    if (tid < kSelCluster) {  // every CTA learns every count (and, for top-p, every total weight)
+      *cl.map_shared_rank(&sh.cnt_all[rank], tid) = cnt;
+      *cl.map_shared_rank(&sh.z_all[rank], tid) = z_cta;
+    }
     cl.sync();  // lists and counts delivered; no shared memory of another CTA is read after this
     int m_all = 0, most = 0;
     for (int r = 0; r < kSelCluster; ++r) {
@@ -556,33 +641,30 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     }
     // the same decision in every CTA; CTA 0's survivors (16 bytes each) fit its key area
     if (most <= cap && m_all <= a.chunk / 4) {
-      if (rank == 0)
-        select_ranked(a, sh, reinterpret_cast<const uint2*>(list_base), cap, m_all,
-                      reinterpret_cast<SelSurvivor*>(smem), T, row);
-      return;
+      const uint2* buf = reinterpret_cast<const uint2*>(list_base);
+      if (topk_cut) {
+        if (rank == 0) select_ranked(a, sh, buf, cap, m_all, reinterpret_cast<SelSurvivor*>(smem), T, row, kc, 0ull);
+        return;
+      }
+      // speculative top-p: CTA 0's verdict, then the row is done or every CTA searches
+      if (rank == 0) {
+        const bool inside = spec_nucleus_inside(a, sh, buf, cap, m_all, kc,
+                                                key_value(static_cast<uint32_t>(best >> 32)), T);
+        if (tid < kSelCluster) *cl.map_shared_rank(&sh.verdict, tid) = inside ? 1 : 0;
+      }
+      cl.sync();  // the verdict delivered; CTA 0's keys are still intact
+      if (sh.verdict) {
+        if (rank == 0) {
+          u64 zrow = 0ull;
+#pragma unroll
+          for (int c = 0; c < kSelCluster; ++c) zrow += sh.z_all[c];
+          select_ranked(a, sh, buf, cap, m_all, reinterpret_cast<SelSurvivor*>(smem), T, row, kc, zrow);
+        }
+        return;
+      }
     }
-  } else {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
   }
-
-  // ---- the row maximum (smallest index on ties): one exchange
-  {
-    best = warp_max(best);
-    if (lane == 0) sh.warp_max[warp] = best;
-    __syncthreads();
-    if (tid < 32) {
-      const u64 v = warp_max(tid < kSelWarps ? sh.warp_max[tid] : 0ull);
-      if (tid == 0) sh.max_slot = v;
-    }
-    cl.sync();
-    if (tid < 32) {
-      const u64 v = warp_max(tid < kSelCluster ? *cl.map_shared_rank(&sh.max_slot, tid) : 0ull);
-      if (tid == 0) sh.max_bcast = v;
-    }
-    __syncthreads();
-    best = sh.max_bcast;
-    ++phase;
-  }
+  if (!have_max) exchange_max();
   const int32_t greedy = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
 
   if (!(T > 0.f)) {

@@ -89,3 +89,37 @@ def test_candidate_rule_with_distinct_values():
             assert len(got) == k
             applied += 1
     assert applied >= 9
+
+
+def kept_by_definition(w, z, target):
+    """Top-p over the whole row: v is kept iff the tokens with a larger logit
+    weigh less than the target."""
+    return {v for v in range(len(z)) if float(np.sum(w[z > z[v]])) < target}
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_speculative_top_p_check(seed):
+    """Top-p without top-k runs the candidate rule as a top-kc cut: when the
+    cut's survivors S already weigh the target, every kept token is in S and
+    the kept set computed inside S equals the one over the whole row."""
+    rng = np.random.default_rng(100 + seed)
+    V = int(rng.choice([1024, 4104, 8192]))
+    scale = float(rng.choice([0.5, 2.0, 6.0]))
+    z = np.round(rng.standard_normal(V) * scale * 8) / 8  # ties from rounding
+    w = np.exp(z - z.max())
+    Z = float(np.sum(w))
+    decided = 0
+    for kc in (16, 64, 128):
+        S = survivors_by_candidates(z, kc)
+        if S is None:
+            continue
+        for p in (0.3, 0.9, 0.99):
+            target = p * Z
+            if float(np.sum(w[sorted(S)])) < target:
+                continue  # the kernel would fall back to the searches
+            kept = kept_by_definition(w, z, target)
+            assert kept <= S
+            inside = {v for v in S if float(sum(w[u] for u in S if z[u] > z[v])) < target}
+            assert inside == kept
+            decided += 1
+    assert decided > 0 or scale < 1.0
