@@ -39,8 +39,12 @@
 // are few, each CTA orders its own and writes them into CTA 0, which ranks
 // them by binary search, applies top-p and draws, with the same integer
 // weights and rules; one cluster barrier in all (the row maximum is the best
-// head of the CTA lists).  Otherwise (large top_k, wide ties at the cut, no
-// top-k) the row maximum is exchanged and the searches run as above.
+// head of the CTA lists).  Top-p without a top-k cut runs the same path as a
+// speculative top-(cap/2) cut, after the row maximum and every CTA's total
+// weight are known: CTA 0 checks that the survivors already weigh the top-p
+// target (the nucleus then lies among them) and tells the others.  Otherwise
+// (large top_k, wide ties at the cut, a wider nucleus) the row maximum is
+// exchanged if it was not yet and the searches run as above.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
