@@ -81,8 +81,7 @@ struct SelShared {
   uint32_t ckey[kSelCandMax];      // this CTA's candidates: keys and slice indices
   uint16_t cand[kSelCandMax];
   int cand_n, surv_n, token;
-  int cnt_slot;                    // read by the other CTAs of the cluster
-  int cnt_all[kSelCluster];
+  int cnt_all[kSelCluster];        // written by every CTA of the cluster
   u64 z_all[kSelCluster];          // speculative top-p: each CTA's total weight
   int verdict;                     // speculative top-p: CTA 0's answer (the nucleus is among the survivors)
 };
